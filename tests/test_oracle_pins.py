@@ -1,0 +1,446 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each ``check_*`` function raises AssertionError when the oracle disagrees with
+what the source pages or the mathematics fix; the ``test_*`` functions run them,
+and ``test_planted_mistakes_are_caught`` plants plausible mistakes in the oracle
+(on the CPU) and requires that some check fails for each.
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as mo
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield [p.strip() for p in line.split("|")]
+
+
+# ---------------------------------------------------------------- f16 decode
+
+def check_half_decode():
+    # every finite f16 pattern against numpy's own binary16 conversion
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = mo.half_to_float(bits)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.all(np.isinf(got[np.isinf(ref)]))
+    assert np.all(np.isnan(got[np.isnan(ref)]))
+    # hand values: 1, -2, smallest subnormal, largest finite, 1/3 rounded
+    hand = {0x3C00: 1.0, 0xC000: -2.0, 0x0001: 2.0 ** -24, 0x7BFF: 65504.0,
+            0x3555: 0.333251953125, 0x0400: 2.0 ** -14, 0x8000: -0.0}
+    for b, v in hand.items():
+        assert mo.half_to_float(b) == v, hex(b)
+
+
+def test_half_decode():
+    check_half_decode()
+
+
+# ---------------------------------------------------------------- blocks
+
+def check_golden_blocks():
+    n = 0
+    for name, qt, hexbytes, values in _golden_lines("q4_blocks.txt"):
+        qt = int(qt)
+        raw = np.array([int(h, 16) for h in hexbytes.split()], np.uint8)
+        assert len(raw) == mo.BLOCK_BYTES[qt], name
+        want = np.array([float(v) for v in values.split()])
+        got = mo.dequant_rows(raw, 1, 32, qt)[0]
+        assert np.array_equal(got, want), (name, got, want)
+        n += 1
+    assert n >= 6
+
+
+def test_golden_blocks():
+    check_golden_blocks()
+
+
+def check_q4_0_is_q4_1_with_offset():
+    # Q4_0 (d, q) equals Q4_1 (d, m = -8d, q): -8d is exact in f16 (a power-of-two
+    # scaling that stays normal for these d), so the two decodes agree exactly.
+    rng = np.random.default_rng(11)
+    nb = 64
+    d = rng.uniform(0.005, 0.02, nb).astype("<f2")
+    qs = rng.integers(0, 256, (nb, 16), dtype=np.uint8)
+    b0 = np.concatenate([d.view(np.uint8).reshape(nb, 2), qs], axis=1)
+    m = (-8 * d.astype(np.float32)).astype("<f2")
+    assert np.array_equal(m.astype(np.float64), -8.0 * d.astype(np.float64))
+    b1 = np.concatenate([d.view(np.uint8).reshape(nb, 2), m.view(np.uint8).reshape(nb, 2), qs], axis=1)
+    v0 = mo.dequant_rows(b0.reshape(-1), 2, 32 * nb // 2, mo.Q4_0)
+    v1 = mo.dequant_rows(b1.reshape(-1), 2, 32 * nb // 2, mo.Q4_1)
+    assert np.array_equal(v0, v1)
+
+
+def test_q4_0_is_q4_1_with_offset():
+    check_q4_0_is_q4_1_with_offset()
+
+
+def check_block_dot_identity():
+    # The pages' block dot: dot(block, x) = d * sum(q x) + m * sum(x) (flint_moe_ssd.js,
+    # Q41DOT). q is read with plain integer shifts here, independently of the oracle.
+    rng = np.random.default_rng(12)
+    raw = np.concatenate([np.frombuffer(np.float16(0.0125).tobytes(), np.uint8),
+                          np.frombuffer(np.float16(-0.0625).tobytes(), np.uint8),
+                          rng.integers(0, 256, 16, dtype=np.uint8)])
+    x = rng.standard_normal(32)
+    q = [(raw[4 + i] & 15) if i < 16 else (raw[4 + i - 16] >> 4) for i in range(32)]
+    d16 = float(np.float16(0.0125))  # 0.0125 rounded to f16; -0.0625 is exact
+    want = d16 * sum(qi * xi for qi, xi in zip(q, x)) + (-0.0625) * sum(x)
+    got = float(mo.dequant_rows(raw, 1, 32, mo.Q4_1)[0] @ x)
+    assert math.isclose(got, want, rel_tol=1e-12, abs_tol=1e-12)
+
+
+def test_block_dot_identity():
+    check_block_dot_identity()
+
+
+# ---------------------------------------------------------------- routing
+
+def check_golden_routing():
+    n = 0
+    for name, kgg, svals, picks in _golden_lines("routing_cases.txt"):
+        k, g, gu = (int(v) for v in kgg.split())
+        s = np.array([float(v) for v in svals.split()])
+        want = [int(v) for v in picks.split()]
+        got = mo.select_experts(s, k, g, gu)
+        assert got == want, (name, got, want)
+        n += 1
+    assert n >= 6
+
+
+def test_golden_routing():
+    check_golden_routing()
+
+
+def _brute_force_picks(s, k, n_groups, groups_used):
+    """Selection by exhaustive search: the kept groups are the subset of size
+    groups_used with the largest summed group score (group score from a full
+    sort of the group), then a full sort of the allowed experts by (-s, index)."""
+    E = len(s)
+    per = E // n_groups
+    if n_groups > 1:
+        gsc = [sum(sorted(s[g * per:(g + 1) * per], reverse=True)[:2]) for g in range(n_groups)]
+        best = max(itertools.combinations(range(n_groups), groups_used),
+                   key=lambda c: (sum(gsc[g] for g in c), [-g for g in c]))
+        allowed = [e for e in range(E) if e // per in best]
+    else:
+        allowed = list(range(E))
+    return sorted(allowed, key=lambda e: (-s[e], e))[:k]
+
+
+def check_routing_brute_force():
+    rng = np.random.default_rng(13)
+    for trial in range(300):
+        n_groups = int(rng.choice([1, 2, 4, 8]))
+        per = int(rng.integers(2, 9))
+        E = n_groups * per
+        groups_used = int(rng.integers(1, n_groups + 1))
+        k = int(rng.integers(1, groups_used * per + 1))
+        s = rng.standard_normal(E)  # continuous: no ties
+        got = mo.select_experts(s, k, n_groups, groups_used)
+        want = _brute_force_picks(s, k, n_groups, groups_used)
+        assert got == want, (trial, got, want)
+
+
+def test_routing_brute_force():
+    check_routing_brute_force()
+
+
+def check_routing_reductions():
+    rng = np.random.default_rng(14)
+    for _ in range(50):
+        E, k = 32, int(rng.integers(1, 9))
+        s = rng.standard_normal(E)
+        plain = mo.select_experts(s, k)
+        # one group, or every group kept, is plain top-k
+        assert mo.select_experts(s, k, 4, 4) == plain
+        assert mo.select_experts(s, k, 1, 1) == plain
+        # zero bias: the picks follow the logits' order (sigmoid is increasing)
+        logits = rng.standard_normal(E) * 3
+        p = mo.sigmoid(logits)
+        assert mo.select_experts(p, k) == list(np.argsort(-logits, kind="stable")[:k])
+        # k = E: a permutation sorted by descending s
+        allp = mo.select_experts(s, E)
+        assert sorted(allp) == list(range(E))
+        assert all(s[allp[i]] >= s[allp[i + 1]] for i in range(E - 1))
+
+
+def test_routing_reductions():
+    check_routing_reductions()
+
+
+def check_route_weights_closed_form():
+    # logits ln 3, 0, -ln 3, ln 9 give sigmoids 3/4, 1/2, 1/4, 9/10 exactly (up to rounding)
+    logits = np.array([math.log(3), 0.0, -math.log(3), math.log(9)])
+    router_w = np.diag([1.0, 1.0, 1.0, 1.0]).astype(np.float32)
+    # x equal to the logits through an identity router; f32 rounding of x is the only error
+    x = logits.astype(np.float32)
+    cfg = mo.MoeConfig(hidden=4, n_experts=4, top_k=2, expert_ff=32)
+    ids, w, _ = mo.route(x, router_w, None, cfg)
+    assert list(ids[0]) == [3, 0]
+    assert np.allclose(w[0], [0.9 / 1.65, 0.75 / 1.65], rtol=1e-7)  # = 6/11, 5/11
+    # the bias changes the picks but never enters the weights; scale multiplies after
+    cfg2 = mo.MoeConfig(hidden=4, n_experts=4, top_k=2, expert_ff=32, weights_scale=2.5)
+    bias = np.array([0.0, 0.5, 0.0, -0.5], np.float32)
+    ids, w, s = mo.route(x, router_w, bias, cfg2)
+    assert list(ids[0]) == [1, 0]  # s = 0.75, 1.0, 0.25, 0.4
+    assert np.allclose(w[0], [2.5 * 0.5 / 1.25, 2.5 * 0.75 / 1.25], rtol=1e-7)
+    # the weights sum to the scale whenever the picked sigmoids sum past 2^-14
+    rng = np.random.default_rng(15)
+    for _ in range(20):
+        E = 16
+        rw = rng.standard_normal((E, 8)).astype(np.float32)
+        xx = rng.standard_normal(8).astype(np.float32)
+        c = mo.MoeConfig(hidden=8, n_experts=E, top_k=4, expert_ff=32, weights_scale=1.75)
+        _, ww, _ = mo.route(xx, rw, None, c)
+        assert math.isclose(ww.sum(), 1.75, rel_tol=1e-12)
+    # clamp: logits of -30 give sigmoids far below 2^-14, so w = p * 2^14 * scale
+    x = np.full(4, -30.0, np.float32)
+    ids, w, _ = mo.route(x, router_w, None, cfg2)
+    pz = 1.0 / (1.0 + math.exp(30.0))
+    assert 2 * pz < 2.0 ** -14
+    assert np.allclose(w[0], [pz * 2 ** 14 * 2.5] * 2, rtol=1e-12)
+
+
+def test_route_weights_closed_form():
+    check_route_weights_closed_form()
+
+
+# ---------------------------------------------------------------- SwiGLU and combine
+
+def _q4_1_block(d, m, q):
+    """One Q4_1 block from d, m and 32 nibble values (value i -> low nibble of
+    byte i for i < 16, high nibble of byte i - 16 otherwise)."""
+    q = list(q)
+    qs = bytes((q[i] & 15) | ((q[16 + i] & 15) << 4) for i in range(16))
+    return (np.float16(d).tobytes() + np.float16(m).tobytes() + qs)
+
+
+def check_swiglu_closed_form():
+    # One expert, H = F = 32. Gate row f picks x_f (q = 1 at column f), up row f
+    # picks 2 * x_{f+1}, down row h picks act_h / 2. So y_h = silu(x_h) * x_{h+1}
+    # exactly, gate rows first then up rows (flint_moe_ssd.js planLayoutFlint).
+    H = F = 32
+    one_hot = lambda c, v: [v if i == c else 0 for i in range(32)]
+    rec = b"".join(_q4_1_block(1.0, 0.0, one_hot(f, 1)) for f in range(F))
+    rec += b"".join(_q4_1_block(1.0, 0.0, one_hot((f + 1) % 32, 2)) for f in range(F))
+    rec += b"".join(_q4_1_block(0.5, 0.0, one_hot(h, 1)) for h in range(H))
+    rec = np.frombuffer(rec, np.uint8)
+    ln3 = math.log(3.0)
+    x = np.zeros(H, np.float32)
+    x[:4] = [ln3, 2.0, -ln3, 0.5]
+    x = x.astype(np.float32)
+    x64 = x.astype(np.float64)
+    cfg = mo.MoeConfig(hidden=H, n_experts=1, top_k=1, expert_ff=F, weights_scale=1.0)
+    out, ids, w = mo.moe_ffn(x, np.zeros((1, H), np.float32), None, rec, None, cfg)
+    silu = lambda z: z / (1.0 + math.exp(-z))
+    want = np.array([silu(x64[h]) * x64[(h + 1) % 32] for h in range(H)])
+    assert list(ids[0]) == [0] and w[0, 0] == 1.0
+    assert np.allclose(out[0], want, rtol=1e-12, atol=1e-15)
+    # the closed form at the chosen points: silu(ln 3) = 0.75 ln 3, silu(-ln 3) = -0.25 ln 3
+    assert math.isclose(out[0][0], 0.75 * ln3 * 2.0, rel_tol=1e-6)
+    assert math.isclose(out[0][2], -0.25 * ln3 * 0.5, rel_tol=1e-6)
+
+
+def test_swiglu_closed_form():
+    check_swiglu_closed_form()
+
+
+def _random_cfg_layer(seed, shared=True, groups=False):
+    from expert_ffn_decode_gb300 import synth
+    w = dict(hidden=64, n_experts=8, top_k=3, expert_ff=32, shared_ff=64 if shared else 0,
+             n_groups=2 if groups else 1, groups_used=1 if groups else 1, qtype=mo.Q4_1,
+             weights_scale=1.5, router_std=0.5, bias_std=0.1, seed=seed)
+    layer = synth.make_layer(w)
+    cfg = mo.MoeConfig(hidden=64, n_experts=8, top_k=3, expert_ff=32, shared_ff=w["shared_ff"],
+                       n_groups=w["n_groups"], groups_used=w["groups_used"], qtype=mo.Q4_1,
+                       weights_scale=1.5)
+    return layer, cfg
+
+
+def check_combine_invariants():
+    layer, cfg = _random_cfg_layer(21)
+    x = np.random.default_rng(22).standard_normal((3, 64)).astype(np.float32)
+    rb = mo.record_bytes(64, 32, mo.Q4_1)
+    # every expert identical: out = scale * E(x) + S(x), whatever the picks
+    same = np.tile(layer["expert_blocks"][:rb], cfg.n_experts)
+    out, _, _ = mo.moe_ffn(x, layer["router_w"], layer["bias"], same, layer["shared_blocks"], cfg)
+    w_gu, w_dn = mo.expert_matrices(same[:rb], 64, 32, mo.Q4_1)
+    s_gu, s_dn = mo.expert_matrices(layer["shared_blocks"], 64, 64, mo.Q4_1)
+    for t in range(3):
+        want = cfg.weights_scale * mo.swiglu(x[t], w_gu, w_dn) + mo.swiglu(x[t], s_gu, s_dn)
+        assert np.allclose(out[t], want, rtol=1e-12, atol=1e-12)
+    # the shared expert adds linearly with weight 1
+    cfg0 = mo.MoeConfig(**{**cfg.__dict__, "shared_ff": 0})
+    o1, _, _ = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"], layer["shared_blocks"], cfg)
+    o0, _, _ = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"], None, cfg0)
+    for t in range(3):
+        assert np.allclose(o1[t] - o0[t], mo.swiglu(x[t], s_gu, s_dn), rtol=1e-10, atol=1e-12)
+    # accumulate adds out_in; residual adds x
+    base = np.random.default_rng(23).standard_normal((3, 64))
+    cfga = mo.MoeConfig(**{**cfg.__dict__, "flags": mo.ACCUMULATE})
+    oa, _, _ = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"], layer["shared_blocks"], cfga, out_in=base)
+    assert np.allclose(oa - base, o1, rtol=1e-12, atol=1e-12)
+    cfgr = mo.MoeConfig(**{**cfg.__dict__, "flags": mo.RESIDUAL})
+    orr, _, _ = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"], layer["shared_blocks"], cfgr)
+    assert np.allclose(orr - x.astype(np.float64), o1, rtol=1e-12, atol=1e-12)
+
+
+def test_combine_invariants():
+    check_combine_invariants()
+
+
+def check_expert_matches_textbook_dense():
+    # A dense SwiGLU written from the textbook definition with scipy's expit, on
+    # matrices dequantised by plain per-element integer reads of the block bytes.
+    from scipy.special import expit
+    rng = np.random.default_rng(24)
+    H, F = 64, 32
+    from expert_ffn_decode_gb300 import synth
+    rec = synth.q4_blocks(rng, mo.Q4_0, 3 * F * H // 32)
+
+    def deq(raw, rows, cols):
+        out = np.zeros((rows, cols))
+        nb = cols // 32
+        for r in range(rows):
+            for b in range(nb):
+                blk = raw[(r * nb + b) * 18:(r * nb + b + 1) * 18]
+                d = float(np.frombuffer(bytes(blk[0:2]), "<f2")[0])
+                for i in range(32):
+                    byte = blk[2 + (i % 16)]
+                    q = (byte & 15) if i < 16 else (byte >> 4)
+                    out[r, b * 32 + i] = d * (int(q) - 8)
+        return out
+
+    gu_bytes = 2 * F * (H // 32) * 18
+    w_gu = deq(rec[:gu_bytes], 2 * F, H)
+    w_dn = deq(rec[gu_bytes:], H, F)
+    x = rng.standard_normal(H)
+    g, u = w_gu[:F] @ x, w_gu[F:] @ x
+    want = w_dn @ (g * expit(g) * u)
+    a, b = mo.expert_matrices(rec, H, F, mo.Q4_0)
+    assert np.allclose(mo.swiglu(x, a, b), want, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_matches_textbook_dense():
+    check_expert_matches_textbook_dense()
+
+
+ALL_CHECKS = [check_half_decode, check_golden_blocks, check_q4_0_is_q4_1_with_offset,
+              check_block_dot_identity, check_golden_routing, check_routing_brute_force,
+              check_routing_reductions, check_route_weights_closed_form,
+              check_swiglu_closed_form, check_combine_invariants,
+              check_expert_matches_textbook_dense]
+
+
+def _some_check_fails():
+    for chk in ALL_CHECKS:
+        try:
+            chk()
+        except AssertionError:
+            return True
+    return False
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _mut_nibble_order(blocks, n_rows, n_cols, qtype):
+    # high nibble read as value i, low as 16 + i
+    v = ORIG["dequant_rows"](blocks, n_rows, n_cols, qtype).reshape(n_rows, -1, 32)
+    return np.concatenate([v[..., 16:], v[..., :16]], axis=-1).reshape(n_rows, n_cols)
+
+
+def _mut_drop_m(blocks, n_rows, n_cols, qtype):
+    if qtype == mo.Q4_1:
+        b = np.array(blocks, np.uint8).reshape(n_rows, n_cols // 32, 20).copy()
+        b[..., 2:4] = 0
+        return ORIG["dequant_rows"](b.reshape(-1), n_rows, n_cols, qtype)
+    return ORIG["dequant_rows"](blocks, n_rows, n_cols, qtype)
+
+
+def _mut_q4_0_no_offset(blocks, n_rows, n_cols, qtype):
+    v = ORIG["dequant_rows"](blocks, n_rows, n_cols, qtype)
+    if qtype == mo.Q4_0:
+        b = np.array(blocks, np.uint8).reshape(n_rows, n_cols // 32, 18).astype(np.int64)
+        d = mo.half_to_float(b[..., 0] | (b[..., 1] << 8))
+        v = v + 8.0 * np.repeat(d, 32, axis=-1).reshape(v.shape)
+    return v
+
+
+def _mut_ties_highest(s, top_k, n_groups=1, groups_used=1):
+    # ties broken toward the highest index
+    r = ORIG["select_experts"](np.asarray(s)[::-1], top_k, 1, 1) if n_groups == 1 else None
+    if r is None:
+        return ORIG["select_experts"](s, top_k, n_groups, groups_used)
+    return [len(s) - 1 - e for e in r]
+
+
+def _mut_group_top1(s, n_groups):
+    per = len(s) // n_groups
+    return np.array([max(s[g * per:(g + 1) * per]) for g in range(n_groups)])
+
+
+def _mut_weights_bias(p, picks, scale, norm_min=mo.NORM_MIN):
+    # normalising s instead of p is caught by the bias closed form; here: no clamp
+    pp = np.array([p[e] for e in picks])
+    return pp / pp.sum() * scale
+
+
+def _mut_scale_inside(p, picks, scale, norm_min=mo.NORM_MIN):
+    pp = np.array([p[e] for e in picks])
+    return pp / max(pp.sum() * scale, norm_min)
+
+
+def _mut_swiglu_swap(x, w_gu, w_dn):
+    ff = w_gu.shape[0] // 2
+    gu = w_gu @ np.asarray(x, np.float64)
+    u, g = gu[:ff], gu[ff:]
+    return w_dn @ (g / (1.0 + np.exp(-g)) * u)
+
+
+def _mut_silu_sign(x, w_gu, w_dn):
+    ff = w_gu.shape[0] // 2
+    gu = w_gu @ np.asarray(x, np.float64)
+    g, u = gu[:ff], gu[ff:]
+    return w_dn @ (g / (1.0 + np.exp(g)) * u)
+
+
+def _mut_half_no_subnormal(bits):
+    v = ORIG["half_to_float"](bits)
+    h = np.asarray(bits, np.int64)
+    return np.where(((h >> 10) & 0x1F) == 0, 0.0, v)
+
+
+ORIG = {name: getattr(mo, name) for name in
+        ["dequant_rows", "select_experts", "group_scores", "route_weights", "swiglu", "half_to_float"]}
+
+MUTANTS = [
+    ("dequant_rows", _mut_nibble_order),
+    ("dequant_rows", _mut_drop_m),
+    ("dequant_rows", _mut_q4_0_no_offset),
+    ("select_experts", _mut_ties_highest),
+    ("group_scores", _mut_group_top1),
+    ("route_weights", _mut_weights_bias),
+    ("route_weights", _mut_scale_inside),
+    ("swiglu", _mut_swiglu_swap),
+    ("swiglu", _mut_silu_sign),
+    ("half_to_float", _mut_half_no_subnormal),
+]
+
+
+@pytest.mark.parametrize("target,mutant", MUTANTS, ids=[m.__name__ for _, m in MUTANTS])
+def test_planted_mistakes_are_caught(monkeypatch, target, mutant):
+    monkeypatch.setattr(mo, target, mutant)
+    assert _some_check_fails(), f"planted mistake {mutant.__name__} passed every pin"
