@@ -1,0 +1,353 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE-FFN step on GB300: tokens/s and HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one token through one MoE-FFN layer (router, top-k, routed experts,
+shared expert, combine) of the Flint-shaped decode layer (H=2048, 256 experts,
+top-6, F=512, shared F=1024, Q4_1). Weights are synthetic (seeded, drawn on the
+device) and rotate over enough distinct layers that every weight byte is cold
+in L2 when it is read again. Timed on the device with CUDA events around a
+replayed CUDA graph of the steps; rank 0 prints one JSON line.
+
+``--impl reference`` times the CPU oracle (float64, one thread) on a bounded
+sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-FFN tokens/s (decode T=1, prefill T=512); % of HBM/tensor roofline"
+UNIT = "tokens/s"
+
+
+def layer_bytes(w):
+    """Algorithmic bytes of one token's step: router, the k picked experts, the
+    shared expert, x and out (the experts not picked are never read)."""
+    bb = 18 if w["qtype"] == 2 else 20
+    H, E, K, F, Fs = w["hidden"], w["n_experts"], w["top_k"], w["expert_ff"], w["shared_ff"]
+    rec = lambda ff: 3 * ff * (H // 32) * bb
+    router = E * H * 4 + (E * 4 if w.get("bias_std") is not None else 0)
+    return router + K * rec(F) + (rec(Fs) if Fs else 0) + 2 * H * 4
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(workload: str, seconds: float = 12.0):
+    """The oracle, as it stands, on one thread, on a bounded sample of the workload."""
+    code = f"""
+import json, os, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+from expert_ffn_decode_gb300 import synth
+from oracle import moe_oracle as mo
+w = synth.WORKLOADS[{workload!r}]
+layer = synth.make_layer(w)
+cfg = mo.MoeConfig(hidden=w["hidden"], n_experts=w["n_experts"], top_k=w["top_k"], expert_ff=w["expert_ff"],
+                   shared_ff=w["shared_ff"], n_groups=w["n_groups"], groups_used=w["groups_used"],
+                   qtype=w["qtype"], weights_scale=w["weights_scale"])
+it = synth.token_stream(w["seed"], w["hidden"], 9)
+n, t0 = 0, time.perf_counter()
+while time.perf_counter() - t0 < {seconds}:
+    x = next(it)[None]
+    mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"], layer["shared_blocks"], cfg)
+    n += 1
+dt = time.perf_counter() - t0
+print(json.dumps({{"tokens": n, "seconds": dt}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return None, r.stderr[-400:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d, None
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from expert_ffn_decode_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    per_step = max(1.0, 12.0 / max(1, args.steps + args.warmup))
+    # warm-up steps, then exactly `steps` timed steps, each a bounded oracle sample
+    for _ in range(args.warmup):
+        cpu_baseline(args.workload, seconds=min(per_step, 2.0))
+    vals = []
+    for _ in range(args.steps):
+        d, err = cpu_baseline(args.workload, seconds=per_step)
+        if d is None:
+            print(json.dumps({"impl": "reference", "unavailable": f"oracle failed: {err}"}))
+            return
+        vals.append(d["tokens"] / d["seconds"] * w["n_tokens"])
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "T": w["n_tokens"]},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step:.1f} s of single-token oracle calls per step on one layer "
+                                   f"of the workload (numpy float64, one thread)"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--workload", default="flint_decode_t1")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="distinct layers to rotate (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=3000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import expert_ffn_decode_gb300 as ffn
+    from expert_ffn_decode_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(ffn.LIB_PATH):
+        from expert_ffn_decode_gb300 import build
+        build.build()
+    w = synth.WORKLOADS[args.workload]
+    T, H = w["n_tokens"], w["hidden"]
+    if T != 1:
+        raise SystemExit("this bench times the decode step (T = 1)")
+    step_bytes = layer_bytes(w)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    L = args.layers or max(8, math.ceil(4 * l2 / step_bytes) + 1)
+    layers = [synth.make_layer_torch(w, seed=1000 + 7919 * rank + i, device=dev) for i in range(L)]
+    NX = 64
+    xs = synth.make_tokens_torch(77 + rank, H, NX, dev)
+    outs = torch.zeros((2, H), device=dev)
+    flags = ffn.MOE_NO_PDL if args.no_pdl else 0
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags})
+    ws_bytes = ffn.moe_workspace_size(cfg)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i, st):
+        lay = layers[i % L]
+        rc = ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                    lay["shared_blocks"], cfg, outs[i % 2], ws, ws_bytes, st)
+        if rc != 0:
+            raise RuntimeError(ffn.moe_last_error())
+
+    # one graph of G steps (a whole number of layer sweeps), replayed
+    G = L * max(1, 320 // L)
+    with torch.cuda.stream(stream):
+        for i in range(2 * L):  # eager warm-up (plans, lazy module loading)
+            step(i, stream)
+    stream.synchronize()
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i, stream)
+        return g
+
+    g_main = capture(G)
+    tail = args.steps % G
+    g_tail = capture(tail) if tail else None
+    wg = capture(args.warmup % G) if args.warmup % G else None
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup // G):
+            g_main.replay()
+        if wg is not None:
+            wg.replay()
+    stream.synchronize()
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps // G):
+                g_main.replay()
+            if g_tail is not None:
+                g_tail.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    sec = elapsed_ms / 1e3
+    value = args.steps * T * world / sec
+    ms_per_step = elapsed_ms / args.steps
+
+    # ---- end to end through the C ABI with host buffers (pinned) ----
+    cfg_h = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags | ffn.MOE_HOST_IO})
+    wsh_bytes = ffn.moe_workspace_size(cfg_h)
+    wsh = torch.zeros(wsh_bytes, dtype=torch.uint8, device=dev)
+    xh = torch.empty((NX, H), dtype=torch.float32).pin_memory()
+    xh.copy_(xs.cpu())
+    oh = torch.empty((H,), dtype=torch.float32).pin_memory()
+    n_e2e = args.e2e_steps
+    torch.cuda.synchronize()
+    for i in range(20):
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream))
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        lay = layers[i % L]
+        rc = ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                    lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream)
+        if rc != 0:
+            raise RuntimeError(ffn.moe_last_error())
+        stream.synchronize()  # the step's result is on the host
+    e2e_sec = time.perf_counter() - t0
+    ffn.check(ffn.moe_workspace_status(wsh, stream))
+    e2e_val = n_e2e * T / e2e_sec
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_sec], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_val = n_e2e * T * world / float(t.item())
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+            "kernel": "moe_decode_kernel", "bytes_per_launch": step_bytes}
+    cpu = None
+    if not args.no_cpu_baseline:
+        d, err = cpu_baseline(args.workload)
+        if d is not None:
+            cpu = {"value": d["tokens"] / d["seconds"] * T, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{d['tokens']} single-token oracle calls in {d['seconds']:.1f} s on one "
+                             f"layer of the workload (numpy float64, one thread)"}
+        else:
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {err}"}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "T": T, "hidden": H, "n_experts": w["n_experts"],
+                   "top_k": w["top_k"], "expert_ff": w["expert_ff"], "shared_ff": w["shared_ff"],
+                   "qtype": "Q4_1" if w["qtype"] == 3 else "Q4_0", "parallelism": f"replicas{world}",
+                   "layers_rotated": L,
+                   "l2": f"inputs larger than L2: {L} distinct layers, {L * step_bytes / 1e6:.0f} MB of "
+                         f"step bytes between reuses of any weight byte (L2 {l2 / 1e6:.0f} MB)",
+                   "pdl": not args.no_pdl, "graph_steps": G},
+        "arith": "4-bit weights x activations in 22-bit block fixed point: exact int32 block dots (dp4a), "
+                 "fp32 scaling and accumulation; router and routing in fp32",
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": H * 4 * T,
+                "d2h_bytes_per_step": H * 4 * T, "steps": n_e2e,
+                "how": "moe_ffn_forward_ex with MOE_HOST_IO from pinned host memory, stream synchronised "
+                       "every step"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

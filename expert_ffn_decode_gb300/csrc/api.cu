@@ -1,0 +1,426 @@
+// C ABI of the routed MoE-FFN step: validation, workspace, planning, launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/moeffn.h"
+#include "common.cuh"
+#include "decode_host.h"
+#include "plan.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();  // clear the sticky launch error, if any
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int block_bytes(int qtype) { return qtype == MOE_Q4_0 ? 18 : 20; }
+
+// ---- configuration checks ------------------------------------------------------
+int check_cfg(const moe_cfg* c) {
+  if (!c) return fail(MOE_ERR_NULL_PTR, "cfg is NULL");
+  if (c->qtype != MOE_Q4_0 && c->qtype != MOE_Q4_1)
+    return fail(MOE_ERR_INVALID_CFG, "qtype %d: expected MOE_Q4_0 (2) or MOE_Q4_1 (3)", c->qtype);
+  if (c->hidden <= 0 || c->hidden % 32 || c->hidden > 3072)
+    return fail(MOE_ERR_INVALID_CFG, "hidden %d: must be a positive multiple of 32, at most 3072", c->hidden);
+  if (c->expert_ff <= 0 || c->expert_ff % 32 || c->expert_ff > 3072)
+    return fail(MOE_ERR_INVALID_CFG, "expert_ff %d: must be a positive multiple of 32, at most 3072",
+                c->expert_ff);
+  if (c->shared_ff < 0 || c->shared_ff % 32 || c->shared_ff > 3072)
+    return fail(MOE_ERR_INVALID_CFG, "shared_ff %d: must be 0 or a multiple of 32, at most 3072",
+                c->shared_ff);
+  if (c->n_experts < 1 || c->n_experts > 1024)
+    return fail(MOE_ERR_INVALID_CFG, "n_experts %d: must be in [1, 1024]", c->n_experts);
+  if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts)
+    return fail(MOE_ERR_INVALID_CFG, "top_k %d: must be in [1, min(n_experts, 32)]", c->top_k);
+  if (c->n_groups < 1 || c->n_experts % c->n_groups)
+    return fail(MOE_ERR_INVALID_CFG, "n_groups %d must divide n_experts %d", c->n_groups, c->n_experts);
+  if (c->n_groups > 1) {
+    const int per = c->n_experts / c->n_groups;
+    if (per < 2) return fail(MOE_ERR_INVALID_CFG, "groups of %d expert: need at least 2 per group", per);
+    if (c->n_groups > 64) return fail(MOE_ERR_INVALID_CFG, "n_groups %d > 64", c->n_groups);
+    if (c->groups_used < 1 || c->groups_used > c->n_groups)
+      return fail(MOE_ERR_INVALID_CFG, "groups_used %d: must be in [1, n_groups]", c->groups_used);
+    if (c->top_k > c->groups_used * per)
+      return fail(MOE_ERR_INVALID_CFG, "top_k %d exceeds the %d experts of the kept groups", c->top_k,
+                  c->groups_used * per);
+  }
+  if (c->n_tokens < 0) return fail(MOE_ERR_INVALID_CFG, "n_tokens %d < 0", c->n_tokens);
+  if (!std::isfinite(c->weights_scale))
+    return fail(MOE_ERR_INVALID_CFG, "weights_scale is not finite");
+  if (!(c->norm_min >= 0.f) || !std::isfinite(c->norm_min))
+    return fail(MOE_ERR_INVALID_CFG, "norm_min must be finite and >= 0");
+  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL))
+    return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
+  return MOE_OK;
+}
+
+// ---- workspace layout -----------------------------------------------------------
+struct WsLayout {
+  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, total;
+};
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+WsLayout ws_layout(const moe_cfg* c) {
+  WsLayout L;
+  size_t o = 0;
+  L.ctrl = o;
+  o += moe::CTRL_BYTES;
+  L.logits = o;
+  o = up256(o + (size_t)c->n_experts * 4);
+  L.act = o;
+  o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
+  const size_t T = (size_t)c->n_tokens;
+  L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
+  if (c->flags & MOE_HOST_IO) {
+    L.x_stage = o;
+    o = up256(o + T * c->hidden * 4);
+    L.out_stage = o;
+    o = up256(o + T * c->hidden * 4);
+    L.ids_stage = o;
+    o = up256(o + T * c->top_k * 4);
+    L.w_stage = o;
+    o = up256(o + T * c->top_k * 4);
+  }
+  L.total = o;
+  return L;
+}
+
+// ---- decode plans (cached per device and layer shape) ------------------------------
+struct PlanEntry {
+  int device;
+  moe_cfg key;
+  moe::DecodePlan plan;
+  uint32_t smem;
+  int maxb;
+};
+std::mutex g_mu;
+std::vector<PlanEntry> g_plans;
+
+bool same_shape(const moe_cfg& a, const moe_cfg& b) {
+  return a.hidden == b.hidden && a.n_experts == b.n_experts && a.top_k == b.top_k &&
+         a.expert_ff == b.expert_ff && a.shared_ff == b.shared_ff && a.n_groups == b.n_groups &&
+         (a.n_groups == 1 || a.groups_used == b.groups_used) && a.qtype == b.qtype;
+}
+
+int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
+  moe::DecodePlan p{};
+  p.H = c->hidden;
+  p.E = c->n_experts;
+  p.K = c->top_k;
+  p.F = c->expert_ff;
+  p.Fs = c->shared_ff;
+  p.G = c->n_groups;
+  p.Gu = c->n_groups > 1 ? c->groups_used : 1;
+  p.qtype = c->qtype;
+  p.blk = (uint32_t)block_bytes(c->qtype);
+  p.rb_h = (uint32_t)(p.H / 32) * p.blk;
+  p.rb_f = (uint32_t)(p.F / 32) * p.blk;
+  p.rb_fs = p.Fs ? (uint32_t)(p.Fs / 32) * p.blk : p.rb_f;
+  p.rec_bytes = (uint64_t)3 * p.F * (p.H / 32) * p.blk;
+  p.gu_align = moe::align_rows(p.rb_h);
+  int a_f = moe::align_rows(p.rb_f), a_fs = moe::align_rows(p.rb_fs);
+  p.dn_align = a_f > a_fs ? a_f : a_fs;
+
+  int sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  int maxb = 1;
+  for (int nb : {p.H / 32, p.F / 32, p.Fs / 32})
+    if ((nb + 31) / 32 > maxb) maxb = (nb + 31) / 32;
+
+  // ring slots: big enough for a router row and one aligned run of every row kind
+  uint32_t slot = 8192;
+  auto need = [&](uint32_t b) { if (b > slot) slot = b; };
+  need((uint32_t)p.H * 4u);
+  need(2u * (uint32_t)p.gu_align * p.rb_h);
+  need((uint32_t)p.dn_align * p.rb_f);
+  need((uint32_t)p.dn_align * p.rb_fs);
+  slot = (slot + 127) / 128 * 128;
+  p.slot_bytes = slot;
+  p.gu_r = (int)(slot / (2u * p.rb_h)) / p.gu_align * p.gu_align;
+  p.dn_r = (int)(slot / p.rb_f) / p.dn_align * p.dn_align;
+  p.dn_r_s = (int)(slot / p.rb_fs) / p.dn_align * p.dn_align;
+  p.nc = sms;
+
+  // busiest CTA
+  p.max_items = 0;
+  p.max_dn_rows = 0;
+  for (int cta = 0; cta < p.nc; ++cta) {
+    int lo, hi;
+    int n = moe::build_items(p, cta, nullptr, nullptr, nullptr, &lo, &hi);
+    if (n > p.max_items) p.max_items = n;
+    if (hi - lo > p.max_dn_rows) p.max_dn_rows = hi - lo;
+  }
+  // as many slots as fit next to the rest while keeping two CTAs per SM
+  const uint32_t budget2 = 113u * 1024u, budget1 = 226u * 1024u;
+  int nslots = 16;
+  uint32_t smem = 0;
+  for (; nslots >= 3; --nslots) {
+    p.nslots = nslots;
+    smem = moe::decode_smem_bytes(p);
+    if (smem <= budget2 && (uint64_t)nslots * slot <= 80u * 1024u) break;
+  }
+  if (nslots < 3) {
+    for (nslots = 4; nslots >= 3; --nslots) {
+      p.nslots = nslots;
+      smem = moe::decode_smem_bytes(p);
+      if (smem <= budget1) break;
+    }
+    if (nslots < 3) return fail(MOE_ERR_UNSUPPORTED, "layer too large for the decode kernel's shared memory");
+  }
+  int occ = 0;
+  e = moe::decode_occupancy(c->qtype, maxb, smem, &occ);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  if (occ < 1) return fail(MOE_ERR_UNSUPPORTED, "decode kernel does not fit on an SM (%u bytes shared)", smem);
+  out->device = device;
+  out->key = *c;
+  out->plan = p;
+  out->smem = smem;
+  out->maxb = maxb;
+  return MOE_OK;
+}
+
+int get_plan(const moe_cfg* c, PlanEntry* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const auto& pe : g_plans)
+    if (pe.device == dev && same_shape(pe.key, *c)) {
+      *out = pe;
+      return MOE_OK;
+    }
+  PlanEntry pe;
+  int rc = make_plan(c, dev, &pe);
+  if (rc != MOE_OK) return rc;
+  g_plans.push_back(pe);
+  *out = pe;
+  return MOE_OK;
+}
+
+// ---- library-owned workspaces -----------------------------------------------------
+struct OwnedWs {
+  int device;
+  void* ptr;
+  size_t bytes;
+};
+std::vector<OwnedWs> g_ws;
+
+int owned_workspace(size_t bytes, void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& w : g_ws)
+    if (w.device == dev) {
+      if (w.bytes >= bytes) {
+        *ptr = w.ptr;
+        return MOE_OK;
+      }
+      e = cudaFree(w.ptr);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFree");
+      w.ptr = nullptr;
+      w.bytes = 0;
+      e = cudaMalloc(&w.ptr, bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+      e = cudaMemset(w.ptr, 0, bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+      w.bytes = bytes;
+      *ptr = w.ptr;
+      return MOE_OK;
+    }
+  OwnedWs w{dev, nullptr, bytes};
+  e = cudaMalloc(&w.ptr, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  e = cudaMemset(w.ptr, 0, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  g_ws.push_back(w);
+  *ptr = w.ptr;
+  return MOE_OK;
+}
+
+int run(const float* x, const float* router_w, const float* bias, const void* experts,
+        const void* shared, const moe_cfg* c, float* out, void* ws, size_t ws_bytes, cudaStream_t st,
+        int32_t* ids, float* wts) {
+  int rc = check_cfg(c);
+  if (rc != MOE_OK) return rc;
+  const int T = c->n_tokens;
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !experts || !out) return fail(MOE_ERR_NULL_PTR, "x, router_w, expert_blocks and out must not be NULL");
+  if (c->shared_ff > 0 && !shared) return fail(MOE_ERR_NULL_PTR, "shared_ff > 0 needs shared_blocks");
+  if (!ws) return fail(MOE_ERR_NULL_PTR, "workspace is NULL");
+  if (!aligned(router_w, 16) || !aligned(experts, 16) || (shared && !aligned(shared, 16)))
+    return fail(MOE_ERR_ALIGNMENT, "router_w, expert_blocks and shared_blocks must be 16-byte aligned");
+  if (!(c->flags & MOE_HOST_IO) && (!aligned(x, 16) || !aligned(out, 16)))
+    return fail(MOE_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
+  if (bias && !aligned(bias, 4)) return fail(MOE_ERR_ALIGNMENT, "router_bias must be 4-byte aligned");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const size_t xbytes = (size_t)T * c->hidden * 4;
+  {
+    const char* xa = reinterpret_cast<const char*>(x);
+    const char* oa = reinterpret_cast<const char*>(out);
+    if (xa < oa + xbytes && oa < xa + xbytes) return fail(MOE_ERR_INVALID_CFG, "x and out overlap");
+  }
+  const WsLayout W = ws_layout(c);
+  if (ws_bytes < W.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, this call needs %zu", ws_bytes, W.total);
+
+  PlanEntry pe;
+  rc = get_plan(c, &pe);
+  if (rc != MOE_OK) return rc;
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const bool host = (c->flags & MOE_HOST_IO) != 0;
+  const float* dx = x;
+  float* dout = out;
+  int32_t* dids = ids;
+  float* dw = wts;
+  cudaError_t e;
+  if (host) {
+    dx = reinterpret_cast<const float*>(wsb + W.x_stage);
+    dout = reinterpret_cast<float*>(wsb + W.out_stage);
+    dids = ids ? reinterpret_cast<int32_t*>(wsb + W.ids_stage) : nullptr;
+    dw = wts ? reinterpret_cast<float*>(wsb + W.w_stage) : nullptr;
+    e = cudaMemcpyAsync(const_cast<float*>(dx), x, xbytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of x to the device");
+    if (c->flags & MOE_ACCUMULATE) {
+      e = cudaMemcpyAsync(dout, out, xbytes, cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) return cuda_fail(e, "copy of out to the device");
+    }
+  }
+
+  moe::DecodeArgs a{};
+  a.router_w = router_w;
+  a.bias = bias;
+  a.experts = static_cast<const uint8_t*>(experts);
+  a.shared = static_cast<const uint8_t*>(shared);
+  a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
+  a.logits = reinterpret_cast<float*>(wsb + W.logits);
+  a.act = reinterpret_cast<float*>(wsb + W.act);
+  a.scale = c->weights_scale;
+  a.norm_min = c->norm_min;
+  a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
+  a.p = pe.plan;
+  const bool pdl = (c->flags & MOE_NO_PDL) == 0;
+  for (int t = 0; t < T; ++t) {
+    a.x = dx + (size_t)t * c->hidden;
+    a.out = dout + (size_t)t * c->hidden;
+    a.topk_ids = dids ? dids + (size_t)t * c->top_k : nullptr;
+    a.topk_w = dw ? dw + (size_t)t * c->top_k : nullptr;
+    e = moe::decode_launch(a, c->qtype, pe.maxb, pe.smem, st, pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  }
+  if (host) {
+    e = cudaMemcpyAsync(out, dout, xbytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of out to the host");
+    if (ids) {
+      e = cudaMemcpyAsync(ids, dids, (size_t)T * c->top_k * 4, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess) return cuda_fail(e, "copy of topk_ids to the host");
+    }
+    if (wts) {
+      e = cudaMemcpyAsync(wts, dw, (size_t)T * c->top_k * 4, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess) return cuda_fail(e, "copy of topk_w to the host");
+    }
+  }
+  return MOE_OK;
+}
+
+int read_status(void* ws, cudaStream_t st) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t ctrl[16];
+  e = cudaMemcpy(ctrl, ws, sizeof ctrl, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (ctrl[moe::CTRL_STATUS] != 0) {
+    uint32_t st_bits = ctrl[moe::CTRL_STATUS], where = ctrl[moe::CTRL_WHERE];
+    e = cudaMemset(ws, 0, moe::CTRL_BYTES);
+    if (e != cudaSuccess) return cuda_fail(e, "control block reset");
+    return fail(MOE_ERR_TIMEOUT, "device wait timed out (status 0x%x, at %u); control words reset", st_bits,
+                where);
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_ffn_forward(const float* x, const float* router_w, const float* router_bias,
+                    const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg, float* out) {
+  g_err.clear();
+  int rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (cfg->n_tokens == 0) return MOE_OK;
+  const size_t need = ws_layout(cfg).total;
+  void* ws = nullptr;
+  rc = owned_workspace(need, &ws);
+  if (rc != MOE_OK) return rc;
+  rc = run(x, router_w, router_bias, expert_blocks, shared_blocks, cfg, out, ws, need, nullptr, nullptr,
+           nullptr);
+  if (rc != MOE_OK) return rc;
+  return read_status(ws, nullptr);
+}
+
+int moe_ffn_forward_ex(const float* x, const float* router_w, const float* router_bias,
+                       const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg, float* out,
+                       void* workspace, size_t workspace_bytes, void* stream, int32_t* topk_ids,
+                       float* topk_w) {
+  g_err.clear();
+  return run(x, router_w, router_bias, expert_blocks, shared_blocks, cfg, out, workspace, workspace_bytes,
+             static_cast<cudaStream_t>(stream), topk_ids, topk_w);
+}
+
+size_t moe_workspace_size(const moe_cfg* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return ws_layout(cfg).total;
+}
+
+int moe_workspace_status(void* workspace, void* stream) {
+  g_err.clear();
+  if (!workspace) return fail(MOE_ERR_NULL_PTR, "workspace is NULL");
+  return read_status(workspace, static_cast<cudaStream_t>(stream));
+}
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+int moe_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = MOE_OK;
+  for (auto& w : g_ws) {
+    if (w.ptr) {
+      int prev = 0;
+      cudaGetDevice(&prev);
+      cudaSetDevice(w.device);
+      if (cudaFree(w.ptr) != cudaSuccess) rc = MOE_ERR_CUDA;
+      cudaSetDevice(prev);
+    }
+  }
+  g_ws.clear();
+  g_plans.clear();
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// Small device helpers for sm_103a: mbarriers, 1-D bulk async copies,
+// programmatic-dependent-launch control, acquire/release flags, timers and the
+// integer dot products used by the 4-bit kernels. Every wait here is bounded.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace moe {
+
+// ---- control block (first 256 bytes of every workspace) ---------------------
+// Word layout. Every call leaves words 0..3 at zero when it returns normally;
+// the status word is sticky until the host clears it.
+enum CtrlWord : int {
+  CTRL_BAR_A = 0,    // arrivals at the router barrier
+  CTRL_BAR_B = 1,    // arrivals at the activation barrier
+  CTRL_EXIT = 2,     // CTAs that finished (the last one resets the counters)
+  CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
+  CTRL_WHERE = 9,    // first place that timed out (for diagnostics)
+};
+constexpr int CTRL_BYTES = 256;
+
+enum DevErr : uint32_t {
+  DEV_ERR_BARRIER_TIMEOUT = 1u,
+  DEV_ERR_MBAR_TIMEOUT = 2u,
+};
+
+// Spin limits, measured on %globaltimer: a grid barrier or an mbarrier wait
+// gives up after this many nanoseconds.
+constexpr unsigned long long BARRIER_TIMEOUT_NS = 200ull * 1000 * 1000;  // 0.2 s
+constexpr unsigned long long MBAR_TIMEOUT_NS = 500ull * 1000 * 1000;     // 0.5 s
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && globaltimer() - t0 > MBAR_TIMEOUT_NS) return false;
+  }
+}
+
+// ---- bulk async copy global -> shared (no tensor map) -------------------------
+// Both addresses 16-byte aligned, size a multiple of 16; completion is counted
+// in bytes on the mbarrier. `policy` is an L2 cache-policy descriptor.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---- programmatic dependent launch --------------------------------------------
+__device__ __forceinline__ void pdl_wait_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- gpu-scope flags -------------------------------------------------------------
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Named barriers (bar.sync / bar.arrive are warp-aligned: the warp reconverges first).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  __syncwarp();
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---- integer dot products ---------------------------------------------------------
+// dp4a with unsigned bytes in a and unsigned (uu) or signed (us) bytes in b.
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Round-to-nearest-even of |y| < 2^22 to an integer by the add-and-subtract of
+// 1.5 * 2^23 (the float then holds the integer in its low mantissa bits).
+__device__ __forceinline__ int round_small(float y) {
+  return __float_as_int(y + 12582912.0f) - 0x4B400000;
+}
+
+// Float -> 32-bit key whose unsigned order is the float order (-0 taken as +0).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace moe

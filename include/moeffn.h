@@ -1,0 +1,142 @@
+/*
+ * moeffn.h - C ABI of the routed MoE-FFN step on GB300 (sm_103a).
+ *
+ * The step, for each token t (diskformer engine modules, as shown by diffend.io):
+ *   logit_e = sum_h Wr[e][h] x[t][h]                      router, F32 "ffn_gate_inp"
+ *                                                          (lfm2_moe_ssd.js, initBuffers: router binding)
+ *   p_e = 1 / (1 + exp(-logit_e)); s_e = p_e + bias_e      bias only selects
+ *                                                          (lfm2_moe_ssd.js, TOPK_SIG_BODY and its comment)
+ *   groups (n_groups > 1): group score = the two largest s of the group summed;
+ *   keep the groups_used best groups, lowest group on ties  (ling_moe_ssd.js, routeLing)
+ *   picks: top_k rounds of argmax over the kept s, lowest index on ties, in
+ *   selection order                                         (TOPK_SIG_BODY)
+ *   w_j = p_pick_j / max(sum_j p_pick_j, norm_min) * weights_scale   (TOPK_SIG_BODY, routeLing)
+ *   expert: [g; u] = W_gu x (gate rows then up rows), y = W_down (silu(g) * u)
+ *                                                          (ling_moe_ssd.js, swiglu without clamp;
+ *                                                           flint_moe_ssd.js, planLayoutFlint record)
+ *   shared expert: the same SwiGLU with weight 1, no gate  (flint_moe_ssd.js, file header)
+ *   out[t] = sum_j w_j y_j + shared                         (ling_moe_ssd.js, moeAccum)
+ * Weights are ggml 4-bit blocks of 32 values (flint_moe_ssd.js, WGSL section,
+ * comment above Q41DOT): Q4_1 = f16 d, f16 m, 16 nibble bytes, value d*q + m;
+ * Q4_0 = f16 d, 16 nibble bytes, value d*(q - 8). In a block the low nibble of
+ * byte i is value i and its high nibble is value 16 + i.
+ *
+ * Layouts (all row-major, little-endian):
+ *   x, out         [n_tokens][hidden] f32
+ *   router_w       [n_experts][hidden] f32 (row e = expert e)
+ *   router_bias    [n_experts] f32, or NULL for no selection bias
+ *   expert_blocks  n_experts records back to back; record = gate [expert_ff][hidden/32 blocks],
+ *                  up [expert_ff][hidden/32 blocks], down [hidden][expert_ff/32 blocks];
+ *                  record bytes = 3 * expert_ff * hidden / 32 * block_bytes (18 or 20)
+ *   shared_blocks  one record of the same form with shared_ff, or NULL when shared_ff == 0
+ *   topk_ids       [n_tokens][top_k] int32 picks in selection order (optional output)
+ *   topk_w         [n_tokens][top_k] f32 weights (optional output)
+ *
+ * Ownership: the caller owns every buffer; the library never frees caller memory.
+ * Device pointers unless MOE_HOST_IO is set. Weights must not change while a call
+ * that reads them is in flight: calls read weights before the previous kernel on
+ * the stream has finished (programmatic dependent launch) unless MOE_NO_PDL is set.
+ * x and out must not overlap.
+ *
+ * Errors: every entry point returns MOE_OK (0) or a negative MOE_ERR_* code and
+ * sets a thread-local message (moe_last_error). Configurations and pointers are
+ * checked on the host before anything is launched. Kernels never trap: a device
+ * wait that runs out of time sets a status word in the workspace, which
+ * moe_workspace_status reports as MOE_ERR_TIMEOUT.
+ */
+#ifndef MOEFFN_H
+#define MOEFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ggml block type ids (flint_moe_ssd.js: GGML_Q4_1 = 3). */
+#define MOE_Q4_0 2
+#define MOE_Q4_1 3
+
+/* moe_cfg.flags */
+#define MOE_ACCUMULATE 1u /* out = out + contribution (the pages' x += ...)          */
+#define MOE_RESIDUAL 2u   /* out = x + contribution                                 */
+#define MOE_HOST_IO 4u    /* x, out, topk_ids, topk_w are host pointers, staged       */
+#define MOE_NO_PDL 8u     /* launch without programmatic dependent launch             */
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_CFG = -1,
+  MOE_ERR_NULL_PTR = -2,
+  MOE_ERR_ALIGNMENT = -3,
+  MOE_ERR_UNSUPPORTED = -4,
+  MOE_ERR_CUDA = -5,
+  MOE_ERR_TIMEOUT = -6,
+  MOE_ERR_WORKSPACE = -7
+};
+
+/* One MoE layer and one batch of tokens. The knobs are the layer's GGUF keys
+ * (expert_count, expert_used_count, expert_feed_forward_length,
+ * expert_shared_feed_forward_length, expert_group_count, expert_group_used_count,
+ * expert_weights_scale; flint_moe_ssd.js configFromGgufFlint, ling_moe_ssd.js
+ * configFromGgufLing). Limits checked by every entry point:
+ *   hidden, expert_ff, shared_ff multiples of 32 (shared_ff may be 0), at most 3072;
+ *   1 <= top_k <= min(n_experts, 32); n_experts <= 1024;
+ *   n_groups divides n_experts; n_groups > 1 needs n_experts / n_groups >= 2,
+ *   n_groups <= 64, 1 <= groups_used <= n_groups, top_k <= groups_used * n_experts / n_groups;
+ *   n_tokens >= 0 (0: nothing is launched); qtype MOE_Q4_0 or MOE_Q4_1;
+ *   norm_min >= 0 (the pages use 2^-14 = 6.103515625e-5). */
+typedef struct moe_cfg {
+  int32_t hidden;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t expert_ff;
+  int32_t shared_ff;
+  int32_t n_groups;    /* 1 = plain top-k */
+  int32_t groups_used; /* ignored when n_groups == 1 */
+  int32_t n_tokens;
+  int32_t qtype;
+  float weights_scale; /* 1.0 unless the layer says otherwise */
+  float norm_min;      /* clamp on the sum of the picked sigmoids */
+  uint32_t flags;      /* MOE_* flags above */
+} moe_cfg;
+
+/* The step on the default stream with a library-owned workspace (one per
+ * device, grown on demand, freed by moe_shutdown). Blocks until the step is
+ * done and returns device-side errors directly. Pointer alignment: x, out,
+ * router_w, expert_blocks, shared_blocks 16 bytes; router_bias 4 bytes. */
+int moe_ffn_forward(const float* x, const float* router_w, const float* router_bias,
+                    const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg,
+                    float* out);
+
+/* The step enqueued on `stream` (a cudaStream_t, NULL = legacy default stream)
+ * with a caller-owned device workspace of at least moe_workspace_size(cfg) bytes,
+ * 256-byte aligned. The first 256 bytes of a workspace must be zero before its
+ * first use; every call leaves them as it found them when it completes normally.
+ * Calls sharing one workspace must be ordered (same stream, or synchronised).
+ * Asynchronous: device-side errors surface through moe_workspace_status.
+ * topk_ids / topk_w may be NULL. */
+int moe_ffn_forward_ex(const float* x, const float* router_w, const float* router_bias,
+                       const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg,
+                       float* out, void* workspace, size_t workspace_bytes, void* stream,
+                       int32_t* topk_ids, float* topk_w);
+
+/* Workspace bytes a call with this configuration needs (0 for an invalid cfg). */
+size_t moe_workspace_size(const moe_cfg* cfg);
+
+/* Waits for `stream`, then reads and clears the workspace's status word:
+ * MOE_OK, or MOE_ERR_TIMEOUT when a device-side wait ran out of time (the
+ * workspace's control words are zeroed again so it can be reused). */
+int moe_workspace_status(void* workspace, void* stream);
+
+/* Text of the last error on the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Frees the library-owned workspaces. Returns MOE_OK or MOE_ERR_CUDA. */
+int moe_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEFFN_H */

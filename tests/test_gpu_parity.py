@@ -1,0 +1,177 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Bars: identical ordered picks, routing weights within W_REL, each token's
+output within relative L2 OUT_REL_L2 (2e-3). Tokens are drawn with a selection
+margin so fp32/fp64 rounding cannot reorder the picks.
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+from expert_ffn_decode_gb300 import synth
+from oracle import moe_oracle as mo
+from tests.helpers import GpuLayer, compare, margin_tokens, oracle_cfg, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+_layers = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import expert_ffn_decode_gb300 as ffn
+    if not os.path.exists(ffn.LIB_PATH):
+        from expert_ffn_decode_gb300 import build
+        build.build()
+    import torch
+    assert torch.cuda.is_available()
+    yield
+    ffn.moe_shutdown()
+
+
+def layer_of(name):
+    if name not in _layers:
+        w = synth.WORKLOADS[name]
+        _layers[name] = (w, synth.make_layer(w))
+    return _layers[name]
+
+
+DECODE = ["tiny_q4_0_t4", "flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1"]
+
+
+@pytest.mark.parametrize("name", DECODE)
+def test_workload_parity(name):
+    w, layer = layer_of(name)
+    T = w["n_tokens"]
+    x, _ = margin_tokens(layer, w, T, seed=w["seed"])
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    g = GpuLayer(layer, w)
+    out, ids, wts = g.run(x)
+    err = compare(out, ids, wts, ref, rid, rwt, name)
+    print(f"{name}: max rel-L2 {err:.3e}")
+
+
+@pytest.mark.parametrize("name", DECODE[1:])
+def test_workload_more_tokens(name):
+    # eight more tokens of the decode layers, as one call of T = 8 (run token by token)
+    w, layer = layer_of(name)
+    x, redraws = margin_tokens(layer, w, 8, seed=w["seed"], stream=2)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    compare(out, ids, wts, ref, rid, rwt, name)
+
+
+def _small(seed, **kw):
+    w = dict(hidden=256, n_experts=16, top_k=4, expert_ff=128, shared_ff=0, n_groups=1, groups_used=1,
+             qtype=mo.Q4_1, weights_scale=1.0, n_tokens=3, router_std=0.1, bias_std=None, seed=seed)
+    w.update(kw)
+    return w
+
+
+RANDOM = [
+    _small(10),
+    _small(11, qtype=mo.Q4_0, shared_ff=64),
+    _small(12, hidden=96, expert_ff=96, qtype=mo.Q4_0),                 # odd block count per row
+    _small(13, hidden=96, expert_ff=160, shared_ff=96, qtype=mo.Q4_1),
+    _small(14, n_experts=40, top_k=7, bias_std=0.1),                    # E not a multiple of 32
+    _small(15, n_experts=12, top_k=12),                                 # k = E
+    _small(16, n_experts=32, n_groups=4, groups_used=2, top_k=5, bias_std=0.1, weights_scale=2.5),
+    _small(17, n_experts=64, n_groups=8, groups_used=3, top_k=6, bias_std=0.1, qtype=mo.Q4_0),
+    _small(18, hidden=3072, expert_ff=64, shared_ff=3072, n_experts=8, top_k=2, router_std=0.02),
+    _small(19, hidden=512, expert_ff=3072, n_experts=6, top_k=3, router_std=0.05, qtype=mo.Q4_0),
+    _small(20, hidden=1024, expert_ff=32, shared_ff=32, n_experts=1000, top_k=32, router_std=0.05),
+    _small(21, n_experts=128, n_groups=64, groups_used=5, top_k=9, bias_std=0.1),
+    _small(22, hidden=32, expert_ff=32, n_experts=2, top_k=1),
+]
+
+
+@pytest.mark.parametrize("w", RANDOM, ids=[f"s{w['seed']}" for w in RANDOM])
+def test_random_shapes(w):
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']}")
+
+
+def test_flags_accumulate_residual_hostio_nopdl():
+    import expert_ffn_decode_gb300 as ffn
+    w, layer = layer_of("flint_decode_t1")
+    x, _ = margin_tokens(layer, w, 2, seed=5, stream=3)
+    g = GpuLayer(layer, w)
+    base, ids, wts = g.run(x)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    compare(base, ids, wts, ref, rid, rwt, "plain")
+    init = np.random.default_rng(6).standard_normal(x.shape).astype(np.float32)
+    acc, _, _ = g.run(x, flags=ffn.MOE_ACCUMULATE, out_init=init)
+    assert rel_l2(acc - init, base) < 1e-6
+    res, _, _ = g.run(x, flags=ffn.MOE_RESIDUAL)
+    assert rel_l2(res - x, base) < 1e-6
+    nopdl, _, _ = g.run(x, flags=ffn.MOE_NO_PDL)
+    assert np.array_equal(nopdl, base)
+    # host buffers: the library stages x and out through its workspace
+    import torch
+    T, H = x.shape
+    cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": ffn.MOE_HOST_IO})
+    ws = torch.zeros(ffn.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    xh = np.ascontiguousarray(x, np.float32)
+    oh = np.full((T, H), np.nan, np.float32)
+    ih = np.full((T, w["top_k"]), -1, np.int32)
+    wh = np.full((T, w["top_k"]), np.nan, np.float32)
+    st = torch.cuda.current_stream()
+    ffn.check(ffn.moe_ffn_forward_ex(xh, g.router_w, g.bias, g.experts, g.shared, cfg, oh, ws, ws.numel(),
+                                     st, ih, wh))
+    ffn.check(ffn.moe_workspace_status(ws, st))
+    assert np.array_equal(oh, base) and np.array_equal(ih, ids) and np.array_equal(wh, wts)
+
+
+def test_plain_entry_point_and_repeat_determinism():
+    import expert_ffn_decode_gb300 as ffn
+    import torch
+    w, layer = layer_of("lfm25_decode_t1")
+    x, _ = margin_tokens(layer, w, 1, seed=7, stream=4)
+    g = GpuLayer(layer, w)
+    first, ids, wts = g.run(x)
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1})
+    xd = torch.from_numpy(x).cuda()
+    out = torch.empty_like(xd)
+    ffn.check(ffn.moe_ffn_forward(xd, g.router_w, g.bias, g.experts, g.shared, cfg, out))
+    assert np.array_equal(out.cpu().numpy(), first)
+    # one workspace reused for many calls in a row: control words reset every call
+    ws = torch.zeros(ffn.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    for _ in range(20):
+        again, _, _ = g.run(x, workspace=ws)
+        assert np.array_equal(again, first)
+
+
+def test_bias_none_equals_zero_bias_and_empty_batch():
+    import expert_ffn_decode_gb300 as ffn
+    w = _small(30, bias_std=None)
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, 2, seed=30)
+    a, ia, wa = GpuLayer(layer, w).run(x)
+    layer0 = dict(layer, bias=np.zeros(w["n_experts"], np.float32))
+    b, ib, wb = GpuLayer(layer0, w).run(x)
+    assert np.array_equal(a, b) and np.array_equal(ia, ib)
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 0})
+    assert ffn.moe_ffn_forward_ex(None, None, None, None, None, cfg, None, None, 0, None) == ffn.MOE_OK
+
+
+def test_weight_clamp_case():
+    # every logit about -30: the picked sigmoids sum far below 2^-14, so w = p / 2^-14 * scale;
+    # equal logits tie exactly and both sides pick the lowest indices
+    w = _small(31, n_experts=8, top_k=3, weights_scale=2.5)
+    layer = synth.make_layer(w)
+    H = w["hidden"]
+    layer["router_w"] = np.full((8, H), -30.0 / H, np.float32)
+    x = np.ones((1, H), np.float32)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], None, layer["expert_blocks"], None, oracle_cfg(w))
+    assert list(rid[0]) == [0, 1, 2]
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    compare(out, ids, wts, ref, rid, rwt, "clamp")
