@@ -100,8 +100,9 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(workload: str, seconds: float = 12.0):
-    """The oracle, as it stands, on one thread, on a bounded sample of the workload."""
+def cpu_baseline(workload: str, seconds: float = 12.0, warmup: int = 0, max_tokens: int = 10 ** 9):
+    """The oracle, as it stands, on one thread, on a bounded sample of the workload:
+    single-token calls on one synthetic layer until `seconds` or `max_tokens` is reached."""
     code = f"""
 import json, os, sys, time
 sys.path.insert(0, {ROOT!r})
@@ -114,16 +115,19 @@ cfg = mo.MoeConfig(hidden=w["hidden"], n_experts=w["n_experts"], top_k=w["top_k"
                    shared_ff=w["shared_ff"], n_groups=w["n_groups"], groups_used=w["groups_used"],
                    qtype=w["qtype"], weights_scale=w["weights_scale"])
 it = synth.token_stream(w["seed"], w["hidden"], 9)
+call = lambda x: mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                            layer["shared_blocks"], cfg)
+for _ in range({warmup}):
+    call(next(it)[None])
 n, t0 = 0, time.perf_counter()
-while time.perf_counter() - t0 < {seconds}:
-    x = next(it)[None]
-    mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"], layer["shared_blocks"], cfg)
+while n < {max_tokens} and (n == 0 or time.perf_counter() - t0 < {seconds}):
+    call(next(it)[None])
     n += 1
 dt = time.perf_counter() - t0
 print(json.dumps({{"tokens": n, "seconds": dt}}))
 """
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         return None, r.stderr[-400:]
     d = json.loads(r.stdout.strip().splitlines()[-1])
@@ -141,33 +145,61 @@ def dist_setup(n_gpus):
 
 
 def run_reference(args, rank, world):
+    """The oracle arm: warm-up steps, then the timed steps, one oracle token per
+    step, within a 90 s budget (steps past the budget are not run; the line says
+    how many were)."""
     if rank != 0:
         return
     from expert_ffn_decode_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    per_step = max(1.0, 12.0 / max(1, args.steps + args.warmup))
-    # warm-up steps, then exactly `steps` timed steps, each a bounded oracle sample
-    for _ in range(args.warmup):
-        cpu_baseline(args.workload, seconds=min(per_step, 2.0))
-    vals = []
-    for _ in range(args.steps):
-        d, err = cpu_baseline(args.workload, seconds=per_step)
-        if d is None:
-            print(json.dumps({"impl": "reference", "unavailable": f"oracle failed: {err}"}))
-            return
-        vals.append(d["tokens"] / d["seconds"] * w["n_tokens"])
-    v = statistics.median(vals)
+    d, err = cpu_baseline(args.workload, seconds=90.0, warmup=min(args.warmup, 3), max_tokens=args.steps)
+    if d is None:
+        print(json.dumps({"impl": "reference", "unavailable": f"oracle failed: {err}"}))
+        return
+    v = d["tokens"] / d["seconds"] * w["n_tokens"]
+    sample = (f"{d['tokens']} of the {args.steps} requested steps (one single-token oracle call each, "
+              f"{d['seconds']:.1f} s) on one synthetic layer of the workload; numpy float64, one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "T": w["n_tokens"]},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step:.1f} s of single-token oracle calls per step on one layer "
-                                   f"of the workload (numpy float64, one thread)"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
+    """Per-phase timeline of the last launch of a chain of `chain` steps: for each
+    trace point, the median and the max over CTAs of (time - earliest CTA start), us."""
+    import torch
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags | ffn.MOE_TRACE})
+    nbytes = ffn.moe_workspace_size(cfg)
+    off = ffn.moe_trace_offset(cfg)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(w["hidden"], device=dev)
+    nc = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows = []
+    for rep in range(reps):
+        with torch.cuda.stream(stream):
+            for i in range(chain):
+                lay = layers[(rep * chain + i) % L]
+                ffn.check(ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                                 lay["shared_blocks"], cfg, out, ws, nbytes, stream))
+        stream.synchronize()
+        ffn.check(ffn.moe_workspace_status(ws, stream))
+        rows.append(ws[off:off + nc * ffn.TRACE_STRIDE * 8].view(torch.int64).view(nc, ffn.TRACE_STRIDE).cpu().double())
+    summary = {}
+    for k, name in enumerate(ffn.TRACE_POINTS):
+        med, mx = [], []
+        for t in rows:
+            d = (t[:, k] - t[:, 0].min()) / 1e3
+            med.append(float(d.median()))
+            mx.append(float(d.max()))
+        summary[name] = [round(statistics.median(med), 2), round(statistics.median(mx), 2)]
+    print("trace (us since first CTA start: [median over CTAs, max over CTAs]): " + json.dumps(summary),
+          file=sys.stderr)
 
 
 def main():
@@ -181,6 +213,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="after timing, print the kernel's per-CTA phase timeline (stderr)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -275,6 +309,9 @@ def main():
     sec = elapsed_ms / 1e3
     value = args.steps * T * world / sec
     ms_per_step = elapsed_ms / args.steps
+
+    if args.trace:
+        print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream)
 
     # ---- end to end through the C ABI with host buffers (pinned) ----
     cfg_h = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags | ffn.MOE_HOST_IO})

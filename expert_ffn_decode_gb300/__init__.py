@@ -26,6 +26,7 @@ MOE_ACCUMULATE = 1
 MOE_RESIDUAL = 2
 MOE_HOST_IO = 4
 MOE_NO_PDL = 8
+MOE_TRACE = 16
 
 MOE_OK = 0
 MOE_ERR_INVALID_CFG = -1
@@ -39,8 +40,8 @@ MOE_ERR_WORKSPACE = -7
 NORM_MIN = 6.103515625e-05  # 2^-14
 
 # Every symbol include/moeffn.h declares.
-EXPORTS = ("moe_ffn_forward", "moe_ffn_forward_ex", "moe_workspace_size", "moe_workspace_status",
-           "moe_last_error", "moe_shutdown")
+EXPORTS = ("moe_ffn_forward", "moe_ffn_forward_ex", "moe_workspace_size", "moe_trace_offset",
+           "moe_workspace_status", "moe_last_error", "moe_shutdown")
 
 
 class moe_cfg(ctypes.Structure):
@@ -90,6 +91,8 @@ def lib():
         L.moe_ffn_forward_ex.restype = ctypes.c_int
         L.moe_workspace_size.argtypes = [cp]
         L.moe_workspace_size.restype = ctypes.c_size_t
+        L.moe_trace_offset.argtypes = [cp]
+        L.moe_trace_offset.restype = ctypes.c_size_t
         L.moe_workspace_status.argtypes = [vp, vp]
         L.moe_workspace_status.restype = ctypes.c_int
         L.moe_last_error.argtypes = []
@@ -134,6 +137,18 @@ def moe_ffn_forward_ex(x, router_w, router_bias, expert_blocks, shared_blocks, c
 
 def moe_workspace_size(cfg):
     return lib().moe_workspace_size(ctypes.byref(cfg))
+
+
+def moe_trace_offset(cfg):
+    return lib().moe_trace_offset(ctypes.byref(cfg))
+
+
+# Names of the MOE_TRACE timeline points, in order.
+TRACE_POINTS = ("start", "prev_grid_done", "x_ready", "pre_routing_done", "logits_seen", "routed",
+                "gate_up_done", "act_seen", "down_done", "end", "producer_ready", "producer_routed",
+                "producer_done", "router_data", "router_done", "act_counted", "dn_first_data",
+                "dn_first_done")
+TRACE_STRIDE = 24  # u64 words per CTA
 
 
 def moe_workspace_status(workspace, stream=None):

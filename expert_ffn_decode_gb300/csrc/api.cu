@@ -71,14 +71,14 @@ int check_cfg(const moe_cfg* c) {
     return fail(MOE_ERR_INVALID_CFG, "weights_scale is not finite");
   if (!(c->norm_min >= 0.f) || !std::isfinite(c->norm_min))
     return fail(MOE_ERR_INVALID_CFG, "norm_min must be finite and >= 0");
-  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL))
+  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
 }
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, total;
+  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, total;
 };
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
@@ -89,9 +89,9 @@ WsLayout ws_layout(const moe_cfg* c) {
   L.ctrl = o;
   o += moe::CTRL_BYTES;
   L.logits = o;
-  o = up256(o + (size_t)c->n_experts * 4);
+  o = up256(o + (size_t)c->n_experts * 8);
   L.act = o;
-  o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
+  o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 8);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -103,6 +103,15 @@ WsLayout ws_layout(const moe_cfg* c) {
     o = up256(o + T * c->top_k * 4);
     L.w_stage = o;
     o = up256(o + T * c->top_k * 4);
+  }
+  L.trace = 0;
+  if (c->flags & MOE_TRACE) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1024;  // no device: size for the largest part
+    L.trace = o;
+    o = up256(o + (size_t)sms * 24 * 8);
   }
   L.total = o;
   return L;
@@ -151,46 +160,31 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   for (int nb : {p.H / 32, p.F / 32, p.Fs / 32})
     if ((nb + 31) / 32 > maxb) maxb = (nb + 31) / 32;
 
-  // ring slots: big enough for a router row and one aligned run of every row kind
-  uint32_t slot = 8192;
-  auto need = [&](uint32_t b) { if (b > slot) slot = b; };
-  need((uint32_t)p.H * 4u);
-  need(2u * (uint32_t)p.gu_align * p.rb_h);
-  need((uint32_t)p.dn_align * p.rb_f);
-  need((uint32_t)p.dn_align * p.rb_fs);
+  // ring slots: big enough for a router row and one aligned run of gate/up pairs
+  uint32_t slot = 16384;
+  if ((uint32_t)p.H * 4u > slot) slot = (uint32_t)p.H * 4u;
+  if (2u * (uint32_t)p.gu_align * p.rb_h > slot) slot = 2u * (uint32_t)p.gu_align * p.rb_h;
   slot = (slot + 127) / 128 * 128;
   p.slot_bytes = slot;
   p.gu_r = (int)(slot / (2u * p.rb_h)) / p.gu_align * p.gu_align;
-  p.dn_r = (int)(slot / p.rb_f) / p.dn_align * p.dn_align;
-  p.dn_r_s = (int)(slot / p.rb_fs) / p.dn_align * p.dn_align;
   p.nc = sms;
 
   // busiest CTA
-  p.max_items = 0;
   p.max_dn_rows = 0;
   for (int cta = 0; cta < p.nc; ++cta) {
-    int lo, hi;
-    int n = moe::build_items(p, cta, nullptr, nullptr, nullptr, &lo, &hi);
-    if (n > p.max_items) p.max_items = n;
-    if (hi - lo > p.max_dn_rows) p.max_dn_rows = hi - lo;
+    const moe::CtaShare s = moe::cta_share(p, cta);
+    if (s.d_len > p.max_dn_rows) p.max_dn_rows = s.d_len;
   }
-  // as many slots as fit next to the rest while keeping two CTAs per SM
-  const uint32_t budget2 = 113u * 1024u, budget1 = 226u * 1024u;
+  // one CTA per SM: as many ring slots as fit next to the rest (at most 16)
+  const uint32_t budget = 220u * 1024u;
   int nslots = 16;
   uint32_t smem = 0;
-  for (; nslots >= 3; --nslots) {
+  for (; nslots >= 2; --nslots) {
     p.nslots = nslots;
     smem = moe::decode_smem_bytes(p);
-    if (smem <= budget2 && (uint64_t)nslots * slot <= 80u * 1024u) break;
+    if (smem <= budget) break;
   }
-  if (nslots < 3) {
-    for (nslots = 4; nslots >= 3; --nslots) {
-      p.nslots = nslots;
-      smem = moe::decode_smem_bytes(p);
-      if (smem <= budget1) break;
-    }
-    if (nslots < 3) return fail(MOE_ERR_UNSUPPORTED, "layer too large for the decode kernel's shared memory");
-  }
+  if (nslots < 2) return fail(MOE_ERR_UNSUPPORTED, "layer too large for the decode kernel's shared memory");
   int occ = 0;
   e = moe::decode_occupancy(c->qtype, maxb, smem, &occ);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
@@ -318,8 +312,9 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.experts = static_cast<const uint8_t*>(experts);
   a.shared = static_cast<const uint8_t*>(shared);
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
-  a.logits = reinterpret_cast<float*>(wsb + W.logits);
-  a.act = reinterpret_cast<float*>(wsb + W.act);
+  a.logits = reinterpret_cast<uint64_t*>(wsb + W.logits);
+  a.act = reinterpret_cast<uint64_t*>(wsb + W.act);
+  a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
@@ -355,11 +350,11 @@ int read_status(void* ws, cudaStream_t st) {
   e = cudaMemcpy(ctrl, ws, sizeof ctrl, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (ctrl[moe::CTRL_STATUS] != 0) {
-    uint32_t st_bits = ctrl[moe::CTRL_STATUS], where = ctrl[moe::CTRL_WHERE];
+    // the counters of an interrupted call are not trustworthy: restart the control block
+    const uint32_t bits = ctrl[moe::CTRL_STATUS];
     e = cudaMemset(ws, 0, moe::CTRL_BYTES);
     if (e != cudaSuccess) return cuda_fail(e, "control block reset");
-    return fail(MOE_ERR_TIMEOUT, "device wait timed out (status 0x%x, at %u); control words reset", st_bits,
-                where);
+    return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out (status bits 0x%x); control block reset", bits);
   }
   return MOE_OK;
 }
@@ -396,6 +391,11 @@ int moe_ffn_forward_ex(const float* x, const float* router_w, const float* route
 size_t moe_workspace_size(const moe_cfg* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   return ws_layout(cfg).total;
+}
+
+size_t moe_trace_offset(const moe_cfg* cfg) {
+  if (check_cfg(cfg) != MOE_OK || !(cfg->flags & MOE_TRACE)) return 0;
+  return ws_layout(cfg).trace;
 }
 
 int moe_workspace_status(void* workspace, void* stream) {

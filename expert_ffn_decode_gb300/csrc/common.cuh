@@ -1,6 +1,6 @@
 // Small device helpers for sm_103a: mbarriers, 1-D bulk async copies,
-// programmatic-dependent-launch control, acquire/release flags, timers and the
-// integer dot products used by the 4-bit kernels. Every wait here is bounded.
+// programmatic-dependent-launch control, acquire/release counters, timers and
+// the integer dot products used by the 4-bit kernels. Every wait here is bounded.
 #pragma once
 
 #include <cstdint>
@@ -9,26 +9,28 @@
 namespace moe {
 
 // ---- control block (first 256 bytes of every workspace) ---------------------
-// Word layout. Every call leaves words 0..3 at zero when it returns normally;
-// the status word is sticky until the host clears it.
+// Word layout. A workspace starts zeroed. A call with generation g counts
+// arrivals in the counters of parity g & 1; its last CTA out zeroes the exit
+// counter and the counters of parity (g + 1) & 1 for the next call and advances
+// the generation word. The status word is sticky until the host clears it.
 enum CtrlWord : int {
-  CTRL_BAR_A = 0,    // arrivals at the router barrier
-  CTRL_BAR_B = 1,    // arrivals at the activation barrier
-  CTRL_EXIT = 2,     // CTAs that finished (the last one resets the counters)
+  CTRL_GEN = 0,      // calls completed on this workspace (call g runs with generation g + 1)
+  CTRL_EXIT = 1,     // CTAs of the running call that finished (reset by the last one)
+  CTRL_LOGITS = 2,   // [2], [3]: CTAs whose router rows are written, by generation parity
+  CTRL_ACT = 4,      // [4], [5]: CTAs whose gate/up rows are written, by generation parity
   CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
-  CTRL_WHERE = 9,    // first place that timed out (for diagnostics)
 };
 constexpr int CTRL_BYTES = 256;
 
 enum DevErr : uint32_t {
-  DEV_ERR_BARRIER_TIMEOUT = 1u,
-  DEV_ERR_MBAR_TIMEOUT = 2u,
+  DEV_ERR_POLL_TIMEOUT = 1u,   // other CTAs' results never arrived
+  DEV_ERR_MBAR_TIMEOUT = 2u,   // a copy or a slot release never arrived
 };
 
-// Spin limits, measured on %globaltimer: a grid barrier or an mbarrier wait
-// gives up after this many nanoseconds.
-constexpr unsigned long long BARRIER_TIMEOUT_NS = 200ull * 1000 * 1000;  // 0.2 s
-constexpr unsigned long long MBAR_TIMEOUT_NS = 500ull * 1000 * 1000;     // 0.5 s
+// Spin limits, measured on %globaltimer: a poll of an arrival counter or an
+// mbarrier wait gives up after this many nanoseconds.
+constexpr unsigned long long POLL_TIMEOUT_NS = 200ull * 1000 * 1000;  // 0.2 s
+constexpr unsigned long long MBAR_TIMEOUT_NS = 500ull * 1000 * 1000;  // 0.5 s
 
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
@@ -83,6 +85,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -97,23 +103,65 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ---- gpu-scope flags -------------------------------------------------------------
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// ---- gpu-scope counters and published values -----------------------------------
+// A value crosses CTAs as one 64-bit word {generation, f32 bits}: a single aligned
+// store is seen whole, so a reader that sees its own call's generation also sees
+// the value, with no fence between writer and reader. Arrival counters are only
+// hints of when to look; the generation check decides.
+__device__ __forceinline__ void red_relaxed_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t tagged(uint32_t gen, float v) {
+  return ((uint64_t)gen << 32) | (uint64_t)__float_as_uint(v);
+}
+__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float value_of(uint64_t w) { return __uint_as_float((uint32_t)w); }
+// The value at p once it carries generation gen (bounded; `ok` cleared on timeout).
+__device__ __forceinline__ float await_tagged(const uint64_t* p, uint64_t w, uint32_t gen, bool& ok) {
+  if (tag_of(w) != gen && ok) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1; tag_of(w) != gen; ++it) {
+      if ((it & 15u) == 0 && globaltimer() - t0 > POLL_TIMEOUT_NS) {
+        ok = false;
+        break;
+      }
+      w = ld_relaxed_u64(p);
+    }
+  }
+  return value_of(w);
 }
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// One thread waits until *ctr >= target, bounded in time.
+__device__ __forceinline__ bool await_count(const uint32_t* ctr, uint32_t target) {
+  if (ld_relaxed(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_relaxed(ctr) >= target) return true;
+    if ((it & 15u) == 0 && globaltimer() - t0 > POLL_TIMEOUT_NS) return false;
+  }
+}
+
 // Named barriers (bar.sync / bar.arrive are warp-aligned: the warp reconverges first).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
-  __syncwarp();
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---- integer dot products ---------------------------------------------------------
@@ -129,7 +177,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// Round-to-nearest-even of |y| < 2^22 to an integer by the add-and-subtract of
+// Round-to-nearest-even of |y| <= 2^22 to an integer by the add-and-subtract of
 // 1.5 * 2^23 (the float then holds the integer in its low mantissa bits).
 __device__ __forceinline__ int round_small(float y) {
   return __float_as_int(y + 12582912.0f) - 0x4B400000;

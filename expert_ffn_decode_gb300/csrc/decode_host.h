@@ -7,9 +7,7 @@
 
 namespace moe {
 
-struct DecodeArgs;
-
-constexpr int DECODE_THREADS = 256;  // 7 consumer warps + 1 producer warp
+constexpr int DECODE_THREADS = 384;  // 11 consumer warps + 1 producer warp
 
 // Launches the decode kernel for one token (grid = a.p.nc CTAs).
 cudaError_t decode_launch(const DecodeArgs& a, int qtype, int maxb, uint32_t smem, cudaStream_t st,

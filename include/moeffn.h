@@ -63,6 +63,7 @@ extern "C" {
 #define MOE_RESIDUAL 2u   /* out = x + contribution                                 */
 #define MOE_HOST_IO 4u    /* x, out, topk_ids, topk_w are host pointers, staged       */
 #define MOE_NO_PDL 8u     /* launch without programmatic dependent launch             */
+#define MOE_TRACE 16u     /* record a per-CTA timeline in the workspace (see below)   */
 
 enum {
   MOE_OK = 0,
@@ -111,9 +112,11 @@ int moe_ffn_forward(const float* x, const float* router_w, const float* router_b
 
 /* The step enqueued on `stream` (a cudaStream_t, NULL = legacy default stream)
  * with a caller-owned device workspace of at least moe_workspace_size(cfg) bytes,
- * 256-byte aligned. The first 256 bytes of a workspace must be zero before its
- * first use; every call leaves them as it found them when it completes normally.
- * Calls sharing one workspace must be ordered (same stream, or synchronised).
+ * 256-byte aligned. A workspace must be zero-filled before its first use and then
+ * only touched by this library: its first 256 bytes are control words (a call
+ * counter, arrival counters and a status word). Calls sharing one workspace must
+ * be ordered (same stream, or synchronised); calls with different configurations
+ * may share one.
  * Asynchronous: device-side errors surface through moe_workspace_status.
  * topk_ids / topk_w may be NULL. */
 int moe_ffn_forward_ex(const float* x, const float* router_w, const float* router_bias,
@@ -124,9 +127,20 @@ int moe_ffn_forward_ex(const float* x, const float* router_w, const float* route
 /* Workspace bytes a call with this configuration needs (0 for an invalid cfg). */
 size_t moe_workspace_size(const moe_cfg* cfg);
 
+/* Byte offset of the MOE_TRACE timeline in the workspace (0 when cfg is invalid or
+ * has no MOE_TRACE). The timeline holds, for each CTA (one per SM), 24 u64
+ * %globaltimer readings in nanoseconds written by the last token's launch:
+ * 0 start, 1 previous grid done, 2 activations quantised, 3 routing-independent
+ * rows done, 4 all logits written, 5 picks made, 6 gate/up done, 7 activations of
+ * every slot quantised, 8 down rows done, 9 end, 10 producer ready, 11 producer
+ * released for the picked experts, 12 producer done, 13 first router row in
+ * shared memory, 14 router rows done, 15 every CTA's activations written, 16 first
+ * down rows in shared memory, 17 first down rows done (unused points stay 0). */
+size_t moe_trace_offset(const moe_cfg* cfg);
+
 /* Waits for `stream`, then reads and clears the workspace's status word:
  * MOE_OK, or MOE_ERR_TIMEOUT when a device-side wait ran out of time (the
- * workspace's control words are zeroed again so it can be reused). */
+ * workspace's control block is zeroed again so it can be reused). */
 int moe_workspace_status(void* workspace, void* stream);
 
 /* Text of the last error on the calling thread ("" if none). */
