@@ -41,7 +41,7 @@ NORM_MIN = 6.103515625e-05  # 2^-14
 
 # Every symbol include/moeffn.h declares.
 EXPORTS = ("moe_ffn_forward", "moe_ffn_forward_ex", "moe_workspace_size", "moe_trace_offset",
-           "moe_workspace_status", "moe_last_error", "moe_shutdown")
+           "moe_workspace_status", "moe_ffn_forward_noalloc", "moe_last_error", "moe_shutdown")
 
 
 class moe_cfg(ctypes.Structure):
@@ -95,6 +95,8 @@ def lib():
         L.moe_trace_offset.restype = ctypes.c_size_t
         L.moe_workspace_status.argtypes = [vp, vp]
         L.moe_workspace_status.restype = ctypes.c_int
+        L.moe_ffn_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, cp, vp, vp]
+        L.moe_ffn_forward_noalloc.restype = ctypes.c_int
         L.moe_last_error.argtypes = []
         L.moe_last_error.restype = ctypes.c_char_p
         L.moe_shutdown.argtypes = []
@@ -153,6 +155,12 @@ TRACE_STRIDE = 24  # u64 words per CTA
 
 def moe_workspace_status(workspace, stream=None):
     return lib().moe_workspace_status(_ptr(workspace), _stream(stream))
+
+
+def moe_ffn_forward_noalloc(x, router_w, router_bias, expert_blocks, shared_blocks, cfg, out, stream=None):
+    """The step without any allocation (fixed 256 KiB device scratch; blocking)."""
+    return lib().moe_ffn_forward_noalloc(_ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(expert_blocks),
+                                         _ptr(shared_blocks), ctypes.byref(cfg), _ptr(out), _stream(stream))
 
 
 def moe_last_error():

@@ -424,3 +424,113 @@ int moe_shutdown(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The step without any allocation, for callers that cannot allocate memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits and the
+// activations of one token. It is device memory that exists from the moment the
+// library's code is loaded on a device until the process exits; every call on
+// that device shares it.
+constexpr size_t NOALLOC_SCRATCH_BYTES = 256 * 1024;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch per device, looked up on the first call there.
+// In host code the array's name only stands in for the symbol; the address the
+// kernel needs comes from cudaGetSymbolAddress with that device current.
+constexpr int NOALLOC_MAX_DEVICES = 64;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(int dev, void** ptr) {
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return fail(MOE_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch");
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, const float* router_bias,
+                                       const void* expert_blocks, const void* shared_blocks,
+                                       const moe_cfg* c, float* out, void* stream) {
+  g_err.clear();
+  int rc = check_cfg(c);
+  if (rc != MOE_OK) return rc;
+  if (c->flags & (MOE_HOST_IO | MOE_TRACE))
+    return fail(MOE_ERR_UNSUPPORTED, "moe_ffn_forward_noalloc takes device buffers only, without MOE_TRACE");
+  const int T = c->n_tokens;
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !expert_blocks || !out)
+    return fail(MOE_ERR_NULL_PTR, "x, router_w, expert_blocks and out must not be NULL");
+  if (c->shared_ff > 0 && !shared_blocks) return fail(MOE_ERR_NULL_PTR, "shared_ff > 0 needs shared_blocks");
+  if (!aligned(router_w, 16) || !aligned(expert_blocks, 16) || (shared_blocks && !aligned(shared_blocks, 16)) ||
+      !aligned(x, 16) || !aligned(out, 16) || (router_bias && !aligned(router_bias, 4)))
+    return fail(MOE_ERR_ALIGNMENT, "x, out, router_w and the blocks must be 16-byte aligned, the bias 4-byte");
+  const size_t xbytes = (size_t)T * c->hidden * 4;
+  {
+    const char* xa = reinterpret_cast<const char*>(x);
+    const char* oa = reinterpret_cast<const char*>(out);
+    if (xa < oa + xbytes && oa < xa + xbytes) return fail(MOE_ERR_INVALID_CFG, "x and out overlap");
+  }
+  const WsLayout W = ws_layout(c);
+  if (W.total > NOALLOC_SCRATCH_BYTES)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "this layer needs %zu bytes of scratch; the fixed scratch of moe_ffn_forward_noalloc holds %zu",
+                W.total, NOALLOC_SCRATCH_BYTES);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  void* scratch = nullptr;
+  rc = noalloc_scratch(dev, &scratch);
+  if (rc != MOE_OK) return rc;
+  PlanEntry pe;  // planned on every call: the plan cache of the other entry points would grow
+  rc = make_plan(c, dev, &pe);
+  if (rc != MOE_OK) return rc;
+
+  uint8_t* wsb = static_cast<uint8_t*>(scratch);
+  moe::DecodeArgs a{};
+  a.router_w = router_w;
+  a.bias = router_bias;
+  a.experts = static_cast<const uint8_t*>(expert_blocks);
+  a.shared = static_cast<const uint8_t*>(shared_blocks);
+  a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
+  a.logits = reinterpret_cast<uint64_t*>(wsb + W.logits);
+  a.act = reinterpret_cast<uint64_t*>(wsb + W.act);
+  a.trace = nullptr;
+  a.scale = c->weights_scale;
+  a.norm_min = c->norm_min;
+  a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
+  a.p = pe.plan;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool pdl = (c->flags & MOE_NO_PDL) == 0;
+  for (int t = 0; t < T; ++t) {
+    a.x = x + (size_t)t * c->hidden;
+    a.out = out + (size_t)t * c->hidden;
+    a.topk_ids = nullptr;
+    a.topk_w = nullptr;
+    e = moe::decode_launch(a, c->qtype, pe.maxb, pe.smem, st, pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  }
+  // wait, then read the status word; after a device-side timeout the control block
+  // is zeroed so the next call starts clean
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t status = 0;
+  e = cudaMemcpy(&status, wsb + moe::CTRL_STATUS * 4, sizeof status, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (status != 0) {
+    e = cudaMemset(wsb + W.ctrl, 0, moe::CTRL_BYTES);
+    if (e != cudaSuccess) return cuda_fail(e, "control block reset");
+    return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out (status bits 0x%x); control block reset", status);
+  }
+  return MOE_OK;
+}

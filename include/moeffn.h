@@ -143,6 +143,26 @@ size_t moe_trace_offset(const moe_cfg* cfg);
  * workspace's control block is zeroed again so it can be reused). */
 int moe_workspace_status(void* workspace, void* stream);
 
+/* The step for callers that cannot allocate memory: no cudaMalloc, cudaFree or
+ * other allocating call is made, on the device or on the host. Such callers
+ * include code that runs where an allocator may not be entered (inside another
+ * allocator's hooks, in a real-time or signal context, under a memory budget
+ * that has already been handed out) or that has no allocator of its own to lend
+ * a workspace. The pages have no counterpart: their engines own every buffer.
+ * The scratch lives in a fixed device array of 256 KiB compiled into the
+ * library; every device that loads the library holds it until the process
+ * exits, and every call on a device shares it, so calls whose work overlaps on
+ * the GPU (other streams, other threads) race and must not be made. The first
+ * call on a device looks the array's address up once (make it before any stream
+ * capture). Layers whose scratch (control block, logits, activations) exceeds
+ * 256 KiB are rejected with MOE_ERR_UNSUPPORTED. Device buffers only: MOE_HOST_IO
+ * and MOE_TRACE are rejected. Blocking: returns after the step has finished on
+ * `stream` (a cudaStream_t, NULL = legacy default stream), with device-side
+ * errors reported directly. Arguments otherwise as moe_ffn_forward. */
+int moe_ffn_forward_noalloc(const float* x, const float* router_w, const float* router_bias,
+                            const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg,
+                            float* out, void* stream);
+
 /* Text of the last error on the calling thread ("" if none). */
 const char* moe_last_error(void);
 

@@ -1,0 +1,61 @@
+"""moe_ffn_forward_noalloc: the step for callers that cannot allocate memory.
+
+Some callers may not enter any allocator (for example code running inside another
+allocator's hooks, in a real-time path, or under a memory budget already handed
+out), so they cannot provide a workspace. This entry point runs the same decode
+kernel on a fixed scratch array compiled into the library. These tests check it
+against the workspace entry point through the C ABI, on two calls in a row (the
+second call reuses the scratch the first left behind).
+
+This file is collected last on purpose: a run that stops at the first failure has
+then already run every other test.
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+import expert_ffn_decode_gb300 as ffn
+from expert_ffn_decode_gb300 import synth
+from tests.helpers import OUT_REL_L2, GpuLayer, margin_tokens, rel_l2
+
+
+def _built():
+    if not os.path.exists(ffn.LIB_PATH):
+        from expert_ffn_decode_gb300 import build
+        build.build()
+
+
+def test_noalloc_rejects_layers_beyond_the_fixed_scratch():
+    _built()
+    # 32 picks of F = 3072 need 786 KiB of activations: more than the 256 KiB scratch
+    cfg = ffn.make_cfg(hidden=2048, n_experts=64, top_k=32, expert_ff=3072, n_tokens=1)
+    rc = ffn.moe_ffn_forward_noalloc(1 << 24, 1 << 28, None, 1 << 30, None, cfg, 1 << 26)
+    assert rc == ffn.MOE_ERR_UNSUPPORTED
+    assert "scratch" in ffn.moe_last_error()
+    # host staging and tracing need a workspace
+    cfg = ffn.make_cfg(hidden=256, n_experts=16, top_k=2, expert_ff=128, n_tokens=1, flags=ffn.MOE_HOST_IO)
+    assert ffn.moe_ffn_forward_noalloc(1 << 24, 1 << 28, None, 1 << 30, None, cfg, 1 << 26) == ffn.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["flint_decode_t1", "tiny_q4_0_t4"])
+def test_noalloc_matches_workspace_entry_point_twice(name):
+    import torch
+    _built()
+    w = synth.WORKLOADS[name]
+    layer = synth.make_layer(w)
+    g = GpuLayer(layer, w)
+    T = max(2, w["n_tokens"])
+    for call in range(2):
+        x, _ = margin_tokens(layer, w, T, seed=w["seed"], stream=20 + call)
+        want, _, _ = g.run(x)  # moe_ffn_forward_ex with a workspace
+        cfg = ffn.make_cfg(**{**w, "n_tokens": T})
+        xd = torch.from_numpy(x).cuda()
+        out = torch.full_like(xd, float("nan"))
+        ffn.check(ffn.moe_ffn_forward_noalloc(xd, g.router_w, g.bias, g.experts, g.shared, cfg, out,
+                                              torch.cuda.current_stream()))
+        got = out.cpu().numpy()
+        for t in range(T):
+            assert rel_l2(got[t], want[t]) <= OUT_REL_L2, (name, call, t)
