@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "decode_host.h"
 #include "plan.h"
+#include "prefill_host.h"
 
 namespace {
 
@@ -78,8 +79,14 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, total;
+  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
 };
+
+// Tokens of one prefill pass for a call of T tokens (0: the call decodes token by token).
+int prefill_pass_tokens(int T) {
+  if (T < moe::PREFILL_MIN_T) return 0;
+  return T < moe::PREFILL_CHUNK_T ? T : moe::PREFILL_CHUNK_T;
+}
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -112,6 +119,11 @@ WsLayout ws_layout(const moe_cfg* c) {
       sms = 1024;  // no device: size for the largest part
     L.trace = o;
     o = up256(o + (size_t)sms * 24 * 8);
+  }
+  L.prefill = 0;
+  if (const int tp = prefill_pass_tokens(c->n_tokens)) {
+    L.prefill = o;
+    o = up256(o + moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff, c->shared_ff).total);
   }
   L.total = o;
   return L;
@@ -306,6 +318,59 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     }
   }
 
+  if (const int tp = prefill_pass_tokens(T)) {
+    // batched path: router, top-k, expert sort and grouped tensor-core GEMMs
+    const moe::PrefillWs P = moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff,
+                                                    c->shared_ff);
+    uint8_t* pb = wsb + W.prefill;
+    moe::PrefillArgs pa{};
+    pa.router_w = router_w;
+    pa.bias = bias;
+    pa.experts = static_cast<const uint8_t*>(experts);
+    pa.shared = static_cast<const uint8_t*>(shared);
+    pa.logits = reinterpret_cast<float*>(pb + P.logits);
+    pa.ids = reinterpret_cast<int32_t*>(pb + P.ids);
+    pa.wts = reinterpret_cast<float*>(pb + P.wts);
+    pa.offsets = reinterpret_cast<uint32_t*>(pb + P.offsets);
+    pa.table = reinterpret_cast<uint16_t*>(pb + P.table);
+    pa.perm = reinterpret_cast<uint32_t*>(pb + P.perm);
+    pa.wsorted = reinterpret_cast<float*>(pb + P.wsorted);
+    pa.pos_of = reinterpret_cast<uint32_t*>(pb + P.pos_of);
+    pa.chunks = reinterpret_cast<moe::GemmChunk*>(pb + P.chunks);
+    pa.nchunks = reinterpret_cast<uint32_t*>(pb + P.nchunks);
+    pa.x16 = reinterpret_cast<__half*>(pb + P.x16);
+    pa.act16 = reinterpret_cast<__half*>(pb + P.act16);
+    pa.act16s = reinterpret_cast<__half*>(pb + P.act16s);
+    pa.ybuf = reinterpret_cast<float*>(pb + P.ybuf);
+    pa.sbuf = reinterpret_cast<float*>(pb + P.sbuf);
+    pa.status = reinterpret_cast<uint32_t*>(wsb + W.ctrl) + moe::CTRL_STATUS;
+    pa.H = c->hidden;
+    pa.E = c->n_experts;
+    pa.K = c->top_k;
+    pa.F = c->expert_ff;
+    pa.Fs = c->shared_ff;
+    pa.G = c->n_groups;
+    pa.Gu = c->n_groups > 1 ? c->groups_used : 1;
+    pa.qtype = c->qtype;
+    pa.scale = c->weights_scale;
+    pa.norm_min = c->norm_min;
+    pa.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
+    pa.rb_h = pe.plan.rb_h;
+    pa.rb_f = pe.plan.rb_f;
+    pa.rb_fs = pe.plan.rb_fs;
+    pa.rec_bytes = pe.plan.rec_bytes;
+    pa.nc = pe.plan.nc;
+    for (int t0 = 0; t0 < T; t0 += tp) {
+      pa.T = T - t0 < tp ? T - t0 : tp;
+      pa.x = dx + (size_t)t0 * c->hidden;
+      pa.out = dout + (size_t)t0 * c->hidden;
+      pa.topk_ids = dids ? dids + (size_t)t0 * c->top_k : nullptr;
+      pa.topk_w = dw ? dw + (size_t)t0 * c->top_k : nullptr;
+      e = moe::prefill_launch(pa, st);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
+    }
+  }
+
   moe::DecodeArgs a{};
   a.router_w = router_w;
   a.bias = bias;
@@ -320,7 +385,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
-  for (int t = 0; t < T; ++t) {
+  for (int t = 0; t < T && !prefill_pass_tokens(T); ++t) {
     a.x = dx + (size_t)t * c->hidden;
     a.out = dout + (size_t)t * c->hidden;
     a.topk_ids = dids ? dids + (size_t)t * c->top_k : nullptr;

@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "plan.h"
+#include "select.cuh"
 
 namespace moe {
 
@@ -274,54 +275,6 @@ constexpr int ROWS_PER_STEP = 4;  // row steps a warp keeps in flight together
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
-// Top-k by one warp: k rounds, each taking the largest key, the lowest expert
-// index among equal keys. Lane l holds the keys of experts l + 32 i (i < EPL) in
-// registers; key 0 marks an expert that cannot be picked (every real key is at
-// least 0x007FFFFF, the key of -inf). Writes the picks in order to ids[0, k).
-template <int EPL>
-__device__ __forceinline__ void lane_best(const uint32_t (&kv)[EPL], int lane, uint32_t& bk, int& bi) {
-  // a max tree over the lane's keys that keeps the lower index on ties
-  uint32_t tk[EPL];
-  int ti[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    tk[i] = kv[i];
-    ti[i] = i;
-  }
-#pragma unroll
-  for (int w = 1; w < EPL; w *= 2)
-#pragma unroll
-    for (int i = 0; i + w < EPL; i += 2 * w) {
-      const bool right = tk[i + w] > tk[i];
-      tk[i] = right ? tk[i + w] : tk[i];
-      ti[i] = right ? ti[i + w] : ti[i];
-    }
-  bk = tk[0];
-  bi = lane + 32 * ti[0];
-}
-
-template <int EPL>
-__device__ __forceinline__ void topk_rounds(const uint32_t* keys, int E, int k, int* ids, int lane) {
-  uint32_t kv[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    kv[i] = e < E ? keys[e] : 0u;
-  }
-  uint32_t bk;
-  int bi;
-  lane_best(kv, lane, bk, bi);
-  for (int j = 0; j < k; ++j) {
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-    const unsigned cand = (bk == mk && mk != 0u) ? (unsigned)bi : 0xffffffffu;
-    int win = (int)__reduce_min_sync(0xffffffffu, cand);
-    if (win < 0 || win >= E) win = j % E;  // unreachable for a valid configuration
-    if (lane == 0) ids[j] = win;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) kv[i] = (lane + 32 * i == win) ? 0u : kv[i];
-    if ((win & 31) == lane) lane_best(kv, lane, bk, bi);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // The kernel

@@ -1,0 +1,589 @@
+// Batched MoE-FFN step (prefill: T tokens at once) for sm_103a.
+//
+// Passes, each a kernel on the caller's stream:
+//   router      logits[T][E] = X Wr^T                       (f32, tiled SIMT)
+//   top-k       per token: sigmoid, bias, (group) top-k, weights; expert histogram
+//   sort        stable counting sort of the T*K (token, pick) pairs by expert, and
+//               the GEMM chunk lists (at most PREFILL_NMAX rows a chunk)
+//   x16         X -> two f16 rows per token, hi = f16(x) and lo = f16(x - hi), with
+//               the K order permuted inside every 32-value block
+//   gate/up     grouped GEMM on the tensor cores: per (chunk, 64 pairs of rows)
+//               D[128 x 2N] = W_gu (dequantised to f16 in shared memory) * [X_hi X_lo]^T,
+//               accumulated in TMEM; the epilogue adds the hi and lo columns and
+//               applies SwiGLU -> act16
+//   down        grouped GEMM: per (chunk, 128 output rows) D = W_down * act_chunk^T,
+//               epilogue scales by the pair's routing weight -> ybuf (shared: sbuf)
+//   combine     out[t] = sum_j ybuf[pos(t, j)] + sbuf[t] (fixed order: deterministic)
+//
+// Weights are the MMA's A operand (M = 128 rows), tokens the B operand (N = the
+// chunk's rows rounded up to 16), so a work unit streams its expert's rows once
+// whatever the number of tokens that picked it. The token rows enter the gate/up
+// GEMM as hi + lo f16 pairs: the rounding of x to f16 is the same for every row of
+// W, so its error would add up coherently over the down projection; the pair
+// carries x to 22 bits. The activations (one rounding per value, independent
+// across rows) and the weights go in as single f16 values. The 4-bit blocks are dequantised
+// exactly (nibble -> f16 integer, then d*q + m rounded once) into f16; the
+// products are summed in f32 in TMEM. Inside each 32-value block the K order is
+// permuted so that one 32-bit nibble word fills one 16-byte row of a core matrix:
+// slot 8w + (0..7) holds values 4w, 4w+2, 4w+1, 4w+3, 16+4w, 16+4w+2, 16+4w+1,
+// 16+4w+3. Every operand uses the same order, so the dot products are unchanged.
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "plan.h"
+#include "prefill_host.h"
+#include "select.cuh"
+#include "tc.cuh"
+
+namespace moe {
+
+// Slot of value e (0..31) of a block in the permuted K order.
+__host__ __device__ __forceinline__ int kslot(int e) {
+  const int hi = e >> 4, r = e & 15, w = r >> 2, j = r & 3;
+  const int jj = (j == 1) ? 2 : (j == 2 ? 1 : j);  // 0, 2, 1, 3
+  return 8 * w + 4 * hi + jj;
+}
+__host__ __device__ __forceinline__ int kpos(int k) { return (k & ~31) | kslot(k & 31); }
+
+// ---------------------------------------------------------------------------
+// router: logits[t][e] = sum_h x[t][h] * Wr[e][h]
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prefill_router(const PrefillArgs a) {
+  __shared__ float xs[32][33], ws[32][33];
+  const int t0 = blockIdx.y * 32, e0 = blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 < a.H; k0 += 32) {
+    for (int i = ty; i < 32; i += 8) {
+      const int t = t0 + i, e = e0 + i;
+      xs[i][tx] = t < a.T ? __ldg(a.x + (size_t)t * a.H + k0 + tx) : 0.f;
+      ws[i][tx] = e < a.E ? __ldg(a.router_w + (size_t)e * a.H + k0 + tx) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float wv = ws[tx][k];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] = fmaf(xs[ty + 8 * j][k], wv, acc[j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = t0 + ty + 8 * j, e = e0 + tx;
+    if (t < a.T && e < a.E) a.logits[(size_t)t * a.E + e] = acc[j];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// top-k: one warp per token
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prefill_topk(const PrefillArgs a) {
+  extern __shared__ __align__(16) uint8_t tsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= a.T) return;  // whole warp
+  uint8_t* base = tsm + (size_t)warp * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(base);
+  float* probs = reinterpret_cast<float*>(base + (size_t)a.E * 4);
+  float* gscore = reinterpret_cast<float*>(base + (size_t)a.E * 8);
+  int* picks = reinterpret_cast<int*>(base + (size_t)a.E * 8 + 64 * 4);
+  for (int e = lane; e < a.E; e += 32) {
+    const float l = a.logits[(size_t)t * a.E + e];
+    const float pr = 1.f / (1.f + expf(-l));
+    probs[e] = pr;
+    keys[e] = order_key(pr + (a.bias ? __ldg(a.bias + e) : 0.f));
+  }
+  __syncwarp();
+  if (a.G > 1) {
+    // group score: the two largest s of the group, summed (multiset top-2)
+    const int per = a.E / a.G;
+    for (int g = lane; g < a.G; g += 32) {
+      float x1 = -INFINITY, x2 = -INFINITY;
+      for (int e = g * per; e < (g + 1) * per; ++e) {
+        const uint32_t k = keys[e];
+        const float v = __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+        if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
+      }
+      gscore[g] = x1 + x2;
+    }
+    __syncwarp();
+    // kept groups: groups_used rounds of the largest score, lowest group on ties
+    uint32_t keep_lo = 0, keep_hi = 0;
+    for (int j = 0; j < a.Gu; ++j) {
+      int best = -1;
+      float bv = 0.f;
+      for (int g = 0; g < a.G; ++g) {
+        const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
+        if (!kept && (best < 0 || gscore[g] > bv)) { best = g; bv = gscore[g]; }
+      }
+      if (best < 32) keep_lo |= 1u << best; else keep_hi |= 1u << (best - 32);
+    }
+    for (int e = lane; e < a.E; e += 32) {
+      const int g = e / per;
+      const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
+      if (!kept) keys[e] = 0u;
+    }
+    __syncwarp();
+  }
+  if (a.E <= 256) topk_rounds<8>(keys, a.E, a.K, picks, lane);
+  else if (a.E <= 512) topk_rounds<16>(keys, a.E, a.K, picks, lane);
+  else topk_rounds<32>(keys, a.E, a.K, picks, lane);
+  __syncwarp();
+  const float pj = lane < a.K ? probs[picks[lane]] : 0.f;
+  const float wsum = fmaxf(warp_sum(pj), a.norm_min);
+  if (lane < a.K) {
+    const int id = picks[lane];
+    const float wj = pj / wsum * a.scale;
+    a.ids[(size_t)t * a.K + lane] = id;
+    a.wts[(size_t)t * a.K + lane] = wj;
+    if (a.topk_ids) a.topk_ids[(size_t)t * a.K + lane] = id;
+    if (a.topk_w) a.topk_w[(size_t)t * a.K + lane] = wj;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// sort: one CTA of 1024 threads (E <= 1024: thread e owns expert e)
+// ---------------------------------------------------------------------------
+// Exclusive prefix sum of v over the CTA; `total` gets the sum of all v.
+__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const uint32_t ex = inc - v + (warp ? wsum[warp - 1] : 0u);
+  total = wsum[31];
+  __syncthreads();  // wsum is reused by the next scan
+  return ex;
+}
+
+__global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
+  __shared__ uint32_t offs[1024];
+  __shared__ uint32_t wsum[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = a.T * a.K, nch = (P + 31) / 32, E = a.E;
+  const uint32_t lt = (1u << lane) - 1u;
+  // (a) per 32-pair chunk: how many of its pairs picked each expert
+  for (int i = tid; i < nch * E; i += 1024) a.table[i] = 0;
+  __syncthreads();
+  for (int c = warp; c < nch; c += 32) {
+    const int p = c * 32 + lane;
+    const int e = p < P ? a.ids[p] : E;
+    const uint32_t m = __match_any_sync(0xffffffffu, e);
+    if (e < E && (m & lt) == 0) a.table[(size_t)c * E + e] = (uint16_t)__popc(m);
+  }
+  __syncthreads();
+  // (b) per expert: counts of the earlier chunks (in place), total
+  uint32_t cnt = 0;
+  if (tid < E)
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t v = a.table[(size_t)c * E + tid];
+      a.table[(size_t)c * E + tid] = (uint16_t)cnt;
+      cnt += v;
+    }
+  // (c) first sorted position of each expert; first chunk of each expert
+  uint32_t total = 0, nrouted = 0;
+  const uint32_t off = cta_excl_scan(cnt, wsum, total);
+  const uint32_t nck = (cnt + PREFILL_NMAX - 1) / PREFILL_NMAX;
+  const uint32_t cbase = cta_excl_scan(nck, wsum, nrouted);
+  if (tid < E) {
+    offs[tid] = off;
+    a.offsets[tid] = off;
+    for (uint32_t r = 0; r < nck; ++r) {
+      const int row0 = (int)(off + r * PREFILL_NMAX), n = (int)min(cnt - r * PREFILL_NMAX, (uint32_t)PREFILL_NMAX);
+      a.chunks[cbase + r] = GemmChunk{tid, row0, n, 0};
+    }
+  }
+  if (tid == 0) a.offsets[E] = total;
+  // shared-expert chunks follow the routed ones
+  const int nsh = a.Fs ? (a.T + PREFILL_NMAX - 1) / PREFILL_NMAX : 0;
+  if (tid < nsh) a.chunks[nrouted + tid] = GemmChunk{E, tid * PREFILL_NMAX, min(a.T - tid * PREFILL_NMAX, PREFILL_NMAX), 0};
+  if (tid == 0) {
+    a.nchunks[0] = nrouted;
+    a.nchunks[1] = nrouted + (uint32_t)nsh;
+  }
+  __syncthreads();
+  // (d) stable positions: expert's first position + earlier chunks + earlier lanes
+  for (int c = warp; c < nch; c += 32) {
+    const int p = c * 32 + lane;
+    const int e = p < P ? a.ids[p] : E;
+    const uint32_t m = __match_any_sync(0xffffffffu, e);
+    if (e < E) {
+      const uint32_t pos = offs[e] + a.table[(size_t)c * E + e] + __popc(m & lt);
+      a.perm[pos] = (uint32_t)p;
+      a.pos_of[p] = pos;
+      a.wsorted[pos] = a.wts[p];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// x16: X -> hi and lo f16 rows in the permuted K order (row 2t: hi, row 2t + 1: lo)
+// ---------------------------------------------------------------------------
+__global__ void prefill_x16(const PrefillArgs a) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t n = (size_t)a.T * a.H;
+  if (i >= n) return;
+  const int k = (int)(i % a.H);
+  const size_t t = i / a.H;
+  const float v = __ldg(a.x + i);
+  const __half hi = __float2half_rn(v);
+  a.x16[(2 * t) * a.H + kpos(k)] = hi;
+  a.x16[(2 * t + 1) * a.H + kpos(k)] = __float2half_rn(v - __half2float(hi));
+}
+
+// ---------------------------------------------------------------------------
+// grouped Q4 GEMM on the tensor cores (MODE 0: gate/up + SwiGLU, 1: down + weight)
+// ---------------------------------------------------------------------------
+constexpr int KC = 128;                      // K values per pipeline chunk (4 blocks)
+constexpr int A_STAGE = 128 * KC * 2;        // 32 KB f16
+// B stage: up to 2 * PREFILL_NMAX rows (gate/up: hi and lo rows of each token)
+constexpr int B_STAGE_GU = 2 * PREFILL_NMAX * KC * 2;  // 64 KB f16
+constexpr int B_STAGE_DN = PREFILL_NMAX * KC * 2;      // 32 KB f16
+constexpr uint32_t TMEM_COLS = 256;
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+  return d;
+}
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// One nibble word (values 4w..4w+3 and 16+4w..16+4w+3 of a block) -> the 16-byte
+// core-matrix row of slots 8w .. 8w+7, value = d*q + m (Q4_1) or d*(q - 8) (Q4_0).
+template <int QT>
+__device__ __forceinline__ uint4 dequant_word(uint32_t qw, __half2 d2, __half2 m2) {
+  const uint32_t MAGIC = 0x64006400u;  // f16 1024 in both halves
+  const uint32_t sh = qw >> 8;
+  __half2 lo02 = bits2h(lop3_and_or(qw, 0x000F000Fu, MAGIC));  // 1024 + q
+  __half2 lo13 = bits2h(lop3_and_or(sh, 0x000F000Fu, MAGIC));
+  __half2 hi02 = bits2h(lop3_and_or(qw, 0x00F000F0u, MAGIC));  // 1024 + 16 q
+  __half2 hi13 = bits2h(lop3_and_or(sh, 0x00F000F0u, MAGIC));
+  const __half2 k16 = __float2half2_rn(0.0625f);
+  if constexpr (QT == 3) {
+    const __half2 b1024 = __float2half2_rn(1024.f), b64 = __float2half2_rn(-64.f);
+    lo02 = __hfma2(__hsub2(lo02, b1024), d2, m2);
+    lo13 = __hfma2(__hsub2(lo13, b1024), d2, m2);
+    hi02 = __hfma2(__hfma2(hi02, k16, b64), d2, m2);
+    hi13 = __hfma2(__hfma2(hi13, k16, b64), d2, m2);
+  } else {
+    const __half2 b1032 = __float2half2_rn(1032.f), b72 = __float2half2_rn(-72.f);
+    lo02 = __hmul2(__hsub2(lo02, b1032), d2);
+    lo13 = __hmul2(__hsub2(lo13, b1032), d2);
+    hi02 = __hmul2(__hfma2(hi02, k16, b72), d2);
+    hi13 = __hmul2(__hfma2(hi13, k16, b72), d2);
+  }
+  return make_uint4(h2bits(lo02), h2bits(lo13), h2bits(hi02), h2bits(hi13));
+}
+
+// Loads block `blk` of a weight row from global memory: d, m and the four nibble words.
+template <int QT>
+__device__ __forceinline__ void load_block(const uint8_t* row, int blk, __half2& d2, __half2& m2, uint32_t (&qw)[4]) {
+  if constexpr (QT == 3) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 20 * blk);
+    const uint32_t dm = __ldg(w);
+    qw[0] = __ldg(w + 1);
+    qw[1] = __ldg(w + 2);
+    qw[2] = __ldg(w + 3);
+    qw[3] = __ldg(w + 4);
+    const __half2 h = bits2h(dm);
+    d2 = __low2half2(h);
+    m2 = __high2half2(h);
+  } else {
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(row + 18 * blk);
+    unsigned short u[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) u[i] = __ldg(h + i);
+    qw[0] = (uint32_t)u[1] | ((uint32_t)u[2] << 16);
+    qw[1] = (uint32_t)u[3] | ((uint32_t)u[4] << 16);
+    qw[2] = (uint32_t)u[5] | ((uint32_t)u[6] << 16);
+    qw[3] = (uint32_t)u[7] | ((uint32_t)u[8] << 16);
+    d2 = __half2half2(__ushort_as_half(u[0]));
+    m2 = d2;
+  }
+}
+
+// L2 prefetch of the 16-byte-aligned part of [p, p + bytes).
+__device__ __forceinline__ void prefetch_span(const void* p, uint32_t bytes) {
+  const uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15);
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
+  if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+}
+
+template <int QT, int MODE>
+__global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const PrefillArgs a) {
+  extern __shared__ __align__(1024) uint8_t gsm[];
+  uint8_t* As = gsm;                      // [2][A_STAGE]
+  constexpr int B_STAGE = MODE == 0 ? B_STAGE_GU : B_STAGE_DN;
+  uint8_t* Bs = gsm + 2 * A_STAGE;        // [2][B_STAGE]
+  __shared__ __align__(8) uint64_t mma_bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ uint32_t rowsrc[PREFILL_NMAX];  // B source row of each chunk row
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 0) tmem_alloc(&tmem_base, TMEM_COLS);
+  if (tid == 0) {
+    mbar_init(&mma_bar[0], 1);
+    mbar_init(&mma_bar[1], 1);
+    fence_mbar_init();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  const int nr = (int)a.nchunks[0], ntot = (int)a.nchunks[1];
+  // M tiles per chunk: gate/up 64 pairs (128 rows) a tile, down 128 output rows a tile
+  const int mt_r = MODE == 0 ? ceil_div(a.F, 64) : ceil_div(a.H, 128);
+  const int mt_s = MODE == 0 ? ceil_div(a.Fs > 0 ? a.Fs : 1, 64) : ceil_div(a.H, 128);
+  const int units = nr * mt_r + (ntot - nr) * mt_s;
+  uint32_t g = 0;  // pipeline chunks so far (stage = g % 2, use = g / 2)
+  bool ok = true;
+
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    int ci, mt;
+    if (u < nr * mt_r) { ci = u / mt_r; mt = u % mt_r; }
+    else { ci = nr + (u - nr * mt_r) / mt_s; mt = (u - nr * mt_r) % mt_s; }
+    const GemmChunk ch = a.chunks[ci];
+    const bool sh = ch.slot >= a.E;
+    const int ff = sh ? a.Fs : a.F;
+    const uint8_t* rec = sh ? a.shared : a.experts + (size_t)ch.slot * a.rec_bytes;
+    const int Kdim = MODE == 0 ? a.H : ff;       // reduction length
+    const int nbk = Kdim / 32;                   // blocks per weight row
+    const int nkc = ceil_div(nbk, KC / 32);      // pipeline chunks
+    const int npad = (ch.n + 15) & ~15;      // chunk rows, rounded up for the MMA
+    const int nb = MODE == 0 ? 2 * npad : npad;  // B rows: gate/up takes hi then lo rows
+    // weight rows of this tile
+    const uint32_t rb = MODE == 0 ? a.rb_h : (sh ? a.rb_fs : a.rb_f);
+    int mrows;  // valid M rows of the tile
+    if (MODE == 0) mrows = 2 * min(64, ff - 64 * mt);
+    else mrows = min(128, a.H - 128 * mt);
+    auto wrow = [&](int m) -> const uint8_t* {
+      if (MODE == 0) {
+        const int f = 64 * mt + (m >> 1);
+        return rec + (size_t)((m & 1) ? ff + f : f) * rb;  // even rows gate, odd rows up
+      }
+      return rec + (size_t)2 * ff * a.rb_h + (size_t)(128 * mt + m) * rb;
+    };
+    if (tid == 0) {  // bring this tile's rows into L2 ahead of the loads
+      if (MODE == 0) {
+        const uint32_t bytes = (uint32_t)(mrows / 2) * rb;
+        prefetch_span(wrow(0), bytes);
+        prefetch_span(wrow(1), bytes);
+      } else {
+        prefetch_span(wrow(0), (uint32_t)mrows * rb);
+      }
+    }
+    // B rows: the chunk's tokens (gate/up) or sorted pairs (down)
+    for (int r = tid; r < ch.n; r += PREFILL_THREADS) {
+      if (MODE == 0) rowsrc[r] = sh ? (uint32_t)(ch.row0 + r) : a.perm[ch.row0 + r] / (uint32_t)a.K;
+      else rowsrc[r] = (uint32_t)(ch.row0 + r);
+    }
+    __syncthreads();
+    const __half* bsrc = MODE == 0 ? a.x16 : (sh ? a.act16s : a.act16);
+    const int bld = MODE == 0 ? a.H : ff;  // B row length (values)
+
+    for (int kc = 0; kc < nkc; ++kc, ++g) {
+      const int s = g & 1;
+      const uint32_t use = g >> 1;
+      if (g >= 2 && !mbar_wait(&mma_bar[s], (use - 1) & 1u)) ok = false;  // stage free again
+      uint8_t* A = As + s * A_STAGE;
+      uint8_t* B = Bs + s * B_STAGE;
+      const int kb = min(KC / 32, nbk - kc * (KC / 32));  // blocks in this chunk
+      // A: 128 rows x 4 blocks; a warp takes 32 consecutive rows of one block, so its
+      // 16-byte shared stores of one core row cover all banks
+      for (int pass = 0; pass < 2; ++pass) {
+        const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
+        if (m < mrows && b < kb) {
+          __half2 d2, m2;
+          uint32_t qw[4];
+          load_block<QT>(wrow(m), kc * (KC / 32) + b, d2, m2, qw);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int kcore = 4 * b + w, mcore = m >> 3;
+            *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = dequant_word<QT>(qw[w], d2, m2);
+          }
+        }
+      }
+      // B: rows x (16-byte pieces of this chunk's K slice)
+      {
+        const int pieces = kb * 4;  // 8 values a piece
+        for (int i = tid; i < nb * pieces; i += PREFILL_THREADS) {
+          const int r = i / pieces, pc = i % pieces;
+          const int rr = r < npad ? r : r - npad;  // chunk row (lo rows: second half)
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (rr < ch.n) {
+            const size_t src = MODE == 0 ? 2 * (size_t)rowsrc[rr] + (r >= npad) : (size_t)rowsrc[rr];
+            v = __ldg(reinterpret_cast<const uint4*>(bsrc + src * bld + kc * KC + pc * 8));
+          }
+          *reinterpret_cast<uint4*>(B + (pc * (nb / 8) + (r >> 3)) * 128 + 16 * (r & 7)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after_sync();
+        const uint32_t idesc = idesc_f16_f32(128, nb);
+        for (int j = 0; j < 2 * kb; ++j) {  // K = 16 per MMA: two core matrices along K
+          const uint64_t ad = smem_desc(A + 2 * j * 2048, 2048, 128);
+          const uint64_t bd = smem_desc(B + 2 * j * 16 * nb, 16 * nb, 128);
+          mma_f16(tmem, ad, bd, idesc, kc > 0 || j > 0);
+        }
+        mma_commit(&mma_bar[s]);
+      }
+    }
+    // epilogue: the last commit covers every MMA of the tile
+    {
+      const uint32_t gl = g - 1;
+      if (!mbar_wait(&mma_bar[gl & 1], (gl >> 1) & 1u)) ok = false;
+    }
+    tc_fence_after_sync();
+    if (warp < 4) {
+      const int m = 32 * warp + lane;  // this thread's TMEM lane = tile row
+      for (int c0 = 0; c0 < npad; c0 += 16) {
+        uint32_t r[16];
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        tmem_ld16(lane_base + (uint32_t)c0, r);
+        if (MODE == 0) {
+          uint32_t rl[16];
+          tmem_ld16(lane_base + (uint32_t)(npad + c0), rl);
+          tmem_ld_wait();
+          const int f = 64 * mt + (m >> 1);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float v = __uint_as_float(r[i]) + __uint_as_float(rl[i]);  // x_hi + x_lo parts
+            const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+            const int c = c0 + i;
+            if (!(m & 1) && m < mrows && c < ch.n) {
+              const float act = v / (1.f + expf(-v)) * other;  // silu(gate) * up
+              __half* dst = sh ? a.act16s + (size_t)(ch.row0 + c) * ff : a.act16 + (size_t)(ch.row0 + c) * ff;
+              dst[kpos(f)] = __float2half_rn(act);
+            }
+          }
+        } else {
+          tmem_ld_wait();
+          const int h = 128 * mt + m;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            if (m < mrows && c < ch.n) {
+              const float y = __uint_as_float(r[i]);
+              if (sh) a.sbuf[(size_t)(ch.row0 + c) * a.H + h] = y;
+              else a.ybuf[(size_t)(ch.row0 + c) * a.H + h] = a.wsorted[ch.row0 + c] * y;
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before_sync();
+    // TMEM read and rowsrc used before the next tile reuses them; a timed-out wait
+    // anywhere in the CTA ends its loop
+    const bool failed = __syncthreads_or(!ok);
+    tc_fence_after_sync();
+    if (failed) {
+      ok = false;
+      break;
+    }
+  }
+  if (!ok && tid == 0) atomicOr(a.status, DEV_ERR_MBAR_TIMEOUT);
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// combine: out[t][h] = sum_j ybuf[pos(t, j)][h] + sbuf[t][h] (+ x | + out)
+// ---------------------------------------------------------------------------
+__global__ void prefill_combine(const PrefillArgs a) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)a.T * a.H) return;
+  const int t = (int)(i / a.H), h = (int)(i % a.H);
+  float acc = 0.f;
+  for (int j = 0; j < a.K; ++j) acc += a.ybuf[(size_t)a.pos_of[(size_t)t * a.K + j] * a.H + h];
+  if (a.Fs) acc += a.sbuf[i];
+  if (a.flags & FLAG_RESIDUAL) acc = a.x[i] + acc;
+  if (a.flags & FLAG_ACCUMULATE) acc = a.out[i] + acc;
+  a.out[i] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs) {
+  PrefillWs w;
+  const size_t P = (size_t)T * K;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
+  w.logits = take((size_t)T * E * 4);
+  w.ids = take(P * 4);
+  w.wts = take(P * 4);
+  w.offsets = take((size_t)(E + 1) * 4);
+  w.table = take(((P + 31) / 32) * (size_t)E * 2);
+  w.perm = take(P * 4);
+  w.wsorted = take(P * 4);
+  w.pos_of = take(P * 4);
+  w.chunks = take(((P + PREFILL_NMAX - 1) / PREFILL_NMAX + (size_t)E + (T + PREFILL_NMAX - 1) / PREFILL_NMAX + 1) *
+                  sizeof(GemmChunk));
+  w.nchunks = take(8);
+  w.x16 = take((size_t)T * H * 4);
+  w.act16 = take(P * F * 2);
+  w.act16s = take((size_t)T * (Fs ? Fs : 1) * 2);
+  w.ybuf = take(P * H * 4);
+  w.sbuf = take((size_t)T * H * 4);
+  w.total = o;
+  return w;
+}
+
+template <int QT, int MODE>
+static cudaError_t launch_gemm(const PrefillArgs& a, cudaStream_t st) {
+  auto kern = prefill_gemm<QT, MODE>;
+  const int smem = 2 * A_STAGE + 2 * (MODE == 0 ? B_STAGE_GU : B_STAGE_DN);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<a.nc, PREFILL_THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st) {
+  cudaError_t e;
+  prefill_router<<<dim3((a.E + 31) / 32, (a.T + 31) / 32), 256, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t topk_smem = (size_t)8 * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
+  e = cudaFuncSetAttribute(prefill_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem);
+  if (e != cudaSuccess) return e;
+  prefill_topk<<<(a.T + 7) / 8, 256, topk_smem, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  prefill_sort<<<1, 1024, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t nx = (size_t)a.T * a.H;
+  prefill_x16<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = a.qtype == 3 ? launch_gemm<3, 0>(a, st) : launch_gemm<2, 0>(a, st);
+  if (e != cudaSuccess) return e;
+  e = a.qtype == 3 ? launch_gemm<3, 1>(a, st) : launch_gemm<2, 1>(a, st);
+  if (e != cudaSuccess) return e;
+  prefill_combine<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,68 @@
+// Batched (prefill) MoE-FFN step: arguments and host-visible launcher.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace moe {
+
+constexpr int PREFILL_MIN_T = 8;      // batches of at least this many tokens take the prefill path
+constexpr int PREFILL_CHUNK_T = 512;  // tokens per prefill pass (larger batches run in passes)
+constexpr int PREFILL_NMAX = 128;     // tokens (or pairs) per GEMM work unit
+constexpr int PREFILL_THREADS = 256;
+
+// One token-chunk of a GEMM: `slot` = expert id (or n_experts for the shared expert),
+// rows [row0, row0 + n) of the expert-sorted pair list (or of the tokens, shared).
+struct GemmChunk {
+  int slot, row0, n, pad;
+};
+
+struct PrefillArgs {
+  // caller's buffers (device)
+  const float* x;           // [T][H]
+  const float* router_w;    // [E][H]
+  const float* bias;        // [E] or null
+  const uint8_t* experts;   // E records
+  const uint8_t* shared;    // shared record or null
+  float* out;               // [T][H]
+  int32_t* topk_ids;        // [T][K] or null
+  float* topk_w;            // [T][K] or null
+  // workspace
+  float* logits;            // [T][E]
+  int32_t* ids;             // [T][K]
+  float* wts;               // [T][K]
+  uint32_t* offsets;        // [E + 1] first sorted position of each expert
+  uint16_t* table;          // [ceil(P / 32)][E] per-32-pair counts, then their prefixes
+  uint32_t* perm;           // [P] pair (t * K + j) at each sorted position
+  float* wsorted;           // [P] routing weight at each sorted position
+  uint32_t* pos_of;         // [P] sorted position of each pair
+  GemmChunk* chunks;        // routed chunks (expert order), then shared chunks
+  uint32_t* nchunks;        // [2]: routed chunks, all chunks
+  __half* x16;              // [T][2][H] f16 hi and lo parts, K order permuted within 32-blocks
+  __half* act16;            // [P][F] f16 (sorted-pair rows), permuted K order
+  __half* act16s;           // [T][Fs] f16, permuted K order
+  float* ybuf;              // [P][H] weighted down outputs (sorted-pair rows)
+  float* sbuf;              // [T][H] shared-expert down outputs
+  uint32_t* status;         // device error bits
+  // shape
+  int T, H, E, K, F, Fs, G, Gu, qtype;
+  float scale, norm_min;
+  uint32_t flags;
+  uint32_t rb_h, rb_f, rb_fs;
+  uint64_t rec_bytes;
+  int nc;                   // CTAs of the persistent GEMM kernels
+};
+
+// Bytes of each prefill workspace region for a pass of T tokens (host).
+struct PrefillWs {
+  size_t logits, ids, wts, offsets, table, perm, wsorted, pos_of, chunks, nchunks, x16, act16, act16s,
+      ybuf, sbuf, total;
+};
+PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs);
+
+// Enqueues the whole prefill pass on `st`. Returns the first launch error.
+cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st);
+
+}  // namespace moe

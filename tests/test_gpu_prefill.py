@@ -1,0 +1,149 @@
+"""GPU parity of the batched (prefill) path against the float64 oracle.
+
+Calls of at least eight tokens take the batched path: a router GEMM, one warp
+per token for the selection, a stable counting sort of the (token, pick) pairs
+by expert, and grouped GEMMs on the tensor cores over 4-bit weights dequantised
+to f16. Bars as for decode: identical ordered picks, weights within W_REL, each
+token's output within relative L2 OUT_REL_L2.
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+from expert_ffn_decode_gb300 import synth
+from oracle import moe_oracle as mo
+from tests.helpers import GpuLayer, compare, margin_tokens, oracle_cfg, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import expert_ffn_decode_gb300 as ffn
+    if not os.path.exists(ffn.LIB_PATH):
+        from expert_ffn_decode_gb300 import build
+        build.build()
+    import torch
+    assert torch.cuda.is_available()
+    yield
+    ffn.moe_shutdown()
+
+
+def _small(seed, **kw):
+    w = dict(hidden=256, n_experts=16, top_k=4, expert_ff=128, shared_ff=0, n_groups=1, groups_used=1,
+             qtype=mo.Q4_1, weights_scale=1.0, n_tokens=24, router_std=0.1, bias_std=None, seed=seed)
+    w.update(kw)
+    return w
+
+
+SHAPES = [
+    _small(40, n_tokens=8),                                              # smallest batched call
+    _small(41, qtype=mo.Q4_0, shared_ff=64, n_tokens=37),                # ragged token tail
+    _small(42, hidden=96, expert_ff=96, qtype=mo.Q4_0),                  # K chunk of 3 blocks
+    _small(43, hidden=96, expert_ff=160, shared_ff=96, qtype=mo.Q4_1, n_tokens=130),
+    _small(44, n_experts=40, top_k=7, bias_std=0.1, n_tokens=50),
+    _small(45, n_experts=4, top_k=2, n_tokens=300, shared_ff=32),        # > 128 pairs per expert
+    _small(46, n_experts=32, n_groups=4, groups_used=2, top_k=5, bias_std=0.1, weights_scale=2.5),
+    _small(47, n_experts=64, n_groups=8, groups_used=3, top_k=6, bias_std=0.1, qtype=mo.Q4_0),
+    _small(48, hidden=3072, expert_ff=64, shared_ff=3072, n_experts=8, top_k=2, router_std=0.02, n_tokens=16),
+    _small(49, hidden=512, expert_ff=3072, n_experts=6, top_k=3, router_std=0.05, qtype=mo.Q4_0, n_tokens=20),
+    _small(50, hidden=1024, expert_ff=32, shared_ff=32, n_experts=1000, top_k=32, router_std=0.05, n_tokens=64),
+    _small(51, n_experts=128, n_groups=64, groups_used=5, top_k=9, bias_std=0.1, n_tokens=33),
+    _small(52, hidden=32, expert_ff=32, n_experts=2, top_k=1, n_tokens=9),
+    _small(53, n_experts=12, top_k=12, n_tokens=12),                     # k = E: every expert every token
+]
+
+
+@pytest.mark.parametrize("w", SHAPES, ids=[f"s{w['seed']}_t{w['n_tokens']}" for w in SHAPES])
+def test_prefill_shapes(w):
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    err = compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']}")
+    print(f"seed {w['seed']} T={w['n_tokens']}: max rel-L2 {err:.3e}")
+
+
+def test_prefill_two_passes_and_decode_boundary():
+    # 7 tokens decode token by token, 8 take the batched path, 600 run as passes of 512 + 88
+    w = _small(60, n_experts=16, top_k=3, shared_ff=64)
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, 600, seed=60)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    g = GpuLayer(layer, w)
+    for T in (7, 8, 513, 600):
+        out, ids, wts = g.run(x[:T])
+        compare(out, ids, wts, ref[:T], rid[:T], rwt[:T], f"T={T}")
+
+
+def test_prefill_flags_and_determinism():
+    import expert_ffn_decode_gb300 as ffn
+    import torch
+    w = _small(61, shared_ff=128, n_tokens=40)
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, 40, seed=61)
+    g = GpuLayer(layer, w)
+    base, ids, wts = g.run(x)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    compare(base, ids, wts, ref, rid, rwt, "plain")
+    init = np.random.default_rng(62).standard_normal(x.shape).astype(np.float32)
+    acc, _, _ = g.run(x, flags=ffn.MOE_ACCUMULATE, out_init=init)
+    assert rel_l2(acc - init, base) < 1e-6
+    res, _, _ = g.run(x, flags=ffn.MOE_RESIDUAL)
+    assert rel_l2(res - x, base) < 1e-6
+    for _ in range(3):  # a fixed summation order: repeat calls agree bit for bit
+        again, ia, wa = g.run(x)
+        assert np.array_equal(again, base) and np.array_equal(ia, ids) and np.array_equal(wa, wts)
+    T, H = x.shape
+    cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": ffn.MOE_HOST_IO})
+    ws = torch.zeros(ffn.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    xh = np.ascontiguousarray(x, np.float32)
+    oh = np.full((T, H), np.nan, np.float32)
+    ih = np.full((T, w["top_k"]), -1, np.int32)
+    wh = np.full((T, w["top_k"]), np.nan, np.float32)
+    st = torch.cuda.current_stream()
+    ffn.check(ffn.moe_ffn_forward_ex(xh, g.router_w, g.bias, g.experts, g.shared, cfg, oh, ws, ws.numel(),
+                                     st, ih, wh))
+    ffn.check(ffn.moe_workspace_status(ws, st))
+    assert np.array_equal(oh, base) and np.array_equal(ih, ids) and np.array_equal(wh, wts)
+
+
+def test_flint_prefill_t512_sampled():
+    # the full Flint-shaped batch: every token's picks and weights against the oracle's
+    # routing, and the outputs of a spread of sampled tokens against the oracle's step
+    w = synth.WORKLOADS["flint_prefill_t512"]
+    layer = synth.make_layer(w)
+    T = w["n_tokens"]
+    x, _ = margin_tokens(layer, w, T, seed=w["seed"])
+    cfg = oracle_cfg(w)
+    rid, rwt, _ = mo.route(x, layer["router_w"], layer["bias"], cfg)
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    assert np.array_equal(ids, rid)
+    assert np.max(np.abs(wts - rwt) / np.abs(rwt)) <= 1e-5
+    assert np.all(np.isfinite(out))
+    sample = [0, 1, 63, 127, 128, 200, 255, 256, 383, 400, 510, 511]
+    for t in sample:
+        ref, _, _ = mo.moe_ffn(x[t:t + 1], layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], cfg)
+        e = rel_l2(out[t], ref[0])
+        assert e <= 2e-3, f"token {t}: rel-L2 {e}"
+
+
+def test_prefill_matches_decode_path():
+    # the same tokens decoded one call at a time and as one batch: both near the oracle,
+    # and near each other
+    name = "flint_decode_t1"
+    w = synth.WORKLOADS[name]
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, 8, seed=70)
+    g = GpuLayer(layer, w)
+    batch, ib, wb = g.run(x)
+    one = [g.run(x[t:t + 1]) for t in range(8)]
+    for t in range(8):
+        assert np.array_equal(one[t][1][0], ib[t])
+        assert rel_l2(one[t][0][0], batch[t]) < 2e-3
