@@ -10,6 +10,11 @@ device) and rotate over enough distinct layers that every weight byte is cold
 in L2 when it is read again. Timed on the device with CUDA events around a
 replayed CUDA graph of the steps; rank 0 prints one JSON line.
 
+The line also carries a "prefill" object: the same layer over a batch of 512
+tokens per step (the batched path: router GEMM, selection, expert sort, tensor-
+core grouped GEMMs), timed the same way. With ``--workload flint_prefill_t512``
+the batched step is the headline instead.
+
 ``--impl reference`` times the CPU oracle (float64, one thread) on a bounded
 sample of the same workload instead.
 """
@@ -202,6 +207,95 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
           file=sys.stderr)
 
 
+def prefill_bytes(w, distinct):
+    """Algorithmic bytes of one batched step: the router, every expert some token
+    picked (`distinct` of them, each read once), the shared expert, x and out."""
+    bb = 18 if w["qtype"] == 2 else 20
+    H, E, T, F, Fs = w["hidden"], w["n_experts"], w["n_tokens"], w["expert_ff"], w["shared_ff"]
+    rec = lambda ff: 3 * ff * (H // 32) * bb
+    router = E * H * 4 + (E * 4 if w.get("bias_std") is not None else 0)
+    return router + distinct * rec(F) + (rec(Fs) if Fs else 0) + 2 * T * H * 4
+
+
+def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, layers=0):
+    """Batched steps of `workload` (T tokens per call) on rotating layers; returns a dict
+    with tokens/s, ms per step, the HBM roofline of the step and the end-to-end figure."""
+    import torch
+    w = synth.WORKLOADS[workload]
+    T, H, K = w["n_tokens"], w["hidden"], w["top_k"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    full = prefill_bytes(w, w["n_experts"])
+    L = layers or max(2, math.ceil(2 * l2 / full) + 1)
+    layers = [synth.make_layer_torch(w, seed=5000 + 7919 * rank + i, device=dev) for i in range(L)]
+    NX = 3
+    xs = [synth.make_tokens_torch(300 + 17 * rank + j, H, T, dev) for j in range(NX)]
+    out = torch.zeros((T, H), device=dev)
+    cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": 0})
+    ws_bytes = ffn.moe_workspace_size(cfg)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+
+    def step(i, st, want_ids=False):
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg, out, ws, ws_bytes, st,
+                                         ids if want_ids else None))
+
+    # distinct experts per step, from the routing of each (layer, batch) pair the steps use
+    distinct = []
+    with torch.cuda.stream(stream):
+        for i in range(L * NX):
+            step(i, stream, want_ids=True)
+            stream.synchronize()
+            distinct.append(int(torch.unique(ids).numel()))
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    G = L * NX * max(1, 24 // (L * NX))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):
+            step(i, stream)
+    reps = max(1, steps // G)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, warmup // G)):
+            g.replay()
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    n = reps * G
+    ms = ev0.elapsed_time(ev1) / n
+    step_bytes = prefill_bytes(w, statistics.mean(distinct))
+    # end to end: pinned host x in, host out back, synchronised every step
+    cfg_h = ffn.make_cfg(**{**w, "n_tokens": T, "flags": ffn.MOE_HOST_IO})
+    wsh_bytes = ffn.moe_workspace_size(cfg_h)
+    wsh = torch.zeros(wsh_bytes, dtype=torch.uint8, device=dev)
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    for i in range(3):
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream))
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream))
+        stream.synchronize()
+    e2e = e2e_steps * T / (time.perf_counter() - t0)
+    ffn.check(ffn.moe_workspace_status(wsh, stream))
+    return {"workload": workload, "T": T, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": n, "layers_rotated": L, "distinct_experts_per_step": statistics.mean(distinct),
+            "bytes_per_step": step_bytes, "launches_per_step": 7, "e2e": round(e2e, 1), "e2e_steps": e2e_steps,
+            "h2d_bytes_per_step": T * H * 4, "d2h_bytes_per_step": T * H * 4}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -213,6 +307,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--prefill-steps", type=int, default=480, help="timed batched steps (0: skip)")
     ap.add_argument("--trace", action="store_true",
                     help="after timing, print the kernel's per-CTA phase timeline (stderr)")
     args = ap.parse_args()
@@ -235,7 +330,7 @@ def main():
     w = synth.WORKLOADS[args.workload]
     T, H = w["n_tokens"], w["hidden"]
     if T != 1:
-        raise SystemExit("this bench times the decode step (T = 1)")
+        return main_prefill(args, ffn, synth, dev, rank, world, local)
     step_bytes = layer_bytes(w)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     L = args.layers or max(8, math.ceil(4 * l2 / step_bytes) + 1)
@@ -344,9 +439,22 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_val = n_e2e * T * world / float(t.item())
 
+    pre = None
+    if args.prefill_steps > 0:
+        pre = bench_prefill(ffn, synth, "flint_prefill_t512", dev, rank, args.prefill_steps, 24)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([pre["ms_per_step"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            pre["ms_per_step"] = float(t.item())
+            pre["value"] = round(pre["T"] * world / (pre["ms_per_step"] * 1e-3), 1)
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
+    if pre is not None:
+        a = pre["bytes_per_step"] / (pre["ms_per_step"] * 1e-3) / 1e9
+        pre["roofline"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s",
+                           "frac": round(a / peak, 4), "peak_kind": peak_kind, "over": "the whole batched step"}
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
@@ -382,6 +490,57 @@ def main():
                        "every step"},
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "prefill": pre,
+    }
+    print(json.dumps(line))
+
+
+def main_prefill(args, ffn, synth, dev, rank, world, local):
+    """The batched workload as the headline line."""
+    import torch
+    w = synth.WORKLOADS[args.workload]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        pre = bench_prefill(ffn, synth, args.workload, dev, rank, args.steps, args.warmup,
+                            e2e_steps=min(args.e2e_steps, 50), layers=args.layers)
+    ms = pre["ms_per_step"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    a = pre["bytes_per_step"] / (ms * 1e-3) / 1e9
+    T = w["n_tokens"]
+    cpu = None
+    if not args.no_cpu_baseline:
+        d, err = cpu_baseline(args.workload, max_tokens=64)
+        cpu = ({"value": d["tokens"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{d['tokens']} single-token oracle calls of the workload's layer in {d['seconds']:.1f} s "
+                          f"(numpy float64, one thread)"} if d is not None else
+               {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {err}"})
+    line = {
+        "metric": METRIC, "value": round(T * world / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": pre["steps"], "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32", "data": "synthetic",
+        "config": {"workload": args.workload, "T": T, "hidden": w["hidden"], "n_experts": w["n_experts"],
+                   "top_k": w["top_k"], "expert_ff": w["expert_ff"], "shared_ff": w["shared_ff"],
+                   "qtype": "Q4_1" if w["qtype"] == 3 else "Q4_0", "parallelism": f"replicas{world}",
+                   "layers_rotated": pre["layers_rotated"],
+                   "l2": "inputs larger than L2: every step reads over 400 MB of weights"},
+        "roofline": {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s", "frac": round(a / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind, "over": "the whole batched step",
+                     "bytes_per_launch": pre["bytes_per_step"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": pre["e2e"], "unit": UNIT, "h2d_bytes_per_step": pre["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": pre["d2h_bytes_per_step"], "steps": pre["e2e_steps"]},
+        "gpu_launches": pre["steps"] * pre["launches_per_step"],
+        "clocks": clk.summary(),
+        "detail": pre,
     }
     print(json.dumps(line))
 

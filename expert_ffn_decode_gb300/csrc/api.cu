@@ -123,7 +123,9 @@ WsLayout ws_layout(const moe_cfg* c) {
   L.prefill = 0;
   if (const int tp = prefill_pass_tokens(c->n_tokens)) {
     L.prefill = o;
-    o = up256(o + moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff, c->shared_ff).total);
+    const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype);
+    o = up256(o + moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff, c->shared_ff, tile)
+                      .total);
   }
   L.total = o;
   return L;
@@ -320,8 +322,9 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
 
   if (const int tp = prefill_pass_tokens(T)) {
     // batched path: router, top-k, expert sort and grouped tensor-core GEMMs
+    const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype);
     const moe::PrefillWs P = moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff,
-                                                    c->shared_ff);
+                                                    c->shared_ff, tile);
     uint8_t* pb = wsb + W.prefill;
     moe::PrefillArgs pa{};
     pa.router_w = router_w;
@@ -338,9 +341,18 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     pa.pos_of = reinterpret_cast<uint32_t*>(pb + P.pos_of);
     pa.chunks = reinterpret_cast<moe::GemmChunk*>(pb + P.chunks);
     pa.nchunks = reinterpret_cast<uint32_t*>(pb + P.nchunks);
-    pa.x16 = reinterpret_cast<__half*>(pb + P.x16);
-    pa.act16 = reinterpret_cast<__half*>(pb + P.act16);
-    pa.act16s = reinterpret_cast<__half*>(pb + P.act16s);
+    if (tile) {
+      pa.ximg = pb + P.ximg;
+      pa.ximg_routed = pb + P.ximg_routed;
+      pa.aimg = pb + P.aimg;
+      pa.aimg_s = pb + P.aimg_s;
+    } else {
+      pa.x16 = reinterpret_cast<__half*>(pb + P.x16);
+      pa.act16 = reinterpret_cast<__half*>(pb + P.act16);
+      pa.act16s = reinterpret_cast<__half*>(pb + P.act16s);
+    }
+    pa.tile = tile ? 1 : 0;
+    pa.nmax = tile ? moe::PREFILL_TILE_NMAX : moe::PREFILL_NMAX;
     pa.ybuf = reinterpret_cast<float*>(pb + P.ybuf);
     pa.sbuf = reinterpret_cast<float*>(pb + P.sbuf);
     pa.status = reinterpret_cast<uint32_t*>(wsb + W.ctrl) + moe::CTRL_STATUS;

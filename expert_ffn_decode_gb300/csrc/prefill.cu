@@ -198,23 +198,26 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
       a.table[(size_t)c * E + tid] = (uint16_t)cnt;
       cnt += v;
     }
-  // (c) first sorted position of each expert; first chunk of each expert
-  uint32_t total = 0, nrouted = 0;
+  // (c) first sorted position, first chunk and first padded row of each expert
+  const int nmax = a.nmax;
+  uint32_t total = 0, nrouted = 0, ptotal = 0;
   const uint32_t off = cta_excl_scan(cnt, wsum, total);
-  const uint32_t nck = (cnt + PREFILL_NMAX - 1) / PREFILL_NMAX;
+  const uint32_t nck = (cnt + nmax - 1) / nmax;
   const uint32_t cbase = cta_excl_scan(nck, wsum, nrouted);
+  const uint32_t prows = nck ? (nck - 1) * nmax + ((cnt - (nck - 1) * nmax + 15) & ~15u) : 0u;
+  const uint32_t pbase = cta_excl_scan(prows, wsum, ptotal);
   if (tid < E) {
     offs[tid] = off;
     a.offsets[tid] = off;
     for (uint32_t r = 0; r < nck; ++r) {
-      const int row0 = (int)(off + r * PREFILL_NMAX), n = (int)min(cnt - r * PREFILL_NMAX, (uint32_t)PREFILL_NMAX);
-      a.chunks[cbase + r] = GemmChunk{tid, row0, n, 0};
+      const int row0 = (int)(off + r * nmax), n = (int)min(cnt - r * nmax, (uint32_t)nmax);
+      a.chunks[cbase + r] = GemmChunk{tid, row0, n, (int)(pbase + r * nmax)};
     }
   }
   if (tid == 0) a.offsets[E] = total;
-  // shared-expert chunks follow the routed ones
-  const int nsh = a.Fs ? (a.T + PREFILL_NMAX - 1) / PREFILL_NMAX : 0;
-  if (tid < nsh) a.chunks[nrouted + tid] = GemmChunk{E, tid * PREFILL_NMAX, min(a.T - tid * PREFILL_NMAX, PREFILL_NMAX), 0};
+  // shared-expert chunks (token chunks) follow the routed ones
+  const int nsh = a.Fs ? (a.T + nmax - 1) / nmax : 0;
+  if (tid < nsh) a.chunks[nrouted + tid] = GemmChunk{E, tid * nmax, min(a.T - tid * nmax, nmax), tid * nmax};
   if (tid == 0) {
     a.nchunks[0] = nrouted;
     a.nchunks[1] = nrouted + (uint32_t)nsh;
@@ -529,9 +532,17 @@ __global__ void prefill_combine(const PrefillArgs a) {
 // ---------------------------------------------------------------------------
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs) {
-  PrefillWs w;
+bool prefill_tile_ok(int H, int F, int Fs, int qtype) {
+  const int kc = qtype == 3 ? 128 : 256;
+  return H % kc == 0 && F % kc == 0 && Fs % kc == 0;
+}
+
+PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile) {
+  PrefillWs w{};
   const size_t P = (size_t)T * K;
+  const size_t nmax = tile ? PREFILL_TILE_NMAX : PREFILL_NMAX;
+  const size_t max_routed = (P + nmax - 1) / nmax + (size_t)E;  // routed chunks at most
+  const size_t tok_chunks = ((size_t)T + nmax - 1) / nmax;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
   w.logits = take((size_t)T * E * 4);
@@ -542,14 +553,22 @@ PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs) {
   w.perm = take(P * 4);
   w.wsorted = take(P * 4);
   w.pos_of = take(P * 4);
-  w.chunks = take(((P + PREFILL_NMAX - 1) / PREFILL_NMAX + (size_t)E + (T + PREFILL_NMAX - 1) / PREFILL_NMAX + 1) *
-                  sizeof(GemmChunk));
+  w.chunks = take((max_routed + tok_chunks + 1) * sizeof(GemmChunk));
   w.nchunks = take(8);
-  w.x16 = take((size_t)T * H * 4);
-  w.act16 = take(P * F * 2);
-  w.act16s = take((size_t)T * (Fs ? Fs : 1) * 2);
   w.ybuf = take(P * H * 4);
   w.sbuf = take((size_t)T * H * 4);
+  if (!tile) {
+    w.x16 = take((size_t)T * H * 4);
+    w.act16 = take(P * F * 2);
+    w.act16s = take((size_t)T * (Fs ? Fs : 1) * 2);
+  } else {
+    const size_t prow_routed = P + 15 * max_routed;  // padded rows of all routed chunks, at most
+    const size_t prow_tok = tok_chunks * nmax;
+    w.ximg = take(2 * prow_tok * H * 2);
+    w.ximg_routed = take(2 * prow_routed * H * 2);
+    w.aimg = take(prow_routed * F * 2);
+    w.aimg_s = take(prow_tok * (Fs ? Fs : 32) * 2);
+  }
   w.total = o;
   return w;
 }
@@ -566,8 +585,15 @@ static cudaError_t launch_gemm(const PrefillArgs& a, cudaStream_t st) {
 
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st) {
   cudaError_t e;
-  prefill_router<<<dim3((a.E + 31) / 32, (a.T + 31) / 32), 256, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t nx = (size_t)a.T * a.H;
+  if (a.tile) {
+    // token-chunk images first: the router and the shared expert read them
+    if ((e = tile_images_launch(a, false, st)) != cudaSuccess) return e;
+    if ((e = tile_router_launch(a, st)) != cudaSuccess) return e;
+  } else {
+    prefill_router<<<dim3((a.E + 31) / 32, (a.T + 31) / 32), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const size_t topk_smem = (size_t)8 * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
   e = cudaFuncSetAttribute(prefill_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem);
   if (e != cudaSuccess) return e;
@@ -575,13 +601,18 @@ cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   prefill_sort<<<1, 1024, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t nx = (size_t)a.T * a.H;
-  prefill_x16<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = a.qtype == 3 ? launch_gemm<3, 0>(a, st) : launch_gemm<2, 0>(a, st);
-  if (e != cudaSuccess) return e;
-  e = a.qtype == 3 ? launch_gemm<3, 1>(a, st) : launch_gemm<2, 1>(a, st);
-  if (e != cudaSuccess) return e;
+  if (a.tile) {
+    if ((e = tile_images_launch(a, true, st)) != cudaSuccess) return e;
+    if ((e = tile_gemm_launch(a, 0, st)) != cudaSuccess) return e;
+    if ((e = tile_gemm_launch(a, 1, st)) != cudaSuccess) return e;
+  } else {
+    prefill_x16<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = a.qtype == 3 ? launch_gemm<3, 0>(a, st) : launch_gemm<2, 0>(a, st);
+    if (e != cudaSuccess) return e;
+    e = a.qtype == 3 ? launch_gemm<3, 1>(a, st) : launch_gemm<2, 1>(a, st);
+    if (e != cudaSuccess) return e;
+  }
   prefill_combine<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }

@@ -10,13 +10,16 @@ namespace moe {
 
 constexpr int PREFILL_MIN_T = 8;      // batches of at least this many tokens take the prefill path
 constexpr int PREFILL_CHUNK_T = 512;  // tokens per prefill pass (larger batches run in passes)
-constexpr int PREFILL_NMAX = 128;     // tokens (or pairs) per GEMM work unit
+constexpr int PREFILL_NMAX = 128;     // tokens (or pairs) per GEMM work unit (general path)
+constexpr int PREFILL_TILE_NMAX = 64; // tokens (or pairs) per GEMM work unit (tile pipeline)
 constexpr int PREFILL_THREADS = 256;
 
 // One token-chunk of a GEMM: `slot` = expert id (or n_experts for the shared expert),
 // rows [row0, row0 + n) of the expert-sorted pair list (or of the tokens, shared).
+// `prow`: rows of the earlier chunks of its kind, each rounded up to 16 (the chunk's
+// first row in the tiled operand images of the tile pipeline).
 struct GemmChunk {
-  int slot, row0, n, pad;
+  int slot, row0, n, prow;
 };
 
 struct PrefillArgs {
@@ -41,6 +44,12 @@ struct PrefillArgs {
   GemmChunk* chunks;        // routed chunks (expert order), then shared chunks
   uint32_t* nchunks;        // [2]: routed chunks, all chunks
   __half* x16;              // [T][2][H] f16 hi and lo parts, K order permuted within 32-blocks
+  // tile pipeline: operand images, each chunk's rows tiled as its MMA B operand
+  // ([chunk][128-value K block][rows/8][8 rows x 16 bytes] per 8 K values)
+  uint8_t* ximg;            // x hi/lo: token chunks, then routed chunks from ximg_routed
+  uint8_t* ximg_routed;
+  uint8_t* aimg;            // routed activations (sorted-pair chunks)
+  uint8_t* aimg_s;          // shared-expert activations (token chunks)
   __half* act16;            // [P][F] f16 (sorted-pair rows), permuted K order
   __half* act16s;           // [T][Fs] f16, permuted K order
   float* ybuf;              // [P][H] weighted down outputs (sorted-pair rows)
@@ -53,14 +62,26 @@ struct PrefillArgs {
   uint32_t rb_h, rb_f, rb_fs;
   uint64_t rec_bytes;
   int nc;                   // CTAs of the persistent GEMM kernels
+  int nmax;                 // rows per chunk: PREFILL_NMAX or PREFILL_TILE_NMAX
+  int tile;                 // 1: tile pipeline (prefill_tile_ok), 0: general path
 };
 
 // Bytes of each prefill workspace region for a pass of T tokens (host).
 struct PrefillWs {
   size_t logits, ids, wts, offsets, table, perm, wsorted, pos_of, chunks, nchunks, x16, act16, act16s,
-      ybuf, sbuf, total;
+      ybuf, sbuf, ximg, ximg_routed, aimg, aimg_s, total;
 };
-PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs);
+PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile);
+
+// True when the layer's K dimensions are whole pipeline chunks (128 values for Q4_1,
+// 256 for Q4_0): every weight-row segment a chunk copies then starts and ends on a
+// 16-byte boundary, which the bulk copies of the tile pipeline need.
+bool prefill_tile_ok(int H, int F, int Fs, int qtype);
+
+// Tile pipeline launches (prefill_tc.cu).
+cudaError_t tile_router_launch(const PrefillArgs& a, cudaStream_t st);
+cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t st);
+cudaError_t tile_gemm_launch(const PrefillArgs& a, int mode, cudaStream_t st);
 
 // Enqueues the whole prefill pass on `st`. Returns the first launch error.
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st);

@@ -53,6 +53,13 @@ SHAPES = [
     _small(51, n_experts=128, n_groups=64, groups_used=5, top_k=9, bias_std=0.1, n_tokens=33),
     _small(52, hidden=32, expert_ff=32, n_experts=2, top_k=1, n_tokens=9),
     _small(53, n_experts=12, top_k=12, n_tokens=12),                     # k = E: every expert every token
+    # shapes of whole 128-value (Q4_1) or 256-value (Q4_0) chunks take the tile pipeline
+    _small(54, n_experts=4, top_k=2, n_tokens=300, shared_ff=128),       # > 64 pairs per expert
+    _small(55, hidden=512, expert_ff=256, shared_ff=256, qtype=mo.Q4_0, n_tokens=70),
+    _small(56, hidden=1024, expert_ff=128, shared_ff=128, n_experts=1000, top_k=32, router_std=0.05,
+           n_tokens=40),                                                 # ragged 64-expert router tile
+    _small(57, n_experts=64, n_groups=8, groups_used=3, top_k=6, bias_std=0.1, n_tokens=130,
+           shared_ff=128),
 ]
 
 
@@ -67,9 +74,10 @@ def test_prefill_shapes(w):
     print(f"seed {w['seed']} T={w['n_tokens']}: max rel-L2 {err:.3e}")
 
 
-def test_prefill_two_passes_and_decode_boundary():
+@pytest.mark.parametrize("shared_ff", [64, 128], ids=["general", "tile"])
+def test_prefill_two_passes_and_decode_boundary(shared_ff):
     # 7 tokens decode token by token, 8 take the batched path, 600 run as passes of 512 + 88
-    w = _small(60, n_experts=16, top_k=3, shared_ff=64)
+    w = _small(60, n_experts=16, top_k=3, shared_ff=shared_ff)
     layer = synth.make_layer(w)
     x, _ = margin_tokens(layer, w, 600, seed=60)
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
