@@ -1,27 +1,34 @@
 // Tile pipeline of the batched MoE-FFN step for sm_103a: the router, gate/up and
 // down contractions as warp-specialised persistent kernels on the tensor cores.
 //
-// One CTA per SM, 320 threads:
-//   warp 0      producer: cp.async.bulk copies of the raw weight rows of each
-//               pipeline chunk into a ring of shared-memory stages, and of the
-//               token operand (a pre-tiled image, one copy per 128 K values)
-//   warp 1      MMA issuer: tcgen05.mma with A in tensor memory, B in shared memory,
-//               f32 accumulator in tensor memory; commits release the stages
-//   warps 2..9  converters: raw 4-bit blocks (or f32 router rows) -> f16 rows of A,
-//               written to tensor memory with tcgen05.st (thread = row = TMEM lane);
-//               then the epilogue of each tile (tcgen05.ld)
+// One CTA per SM, 576 threads:
+//   warp 0       weight producer: 2-D TMA tensor copies of the raw weight rows of each
+//                pipeline chunk (one box of 64 or 128 rows) into shared-memory stages
+//   warp 1       MMA issuer: tcgen05.mma with A in tensor memory, B in shared memory,
+//                f32 accumulator in tensor memory; commits release the stages
+//   warp 2       token-operand producer: one bulk copy per 128 K values of a pre-tiled
+//                image of the chunk's token rows
+//   warps 3..18  converters in four groups of four warps (one per TMEM lane quarter;
+//                thread = tile row = TMEM lane). Every converter warp waits for every raw
+//                chunk and releases it; 128-value A unit n of the tile stream goes to group
+//                n % 4, which owns one TMEM A slot: raw 4-bit blocks (or f32 router rows)
+//                -> f16 rows of A, written with tcgen05.st. Groups 0 and 1 then run the
+//                tile's epilogue (tcgen05.ld).
 //
 // Work units (one accumulator tile, M = 128 weight rows x N = chunk tokens):
 //   router   64 experts (f32 rows split into f16 hi rows 0..63 and lo rows 64..127)
 //            x 64 tokens (x hi and lo columns): logit = sum of the four products
-//   gate/up  64 gate/up row pairs (interleaved: even rows gate, odd rows up) of one
+//   gate/up  64 gate rows (rows 0..63) and the matching up rows (64..127) of one
 //            expert x one chunk of its sorted (token, pick) pairs (x hi and lo columns)
 //   down     128 down rows of one expert x the chunk's activations
 // Every stage wait is bounded; a timeout anywhere stops every role of the CTA and
 // sets the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "common.cuh"
 #include "plan.h"
@@ -31,40 +38,37 @@
 namespace moe {
 namespace {
 
-constexpr int TP_THREADS = 320;
-constexpr int TP_CONV_WARPS = 8;
+constexpr int TP_CONV_WARPS = 16;                 // four groups of four (one warp per TMEM lane quarter)
+constexpr int TP_GROUPS = TP_CONV_WARPS / 4;      // chunk k is converted by group k % TP_GROUPS
+constexpr int TP_EPI_WARPS = 8;                   // two per lane quarter run the epilogue
+constexpr int TP_THREADS = 96 + 32 * TP_CONV_WARPS;  // two producer warps, the MMA warp, converters
 constexpr int TP_KB = 128;                        // K values per token-operand stage
 constexpr int TP_B_STAGE = 128 * TP_KB * 2;       // up to 128 rows: 32 KB
-constexpr int TP_NSB = 3;
-constexpr int TP_RAW_BUDGET = 104 * 1024;
-constexpr int TP_SCRATCH = 64 * 65 * 4;           // router epilogue exchange
-constexpr int TP_MAX_NSA = 16;
+constexpr int TP_SCRATCH = 64 * 65 * 4;           // gate/up and router epilogue exchange
+constexpr int TP_SMEM_MAX = 227 * 1024 - 2048;    // dynamic shared memory (static arrays + alignment aside)
 constexpr uint32_t TP_TMEM_COLS = 512;
-constexpr uint32_t TP_A_COL = 128;                // A stages follow the accumulator (128 columns)
+constexpr uint32_t TP_A_COL = 128;                // A slots follow the accumulator columns [0, 128)
 
 // Stage geometry per contraction. MODE 0 gate/up, 1 down, 2 router.
 template <int MODE, int QT>
 struct Geo {
-  static constexpr int ROWS = MODE == 2 ? 64 : 128;             // raw rows per stage
-  static constexpr int SEG = MODE == 2 ? 512 : (QT == 3 ? 80 : 144);  // bytes per row per chunk
-  static constexpr int PITCH = MODE == 2 ? 528 : SEG;           // odd multiple of 16: conflict-free LDS.128
-  static constexpr int KC = MODE == 2 ? 128 : (QT == 3 ? 128 : 256);  // K values per chunk
-  static constexpr int STAGE = ROWS * PITCH;
-  static constexpr int NSA = (TP_RAW_BUDGET / STAGE) < TP_MAX_NSA ? (TP_RAW_BUDGET / STAGE) : TP_MAX_NSA;
-  static constexpr uint32_t ACOLS = KC / 2;                     // TMEM columns per A stage
-  static constexpr int NSUB = KC / TP_KB;                       // token stages per chunk
-  static constexpr int SMEM = NSA * STAGE + TP_NSB * TP_B_STAGE + (MODE == 2 ? TP_SCRATCH : 0);
+  // A raw chunk is ROWS rows x KR K values. Its row segments (SEG bytes) are odd multiples
+  // of 16 bytes, stored densely by the TMA: a quarter warp reading one 16-byte word of 8
+  // consecutive rows then hits 8 different bank groups. Wide segments keep each TMA row
+  // request long (240 and 144 bytes against 80 for a single 128-value unit).
+  static constexpr int ROWS = MODE == 2 ? 64 : 128;                  // raw rows per stage
+  static constexpr int KR = MODE == 2 ? 128 : (QT == 3 ? 384 : 256);  // K values per raw chunk
+  static constexpr int SEG = MODE == 2 ? 512 : KR / 32 * (QT == 3 ? 20 : 18);  // bytes per row
+  static constexpr int STAGE = ROWS * SEG;
+  static constexpr int NAU = KR / TP_KB;                             // 128-value A units per chunk
+  static constexpr int NSB = 2;                                      // token-operand stages
+  static constexpr int SCR = MODE == 1 ? 0 : TP_SCRATCH;
+  static constexpr int NSA0 = (TP_SMEM_MAX - NSB * TP_B_STAGE - SCR - 1024) / STAGE;
+  static constexpr int NSA = NSA0 > 16 ? 16 : NSA0;                  // raw stages (one shared ring)
+  static constexpr int NACC = MODE == 1 ? 2 : 1;                     // accumulators (down tiles: N <= 64)
+  static constexpr int SMEM = NSA * STAGE + NSB * TP_B_STAGE + SCR;
+  static_assert(NSA >= 2 && SMEM + 1024 <= TP_SMEM_MAX, "shared memory");
 };
-
-__device__ __forceinline__ int kslot_dev(int e) {
-  const int hi = e >> 4, r = e & 15, w = r >> 2, j = r & 3;
-  return 8 * w + 4 * hi + ((j == 1) ? 2 : (j == 2 ? 1 : j));
-}
-
-// Byte offset of (row r, slot s) inside one 128-value block of an operand image with nb rows.
-__device__ __forceinline__ uint32_t img_off(int r, int s, int nb) {
-  return (uint32_t)(((s >> 3) * (nb >> 3) + (r >> 3)) * 128 + (r & 7) * 16 + (s & 7) * 2);
-}
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
@@ -106,6 +110,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
       "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -160,47 +172,26 @@ __device__ __forceinline__ void dequant4(uint32_t qw, __half2 d2, __half2 m2, ui
   }
 }
 
-// Q4_1: the thread's two blocks (40 bytes at byte 40h of the 80-byte row segment).
-__device__ __forceinline__ void convert_q41(const uint8_t* row, int h, uint32_t (&o)[32]) {
-  const uint4* p = reinterpret_cast<const uint4*>(row) + (h ? 2 : 0);
-  const uint4 a = p[0], b = p[1], c = p[2];
-  const uint32_t w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
-  // h = 0: blocks at words 0 and 5; h = 1 (window starts at word 8): words 2 and 7
-  const int w0 = h ? 2 : 0;
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {
-    const int base = w0 + 5 * blk;
-    uint32_t dm, q0, q1, q2, q3;
-    if (h) {
-      dm = blk ? w[7] : w[2];
-      q0 = blk ? w[8] : w[3];
-      q1 = blk ? w[9] : w[4];
-      q2 = blk ? w[10] : w[5];
-      q3 = blk ? w[11] : w[6];
-    } else {
-      dm = blk ? w[5] : w[0];
-      q0 = blk ? w[6] : w[1];
-      q1 = blk ? w[7] : w[2];
-      q2 = blk ? w[8] : w[3];
-      q3 = blk ? w[9] : w[4];
-    }
-    (void)base;
-    const __half2 dmh = u2h(dm);
-    const __half2 d2 = __low2half2(dmh), m2 = __high2half2(dmh);
-    dequant4<3>(q0, d2, m2, o + 16 * blk + 0);
-    dequant4<3>(q1, d2, m2, o + 16 * blk + 4);
-    dequant4<3>(q2, d2, m2, o + 16 * blk + 8);
-    dequant4<3>(q3, d2, m2, o + 16 * blk + 12);
-  }
+// Q4_1: the thread's block H (20 bytes at byte 20H of the 80-byte row segment), read as
+// the two 16-byte words that cover it.
+template <int H>
+__device__ __forceinline__ void convert_q41(const uint8_t* row, uint32_t (&o)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(row) + H;
+  const uint4 a = p[0], b = p[1];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const __half2 dmh = u2h(w[H]);  // block H starts at word 5H = 4H + H
+  const __half2 d2 = __low2half2(dmh), m2 = __high2half2(dmh);
+  dequant4<3>(w[H + 1], d2, m2, o + 0);
+  dequant4<3>(w[H + 2], d2, m2, o + 4);
+  dequant4<3>(w[H + 3], d2, m2, o + 8);
+  dequant4<3>(w[H + 4], d2, m2, o + 12);
 }
 
-// Q4_0: two of the thread's four blocks (pair p of 2), 18 bytes each, from the 144-byte
-// row segment; the thread's blocks are 4h .. 4h + 3.
-template <int H>
-__device__ __forceinline__ void convert_q40_pair(const uint8_t* row, int p, uint32_t (&o)[32]) {
-  // blocks b0 = 4H + 2p and b0 + 1 span bytes [18 b0, 18 b0 + 36): load the covering uint4s
-  const int byte0 = 18 * (4 * H + 2 * p);
-  const int u0 = byte0 >> 4;
+// Q4_0: the thread's blocks 2P and 2P + 1 (18 bytes each) of the 144-byte row segment.
+template <int P>
+__device__ __forceinline__ void convert_q40(const uint8_t* row, uint32_t (&o)[32]) {
+  constexpr int byte0 = 36 * P;
+  constexpr int u0 = byte0 >> 4;
   const uint4* q = reinterpret_cast<const uint4*>(row) + u0;
   const uint4 a = q[0], b = q[1], c = q[2];
   const uint32_t w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
@@ -230,45 +221,61 @@ __device__ __forceinline__ void convert_q40_pair(const uint8_t* row, int p, uint
   }
 }
 
-// Router rows: 64 f32 values (values 64h .. 64h + 63 of the 128-value chunk) -> f16 hi
-// or lo parts in the permuted slot order.
-__device__ __forceinline__ void convert_f32(const uint8_t* row, int h, bool lo, uint32_t (&o)[32]) {
-  const float4* p = reinterpret_cast<const float4*>(row) + 16 * h;
+// Router rows: the 32 f32 values of sub-box H of a row (values 32H .. 32H + 31 of the
+// 128-value chunk; the sub-box is stored with the 128-byte swizzle: 16-byte chunk j of
+// row r sits at chunk j ^ (r & 7)) -> f16 hi or lo parts in the permuted slot order.
+__device__ __forceinline__ void convert_f32(const uint8_t* sub, int r, bool lo, uint32_t (&o)[16]) {
+  const uint8_t* rowp = sub + r * 128;
 #pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float4 x0 = p[8 * blk + w], x1 = p[8 * blk + 4 + w];
-      uint32_t* d = o + 16 * blk + 4 * w;
-      const uint32_t h0 = pack_h2(x0.x, x0.z), h1 = pack_h2(x0.y, x0.w);
-      const uint32_t h2 = pack_h2(x1.x, x1.z), h3 = pack_h2(x1.y, x1.w);
-      if (lo) {
-        d[0] = pack_lo(x0.x, x0.z, h0);
-        d[1] = pack_lo(x0.y, x0.w, h1);
-        d[2] = pack_lo(x1.x, x1.z, h2);
-        d[3] = pack_lo(x1.y, x1.w, h3);
-      } else {
-        d[0] = h0;
-        d[1] = h1;
-        d[2] = h2;
-        d[3] = h3;
-      }
+  for (int w = 0; w < 4; ++w) {
+    const float4 x0 = *reinterpret_cast<const float4*>(rowp + ((w ^ (r & 7)) << 4));
+    const float4 x1 = *reinterpret_cast<const float4*>(rowp + (((4 + w) ^ (r & 7)) << 4));
+    uint32_t* d = o + 4 * w;
+    const uint32_t h0 = pack_h2(x0.x, x0.z), h1 = pack_h2(x0.y, x0.w);
+    const uint32_t h2 = pack_h2(x1.x, x1.z), h3 = pack_h2(x1.y, x1.w);
+    if (lo) {
+      d[0] = pack_lo(x0.x, x0.z, h0);
+      d[1] = pack_lo(x0.y, x0.w, h1);
+      d[2] = pack_lo(x1.x, x1.z, h2);
+      d[3] = pack_lo(x1.y, x1.w, h3);
+    } else {
+      d[0] = h0;
+      d[1] = h1;
+      d[2] = h2;
+      d[3] = h3;
     }
   }
 }
 
+// ---- tensor maps of the weight matrices ------------------------------------------------------
+// The expert records are viewed as 2-D byte arrays: with rows of a gate/up row's bytes
+// (each record is 3F such rows: gate, up, then the down matrix) and with rows of a down
+// row's bytes (each record is 3H such rows, the down matrix from row 2H). The router is
+// an E x H f32 array read in 32-value sub-boxes with the 128-byte swizzle.
+struct TileMaps {
+  CUtensorMap gu, gu_s, dn, dn_s, rt;
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // ---- work units ----------------------------------------------------------------------------
 struct TileUnit {
-  const uint8_t* a0;   // raw row 0 of the tile (chunk 0)
-  uint32_t a_rs;       // bytes between consecutive rows (row pairs for gate/up)
-  uint32_t a_odd;      // gate/up: byte distance from a gate row to its up row
-  int mrows;           // valid raw rows
-  const uint8_t* b;    // token-operand image of the chunk (first 128-value block)
-  int nk;              // pipeline chunks
-  int n, npad, nb;     // chunk tokens, rounded to 16, operand rows (hi + lo: 2 npad)
-  int row0, prow, mt;  // chunk's first row, padded-row offset, M tile
-  bool shared;         // shared expert (token chunk)
-  int e0;              // router: first expert of the tile
+  const CUtensorMap* map;  // weight rows
+  int y0, y1;              // first map row of the tile (gate/up: gate rows, up rows)
+  const uint8_t* b;        // token-operand image of the chunk (first 128-value block)
+  int nk;                  // raw chunks (the last one may hold fewer than NAU A units)
+  int kdim;                // reduction length
+  int n, npad, nb;         // chunk tokens, rounded to 16, operand rows (hi + lo: 2 npad)
+  int row0, prow, mt;      // chunk's first row, padded-row offset, M tile
+  bool shared;             // shared expert (token chunk)
+  int e0;                  // router: first expert of the tile
 };
 
 template <int MODE, int QT>
@@ -283,7 +290,7 @@ __device__ __forceinline__ int tile_units(const PrefillArgs& a) {
 }
 
 template <int MODE, int QT>
-__device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, int u) {
+__device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, const TileMaps& maps, int u) {
   using G = Geo<MODE, QT>;
   TileUnit t;
   const int nkh = a.H / TP_KB;
@@ -291,17 +298,16 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, int u) {
     const int et = (a.E + 63) / 64;
     const int j = u / et, e = u % et;
     t.e0 = 64 * e;
-    t.a0 = reinterpret_cast<const uint8_t*>(a.router_w) + (size_t)t.e0 * a.H * 4;
-    t.a_rs = (uint32_t)a.H * 4;
-    t.a_odd = 0;
-    t.mrows = min(64, a.E - t.e0);
+    t.map = &maps.rt;
+    t.y0 = t.y1 = t.e0;
     t.row0 = j * PREFILL_TILE_NMAX;
     t.n = min(PREFILL_TILE_NMAX, a.T - t.row0);
     t.npad = (t.n + 15) & ~15;
     t.nb = 2 * t.npad;
     t.prow = t.row0;
     t.b = a.ximg + (size_t)2 * t.prow * nkh * 256;
-    t.nk = a.H / G::KC;
+    t.nk = (a.H + G::KR - 1) / G::KR;
+    t.kdim = a.H;
     t.mt = 0;
     t.shared = false;
     return t;
@@ -322,7 +328,7 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, int u) {
     const int v = u - nr * mt_r;
     const int j = v / mt_s;
     mt = v % mt_s;
-    slot = a.E;
+    slot = 0;
     t.row0 = j * PREFILL_TILE_NMAX;
     t.n = min(PREFILL_TILE_NMAX, a.T - t.row0);
     t.prow = t.row0;
@@ -332,48 +338,64 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, int u) {
   t.e0 = 0;
   t.npad = (t.n + 15) & ~15;
   const int ff = t.shared ? a.Fs : a.F;
-  const uint8_t* rec = t.shared ? a.shared : a.experts + (size_t)slot * a.rec_bytes;
   if (MODE == 0) {
+    t.map = t.shared ? &maps.gu_s : &maps.gu;
+    t.y0 = slot * 3 * ff + 64 * mt;  // gate rows
+    t.y1 = t.y0 + ff;                // up rows
     t.nb = 2 * t.npad;
-    t.a0 = rec + (size_t)(64 * mt) * a.rb_h;
-    t.a_rs = a.rb_h;
-    t.a_odd = (uint32_t)ff * a.rb_h;
-    t.mrows = 128;
-    t.nk = a.H / G::KC;
+    t.nk = (a.H + G::KR - 1) / G::KR;
+    t.kdim = a.H;
     const uint8_t* img = t.shared ? a.ximg : a.ximg_routed;
     t.b = img + (size_t)2 * t.prow * nkh * 256;
   } else {
-    const uint32_t rb = t.shared ? a.rb_fs : a.rb_f;
+    t.map = t.shared ? &maps.dn_s : &maps.dn;
+    t.y0 = t.y1 = slot * 3 * a.H + 2 * a.H + 128 * mt;
     t.nb = t.npad;
-    t.a0 = rec + (size_t)2 * ff * a.rb_h + (size_t)(128 * mt) * rb;
-    t.a_rs = rb;
-    t.a_odd = 0;
-    t.mrows = 128;
-    t.nk = ff / G::KC;
+    t.nk = (ff + G::KR - 1) / G::KR;
+    t.kdim = ff;
     const uint8_t* img = t.shared ? a.aimg_s : a.aimg;
     t.b = img + (size_t)t.prow * (ff / TP_KB) * 256;
   }
   return t;
 }
 
-// Byte address of raw row m (stage chunk kc) of a tile.
+// Independent accumulators of a tile: as many nb-column chains as fit in the tile's
+// accumulator columns (128; down tiles: 64 each of two), at most 4.
 template <int MODE>
-__device__ __forceinline__ const uint8_t* raw_src(const TileUnit& t, int m, int kc, int seg) {
-  if (MODE == 0) return t.a0 + (size_t)(m >> 1) * t.a_rs + ((m & 1) ? t.a_odd : 0u) + (size_t)kc * seg;
-  return t.a0 + (size_t)m * t.a_rs + (size_t)kc * seg;
+__device__ __forceinline__ int tile_chains(int nb) {
+  const int cols = MODE == 1 ? 64 : 128;
+  return nb * 4 <= cols ? 4 : (nb * 2 <= cols ? 2 : 1);
+}
+
+// Sum over the tile's chains of 8 accumulator columns starting at column c.
+template <int MODE>
+__device__ __forceinline__ void acc_ld8(uint32_t acc, int nb, int c, float (&v)[8]) {
+  const int nch = tile_chains<MODE>(nb);
+  uint32_t r[8];
+  tmem_ld8(acc + (uint32_t)c, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  for (int ch = 1; ch < nch; ++ch) {
+    tmem_ld8(acc + (uint32_t)(ch * nb + c), r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] += __uint_as_float(r[i]);
+  }
 }
 
 // ---- the persistent tile kernel -----------------------------------------------------------
 template <int MODE, int QT>
-__global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) {
+__global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, const __grid_constant__ TileMaps maps) {
   using G = Geo<MODE, QT>;
   extern __shared__ __align__(1024) uint8_t tsm_dyn[];
-  uint8_t* raw = tsm_dyn;                                   // [NSA][STAGE]
-  uint8_t* bring = tsm_dyn + G::NSA * G::STAGE;             // [NSB][B_STAGE]
-  float* scratch = reinterpret_cast<float*>(bring + TP_NSB * TP_B_STAGE);  // router only
+  // stages start on a 1024-byte boundary (the router's swizzled boxes need it)
+  uint8_t* raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tsm_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* bring = raw + G::NSA * G::STAGE;                                 // [NSB][B_STAGE]
+  float* scratch = reinterpret_cast<float*>(bring + G::NSB * TP_B_STAGE);  // gate/up and router epilogues
   __shared__ __align__(8) uint64_t raw_full[G::NSA], raw_empty[G::NSA];
-  __shared__ __align__(8) uint64_t a_full[2], a_empty[2], b_full[TP_NSB], b_empty[TP_NSB];
-  __shared__ __align__(8) uint64_t acc_full, acc_empty, fin, scr_full, scr_empty;
+  __shared__ __align__(8) uint64_t a_full[TP_GROUPS], a_empty[TP_GROUPS], b_full[G::NSB], b_empty[G::NSB];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin, scr_full, scr_empty;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   volatile int* abrt = &abort_flag;
@@ -382,21 +404,23 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) 
   if (tid == 0) {
     for (int i = 0; i < G::NSA; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], TP_CONV_WARPS);
+      mbar_init(&raw_empty[i], TP_CONV_WARPS);  // every converter warp releases every chunk
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], TP_CONV_WARPS);
+    for (int i = 0; i < TP_GROUPS; ++i) {
+      mbar_init(&a_full[i], 4);  // the group's four warps
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < TP_NSB; ++i) {
+    for (int i = 0; i < G::NSB; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, TP_CONV_WARPS);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], TP_EPI_WARPS);
+    }
     mbar_init(&fin, 1);
-    mbar_init(&scr_full, 4);   // router epilogue: the four warps of lanes 64..127
-    mbar_init(&scr_empty, 4);  // ... and the four warps of lanes 0..63
+    mbar_init(&scr_full, TP_EPI_WARPS / 2);   // epilogue warps of lanes 64..127
+    mbar_init(&scr_empty, TP_EPI_WARPS / 2);  // epilogue warps of lanes 0..63
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -408,87 +432,120 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) 
   const int units = tile_units<MODE, QT>(a);
 
   if (warp == 0) {
-    // ------------------------------ producer ------------------------------
+    // ------------------------------ weight producer ------------------------------
     // weight rows stream through L2 once; router rows are read by every token chunk
     const uint64_t pol_w = MODE == 2 ? policy_evict_last() : policy_evict_first();
-    uint32_t ra = 0, rb = 0;
+    uint32_t ka = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const TileUnit t = tile_unit<MODE, QT>(a, u);
-      const uint32_t bbytes = (uint32_t)t.nb * 256u;
-      for (int kc = 0; kc < t.nk && ok; ++kc) {
-        const int sa = (int)(ra % G::NSA);
-        if (ra >= (uint32_t)G::NSA && !tp_wait_warp(&raw_empty[sa], ((ra / G::NSA) - 1) & 1u, abrt)) {
+      const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
+      for (int kc = 0; kc < t.nk && ok; ++kc, ++ka) {
+        const int sa = (int)(ka % G::NSA);
+        if (ka >= (uint32_t)G::NSA && !tp_wait_warp(&raw_empty[sa], ((ka / G::NSA) - 1) & 1u, abrt)) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&raw_full[sa], (uint32_t)t.mrows * G::SEG);
-        __syncwarp();
-        for (int m = lane; m < t.mrows; m += 32)
-          bulk_g2s(raw + sa * G::STAGE + m * G::PITCH, raw_src<MODE>(t, m, kc, G::SEG), G::SEG, &raw_full[sa],
-                   pol_w);
-        ++ra;
-        for (int sub = 0; sub < G::NSUB; ++sub) {
-          const int sb = (int)(rb % TP_NSB);
-          if (rb >= (uint32_t)TP_NSB && !tp_wait_warp(&b_empty[sb], ((rb / TP_NSB) - 1) & 1u, abrt)) {
-            ok = false;
-            break;
+        if (lane == 0) {
+          uint8_t* dst = raw + sa * G::STAGE;
+          mbar_arrive_expect_tx(&raw_full[sa], (uint32_t)G::STAGE);
+          if (MODE == 2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(dst + j * 8192, t.map, kc * 128 + 32 * j, t.y0, &raw_full[sa], pol_w);
+          } else if (MODE == 0) {
+            tma_load_2d(dst, t.map, kc * G::SEG, t.y0, &raw_full[sa], pol_w);
+            tma_load_2d(dst + 64 * G::SEG, t.map, kc * G::SEG, t.y1, &raw_full[sa], pol_w);
+          } else {
+            tma_load_2d(dst, t.map, kc * G::SEG, t.y0, &raw_full[sa], pol_w);
           }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&b_full[sb], bbytes);
-            const uint8_t* src = t.b + (size_t)(kc * G::NSUB + sub) * bbytes;
-            asm volatile(
-                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_addr(bring + sb * TP_B_STAGE)),
-                "l"(src), "r"(bbytes), "r"(smem_addr(&b_full[sb]))
-                : "memory");
-          }
-          __syncwarp();
-          ++rb;
         }
+        __syncwarp();
       }
     }
+    // every copy this warp issued has landed before the CTA may exit (this matters only
+    // when a timed-out wait stopped the consumers early)
+    if (lane == 0) {
+      for (int sa = 0; sa < G::NSA; ++sa) {
+        const uint32_t f = ka > (uint32_t)sa ? (ka - sa - 1) / G::NSA + 1 : 0u;  // fills of this stage
+        if (f) mbar_wait(&raw_full[sa], (f - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------ token-operand producer ------------------------------
+    uint32_t rb = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
+      const uint32_t bbytes = (uint32_t)t.nb * 256u;
+      for (int kk = 0; kk < t.kdim / TP_KB; ++kk) {  // one stage per 128-value A unit
+        const int sb = (int)(rb % G::NSB);
+        if (rb >= (uint32_t)G::NSB && !tp_wait_warp(&b_empty[sb], ((rb / G::NSB) - 1) & 1u, abrt)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&b_full[sb], bbytes);
+          const uint8_t* src = t.b + (size_t)kk * bbytes;
+          asm volatile(
+              "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  smem_addr(bring + sb * TP_B_STAGE)),
+              "l"(src), "r"(bbytes), "r"(smem_addr(&b_full[sb]))
+              : "memory");
+        }
+        __syncwarp();
+        ++rb;
+      }
+    }
+    if (lane == 0) {
+      for (int sb = 0; sb < G::NSB; ++sb) {
+        const uint32_t f = rb > (uint32_t)sb ? (rb - sb - 1) / G::NSB + 1 : 0u;
+        if (f) mbar_wait(&b_full[sb], (f - 1) & 1u);
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      uint32_t ka = 0, rb = 0, uc = 0;
+      uint32_t n = 0, rb = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-        const TileUnit t = tile_unit<MODE, QT>(a, u);
+        const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
         const uint32_t idesc = idesc_f16_f32(128, t.nb);
-        if (uc > 0 && !tp_wait(&acc_empty, (uc - 1) & 1u, abrt)) {
+        const int nch = tile_chains<MODE>(t.nb);
+        const int ab = (int)(uc % G::NACC);
+        const uint32_t acc = tmem + 64u * ab;  // accumulator columns
+        if (uc >= (uint32_t)G::NACC && !tp_wait(&acc_empty[ab], ((uc / G::NACC) - 1) & 1u, abrt)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        for (int kc = 0; kc < t.nk && ok; ++kc) {
-          const int st = (int)(ka & 1u);
-          if (!tp_wait(&a_full[st], (ka >> 1) & 1u, abrt)) {
+        for (int kk = 0; kk < t.kdim / TP_KB && ok; ++kk, ++n) {  // A units in order
+          const int g = (int)(n % TP_GROUPS);  // A unit n was converted by group n % 4
+          if (!tp_wait(&a_full[g], (n / TP_GROUPS) & 1u, abrt)) {
+            ok = false;
+            break;
+          }
+          const int sb = (int)(rb % G::NSB);
+          if (!tp_wait(&b_full[sb], (rb / G::NSB) & 1u, abrt)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          for (int sub = 0; sub < G::NSUB; ++sub) {
-            const int sb = (int)(rb % TP_NSB);
-            if (!tp_wait(&b_full[sb], (rb / TP_NSB) & 1u, abrt)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint8_t* B = bring + sb * TP_B_STAGE;
+          const uint8_t* B = bring + sb * TP_B_STAGE;
+          const uint32_t ta0 = tmem + TP_A_COL + 64u * g;  // the group's A slot
 #pragma unroll
-            for (int j = 0; j < TP_KB / 16; ++j) {
-              const uint64_t bd = smem_desc(B + 2 * j * 16 * t.nb, 16u * t.nb, 128);
-              const uint32_t ta = tmem + TP_A_COL + (uint32_t)st * G::ACOLS + (uint32_t)(sub * 64 + 8 * j);
-              mma_f16_ta(tmem, ta, bd, idesc, (kc | sub | j) != 0);
-            }
-            mma_commit(&b_empty[sb]);
-            ++rb;
+          for (int j = 0; j < TP_KB / 16; ++j) {
+            // MMA j accumulates into chain j % nch: narrow tiles keep several independent
+            // accumulation chains in flight instead of one latency-bound chain
+            const int ch = j & (nch - 1);
+            const uint64_t bd = smem_desc(B + 2 * j * 16 * t.nb, 16u * t.nb, 128);
+            mma_f16_ta(acc + (uint32_t)(ch * t.nb), ta0 + 8u * j, bd, idesc, kk > 0 || j >= nch);
           }
-          mma_commit(&a_empty[st]);
-          ++ka;
+          mma_commit(&b_empty[sb]);
+          mma_commit(&a_empty[g]);
+          ++rb;
         }
-        if (ok) mma_commit(&acc_full);
+        if (ok) mma_commit(&acc_full[ab]);
       }
       // every MMA issued has completed before the columns are freed
       mma_commit(&fin);
@@ -497,78 +554,102 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) 
     __syncwarp();
   } else {
     // ------------------------------ converters + epilogue ------------------------------
-    const int q = warp & 3, h = (warp - 2) >> 2;
-    const int m = 32 * q + lane;  // TMEM lane = tile row
+    const int q = warp & 3, grp = (warp - 3) >> 2;  // lane quarter, converter group
+    const int m = 32 * q + lane;                     // TMEM lane = tile row
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    uint32_t ra = 0, ka = 0, uc = 0;
+    const int h = grp;                               // epilogue: groups 0 and 1 take half the columns each
+    const bool epi = grp < 2;
+    uint32_t ka = 0, n = 0, uc = 0;  // raw chunks, A units and tiles so far
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-      const TileUnit t = tile_unit<MODE, QT>(a, u);
-      for (int kc = 0; kc < t.nk; ++kc) {
-        const int sa = (int)(ra % G::NSA);
-        if (!tp_wait_warp(&raw_full[sa], (ra / G::NSA) & 1u, abrt)) {
+      const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
+      for (int kc = 0; kc < t.nk; ++kc, ++ka) {
+        // every warp waits for every chunk and releases it: a warp can then never release
+        // a stage's next use before its current one has landed
+        const int sa = (int)(ka % G::NSA);
+        if (!tp_wait_warp(&raw_full[sa], (ka / G::NSA) & 1u, abrt)) {
           ok = false;
           break;
         }
-        const int st = (int)(ka & 1u);
-        if (ka >= 2 && !tp_wait_warp(&a_empty[st], ((ka >> 1) - 1) & 1u, abrt)) {
-          ok = false;
-          break;
+        const uint8_t* stage = raw + sa * G::STAGE;
+        const int nau = min(G::NAU, (t.kdim - kc * G::KR) / TP_KB);
+        const uint32_t col = tmem + lane_addr + TP_A_COL + 64u * grp;  // the group's A slot
+        for (int j = 0; j < nau; ++j) {
+          const uint32_t nj = n + j;  // A unit nj goes to group nj % 4
+          if ((int)(nj % TP_GROUPS) != grp) continue;
+          const uint32_t i = nj / TP_GROUPS;  // the group's own A unit count
+          if (i >= 1 && !tp_wait_warp(&a_empty[grp], (i - 1) & 1u, abrt)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if (MODE == 2) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              uint32_t o[16];
+              convert_f32(stage + jj * 8192, m & 63, m >= 64, o);
+              tmem_st16(col + 16u * jj, o);
+            }
+          } else if (QT == 3) {
+            const uint8_t* row = stage + m * G::SEG + 80 * j;  // blocks 4j .. 4j + 3
+            uint32_t o[16];
+            convert_q41<0>(row, o);
+            tmem_st16(col + 0u, o);
+            convert_q41<1>(row, o);
+            tmem_st16(col + 16u, o);
+            convert_q41<2>(row, o);
+            tmem_st16(col + 32u, o);
+            convert_q41<3>(row, o);
+            tmem_st16(col + 48u, o);
+          } else {
+            const uint8_t* row = stage + m * G::SEG;
+            uint32_t o[32];
+            if (j == 0) {
+              convert_q40<0>(row, o);
+              tmem_st32(col + 0u, o);
+              convert_q40<1>(row, o);
+              tmem_st32(col + 32u, o);
+            } else {
+              convert_q40<2>(row, o);
+              tmem_st32(col + 0u, o);
+              convert_q40<3>(row, o);
+              tmem_st32(col + 32u, o);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[grp]);
         }
-        tc_fence_after_sync();
-        const uint32_t col = TP_A_COL + (uint32_t)st * G::ACOLS;
-        if (MODE == 2) {
-          uint32_t o[32];
-          convert_f32(raw + sa * G::STAGE + (m & 63) * G::PITCH, h, m >= 64, o);
-          tmem_st32(tmem + lane_addr + col + 32u * h, o);
-        } else if (QT == 3) {
-          uint32_t o[32];
-          convert_q41(raw + sa * G::STAGE + m * G::PITCH, h, o);
-          tmem_st32(tmem + lane_addr + col + 32u * h, o);
-        } else {
-          uint32_t o[32];
-          const uint8_t* row = raw + sa * G::STAGE + m * G::PITCH;
-          if (h == 0) convert_q40_pair<0>(row, 0, o); else convert_q40_pair<1>(row, 0, o);
-          tmem_st32(tmem + lane_addr + col + 64u * h, o);
-          if (h == 0) convert_q40_pair<0>(row, 1, o); else convert_q40_pair<1>(row, 1, o);
-          tmem_st32(tmem + lane_addr + col + 64u * h + 32u, o);
-        }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        fence_proxy_async_smem();  // raw stage reads done before the next bulk copy into it
+        if (!ok) break;
+        n += nau;
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&raw_empty[sa]);
-          mbar_arrive(&a_full[st]);
-        }
-        ++ra;
-        ++ka;
+        if (lane == 0) mbar_arrive(&raw_empty[sa]);
       }
-      if (!ok) break;
-      // ---- epilogue ----
-      if (!tp_wait_warp(&acc_full, uc & 1u, abrt)) {
+      if (!ok || !epi) continue;
+      // ---- epilogue (warps h = 0, 1: half of the tile's columns each) ----
+      const int ab = (int)(uc % G::NACC);
+      const uint32_t acc = tmem + lane_addr + 64u * ab;
+      if (!tp_wait_warp(&acc_full[ab], (uc / G::NACC) & 1u, abrt)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int half = t.npad >> 1;  // columns per warp of a lane quarter (a multiple of 8)
+      const int half = t.npad >> 1;  // columns per warp (a multiple of 8)
       const int c_lo = h * half;
-      if (MODE == 2) {
-        // logit = (hi.x_hi + hi.x_lo) + (lo.x_hi + lo.x_lo): lanes 64..127 hand their sums
-        // over through shared memory
+      if (MODE == 2 || MODE == 0) {
+        // lanes 64..127 (router: lo rows; gate/up: up rows) hand their column sums over
         if (m >= 64) {
           if (uc > 0 && !tp_wait_warp(&scr_empty, (uc - 1) & 1u, abrt)) {
             ok = false;
             break;
           }
           for (int c0 = c_lo; c0 < c_lo + half; c0 += 8) {
-            uint32_t r0[8], r1[8];
-            tmem_ld8(tmem + lane_addr + (uint32_t)c0, r0);
-            tmem_ld8(tmem + lane_addr + (uint32_t)(t.npad + c0), r1);
-            tmem_ld_wait();
+            float v0[8], v1[8];
+            acc_ld8<MODE>(acc, t.nb, c0, v0);
+            acc_ld8<MODE>(acc, t.nb, t.npad + c0, v1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              scratch[(m - 64) * 65 + c0 + i] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
+            for (int i = 0; i < 8; ++i) scratch[(m - 64) * 65 + c0 + i] = v0[i] + v1[i];
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&scr_full);
@@ -577,55 +658,59 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) 
             ok = false;
             break;
           }
+          const int ff = t.shared ? a.Fs : a.F;
+          const int nkf = ff / TP_KB;
+          const int f0 = 64 * t.mt + 32 * q;  // the warp's 32 gate rows: one 32-value block
+          uint8_t* img = MODE == 0 ? (t.shared ? a.aimg_s : a.aimg) : nullptr;
+          uint8_t* ibase =
+              MODE == 0 ? img + ((size_t)t.prow * nkf + (size_t)(f0 / TP_KB) * t.npad) * 256 : nullptr;
+          const int kcore = ((f0 & (TP_KB - 1)) >> 3) + (lane & 3);  // piece written by lanes 0..3
           for (int c0 = c_lo; c0 < c_lo + half; c0 += 8) {
-            uint32_t r0[8], r1[8];
-            tmem_ld8(tmem + lane_addr + (uint32_t)c0, r0);
-            tmem_ld8(tmem + lane_addr + (uint32_t)(t.npad + c0), r1);
-            tmem_ld_wait();
+            float v0[8], v1[8];
+            acc_ld8<MODE>(acc, t.nb, c0, v0);
+            acc_ld8<MODE>(acc, t.nb, t.npad + c0, v1);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int c = c0 + i;
-              const float v = (__uint_as_float(r0[i]) + __uint_as_float(r1[i])) + scratch[m * 65 + c];
-              if (c < t.n && t.e0 + m < a.E) a.logits[(size_t)(t.row0 + c) * a.E + t.e0 + m] = v;
+              const float v = v0[i] + v1[i];
+              const float other = scratch[m * 65 + c];
+              if (MODE == 2) {
+                if (c < t.n && t.e0 + m < a.E) a.logits[(size_t)(t.row0 + c) * a.E + t.e0 + m] = v + other;
+              } else {
+                // act = silu(gate) * up for f = f0 + lane, gathered into the four 16-byte
+                // pieces of the block (slot 8w + k holds value 4w + {0,2,1,3}[k], +16 for k >= 4)
+                const float act = v / (1.f + expf(-v)) * other;
+                const uint32_t hv = (uint32_t)__half_as_ushort(__float2half_rn(act));
+                const int w = lane & 3;
+                uint32_t pk[4];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                  const int ka2 = 2 * k2, kb2 = 2 * k2 + 1;
+                  const int ea = (ka2 < 4 ? 0 : 16) + 4 * w + ((ka2 & 3) == 1 ? 2 : ((ka2 & 3) == 2 ? 1 : (ka2 & 3)));
+                  const int eb = (kb2 < 4 ? 0 : 16) + 4 * w + ((kb2 & 3) == 1 ? 2 : ((kb2 & 3) == 2 ? 1 : (kb2 & 3)));
+                  const uint32_t va = __shfl_sync(0xffffffffu, hv, ea);
+                  const uint32_t vb = __shfl_sync(0xffffffffu, hv, eb);
+                  pk[k2] = va | (vb << 16);
+                }
+                if (lane < 4 && c < t.n)
+                  *reinterpret_cast<uint4*>(ibase + (kcore * (t.npad >> 3) + (c >> 3)) * 128 + (c & 7) * 16) =
+                      make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&scr_empty);
         }
-      } else if (MODE == 0) {
-        const int ff = t.shared ? a.Fs : a.F;
-        const int f = 64 * t.mt + (m >> 1);
-        const int nkf = ff / TP_KB;
-        uint8_t* img = t.shared ? a.aimg_s : a.aimg;
-        uint8_t* base = img + ((size_t)t.prow * nkf + (size_t)(f / TP_KB) * t.npad) * 256;
-        const int s = kslot_dev(f & 31) + (f & (TP_KB - 1) & ~31);
-        for (int c0 = c_lo; c0 < c_lo + half; c0 += 8) {
-          uint32_t r0[8], r1[8];
-          tmem_ld8(tmem + lane_addr + (uint32_t)c0, r0);
-          tmem_ld8(tmem + lane_addr + (uint32_t)(t.npad + c0), r1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float v = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);  // x_hi + x_lo parts
-            const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-            const int c = c0 + i;
-            if (!(m & 1) && c < t.n) {
-              const float act = v / (1.f + expf(-v)) * other;  // silu(gate) * up
-              *reinterpret_cast<__half*>(base + img_off(c, s, t.npad)) = __float2half_rn(act);
-            }
-          }
-        }
       } else {
         const int hrow = 128 * t.mt + m;
         for (int c0 = c_lo; c0 < c_lo + half; c0 += 8) {
-          uint32_t r0[8];
-          tmem_ld8(tmem + lane_addr + (uint32_t)c0, r0);
-          tmem_ld_wait();
+          float v0[8];
+          acc_ld8<MODE>(acc, t.nb, c0, v0);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int c = c0 + i;
             if (c < t.n) {
-              const float y = __uint_as_float(r0[i]);
+              const float y = v0[i];
               if (t.shared) a.sbuf[(size_t)(t.row0 + c) * a.H + hrow] = y;
               else a.ybuf[(size_t)(t.row0 + c) * a.H + hrow] = a.wsorted[t.row0 + c] * y;
             }
@@ -634,7 +719,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) 
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
   __syncthreads();
@@ -646,10 +731,12 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a) 
 }
 
 // ---- token-operand images ------------------------------------------------------------------
-// x rows of each chunk as f16 hi and lo parts, tiled as the MMA's B operand. Block c of the
-// grid takes chunk c (token chunks, or routed chunks when `routed`).
+// x rows of each chunk as f16 hi and lo parts, tiled as the MMA's B operand. Grid (chunk,
+// row group): warp w of block (c, y) writes row 8y + w of chunk c (token chunks, or routed
+// chunks when `routed`), 8 K values a lane per step.
 __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int routed) {
-  const int c = blockIdx.x;
+  const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = 8 * blockIdx.y + warp;
   int n, row0, prow;
   uint8_t* base;
   const int nkh = a.H / TP_KB;
@@ -667,16 +754,18 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
     prow = row0;
     base = a.ximg;
   }
+  if (r >= n) return;
   const int npad = (n + 15) & ~15, nb = 2 * npad;
   base += (size_t)2 * prow * nkh * 256;
-  const int pieces = a.H / 8;
-  for (int i = threadIdx.x; i < n * pieces; i += blockDim.x) {
-    const int r = i / pieces, p = i % pieces;
-    const int tok = routed ? (int)(a.perm[row0 + r] / (uint32_t)a.K) : row0 + r;
+  const int tok = routed ? (int)(a.perm[row0 + r] / (uint32_t)a.K) : row0 + r;
+  const float* xrow = a.x + (size_t)tok * a.H;
+  const int rl = npad + r;
+  const uint32_t hi_off = (uint32_t)((r >> 3) * 128 + (r & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
+  for (int p = lane; p < a.H / 8; p += 32) {
     const int kk = p >> 4, kc8 = p & 15;
     const int g = kk * TP_KB + 8 * kc8;  // first slot of the piece
     const int b = g >> 5, w = (g & 31) >> 3;
-    const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)tok * a.H + 32 * b);
+    const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * b);
     const float4 x0 = __ldg(xr + w), x1 = __ldg(xr + 4 + w);
     uint4 hi, lo;
     hi.x = pack_h2(x0.x, x0.z);
@@ -687,26 +776,78 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
     lo.y = pack_lo(x0.y, x0.w, hi.y);
     lo.z = pack_lo(x1.x, x1.z, hi.z);
     lo.w = pack_lo(x1.y, x1.w, hi.w);
-    uint8_t* blk = base + (size_t)kk * nb * 256;
-    *reinterpret_cast<uint4*>(blk + ((kc8 * (nb >> 3) + (r >> 3)) * 128 + (r & 7) * 16)) = hi;
-    const int rl = npad + r;
-    *reinterpret_cast<uint4*>(blk + ((kc8 * (nb >> 3) + (rl >> 3)) * 128 + (rl & 7) * 16)) = lo;
+    uint8_t* blk = base + (size_t)kk * nb * 256 + (size_t)kc8 * (nb >> 3) * 128;
+    *reinterpret_cast<uint4*>(blk + hi_off) = hi;
+    *reinterpret_cast<uint4*>(blk + lo_off) = lo;
   }
 }
 
+// ---- host side -----------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over `rows` rows of `row_bytes` bytes (u8 elements) or f32 elements.
+cudaError_t encode_2d(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t rows, uint32_t box_x,
+                      uint32_t box_y, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * (f32 ? 4 : 1)};
+  const cuuint32_t box[2] = {box_x, box_y};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int MODE, int QT>
-cudaError_t launch_tile(const PrefillArgs& a, cudaStream_t st) {
+cudaError_t launch_tile(const PrefillArgs& a, const TileMaps& maps, cudaStream_t st) {
   using G = Geo<MODE, QT>;
   auto kern = tile_gemm<MODE, QT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+  const int smem = G::SMEM + 1024;  // + alignment slack
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<a.nc, TP_THREADS, G::SMEM, st>>>(a);
+  kern<<<a.nc, TP_THREADS, smem, st>>>(a, maps);
   return cudaGetLastError();
+}
+
+cudaError_t make_maps(const PrefillArgs& a, TileMaps* m) {
+  std::memset(m, 0, sizeof *m);
+  const uint32_t seg = a.qtype == 3 ? Geo<0, 3>::SEG : Geo<0, 2>::SEG;
+  cudaError_t e;
+  if ((e = encode_2d(&m->gu, a.experts, false, a.rb_h, (uint64_t)a.E * 3 * a.F, seg, 64, false)) != cudaSuccess)
+    return e;
+  if ((e = encode_2d(&m->dn, a.experts, false, a.rb_f, (uint64_t)a.E * 3 * a.H, seg, 128, false)) != cudaSuccess)
+    return e;
+  if (a.Fs) {
+    if ((e = encode_2d(&m->gu_s, a.shared, false, a.rb_h, (uint64_t)3 * a.Fs, seg, 64, false)) != cudaSuccess)
+      return e;
+    if ((e = encode_2d(&m->dn_s, a.shared, false, a.rb_fs, (uint64_t)3 * a.H, seg, 128, false)) != cudaSuccess)
+      return e;
+  }
+  return encode_2d(&m->rt, a.router_w, true, (uint64_t)a.H, (uint64_t)a.E, 32, 64, true);
 }
 
 }  // namespace
 
-cudaError_t tile_router_launch(const PrefillArgs& a, cudaStream_t st) { return launch_tile<2, 3>(a, st); }
+cudaError_t tile_router_launch(const PrefillArgs& a, cudaStream_t st) {
+  TileMaps maps;
+  cudaError_t e = make_maps(a, &maps);
+  if (e != cudaSuccess) return e;
+  return launch_tile<2, 3>(a, maps, st);
+}
 
 cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t st) {
   int grid;
@@ -716,13 +857,16 @@ cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t s
   } else {
     grid = (a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX;
   }
-  tile_images<<<grid, 256, 0, st>>>(a, routed ? 1 : 0);
+  tile_images<<<dim3(grid, PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
   return cudaGetLastError();
 }
 
 cudaError_t tile_gemm_launch(const PrefillArgs& a, int mode, cudaStream_t st) {
-  if (mode == 0) return a.qtype == 3 ? launch_tile<0, 3>(a, st) : launch_tile<0, 2>(a, st);
-  return a.qtype == 3 ? launch_tile<1, 3>(a, st) : launch_tile<1, 2>(a, st);
+  TileMaps maps;
+  cudaError_t e = make_maps(a, &maps);
+  if (e != cudaSuccess) return e;
+  if (mode == 0) return a.qtype == 3 ? launch_tile<0, 3>(a, maps, st) : launch_tile<0, 2>(a, maps, st);
+  return a.qtype == 3 ? launch_tile<1, 3>(a, maps, st) : launch_tile<1, 2>(a, maps, st);
 }
 
 }  // namespace moe
