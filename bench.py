@@ -47,6 +47,34 @@ def layer_bytes(w):
     return router + K * rec(F) + (rec(Fs) if Fs else 0) + 2 * H * 4
 
 
+# Sources of each profiled kernel: a committed capture's counters are used only while
+# these files hash to what they were when it was taken.
+KERNEL_SOURCES = {
+    "moe_decode_kernel": ["decode.cu", "decode_host.h", "common.cuh", "plan.h", "select.cuh"],
+    "tile_gemm": ["prefill_tc.cu", "prefill.cu", "prefill_host.h", "common.cuh", "plan.h", "tc.cuh", "select.cuh"],
+}
+
+
+def source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "expert_ffn_decode_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def profile_counters(stem, kernel):
+    """Counters of the committed ncu capture profiles/<stem>.json, or None when the kernel's
+    sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", stem + ".json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d if d.get("source_sha256") == source_hash(kernel) else None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -453,12 +481,16 @@ def main():
     peak, peak_kind = measured_peaks()
     if pre is not None:
         a = pre["bytes_per_step"] / (pre["ms_per_step"] * 1e-3) / 1e9
+        pp = profile_counters("tile_gemm_flint_prefill_t512", "tile_gemm")
         pre["roofline"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s",
-                           "frac": round(a / peak, 4), "peak_kind": peak_kind, "over": "the whole batched step"}
+                           "frac": round(a / peak, 4), "peak_kind": peak_kind, "over": "the whole batched step",
+                           "traffic": pp["dram_bytes_per_step"] if pp else None,
+                           "tensor_pipe_active": pp["tensor_pipe_active"] if pp else None}
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+    prof = profile_counters(f"moe_decode_kernel_{args.workload}", "moe_decode_kernel")
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
-            "kernel": "moe_decode_kernel", "bytes_per_launch": step_bytes}
+            "frac": round(achieved / peak, 4), "traffic": prof["dram_bytes_per_launch"] if prof else None,
+            "peak_kind": peak_kind, "kernel": "moe_decode_kernel", "bytes_per_launch": step_bytes}
     cpu = None
     if not args.no_cpu_baseline:
         d, err = cpu_baseline(args.workload)
@@ -516,6 +548,7 @@ def main_prefill(args, ffn, synth, dev, rank, world, local):
     peak, peak_kind = measured_peaks()
     a = pre["bytes_per_step"] / (ms * 1e-3) / 1e9
     T = w["n_tokens"]
+    pp = profile_counters(f"tile_gemm_{args.workload}", "tile_gemm")
     cpu = None
     if not args.no_cpu_baseline:
         d, err = cpu_baseline(args.workload, max_tokens=64)
@@ -533,8 +566,9 @@ def main_prefill(args, ffn, synth, dev, rank, world, local):
                    "layers_rotated": pre["layers_rotated"],
                    "l2": "inputs larger than L2: every step reads over 400 MB of weights"},
         "roofline": {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s", "frac": round(a / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind, "over": "the whole batched step",
-                     "bytes_per_launch": pre["bytes_per_step"]},
+                     "traffic": pp["dram_bytes_per_step"] if pp else None, "peak_kind": peak_kind,
+                     "over": "the whole batched step", "bytes_per_launch": pre["bytes_per_step"],
+                     "tensor_pipe_active": pp["tensor_pipe_active"] if pp else None},
         "cpu_baseline": cpu,
         "e2e": {"value": pre["e2e"], "unit": UNIT, "h2d_bytes_per_step": pre["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": pre["d2h_bytes_per_step"], "steps": pre["e2e_steps"]},

@@ -102,6 +102,26 @@ typedef struct moe_cfg {
   uint32_t flags;      /* MOE_* flags above */
 } moe_cfg;
 
+/* Two execution paths, chosen by n_tokens (both are exact restatements of the step
+ * above; they differ in arithmetic only):
+ *   n_tokens < 8   one fused persistent kernel per token. The router is an f32 dot;
+ *                  the 4-bit blocks meet activations held in 22-bit block fixed point,
+ *                  so each block dot is an exact int32 sum (dp4a), scaled and
+ *                  accumulated in f32.
+ *   n_tokens >= 8  the batched path, in passes of at most 512 tokens. An f32 router
+ *                  contraction; one warp per token for the selection; a stable
+ *                  counting sort of the (token, pick) pairs by expert; grouped
+ *                  contractions on the tensor cores. The blocks are dequantised
+ *                  exactly to f16 before a single rounding. x enters as an f16 hi + lo
+ *                  pair (22 bits). The SwiGLU activations are rounded once to f16.
+ *                  Products accumulate in f32. Requires |x| and every activation to
+ *                  stay below 65504 (the f16 range).
+ *   Layers whose hidden, expert_ff and shared_ff are whole multiples of 128 (Q4_1) or
+ *   256 (Q4_0) run the batched contractions as warp-specialised TMA/TMEM pipelines;
+ *   other shapes run a general form of the same contractions.
+ * Both paths give the same picks; outputs agree to the tolerance of their arithmetic
+ * (relative L2 well under 2e-3 against a float64 evaluation). */
+
 /* The step on the default stream with a library-owned workspace (one per
  * device, grown on demand, freed by moe_shutdown). Blocks until the step is
  * done and returns device-side errors directly. Pointer alignment: x, out,
