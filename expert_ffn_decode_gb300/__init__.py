@@ -146,10 +146,10 @@ def moe_trace_offset(cfg):
 
 
 # Names of the MOE_TRACE timeline points, in order.
-TRACE_POINTS = ("start", "prev_grid_done", "x_ready", "pre_routing_done", "logits_seen", "routed",
-                "gate_up_done", "act_seen", "down_done", "end", "producer_ready", "producer_routed",
-                "producer_done", "router_data", "router_done", "act_counted", "dn_first_data",
-                "dn_first_done")
+TRACE_POINTS = ("start", "prev_grid_done", "router_done", "x_ready", "shared_done", "logits_seen",
+                "keys_ready", "topk_done", "routed", "gate_up_done", "columns_done", "rows_seen", "end",
+                "producer_ready", "producer_routed", "producer_done", "prod_woke", "gu_data",
+                "land_gu0", "gu_last", "land_dn0", "land_gu1", "land_gu2", "land_gu3")
 TRACE_STRIDE = 24  # u64 words per CTA
 
 

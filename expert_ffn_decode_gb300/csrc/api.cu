@@ -79,8 +79,20 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
+  size_t ctrl, logits, act, ys, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
 };
+
+// SMs of the current device (the decode kernel runs one CTA per SM); without a
+// device, an upper bound for sizing.
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    sms = 256;
+  }
+  return sms;
+}
 
 // Tokens of one prefill pass for a call of T tokens (0: the call decodes token by token).
 int prefill_pass_tokens(int T) {
@@ -97,8 +109,10 @@ WsLayout ws_layout(const moe_cfg* c) {
   o += moe::CTRL_BYTES;
   L.logits = o;
   o = up256(o + (size_t)c->n_experts * 8);
-  L.act = o;
+  L.act = o;  // published SwiGLU values of every slot
   o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 8);
+  L.ys = o;   // published weighted down rows of every slot
+  o = up256(o + ((size_t)c->top_k + 1) * c->hidden * 8);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -113,12 +127,8 @@ WsLayout ws_layout(const moe_cfg* c) {
   }
   L.trace = 0;
   if (c->flags & MOE_TRACE) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 1024;  // no device: size for the largest part
     L.trace = o;
-    o = up256(o + (size_t)sms * 24 * 8);
+    o = up256(o + (size_t)device_sms() * 24 * 8);
   }
   L.prefill = 0;
   if (const int tp = prefill_pass_tokens(c->n_tokens)) {
@@ -163,31 +173,33 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.rb_f = (uint32_t)(p.F / 32) * p.blk;
   p.rb_fs = p.Fs ? (uint32_t)(p.Fs / 32) * p.blk : p.rb_f;
   p.rec_bytes = (uint64_t)3 * p.F * (p.H / 32) * p.blk;
-  p.gu_align = moe::align_rows(p.rb_h);
-  int a_f = moe::align_rows(p.rb_f), a_fs = moe::align_rows(p.rb_fs);
-  p.dn_align = a_f > a_fs ? a_f : a_fs;
-
   int sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  int maxb = 1;
+  int maxb = 1;  // blocks per lane of the longest row (gate/up: H values; down: F or Fs)
   for (int nb : {p.H / 32, p.F / 32, p.Fs / 32})
     if ((nb + 31) / 32 > maxb) maxb = (nb + 31) / 32;
 
-  // ring slots: big enough for a router row and one aligned run of gate/up pairs
+  // ring slots: big enough for a router row, one item of gate/up row pairs and one
+  // aligned run of down rows
+  const int a_f = moe::align_rows(p.rb_f), a_fs = moe::align_rows(p.rb_fs);
+  p.dn_align = a_f > a_fs ? a_f : a_fs;
   uint32_t slot = 16384;
+  if (2u * moe::ITEM_PAIRS * p.rb_h > slot) slot = 2u * moe::ITEM_PAIRS * p.rb_h;
   if ((uint32_t)p.H * 4u > slot) slot = (uint32_t)p.H * 4u;
-  if (2u * (uint32_t)p.gu_align * p.rb_h > slot) slot = 2u * (uint32_t)p.gu_align * p.rb_h;
+  const uint32_t rbmax = p.rb_f > p.rb_fs ? p.rb_f : p.rb_fs;
+  if ((uint32_t)p.dn_align * rbmax > slot) slot = (uint32_t)p.dn_align * rbmax;
   slot = (slot + 127) / 128 * 128;
   p.slot_bytes = slot;
-  p.gu_r = (int)(slot / (2u * p.rb_h)) / p.gu_align * p.gu_align;
+  p.dn_r = (int)(slot / p.rb_f) / p.dn_align * p.dn_align;
+  p.dn_rs = (int)(slot / p.rb_fs) / p.dn_align * p.dn_align;
   p.nc = sms;
-
-  // busiest CTA
-  p.max_dn_rows = 0;
+  p.ncol_r = p.K * (p.F / moe::COL_VALUES);
+  p.ncol = p.ncol_r + p.Fs / moe::COL_VALUES;
+  p.max_items = 1;
   for (int cta = 0; cta < p.nc; ++cta) {
-    const moe::CtaShare s = moe::cta_share(p, cta);
-    if (s.d_len > p.max_dn_rows) p.max_dn_rows = s.d_len;
+    const int n = moe::cta_share(p, cta).n_items;
+    if (n > p.max_items) p.max_items = n;
   }
   // one CTA per SM: as many ring slots as fit next to the rest (at most 16)
   const uint32_t budget = 220u * 1024u;
@@ -391,6 +403,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<uint64_t*>(wsb + W.logits);
   a.act = reinterpret_cast<uint64_t*>(wsb + W.act);
+  a.ys = reinterpret_cast<uint64_t*>(wsb + W.ys);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -507,11 +520,11 @@ int moe_shutdown(void) {
 // ---------------------------------------------------------------------------
 namespace {
 
-// Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits and the
-// activations of one token. It is device memory that exists from the moment the
+// Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits, the
+// SwiGLU values and the weighted down rows of one token. It is device memory that exists from the moment the
 // library's code is loaded on a device until the process exits; every call on
 // that device shares it.
-constexpr size_t NOALLOC_SCRATCH_BYTES = 256 * 1024;
+constexpr size_t NOALLOC_SCRATCH_BYTES = 1024 * 1024;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 // Device address of the scratch per device, looked up on the first call there.
@@ -582,6 +595,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<uint64_t*>(wsb + W.logits);
   a.act = reinterpret_cast<uint64_t*>(wsb + W.act);
+  a.ys = reinterpret_cast<uint64_t*>(wsb + W.ys);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;

@@ -19,8 +19,10 @@ enum CtrlWord : int {
   CTRL_LOGITS = 2,   // [2], [3]: CTAs whose router rows are written, by generation parity
   CTRL_ACT = 4,      // [4], [5]: CTAs whose gate/up rows are written, by generation parity
   CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
+  CTRL_SLOT = 16,    // [16, 82): per-slot arrival counters, 33 per generation parity
 };
-constexpr int CTRL_BYTES = 256;
+constexpr int CTRL_SLOTS = 33;  // at most 32 picks and the shared expert
+constexpr int CTRL_BYTES = 512;
 
 enum DevErr : uint32_t {
   DEV_ERR_POLL_TIMEOUT = 1u,   // other CTAs' results never arrived
@@ -49,8 +51,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// The expected-bytes arrival orders nothing of the issuing thread: the copy's own
+// completion is what signals the waiters, so the arrival is relaxed (a release would
+// first wait for the thread's earlier stores).
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;"
                ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -153,11 +158,13 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// One thread waits until *ctr >= target, bounded in time.
+// One thread waits until *ctr >= target, bounded in time. It sleeps briefly between
+// reads: many CTAs polling in a tight loop would load L2 for everyone else.
 __device__ __forceinline__ bool await_count(const uint32_t* ctr, uint32_t target) {
   if (ld_relaxed(ctr) >= target) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
+    __nanosleep(100);
     if (ld_relaxed(ctr) >= target) return true;
     if ((it & 15u) == 0 && globaltimer() - t0 > POLL_TIMEOUT_NS) return false;
   }

@@ -1,20 +1,23 @@
 // Fused single-token MoE-FFN step (decode, T = 1) for sm_103a.
 //
-// One persistent CTA per SM runs the whole step:
-//   router GEMV (F32 router rows, one row per item)          -> logits
-//   all CTAs' logits written (arrival counter); sigmoid, selection bias,
-//   (group) top-k and weight normalisation, computed by every CTA
-//   gate/up GEMV of every pick and of the shared expert, SwiGLU -> act
-//   all CTAs' act written (arrival counter); down GEMV of the output rows the
-//   CTA owns, for every slot; weighted combine                     -> out
+// One persistent CTA per SM runs the whole step. A slot is a pick of the token or
+// the shared expert; a slot with ff intermediate values has ff / 32 columns, dealt to
+// the CTAs in turn. Phases of a CTA:
+//   router rows (F32, one row per ring item)                    -> published logits
+//   x -> activation blocks
+//   its shared-expert columns (they need no routing): 32 gate and 32 up rows ->
+//   SwiGLU values, published; then its share of the shared expert's down rows over
+//   the whole published activation vector -> published output rows
+//   every CTA's logits seen; sigmoid, selection bias, (group) top-k and weight
+//   normalisation, computed by every CTA
+//   its routed columns, the same way, each down row weighted by its pick's weight
+//   every slot's output rows seen; out = their sum in a fixed slot order
 // Weights stream through a ring of shared-memory slots filled by 1-D bulk async
-// copies (cp.async.bulk, completion counted on mbarriers) issued by the lanes
-// of one producer warp; eleven consumer warps compute. Down rows bypass the ring: the
-// producer prefetches the CTA's down rows into L2 (the shared expert's at once,
-// the picks' as soon as they are known) and the consumers read them with plain
-// loads once the activations are complete. Routing-independent rows (router,
-// shared expert) are requested before the kernel waits on the previous grid
-// (programmatic dependent launch).
+// copies (cp.async.bulk, completion counted on mbarriers) issued by the lanes of one
+// producer warp; eleven consumer warps compute. Gate/up rows and down rows are both
+// contiguous runs of a record, so every byte arrives in whole-row copies.
+// Routing-independent rows (router, shared expert) are requested before the kernel
+// waits on the previous grid (programmatic dependent launch).
 //
 // Dequant-dot: a 4-bit block (ggml Q4_0/Q4_1, 32 values) times 32 activations.
 // Activations are held per 32-block as integers v = x * 2^k with |v| <= 2^22
@@ -34,12 +37,13 @@ namespace moe {
 
 constexpr int NCW = 11;              // consumer warps
 constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int NCT = NCW * 32;        // consumer threads
 constexpr int BAR_CONS = 1;          // named barrier: consumer warps only
 constexpr int MAX_SLOTS = 16;        // ring slots (one issuing producer lane each)
 
 // Shared-memory carve-up (byte offsets, computed identically on host and device).
 struct SmemLayout {
-  uint32_t ring, qplanes, qinfo, xf, probs, partial, keys, gscore, rids, rw, bars, misc, total;
+  uint32_t ring, xplanes, xinfo, aplanes, ainfo, probs, keys, gscore, rids, rw, items, bars, misc, total;
 };
 
 MOE_HD uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -49,18 +53,18 @@ MOE_HD SmemLayout smem_layout(const DecodePlan& p) {
   uint32_t o = 0;
   L.ring = o;
   o += (uint32_t)p.nslots * p.slot_bytes;
-  int nb_act = (p.K * p.F + p.Fs) / 32;
-  int nbq = nb_act > p.H / 32 ? nb_act : p.H / 32;
-  L.qplanes = o = align_up(o, 16);
-  o += (uint32_t)nbq * 96u;
-  L.qinfo = o = align_up(o, 16);
-  o += (uint32_t)nbq * 8u;
-  L.xf = o = align_up(o, 16);
-  o += (uint32_t)p.H * 4u;
+  const int nbx = p.H / 32;
+  const int nba = (p.F > p.Fs ? p.F : p.Fs) / 32;  // a slot's activation blocks
+  L.xplanes = o = align_up(o, 16);
+  o += (uint32_t)nbx * 96u;
+  L.xinfo = o = align_up(o, 16);
+  o += (uint32_t)nbx * 8u;
+  L.aplanes = o = align_up(o, 16);
+  o += (uint32_t)nba * 96u;
+  L.ainfo = o = align_up(o, 16);
+  o += (uint32_t)nba * 8u;
   L.probs = o = align_up(o, 16);
   o += (uint32_t)p.E * 4u;
-  L.partial = o = align_up(o, 16);
-  o += (uint32_t)(p.K + 1) * (uint32_t)p.max_dn_rows * 4u;
   L.keys = o = align_up(o, 16);
   o += (uint32_t)p.E * 4u;
   L.gscore = o = align_up(o, 16);
@@ -68,7 +72,9 @@ MOE_HD SmemLayout smem_layout(const DecodePlan& p) {
   L.rids = o = align_up(o, 16);
   o += 32u * 4u;
   L.rw = o;
-  o += 32u * 4u;
+  o += 33u * 4u;
+  L.items = o = align_up(o, 16);
+  o += (uint32_t)p.max_items * (uint32_t)sizeof(Item);
   L.bars = o = align_up(o, 8);
   o += (uint32_t)p.nslots * 16u + 8u;
   L.misc = o = align_up(o, 16);
@@ -88,9 +94,10 @@ MOE_HD SmemLayout smem_layout(const DecodePlan& p) {
 // P*32 + i) and info[b] = {2^-k, sum q_i}. A block whose values are all below
 // 2^-97 in magnitude is taken as zero. When `copy` is not null the f32 values are
 // stored there too. Every thread of a group runs the same number of rounds.
-// The source is either an f32 vector or published words of generation `gen`
-// (then every value is awaited; `ok` is cleared on a timeout).
-template <typename Src>
+// The source is an f32 vector in global memory, an f32 vector in shared memory
+// (kShared), or published words of generation `gen` (then every value is awaited;
+// `ok` is cleared on a timeout). Whole warps call it (the groups use shuffles).
+template <typename Src, bool kShared = false>
 __device__ __forceinline__ void quant_blocks(const Src* src, int nb, uint8_t* planes, float2* info,
                                              float* copy, int t, int nthreads, uint32_t gen, bool& ok) {
   for (int base = 0; base < 4 * nb; base += nthreads) {
@@ -100,7 +107,7 @@ __device__ __forceinline__ void quant_blocks(const Src* src, int nb, uint8_t* pl
     if (active) {
       if constexpr (sizeof(Src) == 4) {
         const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)b * 32 + qq * 8);
-        const float4 a = __ldcg(s4), c = __ldcg(s4 + 1);
+        const float4 a = kShared ? s4[0] : __ldcg(s4), c = kShared ? s4[1] : __ldcg(s4 + 1);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
       } else {
@@ -271,36 +278,36 @@ __device__ __forceinline__ void group_sum_n(float (&v)[N], int lpr) {
     for (int k = 0; k < N; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
   }
 }
-constexpr int ROWS_PER_STEP = 4;  // row steps a warp keeps in flight together
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
-
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 // Timeline points (MOE_TRACE): one u64 %globaltimer value each, per CTA.
 enum TracePoint : int {
-  TR_START = 0, TR_PDL_DONE, TR_X_READY, TR_PRE_DONE, TR_LOGITS, TR_ROUTED, TR_GU_DONE,
-  TR_ACT_READY, TR_DN_DONE, TR_END, TR_PRODUCER_READY, TR_PRODUCER_ROUTED, TR_PRODUCER_DONE,
-  TR_ROUTER_DATA, TR_ROUTER_DONE, TR_ACT_COUNTED, TR_POINTS = 24
+  TR_START = 0, TR_PDL_DONE, TR_ROUTER_DONE, TR_X_READY, TR_SHARED_DONE, TR_LOGITS, TR_KEYS, TR_TOPK,
+  TR_ROUTED, TR_GU_DONE, TR_COLS_DONE, TR_PARTIALS, TR_END, TR_PRODUCER_READY, TR_PRODUCER_ROUTED,
+  TR_PRODUCER_DONE, TR_ROUTER_DATA, TR_GU_DATA, TR_ACT_READY, TR_GU_LAST, TR_DN_DATA, TR_POINTS = 24
 };
 
+// MAXB: activation blocks per lane of a row (every row has at most 1024 * MAXB values).
 template <int QT, int MAXB>
 __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArgs args) {
   extern __shared__ __align__(128) uint8_t smem[];
   const DecodePlan& p = args.p;
   const SmemLayout L = smem_layout(p);
   uint8_t* ring = smem + L.ring;
-  uint8_t* qplanes = smem + L.qplanes;
-  float2* qinfo = reinterpret_cast<float2*>(smem + L.qinfo);
-  float* xf = reinterpret_cast<float*>(smem + L.xf);
+  uint8_t* xplanes = smem + L.xplanes;
+  float2* xinfo = reinterpret_cast<float2*>(smem + L.xinfo);
+  uint8_t* aplanes = smem + L.aplanes;
+  float2* ainfo = reinterpret_cast<float2*>(smem + L.ainfo);
   float* probs = reinterpret_cast<float*>(smem + L.probs);
-  float* partial = reinterpret_cast<float*>(smem + L.partial);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + L.keys);
   float* gscore = reinterpret_cast<float*>(smem + L.gscore);
   int* rids = reinterpret_cast<int*>(smem + L.rids);
-  float* rw = reinterpret_cast<float*>(smem + L.rw);
+  float* rw = reinterpret_cast<float*>(smem + L.rw);  // [K] picks' weights, [K] = 1 (shared)
+  Item* items = reinterpret_cast<Item*>(smem + L.items);  // the CTA's ring items, in order
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + p.nslots;
   uint64_t* routed_bar = empty + p.nslots;  // one arrival: the picks are in shared memory
@@ -327,20 +334,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
     mbar_init(routed_bar, 1);
     fence_mbar_init();
     misc[0] = 0;
+    rw[p.K] = 1.f;  // the shared expert's weight
     for (int s = 0; s < MAX_SLOTS; ++s) s_armed[s] = 0;
   }
+  // the item list, computed once (the producer and every consumer warp read it)
+  for (int n = tid; n < cs.n_items; n += NTHREADS) items[n] = item_at(p, cs, c, n);
   __syncthreads();
   pdl_launch_dependents();
 
   // ======================= producer warp =======================
   // Lane s < nslots owns ring slot s and issues its items n = s, s + nslots, ...
   // in order (one issuing thread per slot: issue cost is per thread, so the
-  // slots fill in parallel). Lanes 16..31 prefetch the CTA's down rows into L2.
+  // slots fill in parallel).
   if (warp == NCW) {
     const uint64_t pol = policy_evict_first();
     trace(TR_PRODUCER_READY);
     auto issue = [&](int n) -> bool {
-      const Item it = item_at(p, cs, n);
+      const Item it = items[n];
       const int s = n % p.nslots, use = n / p.nslots;
       if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1))) return false;
       uint8_t* dst = ring + (size_t)s * p.slot_bytes;
@@ -350,21 +360,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
       } else {
         const uint8_t* base = it.slot < p.K ? args.experts + (size_t)rids[it.slot] * p.rec_bytes : args.shared;
         const int ff = slot_ff(p, it.slot);
-        const uint32_t half = it.bytes / 2;
-        bulk_g2s(dst, base + (size_t)it.row0 * p.rb_h, half, &full[s], pol);
-        bulk_g2s(dst + half, base + (size_t)(ff + it.row0) * p.rb_h, half, &full[s], pol);
+        if (it.kind == ITEM_GU) {
+          const uint32_t half = it.bytes / 2;
+          bulk_g2s(dst, base + (size_t)it.row0 * p.rb_h, half, &full[s], pol);
+          bulk_g2s(dst + half, base + (size_t)(ff + it.row0) * p.rb_h, half, &full[s], pol);
+        } else {
+          const uint8_t* dn = base + (size_t)2 * ff * p.rb_h;
+          bulk_g2s(dst, dn + (size_t)it.row0 * dn_row_bytes(p, it.slot), it.bytes, &full[s], pol);
+        }
       }
-      __threadfence_block();                   // the arrive above is visible before the count
-      armed[s] = (uint32_t)(use + 1);          // this slot's uses are armed in order
+      // Consumers wait for a use only once it is armed. Arming use u follows the
+      // producer's wait for the release of use u - 1, which every consumer warp gave
+      // after seeing use u - 1 land: a consumer that sees the count has seen the
+      // barrier pass the phase before u, so its parity wait for u cannot alias.
+      armed[s] = (uint32_t)(use + 1);
       return true;
-    };
-    // down rows [d_lo, d_lo + d_len) of slot s go to L2 ahead of their use
-    auto prefetch_down = [&](int s) {
-      const uint8_t* base = s < p.K ? args.experts + (size_t)rids[s] * p.rec_bytes : args.shared;
-      const uint32_t rb = dn_row_bytes(p, s);
-      if (cs.d_len > 0)
-        bulk_prefetch_l2(base + (size_t)2 * slot_ff(p, s) * p.rb_h + (size_t)cs.d_lo * rb,
-                         (uint32_t)cs.d_len * rb);
     };
     bool ok = true;
     if (lane < p.nslots) {
@@ -374,17 +384,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
           // the picks (valid ids even when routing failed) are in shared memory after this wait
           ok = mbar_wait(routed_bar, 0);
           routed = true;
-          trace(TR_PRODUCER_ROUTED);
+          if (args.trace && n == cs.n_pre) args.trace[(size_t)c * TR_POINTS + 16] = globaltimer();
           if (!ok) break;
         }
         ok = issue(n);
       }
-    } else if (lane >= 16) {
-      if (lane == 31 && p.Fs) prefetch_down(p.K);
-      if (lane - 16 < p.K) {
-        ok = mbar_wait(routed_bar, 0);
-        if (ok)
-          for (int j = lane - 16; j < p.K; j += 16) prefetch_down(j);
+    } else if (args.trace && lane >= 16 && lane < 21) {
+      // timeline only: when the first routed items land (observing a phase is harmless)
+      const int j = lane - 16, n = cs.n_pre + j;
+      const int pts[5] = {18, 21, 22, 23, 20};
+      if (n < cs.n_items) {
+        const int s = n % p.nslots, use = n / p.nslots;
+        const unsigned long long t0 = globaltimer();
+        while (armed[s] <= (uint32_t)use && globaltimer() - t0 < MBAR_TIMEOUT_NS) __nanosleep(32);
+        if (armed[s] > (uint32_t)use && mbar_wait(&full[s], use & 1u))
+          args.trace[(size_t)c * TR_POINTS + pts[j]] = globaltimer();
       }
     }
     if (!ok) atomicOr(args.ctrl + CTRL_STATUS, DEV_ERR_MBAR_TIMEOUT);
@@ -397,32 +411,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
   // path, so no copy is in flight when the CTA exits. Errors only skip results.
   const int H = p.H, K = p.K;
   const int nbH = H / 32;
-  const int NCT = NCW * 32;
 
   pdl_wait_prior_grids();  // x (and out, when accumulating) may come from the previous kernel
   trace(TR_PDL_DONE);
   if (tid == 0) misc[1] = ld_relaxed(args.ctrl + CTRL_GEN) + 1u;
-
-  // activation blocks of x -> shared planes, and an f32 copy for the router
-  bool err = false;  // this thread saw a timeout
-  {
-    bool ok = true;
-    quant_blocks(args.x, nbH, qplanes, qinfo, xf, tid, NCT, 0u, ok);
-  }
   named_bar_sync(BAR_CONS, NCT);
   const uint32_t gen = misc[1];
   uint32_t* ctr_logits = args.ctrl + CTRL_LOGITS + (gen & 1u);
-  uint32_t* ctr_act = args.ctrl + CTRL_ACT + (gen & 1u);
-  trace(TR_X_READY);
-
-  // this lane's x blocks for gate/up rows, kept in registers
-  const RowMap mh = row_map(nbH, lane);
-  ActBlock xc[MAXB];
-#pragma unroll
-  for (int i = 0; i < MAXB; ++i) {
-    int b = mh.sub + mh.lpr * i;
-    if (b < nbH) load_act_block(xc[i], qplanes, qinfo, b);
-  }
+  uint32_t* ctr_part = args.ctrl + CTRL_ACT + (gen & 1u);
+  uint32_t* ctr_slot = args.ctrl + CTRL_SLOT + (gen & 1u) * CTRL_SLOTS;  // columns published, per slot
+  bool err = false;  // this thread saw a timeout
 
   // Item n's copy is awaited only once its slot's use has been armed: then the
   // slot's full barrier is in the phase of this use (a parity wait cannot alias an
@@ -430,13 +428,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
   auto wait_full = [&](int n) -> bool {
     const int s = n % p.nslots;
     const uint32_t use = (uint32_t)(n / p.nslots);
+    // One lane per warp waits, sleeping briefly between reads (spinning warps would
+    // crowd the shared-memory pipe the producer's barrier and copy instructions use);
+    // then every lane takes the completed phase itself (an immediate try_wait).
     bool ok = true;
-    if (armed[s] <= use) {
+    if (lane == 0) {
       const unsigned long long t0 = globaltimer();
       uint32_t it = 0;
-      while (armed[s] <= use)
-        if ((++it & 63u) == 0 && globaltimer() - t0 > MBAR_TIMEOUT_NS) { ok = false; break; }
+      while (armed[s] <= use) {
+        __nanosleep(64);
+        if ((++it & 15u) == 0 && globaltimer() - t0 > MBAR_TIMEOUT_NS) { ok = false; break; }
+      }
+      if (ok) ok = mbar_wait(&full[s], use & 1u);
     }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) ok = mbar_wait(&full[s], use & 1u);
     if (!ok && lane == 0) atomicOr(args.ctrl + CTRL_STATUS, DEV_ERR_MBAR_TIMEOUT);
     return ok;
@@ -447,60 +452,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
   };
   auto slot_buf = [&](int n) -> const uint8_t* { return ring + (size_t)(n % p.nslots) * p.slot_bytes; };
 
-  // gate/up unit: pairs unit*rps + [0, rps) of an item of slot `slot` (its pairs
-  // [row0, row0 + m), gate rows then up rows in buf), one pair per lane group
-  auto do_gu_unit = [&](const Item& it, const uint8_t* buf, int unit) {
-    const int m = (int)it.nrows;
-    const int r = unit * mh.rps + mh.rsub;
-    float gu[2] = {0.f, 0.f};
-    if (r < m) {
-      const uint8_t* grow = buf + (size_t)r * p.rb_h;
-      const uint8_t* urow = buf + (size_t)(m + r) * p.rb_h;
-#pragma unroll
-      for (int i = 0; i < MAXB; ++i) {
-        const int b = mh.sub + mh.lpr * i;
-        if (b < nbH) {
-          gu[0] += block_dot<QT>(grow, b, xc[i]);
-          gu[1] += block_dot<QT>(urow, b, xc[i]);
-        }
-      }
-    }
-    group_sum_n(gu, mh.lpr);
-    uint64_t* dst = args.act + (it.slot < K ? it.slot * p.F : K * p.F);
-    if (r < m && mh.sub == 0) st_relaxed_u64(dst + it.row0 + r, tagged(gen, silu_mul(gu[0], gu[1])));
-  };
-
-  // router item: one row of H f32 values in buf, dot with the f32 copy of x
-  auto do_router = [&](const Item& it, const float* buf) {
-    float acc = 0.f;
-    for (int h = lane * 4; h < H; h += 128) {
-      float4 wv = *reinterpret_cast<const float4*>(buf + h);
-      float4 xv = *reinterpret_cast<const float4*>(xf + h);
-      acc = fmaf(wv.x, xv.x, acc);
-      acc = fmaf(wv.y, xv.y, acc);
-      acc = fmaf(wv.z, xv.z, acc);
-      acc = fmaf(wv.w, xv.w, acc);
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) st_relaxed_u64(args.logits + it.row0, tagged(gen, acc));
-  };
-
-  // Every warp walks the ring items [n0, n1) in order and releases each; the
-  // items' work units (a router row, or rps gate/up pairs) are dealt to the warps
-  // in turn across the walk, so every warp has work while the copies land.
-  auto walk_items = [&](int n0, int n1) {
-    int ucount = 0;
+  // Every warp walks the ring items [n0, n1) in order and releases each; an item's
+  // work units are dealt to the warps in turn across the walk, so every warp has
+  // work while the copies land. unit(it, buf, u) does unit u of item it.
+  int ucount = 0;
+  auto walk = [&](int n0, int n1, int per_unit, auto&& unit) {
     for (int n = n0; n < n1; ++n) {
-      const Item it = item_at(p, cs, n);
-      const int units = it.kind == ITEM_ROUTER ? 1 : ceil_div((int)it.nrows, mh.rps);
+      const Item it = items[n];
+      const int units = ceil_div((int)it.nrows, per_unit);
       const int first = ucount + (warp - ucount % NCW + NCW) % NCW;
+      // a warp with no unit in the item releases it at once: a warp with units
+      // releases only after the copy landed, so the slot is not refilled early
+      if (first >= ucount + units) {
+        release(n);
+        ucount += units;
+        continue;
+      }
       if (wait_full(n)) {
-        if (n == 0) trace(TR_ROUTER_DATA);
+        if (args.trace && lane == 0 && n == cs.n_pre) args.trace[(size_t)c * TR_POINTS + TR_GU_DATA] = globaltimer();
+        if (args.trace && lane == 0 && n == cs.n_pre + GU_ITEMS * cs.n_rc - 1)
+          args.trace[(size_t)c * TR_POINTS + TR_GU_LAST] = globaltimer();
+        if (args.trace && lane == 0 && n == cs.n_pre + GU_ITEMS * cs.n_rc)
+          args.trace[(size_t)c * TR_POINTS + TR_DN_DATA] = globaltimer();
         const uint8_t* buf = slot_buf(n);
-        for (int u = first; u < ucount + units; u += NCW) {
-          if (it.kind == ITEM_ROUTER) do_router(it, reinterpret_cast<const float*>(buf));
-          else do_gu_unit(it, buf, u - ucount);
-        }
+        for (int u = first; u < ucount + units; u += NCW) unit(it, buf, u - ucount);
       } else {
         err = true;
       }
@@ -509,183 +484,251 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
     }
   };
 
-  // ---- router rows: write the logits, then count this CTA in ----
-  walk_items(0, cs.n_r);
-  named_bar_sync(BAR_CONS, NCT);
-  trace(TR_ROUTER_DONE);
-  if (tid == 0) red_relaxed_add(ctr_logits, 1u);  // a hint: readers check each logit's generation
-  trace(TR_PRE_DONE);
-
-  // ---- routing: every CTA's logits are written; select ----
-  if (tid == 0 && !await_count(ctr_logits, (uint32_t)p.nc)) misc[0] = 1;
-  named_bar_sync(BAR_CONS, NCT);
-  trace(TR_LOGITS);
-  for (int e = tid; e < p.E; e += NCT) {
-    bool ok = true;
-    const float l = await_tagged(args.logits + e, ld_relaxed_u64(args.logits + e), gen, ok);
-    if (!ok) err = true;
-    const float pr = 1.f / (1.f + expf(-l));
-    probs[e] = pr;
-    keys[e] = order_key(pr + (args.bias ? __ldg(args.bias + e) : 0.f));
-  }
-  named_bar_sync(BAR_CONS, NCT);
-  if (p.G > 1) {
-    // group score: the two largest s of the group, summed (multiset top-2)
-    const int per = p.E / p.G;
-    for (int g = warp; g < p.G; g += NCW) {
-      float a = -INFINITY, bsec = -INFINITY;
-      for (int e = g * per + lane; e < (g + 1) * per; e += 32) {
-        uint32_t k = keys[e];
-        float v = __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-        if (v > a) { bsec = a; a = v; } else if (v > bsec) { bsec = v; }
+  // ---- router rows: x (f32, from global) . router row -> published logits ----
+  {
+    walk(0, cs.n_r, 1, [&](const Item& it, const uint8_t* buf, int) {
+      const float* row = reinterpret_cast<const float*>(buf);
+      float acc = 0.f;
+      for (int h = lane * 4; h < H; h += 128) {
+        const float4 wv = *reinterpret_cast<const float4*>(row + h);
+        const float4 xv = __ldcg(reinterpret_cast<const float4*>(args.x + h));
+        acc = fmaf(wv.x, xv.x, acc);
+        acc = fmaf(wv.y, xv.y, acc);
+        acc = fmaf(wv.z, xv.z, acc);
+        acc = fmaf(wv.w, xv.w, acc);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float oa = __shfl_xor_sync(0xffffffffu, a, o);
-        float ob = __shfl_xor_sync(0xffffffffu, bsec, o);
-        float hi = fmaxf(a, oa), lo = fminf(a, oa);
-        bsec = fmaxf(lo, fmaxf(bsec, ob));
-        a = hi;
-      }
-      if (lane == 0) gscore[g] = a + bsec;
-    }
+      acc = warp_sum(acc);
+      if (lane == 0) st_relaxed_u64(args.logits + it.row0, tagged(gen, acc));
+    });
     named_bar_sync(BAR_CONS, NCT);
+    trace(TR_ROUTER_DONE);
+    if (tid == 0) red_relaxed_add(ctr_logits, 1u);  // a hint: readers check each logit's generation
   }
-  if (warp == 0) {
-    // kept groups: groups_used rounds of the largest group score, lowest group on ties;
-    // experts of dropped groups get key 0 (below every real key)
-    if (p.G > 1) {
-      uint32_t keep_lo = 0, keep_hi = 0;  // groups 0..63
-      for (int j = 0; j < p.Gu; ++j) {
-        int best = -1;
-        float bv = 0.f;
-        for (int g = 0; g < p.G; ++g) {
-          bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
-          if (!kept && (best < 0 || gscore[g] > bv)) { best = g; bv = gscore[g]; }
-        }
-        if (best < 32) keep_lo |= 1u << best; else keep_hi |= 1u << (best - 32);
-      }
-      const int per = p.E / p.G;
-      for (int e = lane; e < p.E; e += 32) {
-        const int g = e / per;
-        const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
-        if (!kept) keys[e] = 0u;
-      }
-      __syncwarp();
-    }
-    // k rounds of the largest key, lowest index among equals (keys in registers)
-    if (p.E <= 256) topk_rounds<8>(keys, p.E, K, rids, lane);
-    else if (p.E <= 512) topk_rounds<16>(keys, p.E, K, rids, lane);
-    else topk_rounds<32>(keys, p.E, K, rids, lane);
-    // weights from the picked sigmoids
-    const float pj = lane < K ? probs[rids[lane]] : 0.f;
-    const float wsum = fmaxf(warp_sum(pj), args.norm_min);
-    if (lane < K) {
-      const float wj = pj / wsum * args.scale;
-      rw[lane] = wj;
-      if (c == 0) {
-        if (args.topk_ids) args.topk_ids[lane] = rids[lane];
-        if (args.topk_w) args.topk_w[lane] = wj;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(routed_bar);  // the producer may now fetch the picked experts
-  }
-  trace(TR_ROUTED);
 
-  // ---- gate/up items: the shared expert's (already in the ring), then the picks' ----
-  walk_items(cs.n_r, cs.n_items);
-  named_bar_sync(BAR_CONS, NCT);
-  trace(TR_GU_DONE);
-  if (tid == 0) {
-    red_relaxed_add(ctr_act, 1u);  // a hint: readers check each activation's generation
-    if (!await_count(ctr_act, (uint32_t)p.nc)) misc[0] = 1;
-  }
-  named_bar_sync(BAR_CONS, NCT);
-  trace(TR_ACT_COUNTED);
-
-  // ---- activations of every slot -> shared planes ----
+  // ---- x -> activation blocks ----
   {
     bool ok = true;
-    quant_blocks(args.act, (K * p.F + p.Fs) / 32, qplanes, qinfo, nullptr, tid, NCT, gen, ok);
-    if (!ok) err = true;
+    quant_blocks(args.x, nbH, xplanes, xinfo, nullptr, tid, NCT, 0u, ok);
   }
   named_bar_sync(BAR_CONS, NCT);
-  trace(TR_ACT_READY);
+  trace(TR_X_READY);
 
-  // ---- down rows, read through L2: partial[slot][row] = W_down[row] . act[slot] ----
-  // Tasks: for every slot (shared first), the CTA's output rows in runs of
-  // rps * ROWS_PER_STEP rows (one warp step each), dealt to the warps in turn.
-  {
-    const int nslot = K + (p.Fs ? 1 : 0);
-    int t_first = 0;  // index of the slot's first task in the deal
-    for (int si = 0; si < nslot; ++si) {
-      const int slot = p.Fs ? (si == 0 ? K : si - 1) : si;
-      const int nb = slot_ff(p, slot) / 32;
-      const RowMap mf = row_map(nb, lane);
-      const int run = mf.rps * ROWS_PER_STEP;
-      const int ntask = ceil_div(cs.d_len, run);
-      // this warp's tasks of the slot: t with (t_first + t) % NCW == warp
-      const int t0 = (warp - t_first % NCW + NCW) % NCW;
-      if (t0 < ntask) {
-        const int b0 = (slot < K ? slot * p.F : K * p.F) / 32;  // first act block of the slot
-        const uint32_t rb = dn_row_bytes(p, slot);
-        const uint8_t* base = slot < K ? args.experts + (size_t)rids[slot] * p.rec_bytes : args.shared;
-        const uint8_t* dn = base + (size_t)2 * slot_ff(p, slot) * p.rb_h;
-        ActBlock ac[MAXB];
+  // gate/up items [n0, n1): SwiGLU values of their pairs, published; then each of the
+  // ncols columns (columns col(i)) counts itself in its slot (a hint: readers still
+  // check every value's generation)
+  auto gate_up = [&](int n0, int n1, bool shared, int ncols) {
+    const RowMap mh = row_map(nbH, lane);
+    ActBlock xc[MAXB];
+#pragma unroll
+    for (int i = 0; i < MAXB; ++i) {
+      const int b = mh.sub + mh.lpr * i;
+      if (b < nbH) load_act_block(xc[i], xplanes, xinfo, b);
+    }
+    walk(n0, n1, mh.rps, [&](const Item& it, const uint8_t* buf, int u) {
+      const int r = u * mh.rps + mh.rsub;
+      float gu[2] = {0.f, 0.f};
+      if (r < ITEM_PAIRS) {
+        const uint8_t* grow = buf + (size_t)r * p.rb_h;
+        const uint8_t* urow = buf + (size_t)(ITEM_PAIRS + r) * p.rb_h;
 #pragma unroll
         for (int i = 0; i < MAXB; ++i) {
-          const int b = mf.sub + mf.lpr * i;
-          if (b < nb) load_act_block(ac[i], qplanes, qinfo, b0 + b);
-        }
-        float* part = partial + slot * p.max_dn_rows;
-        for (int t = t0; t < ntask; t += NCW) {
-          float y[ROWS_PER_STEP];
-#pragma unroll
-          for (int k = 0; k < ROWS_PER_STEP; ++k) {
-            const int r = t * run + k * mf.rps + mf.rsub;
-            y[k] = 0.f;
-            if (r < cs.d_len) {
-              const uint8_t* row = dn + (size_t)(cs.d_lo + r) * rb;
-#pragma unroll
-              for (int i = 0; i < MAXB; ++i) {
-                const int b = mf.sub + mf.lpr * i;
-                if (b < nb) y[k] += block_dot_g<QT>(row, b, ac[i]);
-              }
-            }
-          }
-          group_sum_n(y, mf.lpr);
-#pragma unroll
-          for (int k = 0; k < ROWS_PER_STEP; ++k) {
-            const int r = t * run + k * mf.rps + mf.rsub;
-            if (r < cs.d_len && mf.sub == 0) part[r] = y[k];
+          const int b = mh.sub + mh.lpr * i;
+          if (b < nbH) {
+            gu[0] += block_dot<QT>(grow, b, xc[i]);
+            gu[1] += block_dot<QT>(urow, b, xc[i]);
           }
         }
       }
-      t_first += ntask;
+      group_sum_n(gu, mh.lpr);
+      uint64_t* dst = args.act + (it.slot < K ? it.slot * p.F : K * p.F);
+      if (r < ITEM_PAIRS && mh.sub == 0) st_relaxed_u64(dst + it.row0 + r, tagged(gen, silu_mul(gu[0], gu[1])));
+    });
+    named_bar_sync(BAR_CONS, NCT);
+    if (tid < ncols) {
+      int slot, bc;
+      column_at(p, shared ? shared_column(p, cs, c, tid) : routed_column(p, c, tid), slot, bc);
+      red_relaxed_add(ctr_slot + slot, 1u);
     }
+  };
+
+  // down items [n0, n1) of the CTA's columns (shared or routed): per column, the
+  // slot's whole activation vector (every CTA of the slot has published its part)
+  // -> activation blocks, then its down rows -> weighted, published output rows
+  auto down = [&](bool shared, int ncols, int n0) {
+    int n = n0;
+    for (int i = 0; i < ncols; ++i) {
+      const int g = shared ? shared_column(p, cs, c, i) : routed_column(p, c, i);
+      int slot, bc;
+      column_at(p, g, slot, bc);
+      const int m = column_dn_items(p, slot, bc);
+      if (m == 0) continue;
+      const int ff = slot_ff(p, slot), nbF = ff / 32;
+      // every column of the slot has published its values
+      if (tid == 0 && !await_count(ctr_slot + slot, (uint32_t)slot_cols(p, slot))) misc[0] = 1;
+      named_bar_sync(BAR_CONS, NCT);
+      {
+        bool ok = true;
+        quant_blocks(args.act + (slot < K ? slot * p.F : K * p.F), nbF, aplanes, ainfo, nullptr, tid, NCT, gen, ok);
+        if (!ok) err = true;
+      }
+      named_bar_sync(BAR_CONS, NCT);
+      const RowMap mf = row_map(nbF, lane);
+      ActBlock ac[MAXB];
+#pragma unroll
+      for (int j = 0; j < MAXB; ++j) {
+        const int b = mf.sub + mf.lpr * j;
+        if (b < nbF) load_act_block(ac[j], aplanes, ainfo, b);
+      }
+      const float w = rw[slot];
+      const uint32_t rb = dn_row_bytes(p, slot);
+      uint64_t* ys = args.ys + (size_t)slot * H;
+      walk(n, n + m, mf.rps, [&](const Item& it, const uint8_t* buf, int u) {
+        const int r = u * mf.rps + mf.rsub;
+        float y = 0.f;
+        if (r < (int)it.nrows) {
+          const uint8_t* row = buf + (size_t)r * rb;
+#pragma unroll
+          for (int j = 0; j < MAXB; ++j) {
+            const int b = mf.sub + mf.lpr * j;
+            if (b < nbF) y += block_dot<QT>(row, b, ac[j]);
+          }
+        }
+        y = group_sum(y, mf.lpr);
+        if (r < (int)it.nrows && mf.sub == 0) st_relaxed_u64(ys + it.row0 + r, tagged(gen, w * y));
+      });
+      n += m;
+      named_bar_sync(BAR_CONS, NCT);  // the activation blocks are reused by the next column
+    }
+  };
+
+  // ---- two rounds of columns: the shared expert's (no routing needed), then, once the
+  // picks are made, the routed ones; one copy of the code serves both rounds ----
+  for (int round = 0; round < 2; ++round) {
+    const bool shared = round == 0;
+    const int ncols = shared ? cs.n_sc : cs.n_rc;
+    const int n_gu = shared ? cs.n_r : cs.n_pre;  // first gate/up item of the round
+    if (!shared) {
+      // ---- routing: every CTA's logits are written; select ----
+      if (tid == 0 && !await_count(ctr_logits, (uint32_t)p.nc)) misc[0] = 1;
+      named_bar_sync(BAR_CONS, NCT);
+      trace(TR_LOGITS);
+      for (int e = tid; e < p.E; e += NCT) {
+        bool ok = true;
+        const float l = await_tagged(args.logits + e, ld_relaxed_u64(args.logits + e), gen, ok);
+        if (!ok) err = true;
+        const float pr = 1.f / (1.f + expf(-l));
+        probs[e] = pr;
+        keys[e] = order_key(pr + (args.bias ? __ldg(args.bias + e) : 0.f));
+      }
+      named_bar_sync(BAR_CONS, NCT);
+      trace(TR_KEYS);
+      if (p.G > 1) {
+        // group score: the two largest s of the group, summed (multiset top-2)
+        const int per = p.E / p.G;
+        for (int g = warp; g < p.G; g += NCW) {
+          float a = -INFINITY, bsec = -INFINITY;
+          for (int e = g * per + lane; e < (g + 1) * per; e += 32) {
+            uint32_t k = keys[e];
+            float v = __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+            if (v > a) { bsec = a; a = v; } else if (v > bsec) { bsec = v; }
+          }
+    #pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            float oa = __shfl_xor_sync(0xffffffffu, a, o);
+            float ob = __shfl_xor_sync(0xffffffffu, bsec, o);
+            float hi = fmaxf(a, oa), lo = fminf(a, oa);
+            bsec = fmaxf(lo, fmaxf(bsec, ob));
+            a = hi;
+          }
+          if (lane == 0) gscore[g] = a + bsec;
+        }
+        named_bar_sync(BAR_CONS, NCT);
+      }
+      if (warp == 0) {
+        // kept groups: groups_used rounds of the largest group score, lowest group on ties;
+        // experts of dropped groups get key 0 (below every real key)
+        if (p.G > 1) {
+          uint32_t keep_lo = 0, keep_hi = 0;  // groups 0..63
+          for (int j = 0; j < p.Gu; ++j) {
+            int best = -1;
+            float bv = 0.f;
+            for (int g = 0; g < p.G; ++g) {
+              bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
+              if (!kept && (best < 0 || gscore[g] > bv)) { best = g; bv = gscore[g]; }
+            }
+            if (best < 32) keep_lo |= 1u << best; else keep_hi |= 1u << (best - 32);
+          }
+          const int per = p.E / p.G;
+          for (int e = lane; e < p.E; e += 32) {
+            const int g = e / per;
+            const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
+            if (!kept) keys[e] = 0u;
+          }
+          __syncwarp();
+        }
+        // k rounds of the largest key, lowest index among equals (keys in registers)
+        if (p.E <= 256) topk_rounds<8>(keys, p.E, K, rids, lane);
+        else if (p.E <= 512) topk_rounds<16>(keys, p.E, K, rids, lane);
+        else topk_rounds<32>(keys, p.E, K, rids, lane);
+        trace(TR_TOPK);
+        // weights from the picked sigmoids
+        const float pj = lane < K ? probs[rids[lane]] : 0.f;
+        const float wsum = fmaxf(warp_sum(pj), args.norm_min);
+        if (lane < K) {
+          const float wj = pj / wsum * args.scale;
+          rw[lane] = wj;
+          if (c == 0) {
+            if (args.topk_ids) args.topk_ids[lane] = rids[lane];
+            if (args.topk_w) args.topk_w[lane] = wj;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(routed_bar);  // the producer may now fetch the picked experts
+      }
+      named_bar_sync(BAR_CONS, NCT);  // the picks and weights are visible to every consumer
+      trace(TR_ROUTED);
+    }
+    gate_up(n_gu, n_gu + GU_ITEMS * ncols, shared, ncols);
+    trace(shared ? TR_SHARED_DONE : TR_GU_DONE);
+    down(shared, ncols, n_gu + GU_ITEMS * ncols);
+  }
+  trace(TR_COLS_DONE);
+  if (tid == 0) red_relaxed_add(ctr_part, 1u);  // a hint: readers check each value's generation
+
+  // ---- out[h] = sum over the slots of their weighted down rows, in slot order ----
+  if (tid == 0 && !await_count(ctr_part, (uint32_t)p.nc)) misc[0] = 1;
+  named_bar_sync(BAR_CONS, NCT);
+  trace(TR_PARTIALS);
+  const int nslot = K + (p.Fs ? 1 : 0);
+  for (int r = tid; r < cs.d_len; r += NCT) {
+    const int h = cs.d_lo + r;
+    constexpr int BATCH = 8;
+    float acc = 0.f;
+    for (int s0 = 0; s0 < nslot; s0 += BATCH) {
+      uint64_t v[BATCH];
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j)
+        v[j] = s0 + j < nslot ? __ldcg(reinterpret_cast<const unsigned long long*>(args.ys + (size_t)(s0 + j) * H + h))
+                              : 0ull;
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j) {
+        if (s0 + j < nslot) {
+          bool ok = true;
+          // slot order: the picks, then the shared expert (slot K)
+          acc += await_tagged(args.ys + (size_t)(s0 + j) * H + h, v[j], gen, ok);
+          if (!ok) err = true;
+        }
+      }
+    }
+    if (args.flags & FLAG_RESIDUAL) acc = __ldcg(args.x + h) + acc;
+    if (args.flags & FLAG_ACCUMULATE) acc = __ldcg(args.out + h) + acc;
+    if (!err) args.out[h] = acc;
   }
   if (err) misc[0] = 1;
   named_bar_sync(BAR_CONS, NCT);
-  trace(TR_DN_DONE);
-
-  // ---- combine: out[h] = sum_j w_j y_j[h] + shared[h] (+ x[h] | + out[h]) ----
-  if (misc[0] == 0) {
-    for (int r = tid; r < cs.d_len; r += NCT) {
-      float acc = 0.f;
-      for (int j = 0; j < K; ++j) acc = fmaf(rw[j], partial[j * p.max_dn_rows + r], acc);
-      if (p.Fs) acc += partial[K * p.max_dn_rows + r];
-      const int h = cs.d_lo + r;
-      if (args.flags & FLAG_RESIDUAL) acc = __ldcg(args.x + h) + acc;
-      if (args.flags & FLAG_ACCUMULATE) acc = __ldcg(args.out + h) + acc;
-      args.out[h] = acc;
-    }
-  } else if (tid == 0) {
-    atomicOr(args.ctrl + CTRL_STATUS, DEV_ERR_POLL_TIMEOUT);
-  }
+  if (misc[0] != 0 && tid == 0) atomicOr(args.ctrl + CTRL_STATUS, DEV_ERR_POLL_TIMEOUT);
 
   // ---- exit: the last CTA out prepares the next call's counters ----
-  named_bar_sync(BAR_CONS, NCT);
   trace(TR_END);
   if (tid == 0) {
     __threadfence();
@@ -694,6 +737,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_kernel(const DecodeArg
       args.ctrl[CTRL_EXIT] = 0;
       args.ctrl[CTRL_LOGITS + ((gen + 1u) & 1u)] = 0;
       args.ctrl[CTRL_ACT + ((gen + 1u) & 1u)] = 0;
+      for (int j = 0; j < CTRL_SLOTS; ++j) args.ctrl[CTRL_SLOT + ((gen + 1u) & 1u) * CTRL_SLOTS + j] = 0;
       args.ctrl[CTRL_GEN] = gen;
       __threadfence();
     }

@@ -29,8 +29,9 @@ def _built():
 
 def test_noalloc_rejects_layers_beyond_the_fixed_scratch():
     _built()
-    # 32 picks of F = 3072 need 786 KiB of activations: more than the 256 KiB scratch
-    cfg = ffn.make_cfg(hidden=2048, n_experts=64, top_k=32, expert_ff=3072, n_tokens=1)
+    # 32 picks of F = 3072 publish 768 KiB of SwiGLU values and 33 rows of H = 3072
+    # weighted outputs (792 KiB): more than the 1 MiB scratch
+    cfg = ffn.make_cfg(hidden=3072, n_experts=64, top_k=32, expert_ff=3072, n_tokens=1)
     rc = ffn.moe_ffn_forward_noalloc(1 << 24, 1 << 28, None, 1 << 30, None, cfg, 1 << 26)
     assert rc == ffn.MOE_ERR_UNSUPPORTED
     assert "scratch" in ffn.moe_last_error()
