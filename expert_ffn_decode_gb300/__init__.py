@@ -146,10 +146,9 @@ def moe_trace_offset(cfg):
 
 
 # Names of the MOE_TRACE timeline points, in order.
-TRACE_POINTS = ("start", "prev_grid_done", "router_done", "x_ready", "shared_done", "logits_seen",
-                "keys_ready", "topk_done", "routed", "gate_up_done", "columns_done", "rows_seen", "end",
-                "producer_ready", "producer_routed", "producer_done", "prod_woke", "gu_data",
-                "land_gu0", "gu_last", "land_dn0", "land_gu1", "land_gu2", "land_gu3")
+TRACE_POINTS = ("router_start", "router_x_ready", "router_done", "router_picked",
+                "gate_up_start", "gate_up_x_quantised", "gate_up_routed", "gate_up_end",
+                "down_start", "down_rows_requested", "down_act_ready", "down_end")
 TRACE_STRIDE = 24  # u64 words per CTA
 
 
@@ -158,7 +157,7 @@ def moe_workspace_status(workspace, stream=None):
 
 
 def moe_ffn_forward_noalloc(x, router_w, router_bias, expert_blocks, shared_blocks, cfg, out, stream=None):
-    """The step without any allocation (fixed 256 KiB device scratch; blocking)."""
+    """The step without any allocation (fixed 512 KiB device scratch; blocking)."""
     return lib().moe_ffn_forward_noalloc(_ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(expert_blocks),
                                          _ptr(shared_blocks), ctypes.byref(cfg), _ptr(out), _stream(stream))
 

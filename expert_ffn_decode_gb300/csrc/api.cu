@@ -79,10 +79,10 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, ys, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
+  size_t ctrl, logits, ids, wts, aplanes, ainfo, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
 };
 
-// SMs of the current device (the decode kernel runs one CTA per SM); without a
+// SMs of the current device (the timeline keeps one row per SM); without a
 // device, an upper bound for sizing.
 int device_sms() {
   int dev = 0, sms = 0;
@@ -107,12 +107,17 @@ WsLayout ws_layout(const moe_cfg* c) {
   size_t o = 0;
   L.ctrl = o;
   o += moe::CTRL_BYTES;
-  L.logits = o;
-  o = up256(o + (size_t)c->n_experts * 8);
-  L.act = o;  // published SwiGLU values of every slot
-  o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 8);
-  L.ys = o;   // published weighted down rows of every slot
-  o = up256(o + ((size_t)c->top_k + 1) * c->hidden * 8);
+  L.logits = o;  // decode: router logits [E] f32
+  o = up256(o + (size_t)c->n_experts * 4);
+  L.ids = o;     // decode: picks [K]
+  o = up256(o + (size_t)c->top_k * 4);
+  L.wts = o;     // decode: their weights [K]
+  o = up256(o + (size_t)c->top_k * 4);
+  const size_t nact = ((size_t)c->top_k * c->expert_ff + c->shared_ff) / 32;
+  L.aplanes = o;  // decode: activation blocks of every slot, byte planes [nact][96]
+  o = up256(o + nact * 96);
+  L.ainfo = o;    // decode: their {scale, integer sum} [nact]
+  o = up256(o + nact * 8);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -146,8 +151,8 @@ struct PlanEntry {
   int device;
   moe_cfg key;
   moe::DecodePlan plan;
-  uint32_t smem;
-  int maxb;
+  int maxb;  // blocks per lane of a gate/up row
+  int sms;   // SMs of the device
 };
 std::mutex g_mu;
 std::vector<PlanEntry> g_plans;
@@ -173,53 +178,21 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.rb_f = (uint32_t)(p.F / 32) * p.blk;
   p.rb_fs = p.Fs ? (uint32_t)(p.Fs / 32) * p.blk : p.rb_f;
   p.rec_bytes = (uint64_t)3 * p.F * (p.H / 32) * p.blk;
+  p.nbH = p.H / 32;
+  p.nbF = p.F / 32;
+  p.nbFs = p.Fs / 32;
+  p.nact = p.nbFs + p.K * p.nbF;
+  // the down kernel stages the activation blocks in shared memory when they fit in
+  // 48 KiB (every warp of the CTA reads all of them)
+  p.act_smem = (size_t)p.nact * 104 <= 48 * 1024 ? 1 : 0;
   int sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  int maxb = 1;  // blocks per lane of the longest row (gate/up: H values; down: F or Fs)
-  for (int nb : {p.H / 32, p.F / 32, p.Fs / 32})
-    if ((nb + 31) / 32 > maxb) maxb = (nb + 31) / 32;
-
-  // ring slots: big enough for a router row, one item of gate/up row pairs and one
-  // aligned run of down rows
-  const int a_f = moe::align_rows(p.rb_f), a_fs = moe::align_rows(p.rb_fs);
-  p.dn_align = a_f > a_fs ? a_f : a_fs;
-  uint32_t slot = 16384;
-  if (2u * moe::ITEM_PAIRS * p.rb_h > slot) slot = 2u * moe::ITEM_PAIRS * p.rb_h;
-  if ((uint32_t)p.H * 4u > slot) slot = (uint32_t)p.H * 4u;
-  const uint32_t rbmax = p.rb_f > p.rb_fs ? p.rb_f : p.rb_fs;
-  if ((uint32_t)p.dn_align * rbmax > slot) slot = (uint32_t)p.dn_align * rbmax;
-  slot = (slot + 127) / 128 * 128;
-  p.slot_bytes = slot;
-  p.dn_r = (int)(slot / p.rb_f) / p.dn_align * p.dn_align;
-  p.dn_rs = (int)(slot / p.rb_fs) / p.dn_align * p.dn_align;
-  p.nc = sms;
-  p.ncol_r = p.K * (p.F / moe::COL_VALUES);
-  p.ncol = p.ncol_r + p.Fs / moe::COL_VALUES;
-  p.max_items = 1;
-  for (int cta = 0; cta < p.nc; ++cta) {
-    const int n = moe::cta_share(p, cta).n_items;
-    if (n > p.max_items) p.max_items = n;
-  }
-  // one CTA per SM: as many ring slots as fit next to the rest (at most 16)
-  const uint32_t budget = 220u * 1024u;
-  int nslots = 16;
-  uint32_t smem = 0;
-  for (; nslots >= 2; --nslots) {
-    p.nslots = nslots;
-    smem = moe::decode_smem_bytes(p);
-    if (smem <= budget) break;
-  }
-  if (nslots < 2) return fail(MOE_ERR_UNSUPPORTED, "layer too large for the decode kernel's shared memory");
-  int occ = 0;
-  e = moe::decode_occupancy(c->qtype, maxb, smem, &occ);
-  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-  if (occ < 1) return fail(MOE_ERR_UNSUPPORTED, "decode kernel does not fit on an SM (%u bytes shared)", smem);
   out->device = device;
   out->key = *c;
   out->plan = p;
-  out->smem = smem;
-  out->maxb = maxb;
+  out->maxb = (p.nbH + 31) / 32;
+  out->sms = sms;
   return MOE_OK;
 }
 
@@ -383,7 +356,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     pa.rb_f = pe.plan.rb_f;
     pa.rb_fs = pe.plan.rb_fs;
     pa.rec_bytes = pe.plan.rec_bytes;
-    pa.nc = pe.plan.nc;
+    pa.nc = pe.sms;
     for (int t0 = 0; t0 < T; t0 += tp) {
       pa.T = T - t0 < tp ? T - t0 : tp;
       pa.x = dx + (size_t)t0 * c->hidden;
@@ -401,9 +374,11 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.experts = static_cast<const uint8_t*>(experts);
   a.shared = static_cast<const uint8_t*>(shared);
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
-  a.logits = reinterpret_cast<uint64_t*>(wsb + W.logits);
-  a.act = reinterpret_cast<uint64_t*>(wsb + W.act);
-  a.ys = reinterpret_cast<uint64_t*>(wsb + W.ys);
+  a.logits = reinterpret_cast<float*>(wsb + W.logits);
+  a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
+  a.wts = reinterpret_cast<float*>(wsb + W.wts);
+  a.aplanes = wsb + W.aplanes;
+  a.ainfo = reinterpret_cast<float2*>(wsb + W.ainfo);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -415,7 +390,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     a.out = dout + (size_t)t * c->hidden;
     a.topk_ids = dids ? dids + (size_t)t * c->top_k : nullptr;
     a.topk_w = dw ? dw + (size_t)t * c->top_k : nullptr;
-    e = moe::decode_launch(a, c->qtype, pe.maxb, pe.smem, st, pdl);
+    e = moe::decode_launch(a, pe.maxb, st, pdl, pe.sms);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   if (host) {
@@ -521,10 +496,12 @@ int moe_shutdown(void) {
 namespace {
 
 // Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits, the
-// SwiGLU values and the weighted down rows of one token. It is device memory that exists from the moment the
+// picks and their weights, and the activation blocks of one token (at most
+// 327 KiB for the largest layer the checks admit: 32 picks of 3072 values plus a
+// shared expert of 3072). It is device memory that exists from the moment the
 // library's code is loaded on a device until the process exits; every call on
 // that device shares it.
-constexpr size_t NOALLOC_SCRATCH_BYTES = 1024 * 1024;
+constexpr size_t NOALLOC_SCRATCH_BYTES = 512 * 1024;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 // Device address of the scratch per device, looked up on the first call there.
@@ -571,7 +548,9 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     const char* oa = reinterpret_cast<const char*>(out);
     if (xa < oa + xbytes && oa < xa + xbytes) return fail(MOE_ERR_INVALID_CFG, "x and out overlap");
   }
-  const WsLayout W = ws_layout(c);
+  moe_cfg c1 = *c;  // the calls decode token by token: one token's scratch
+  c1.n_tokens = 1;
+  const WsLayout W = ws_layout(&c1);
   if (W.total > NOALLOC_SCRATCH_BYTES)
     return fail(MOE_ERR_UNSUPPORTED,
                 "this layer needs %zu bytes of scratch; the fixed scratch of moe_ffn_forward_noalloc holds %zu",
@@ -593,9 +572,11 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.experts = static_cast<const uint8_t*>(expert_blocks);
   a.shared = static_cast<const uint8_t*>(shared_blocks);
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
-  a.logits = reinterpret_cast<uint64_t*>(wsb + W.logits);
-  a.act = reinterpret_cast<uint64_t*>(wsb + W.act);
-  a.ys = reinterpret_cast<uint64_t*>(wsb + W.ys);
+  a.logits = reinterpret_cast<float*>(wsb + W.logits);
+  a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
+  a.wts = reinterpret_cast<float*>(wsb + W.wts);
+  a.aplanes = wsb + W.aplanes;
+  a.ainfo = reinterpret_cast<float2*>(wsb + W.ainfo);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -608,7 +589,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     a.out = out + (size_t)t * c->hidden;
     a.topk_ids = nullptr;
     a.topk_w = nullptr;
-    e = moe::decode_launch(a, c->qtype, pe.maxb, pe.smem, st, pdl);
+    e = moe::decode_launch(a, pe.maxb, st, pdl, 0);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   // wait, then read the status word; after a device-side timeout the control block

@@ -1,6 +1,6 @@
 // Small device helpers for sm_103a: mbarriers, 1-D bulk async copies,
-// programmatic-dependent-launch control, acquire/release counters, timers and
-// the integer dot products used by the 4-bit kernels. Every wait here is bounded.
+// programmatic-dependent-launch control, timers and the integer dot products used
+// by the 4-bit kernels. Every wait here is bounded.
 #pragma once
 
 #include <cstdint>
@@ -8,30 +8,22 @@
 
 namespace moe {
 
-// ---- control block (first 256 bytes of every workspace) ---------------------
-// Word layout. A workspace starts zeroed. A call with generation g counts
-// arrivals in the counters of parity g & 1; its last CTA out zeroes the exit
-// counter and the counters of parity (g + 1) & 1 for the next call and advances
-// the generation word. The status word is sticky until the host clears it.
+// ---- control block (first 512 bytes of every workspace) ---------------------
+// A workspace starts zeroed. The decode router kernel counts its finished CTAs in
+// CTRL_ROUTER; the last one selects and sets the counter back to zero. The status
+// word is sticky until the host clears it.
 enum CtrlWord : int {
-  CTRL_GEN = 0,      // calls completed on this workspace (call g runs with generation g + 1)
-  CTRL_EXIT = 1,     // CTAs of the running call that finished (reset by the last one)
-  CTRL_LOGITS = 2,   // [2], [3]: CTAs whose router rows are written, by generation parity
-  CTRL_ACT = 4,      // [4], [5]: CTAs whose gate/up rows are written, by generation parity
+  CTRL_ROUTER = 1,   // router CTAs of the running decode call that finished
   CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
-  CTRL_SLOT = 16,    // [16, 82): per-slot arrival counters, 33 per generation parity
 };
-constexpr int CTRL_SLOTS = 33;  // at most 32 picks and the shared expert
 constexpr int CTRL_BYTES = 512;
 
 enum DevErr : uint32_t {
-  DEV_ERR_POLL_TIMEOUT = 1u,   // other CTAs' results never arrived
   DEV_ERR_MBAR_TIMEOUT = 2u,   // a copy or a slot release never arrived
 };
 
-// Spin limits, measured on %globaltimer: a poll of an arrival counter or an
-// mbarrier wait gives up after this many nanoseconds.
-constexpr unsigned long long POLL_TIMEOUT_NS = 200ull * 1000 * 1000;  // 0.2 s
+// Spin limit, measured on %globaltimer: an mbarrier wait gives up after this many
+// nanoseconds.
 constexpr unsigned long long MBAR_TIMEOUT_NS = 500ull * 1000 * 1000;  // 0.5 s
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -111,63 +103,6 @@ __device__ __forceinline__ void pdl_wait_prior_grids() {
 }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// ---- gpu-scope counters and published values -----------------------------------
-// A value crosses CTAs as one 64-bit word {generation, f32 bits}: a single aligned
-// store is seen whole, so a reader that sees its own call's generation also sees
-// the value, with no fence between writer and reader. Arrival counters are only
-// hints of when to look; the generation check decides.
-__device__ __forceinline__ void red_relaxed_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint64_t tagged(uint32_t gen, float v) {
-  return ((uint64_t)gen << 32) | (uint64_t)__float_as_uint(v);
-}
-__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> 32); }
-__device__ __forceinline__ float value_of(uint64_t w) { return __uint_as_float((uint32_t)w); }
-// The value at p once it carries generation gen (bounded; `ok` cleared on timeout).
-__device__ __forceinline__ float await_tagged(const uint64_t* p, uint64_t w, uint32_t gen, bool& ok) {
-  if (tag_of(w) != gen && ok) {
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1; tag_of(w) != gen; ++it) {
-      if ((it & 15u) == 0 && globaltimer() - t0 > POLL_TIMEOUT_NS) {
-        ok = false;
-        break;
-      }
-      w = ld_relaxed_u64(p);
-    }
-  }
-  return value_of(w);
-}
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// One thread waits until *ctr >= target, bounded in time. It sleeps briefly between
-// reads: many CTAs polling in a tight loop would load L2 for everyone else.
-__device__ __forceinline__ bool await_count(const uint32_t* ctr, uint32_t target) {
-  if (ld_relaxed(ctr) >= target) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(100);
-    if (ld_relaxed(ctr) >= target) return true;
-    if ((it & 15u) == 0 && globaltimer() - t0 > POLL_TIMEOUT_NS) return false;
-  }
 }
 
 // Named barriers (bar.sync / bar.arrive are warp-aligned: the warp reconverges first).

@@ -1,4 +1,4 @@
-// Host-visible entry points of the fused decode kernel.
+// Host-visible entry point of the decode chain (router, gate/up, down kernels).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -7,14 +7,9 @@
 
 namespace moe {
 
-constexpr int DECODE_THREADS = 384;  // 11 consumer warps + 1 producer warp
-
-// Launches the decode kernel for one token (grid = a.p.nc CTAs).
-cudaError_t decode_launch(const DecodeArgs& a, int qtype, int maxb, uint32_t smem, cudaStream_t st,
-                          bool pdl);
-// Resident CTAs per SM of the decode kernel at this dynamic shared memory size.
-cudaError_t decode_occupancy(int qtype, int maxb, uint32_t smem, int* blocks);
-// Dynamic shared memory the decode kernel needs for this plan.
-uint32_t decode_smem_bytes(const DecodePlan& p);
+// Enqueues the three kernels for one token on `st` (with programmatic dependent
+// launch when `pdl`). `maxb` = blocks per lane of a gate/up row: ceil(H / 1024).
+// With a trace, CTAs with index below `trows` record their timeline.
+cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, int trows);
 
 }  // namespace moe

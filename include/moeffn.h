@@ -133,8 +133,8 @@ int moe_ffn_forward(const float* x, const float* router_w, const float* router_b
 /* The step enqueued on `stream` (a cudaStream_t, NULL = legacy default stream)
  * with a caller-owned device workspace of at least moe_workspace_size(cfg) bytes,
  * 256-byte aligned. A workspace must be zero-filled before its first use and then
- * only touched by this library: its first 512 bytes are control words (a call
- * counter, arrival counters and a status word). Calls sharing one workspace must
+ * only touched by this library: its first 512 bytes are control words (the
+ * router's arrival counter and a status word). Calls sharing one workspace must
  * be ordered (same stream, or synchronised); calls with different configurations
  * may share one.
  * Asynchronous: device-side errors surface through moe_workspace_status.
@@ -148,15 +148,13 @@ int moe_ffn_forward_ex(const float* x, const float* router_w, const float* route
 size_t moe_workspace_size(const moe_cfg* cfg);
 
 /* Byte offset of the MOE_TRACE timeline in the workspace (0 when cfg is invalid or
- * has no MOE_TRACE). The timeline holds, for each CTA (one per SM), 24 u64
- * %globaltimer readings in nanoseconds written by the last token's launch:
- * 0 start, 1 previous grid done, 2 router rows done, 3 x quantised, 4 shared-expert
- * columns done, 5 every CTA's logits seen, 6 selection keys ready, 7 top-k done,
- * 8 picks published, 9 routed gate/up rows done, 10 routed down rows done, 11 every
- * slot's rows seen, 12 end, 13 producer ready, 14 producer released for the picks,
- * 15 producer done, 16 first router row in shared memory, 17 first routed gate/up rows in
- * shared memory, 18 last slot activation vector quantised, 19 last routed gate/up rows in
- * shared memory, 20 first routed down rows in shared memory (unused points stay 0). */
+ * has no MOE_TRACE). The timeline holds 24 u64 words for each of the first
+ * n_SM CTA indices: %globaltimer readings in nanoseconds, written by thread 0 of
+ * the CTA with that index in each of the three decode kernels of the last token:
+ * router kernel 0 start, 1 x ready (previous kernel done), 2 logits written, 3 picks
+ * written (the selecting CTA only); gate/up kernel 4 start, 5 x quantised, 6 picks
+ * ready, 7 activation block written; down kernel 8 start, 9 weight blocks requested,
+ * 10 activation blocks ready, 11 output row written. Unused words stay 0. */
 size_t moe_trace_offset(const moe_cfg* cfg);
 
 /* Waits for `stream`, then reads and clears the workspace's status word:
@@ -170,13 +168,15 @@ int moe_workspace_status(void* workspace, void* stream);
  * allocator's hooks, in a real-time or signal context, under a memory budget
  * that has already been handed out) or that has no allocator of its own to lend
  * a workspace. The pages have no counterpart: their engines own every buffer.
- * The scratch lives in a fixed device array of 1 MiB compiled into the
+ * The scratch lives in a fixed device array of 512 KiB compiled into the
  * library; every device that loads the library holds it until the process
  * exits, and every call on a device shares it, so calls whose work overlaps on
  * the GPU (other streams, other threads) race and must not be made. The first
  * call on a device looks the array's address up once (make it before any stream
- * capture). Layers whose scratch (control block, logits, SwiGLU values, the
- * weighted down rows of every slot) exceeds 1 MiB are rejected with MOE_ERR_UNSUPPORTED. Device buffers only: MOE_HOST_IO
+ * capture). Tokens are decoded one at a time; a token's scratch (control block,
+ * logits, picks, weights and activation blocks) is at most 327 KiB for every
+ * layer the configuration checks admit, and a layer that needed more would be
+ * rejected with MOE_ERR_UNSUPPORTED. Device buffers only: MOE_HOST_IO
  * and MOE_TRACE are rejected. Blocking: returns after the step has finished on
  * `stream` (a cudaStream_t, NULL = legacy default stream), with device-side
  * errors reported directly. Arguments otherwise as moe_ffn_forward. */

@@ -3,7 +3,7 @@
 Some callers may not enter any allocator (for example code running inside another
 allocator's hooks, in a real-time path, or under a memory budget already handed
 out), so they cannot provide a workspace. This entry point runs the same decode
-kernel on a fixed scratch array compiled into the library. These tests check it
+kernels on a fixed scratch array compiled into the library. These tests check it
 against the workspace entry point through the C ABI, on two calls in a row (the
 second call reuses the scratch the first left behind).
 
@@ -27,17 +27,23 @@ def _built():
         build.build()
 
 
-def test_noalloc_rejects_layers_beyond_the_fixed_scratch():
+NOALLOC_SCRATCH_BYTES = 512 * 1024  # the fixed scratch compiled into the library
+
+
+def test_noalloc_scratch_holds_the_largest_layer_and_rejects_workspace_flags():
     _built()
-    # 32 picks of F = 3072 publish 768 KiB of SwiGLU values and 33 rows of H = 3072
-    # weighted outputs (792 KiB): more than the 1 MiB scratch
-    cfg = ffn.make_cfg(hidden=3072, n_experts=64, top_k=32, expert_ff=3072, n_tokens=1)
-    rc = ffn.moe_ffn_forward_noalloc(1 << 24, 1 << 28, None, 1 << 30, None, cfg, 1 << 26)
-    assert rc == ffn.MOE_ERR_UNSUPPORTED
-    assert "scratch" in ffn.moe_last_error()
-    # host staging and tracing need a workspace
-    cfg = ffn.make_cfg(hidden=256, n_experts=16, top_k=2, expert_ff=128, n_tokens=1, flags=ffn.MOE_HOST_IO)
-    assert ffn.moe_ffn_forward_noalloc(1 << 24, 1 << 28, None, 1 << 30, None, cfg, 1 << 26) == ffn.MOE_ERR_UNSUPPORTED
+    # one token of the largest admitted layer: 32 picks of F = 3072 and a shared expert of
+    # 3072 give 3168 activation blocks of 104 bytes, plus the control block, 1024 logits
+    # and the picks: about 327 KiB
+    cfg = ffn.make_cfg(hidden=3072, n_experts=1024, top_k=32, expert_ff=3072, shared_ff=3072, n_tokens=1)
+    need = ffn.moe_workspace_size(cfg)
+    assert 320 * 1024 < need <= NOALLOC_SCRATCH_BYTES
+    # host staging and tracing need a workspace: rejected before anything is launched
+    for flags in (ffn.MOE_HOST_IO, ffn.MOE_TRACE):
+        cfg = ffn.make_cfg(hidden=256, n_experts=16, top_k=2, expert_ff=128, n_tokens=1, flags=flags)
+        rc = ffn.moe_ffn_forward_noalloc(1 << 24, 1 << 28, None, 1 << 30, None, cfg, 1 << 26)
+        assert rc == ffn.MOE_ERR_UNSUPPORTED
+        assert "device buffers only" in ffn.moe_last_error()
 
 
 @pytest.mark.gpu
