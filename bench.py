@@ -225,6 +225,8 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
         rows.append(ws[off:off + nc * ffn.TRACE_STRIDE * 8].view(torch.int64).view(nc, ffn.TRACE_STRIDE).cpu().double())
     summary = {}
     for k, name in enumerate(ffn.TRACE_POINTS):
+        if not name:
+            continue
         med, mx = [], []
         for t in rows:
             col = t[:, k]

@@ -79,7 +79,7 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, ids, wts, aplanes, ainfo, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
+  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
 };
 
 // SMs of the current device (the timeline keeps one row per SM); without a
@@ -109,15 +109,8 @@ WsLayout ws_layout(const moe_cfg* c) {
   o += moe::CTRL_BYTES;
   L.logits = o;  // decode: router logits [E] f32
   o = up256(o + (size_t)c->n_experts * 4);
-  L.ids = o;     // decode: picks [K]
-  o = up256(o + (size_t)c->top_k * 4);
-  L.wts = o;     // decode: their weights [K]
-  o = up256(o + (size_t)c->top_k * 4);
-  const size_t nact = ((size_t)c->top_k * c->expert_ff + c->shared_ff) / 32;
-  L.aplanes = o;  // decode: activation blocks of every slot, byte planes [nact][96]
-  o = up256(o + nact * 96);
-  L.ainfo = o;    // decode: their {scale, integer sum} [nact]
-  o = up256(o + nact * 8);
+  L.act = o;     // decode: SwiGLU activations of every slot [K * F + Fs] f32
+  o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -182,9 +175,21 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.nbF = p.F / 32;
   p.nbFs = p.Fs / 32;
   p.nact = p.nbFs + p.K * p.nbF;
-  // the down kernel stages the activation blocks in shared memory when they fit in
-  // 48 KiB (every warp of the CTA reads all of them)
-  p.act_smem = (size_t)p.nact * 104 <= 48 * 1024 ? 1 : 0;
+  const uint32_t budget = 200u * 1024u;  // dynamic shared memory of one CTA
+  // gate/up: 4 windows of 8 rows, the x blocks and the selection
+  p.gu_win = moe::window_bytes(8u * p.rb_h);
+  p.gu_smem = 4u * p.gu_win + (uint32_t)p.nbH * 72u + moe::select_smem(p.E);
+  if (p.gu_smem > budget) return fail(MOE_ERR_UNSUPPORTED, "gate/up rows too long for shared memory");
+  // down: the activation blocks in one piece when they fit in 40 KiB, else pieces of
+  // 512; then as many rows per CTA (8, 4, 2, 1) as the windows allow
+  p.dn_piece = (size_t)p.nact * 72 <= 40 * 1024 ? p.nact : 512;
+  for (p.dn_rows = 8; p.dn_rows >= 1; p.dn_rows /= 2) {
+    p.dn_win_f = moe::window_bytes((uint32_t)p.dn_rows * p.rb_f);
+    p.dn_win_fs = p.Fs ? moe::window_bytes((uint32_t)p.dn_rows * p.rb_fs) : 0u;
+    p.dn_smem = p.dn_win_fs + (uint32_t)p.K * p.dn_win_f + (uint32_t)p.dn_piece * 72u + moe::select_smem(p.E);
+    if (p.dn_smem <= budget) break;
+  }
+  if (p.dn_rows < 1) return fail(MOE_ERR_UNSUPPORTED, "down rows too long for shared memory");
   int sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
@@ -375,10 +380,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.shared = static_cast<const uint8_t*>(shared);
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<float*>(wsb + W.logits);
-  a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
-  a.wts = reinterpret_cast<float*>(wsb + W.wts);
-  a.aplanes = wsb + W.aplanes;
-  a.ainfo = reinterpret_cast<float2*>(wsb + W.ainfo);
+  a.act = reinterpret_cast<float*>(wsb + W.act);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -495,10 +497,9 @@ int moe_shutdown(void) {
 // ---------------------------------------------------------------------------
 namespace {
 
-// Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits, the
-// picks and their weights, and the activation blocks of one token (at most
-// 327 KiB for the largest layer the checks admit: 32 picks of 3072 values plus a
-// shared expert of 3072). It is device memory that exists from the moment the
+// Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits and the
+// SwiGLU activations of one token (at most 405 KiB for the largest layer the checks
+// admit: 32 picks of 3072 values plus a shared expert of 3072). It is device memory that exists from the moment the
 // library's code is loaded on a device until the process exits; every call on
 // that device shares it.
 constexpr size_t NOALLOC_SCRATCH_BYTES = 512 * 1024;
@@ -573,10 +574,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.shared = static_cast<const uint8_t*>(shared_blocks);
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<float*>(wsb + W.logits);
-  a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
-  a.wts = reinterpret_cast<float*>(wsb + W.wts);
-  a.aplanes = wsb + W.aplanes;
-  a.ainfo = reinterpret_cast<float2*>(wsb + W.ainfo);
+  a.act = reinterpret_cast<float*>(wsb + W.act);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;

@@ -9,6 +9,7 @@ namespace moe {
 
 // Enqueues the three kernels for one token on `st` (with programmatic dependent
 // launch when `pdl`). `maxb` = blocks per lane of a gate/up row: ceil(H / 1024).
+// The plan's shared-memory sizes and rows per CTA must come from the host planner.
 // With a trace, CTAs with index below `trows` record their timeline.
 cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, int trows);
 

@@ -1,9 +1,11 @@
 // Shape and arguments of the decode pipeline (one token through three kernels):
-//   router   logits = Wr x; the last CTA done picks the top-k and their weights
-//   gate/up  one CTA per 32 intermediate values of a slot (a pick or the shared expert):
-//            their 32 gate and 32 up rows against x -> SwiGLU -> one activation block
-//   down     one warp per output row: the row's blocks of every slot's down matrix
-//            against the activation blocks, each weighted by its slot -> out
+//   router   logits = Wr x
+//   gate/up  one CTA per 16 intermediate values of a slot (a pick or the shared expert):
+//            the picks from the logits, the slot's 16 gate and 16 up rows copied into
+//            shared memory, dotted with x -> SwiGLU -> f32 activations
+//   down     R output rows per CTA: the picks from the logits, the rows' blocks of every
+//            slot's down matrix copied into shared memory, dotted with the activations
+//            (quantised per 32-block in shared memory), each slot weighted -> out
 // Slots in activation order: the shared expert first (it needs no routing), then the
 // k picks in selection order.
 #pragma once
@@ -30,10 +32,28 @@ struct DecodePlan {
   // blocks
   int nbH, nbF, nbFs;   // blocks per gate/up row, routed down row, shared down row
   int nact;             // activation blocks: (K * F + Fs) / 32 (shared expert's first)
-  int act_smem;         // the down kernel stages the activation planes in shared memory
+  // gate/up kernel: two chunks of 8 values, each a gate and an up window of 8 rows
+  uint32_t gu_win;      // bytes of one window (8 rows rounded out to 16-byte bounds)
+  uint32_t gu_smem;     // dynamic shared memory
+  // down kernel
+  int dn_rows;          // output rows per CTA (1, 2, 4 or 8)
+  int dn_piece;         // activation blocks quantised at a time (all, or a multiple of 256)
+  uint32_t dn_win_f;    // bytes of a routed window (dn_rows rows rounded out)
+  uint32_t dn_win_fs;   // bytes of the shared window (0 without a shared expert)
+  uint32_t dn_smem;     // dynamic shared memory
 };
 
+constexpr int GU_VALUES = 16;  // intermediate values per gate/up CTA
+
 MOE_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
+MOE_HD uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
+
+// A window holding `bytes` bytes that start anywhere: the copy is rounded out to
+// 16-byte bounds, so it can take up to 16 more bytes than align16(bytes).
+MOE_HD uint32_t window_bytes(uint32_t bytes) { return align16(bytes) + 16u; }
+
+// Dynamic shared memory of the selection (probabilities and keys of every expert).
+MOE_HD uint32_t select_smem(int E) { return align16((uint32_t)E * 8u); }
 
 constexpr uint32_t FLAG_ACCUMULATE = 1u;  // out = out + contribution
 constexpr uint32_t FLAG_RESIDUAL = 2u;    // out = x + contribution
@@ -48,13 +68,10 @@ struct DecodeArgs {
   float* out;                 // [H]
   int32_t* topk_ids;          // [K] or null
   float* topk_w;              // [K] or null
-  uint32_t* ctrl;             // control block: [1] router CTAs done (the last resets it)
+  uint32_t* ctrl;             // control block (status word)
   unsigned long long* trace;  // timeline (MOE_TRACE) or null
   float* logits;              // [E]
-  int32_t* ids;               // [K] picks
-  float* wts;                 // [K] their weights
-  uint8_t* aplanes;           // [nact][96] activation blocks: byte planes
-  float2* ainfo;              // [nact] {2^-k scale, sum of the block's integers}
+  float* act;                 // [K * F + Fs] SwiGLU activations, shared expert's first
   float scale, norm_min;
   uint32_t flags;
   DecodePlan p;

@@ -151,10 +151,12 @@ size_t moe_workspace_size(const moe_cfg* cfg);
  * has no MOE_TRACE). The timeline holds 24 u64 words for each of the first
  * n_SM CTA indices: %globaltimer readings in nanoseconds, written by thread 0 of
  * the CTA with that index in each of the three decode kernels of the last token:
- * router kernel 0 start, 1 x ready (previous kernel done), 2 logits written, 3 picks
- * written (the selecting CTA only); gate/up kernel 4 start, 5 x quantised, 6 picks
- * ready, 7 activation block written; down kernel 8 start, 9 weight blocks requested,
- * 10 activation blocks ready, 11 output row written. Unused words stay 0. */
+ * router kernel 0 start, 1 x ready (previous kernel done), 2 logits written;
+ * gate/up kernel 4 start, 5 x quantised, 6 logits ready, 7 picks made, 8 the CTA's
+ * first rows in shared memory, 9 activation block written; down kernel 12 start,
+ * 13 picks made, 14 row copies issued, 15 activation blocks ready, 16 activation
+ * blocks staged, 17 rows in shared memory, 18 output rows written. Unused words
+ * stay 0. */
 size_t moe_trace_offset(const moe_cfg* cfg);
 
 /* Waits for `stream`, then reads and clears the workspace's status word:
@@ -174,7 +176,7 @@ int moe_workspace_status(void* workspace, void* stream);
  * the GPU (other streams, other threads) race and must not be made. The first
  * call on a device looks the array's address up once (make it before any stream
  * capture). Tokens are decoded one at a time; a token's scratch (control block,
- * logits, picks, weights and activation blocks) is at most 327 KiB for every
+ * logits and SwiGLU activations) is at most 405 KiB for every
  * layer the configuration checks admit, and a layer that needed more would be
  * rejected with MOE_ERR_UNSUPPORTED. Device buffers only: MOE_HOST_IO
  * and MOE_TRACE are rejected. Blocking: returns after the step has finished on

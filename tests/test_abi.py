@@ -64,8 +64,8 @@ def test_invalid_cfg_rejected(built, kw):
 def test_valid_cfg_workspace_size(built):
     cfg = _cfg()
     n = ffn.moe_workspace_size(cfg)
-    # control block, f32 logits, and one 104-byte activation block per 32 SwiGLU values
-    assert n >= 512 + 256 * 4 + (6 * 512 + 1024) // 32 * 104
+    # control block, f32 logits and the f32 SwiGLU activations
+    assert n >= 512 + 256 * 4 + (6 * 512 + 1024) * 4
     assert n % 256 == 0
     # host staging adds room for x, out and the top-k outputs
     assert ffn.moe_workspace_size(_cfg(flags=ffn.MOE_HOST_IO, n_tokens=4)) > ffn.moe_workspace_size(_cfg(n_tokens=4))

@@ -33,11 +33,11 @@ NOALLOC_SCRATCH_BYTES = 512 * 1024  # the fixed scratch compiled into the librar
 def test_noalloc_scratch_holds_the_largest_layer_and_rejects_workspace_flags():
     _built()
     # one token of the largest admitted layer: 32 picks of F = 3072 and a shared expert of
-    # 3072 give 3168 activation blocks of 104 bytes, plus the control block, 1024 logits
-    # and the picks: about 327 KiB
+    # 3072 give 101376 f32 activations, plus the control block and 1024 logits: about
+    # 401 KiB
     cfg = ffn.make_cfg(hidden=3072, n_experts=1024, top_k=32, expert_ff=3072, shared_ff=3072, n_tokens=1)
     need = ffn.moe_workspace_size(cfg)
-    assert 320 * 1024 < need <= NOALLOC_SCRATCH_BYTES
+    assert 400 * 1024 < need <= NOALLOC_SCRATCH_BYTES
     # host staging and tracing need a workspace: rejected before anything is launched
     for flags in (ffn.MOE_HOST_IO, ffn.MOE_TRACE):
         cfg = ffn.make_cfg(hidden=256, n_experts=16, top_k=2, expert_ff=128, n_tokens=1, flags=flags)
