@@ -190,6 +190,10 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
     if (p.dn_smem <= budget) break;
   }
   if (p.dn_rows < 1) return fail(MOE_ERR_UNSUPPORTED, "down rows too long for shared memory");
+  // row groups: split the threads over the rows while a group still has a thread for
+  // each block of a piece
+  p.dn_rg = 1;
+  while (p.dn_rg < p.dn_rows && 256 / (2 * p.dn_rg) >= p.dn_piece) p.dn_rg *= 2;
   int sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");

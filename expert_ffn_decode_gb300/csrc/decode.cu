@@ -253,24 +253,65 @@ __device__ __forceinline__ void report_timeout(const DecodeArgs& a) {
 // ===========================================================================
 // Selection: the picks and their weights from the complete router logits
 // ===========================================================================
-// Every thread of the CTA calls it (it synchronises the CTA). `sel` holds E probs
-// and E keys; rids/rw receive the k picks in selection order and their weights.
-__device__ void select_picks(const DecodeArgs& a, uint8_t* sel, float* gscore, int* rids, float* rw) {
+// (key, expert) order of the selection: the larger key first, the lower expert among
+// equal keys (expert indices are unique, so the order is strict).
+__device__ __forceinline__ bool before(uint32_t k1, int i1, uint32_t k2, int i2) {
+  return k1 > k2 || (k1 == k2 && i1 < i2);
+}
+// Sorts a lane's N (<= 4) entries into selection order (insertion network).
+template <int N>
+__device__ __forceinline__ void sort_list(uint32_t (&kv)[N], int (&ki)[N]) {
+#pragma unroll
+  for (int a = 1; a < N; ++a)
+#pragma unroll
+    for (int b = a; b > 0; --b)
+      if (before(kv[b], ki[b], kv[b - 1], ki[b - 1])) {
+        const uint32_t tk = kv[b]; kv[b] = kv[b - 1]; kv[b - 1] = tk;
+        const int ti = ki[b]; ki[b] = ki[b - 1]; ki[b - 1] = ti;
+      }
+}
+
+// Every thread of a 256-thread CTA calls it (it synchronises the CTA). `sel` holds E
+// probs, E keys and 256 (key, expert) candidates; rids/rw receive the k picks in
+// selection order and their weights.
+//   1. each thread: sigmoid and selection key of experts tid, tid + 256, ...
+//   2. groups (n_groups > 1): each warp scores groups (the two largest s, summed);
+//      warp 0 keeps groups_used of them, the largest score first, the lowest group
+//      on ties; the keys of the other groups' experts become 0
+//   3. each warp: the top k of its experts (warp w: experts 32 w + lane + 256 i), as
+//      k rounds over the lanes' sorted lists (the winning lane drops its head)
+//   4. warp 0: the top k of the 8 sorted candidate lists (lane l walks list l), then
+//      the weights
+// Key 0 is below every real key (every float's key is at least that of -inf).
+template <int N>
+__device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore, int* rids, float* rw) {
   const DecodePlan& p = a.p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* probs = reinterpret_cast<float*>(sel);
   uint32_t* keys = reinterpret_cast<uint32_t*>(sel + (size_t)p.E * 4);
-  for (int e = tid; e < p.E; e += blockDim.x) {
-    const float l = __ldcg(a.logits + e);
-    const float pr = 1.f / (1.f + expf(-l));
-    probs[e] = pr;
-    keys[e] = order_key(pr + (a.bias ? __ldg(a.bias + e) : 0.f));
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(sel + (size_t)p.E * 8);
+  int* cidx = reinterpret_cast<int*>(sel + (size_t)p.E * 8 + 1024);
+  {
+    float l[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {  // loads first
+      const int e = tid + 256 * i;
+      l[i] = e < p.E ? __ldcg(a.logits + e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int e = tid + 256 * i;
+      if (e < p.E) {
+        const float pr = 1.f / (1.f + expf(-l[i]));
+        probs[e] = pr;
+        keys[e] = order_key(pr + (a.bias ? __ldg(a.bias + e) : 0.f));
+      }
+    }
   }
   __syncthreads();
   if (p.G > 1) {
-    // group score: the two largest s of the group, summed (multiset top-2)
     const int per = p.E / p.G;
-    for (int g = warp; g < p.G; g += nwarps) {
+    for (int g = warp; g < p.G; g += 8) {
       float x1 = -INFINITY, x2 = -INFINITY;
       for (int e = g * per + lane; e < (g + 1) * per; e += 32) {
         const uint32_t k = keys[e];
@@ -288,43 +329,93 @@ __device__ void select_picks(const DecodeArgs& a, uint8_t* sel, float* gscore, i
       if (lane == 0) gscore[g] = x1 + x2;
     }
     __syncthreads();
-  }
-  if (warp == 0) {
-    if (p.G > 1) {
-      // kept groups: groups_used rounds of the largest group score, lowest group on
-      // ties; experts of dropped groups get key 0 (below every real key)
-      uint32_t keep_lo = 0, keep_hi = 0;  // groups 0..63
-      for (int j = 0; j < p.Gu; ++j) {
-        int best = -1;
-        float bv = 0.f;
-        for (int g = 0; g < p.G; ++g) {
-          const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
-          if (!kept && (best < 0 || gscore[g] > bv)) { best = g; bv = gscore[g]; }
-        }
-        if (best < 32) keep_lo |= 1u << best; else keep_hi |= 1u << (best - 32);
+    if (warp == 0) {
+      // groups lane and lane + 32, groups_used rounds of the largest score (a score's
+      // key is never 0: only a NaN's is)
+      uint32_t gk[2];
+      int gi[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        gi[i] = lane + 32 * i;
+        gk[i] = gi[i] < p.G ? order_key(gscore[gi[i]]) : 0u;
       }
-      const int per = p.E / p.G;
+      sort_list(gk, gi);
+      uint32_t kept_lo = 0u, kept_hi = 0u;
+      for (int j = 0; j < p.Gu; ++j) {
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, gk[0]);
+        const int win = (int)__reduce_min_sync(0xffffffffu, gk[0] == mk && mk != 0u ? (unsigned)gi[0] : 0xffffffffu);
+        if (win < 32) kept_lo |= 1u << win; else kept_hi |= 1u << (win - 32);
+        if (gk[0] == mk && gi[0] == win) {
+          gk[0] = gk[1]; gi[0] = gi[1]; gk[1] = 0u;
+        }
+      }
+      // experts of dropped groups get key 0
       for (int e = lane; e < p.E; e += 32) {
         const int g = e / per;
-        const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
+        const bool kept = g < 32 ? ((kept_lo >> g) & 1u) : ((kept_hi >> (g - 32)) & 1u);
         if (!kept) keys[e] = 0u;
       }
-      __syncwarp();
     }
-    // k rounds of the largest key, lowest index among equals (keys in registers up to
-    // 256 experts, else rescanned from shared memory)
-    if (p.E <= 256) {
-      topk_rounds<8>(keys, p.E, p.K, rids, lane);
-      __syncwarp();
-    } else {
-      topk_scan(keys, p.E, p.K, rids, lane);
+    __syncthreads();
+  }
+  {
+    // stage 1: each warp's top k, from lane lists sorted into selection order
+    uint32_t kv[N];
+    int ki[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int e = 32 * warp + lane + 256 * i;
+      ki[i] = e;
+      kv[i] = e < p.E ? keys[e] : 0u;
     }
+    sort_list(kv, ki);
+    for (int j = 0; j < p.K; ++j) {
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, kv[0]);
+      const int win = (int)__reduce_min_sync(0xffffffffu, kv[0] == mk && mk != 0u ? (unsigned)ki[0] : 0xffffffffu);
+      if (lane == 0) {
+        ckey[warp * p.K + j] = mk;
+        cidx[warp * p.K + j] = win;
+      }
+      if (mk != 0u && kv[0] == mk && ki[0] == win) {  // the winner drops its head
+#pragma unroll
+        for (int i = 0; i + 1 < N; ++i) {
+          kv[i] = kv[i + 1];
+          ki[i] = ki[i + 1];
+        }
+        kv[N - 1] = 0u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // stage 2: lane l < 8 walks warp l's sorted candidates
+    int h = 0;
+    uint32_t bk = lane < 8 ? ckey[lane * p.K] : 0u;
+    int bi = lane < 8 ? cidx[lane * p.K] : 0x7fffffff;
+    for (int j = 0; j < p.K; ++j) {
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+      int win = (int)__reduce_min_sync(0xffffffffu, bk == mk && mk != 0u ? (unsigned)bi : 0xffffffffu);
+      if (win < 0 || win >= p.E) win = j % p.E;  // unreachable for a valid configuration
+      if (lane == 0) rids[j] = win;
+      if (lane < 8 && bk == mk && bi == win) {
+        ++h;
+        bk = h < p.K ? ckey[lane * p.K + h] : 0u;
+        bi = h < p.K ? cidx[lane * p.K + h] : 0x7fffffff;
+      }
+    }
+    __syncwarp();
     // weights from the picked sigmoids
     const float pj = lane < p.K ? probs[rids[lane]] : 0.f;
     const float wsum = fmaxf(warp_sum(pj), a.norm_min);
     if (lane < p.K) rw[lane] = pj / wsum * a.scale;
   }
   __syncthreads();
+}
+__device__ __forceinline__ void select_picks(const DecodeArgs& a, uint8_t* sel, float* gscore, int* rids,
+                                             float* rw) {
+  if (a.p.E <= 256) select_picks_n<1>(a, sel, gscore, rids, rw);
+  else if (a.p.E <= 512) select_picks_n<2>(a, sel, gscore, rids, rw);
+  else select_picks_n<4>(a, sel, gscore, rids, rw);
 }
 
 // ===========================================================================
@@ -490,8 +581,10 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
 // ===========================================================================
 // Dynamic shared memory: the shared window, then K routed windows, then one piece of
 // quantised activation blocks (planes [4][piece][16 B], info [piece]), then the
-// selection's probs and keys. Thread t takes blocks t, t + 256, ... of each piece
-// and, for each, all R rows: the activation block is read once for R block dots.
+// selection's probs and keys. The threads form RG row groups of 256 / RG threads;
+// group g owns rows g R / RG .. (g + 1) R / RG - 1, and its thread t takes blocks t,
+// t + 256 / RG, ... of each piece with all of the group's rows: an activation block
+// is read once for R / RG block dots.
 template <int QT>
 __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int trows) {
   extern __shared__ __align__(128) uint8_t dsm[];
@@ -535,6 +628,9 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   pdl_launch_dependents();
   tr(a, TR_DN_WAITED, trows);
   const int nact = p.nact;
+  const int RPG = R / p.dn_rg;                 // rows per group
+  const int TPG = DN_THREADS / p.dn_rg;        // threads per group (a multiple of 32)
+  const int grp = tid / TPG, tl = tid % TPG;
   float acc[8];
 #pragma unroll
   for (int r = 0; r < 8; ++r) acc[r] = 0.f;
@@ -550,7 +646,7 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
       tr(a, TR_DN_DATA, trows);
     }
     if (ok) {
-      for (int i = tid; i < np; i += DN_THREADS) {
+      for (int i = tl; i < np; i += TPG) {
         const int cb = pb + i;
         const bool sh = cb < p.nbFs;
         const int j = sh ? 0 : (cb - p.nbFs) / p.nbF;
@@ -560,11 +656,12 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
         const float wgt = sh ? 1.f : rw[j];
         ActBlock ab;
         load_act_block(ab, aplanes, ainfo, i, p.dn_piece);
+        const uint8_t* wr = w0 + (size_t)(grp * RPG) * rb;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-          if (r < R) {
+          if (r < RPG) {
             RawBlock blk;
-            load_block_s<QT>(w0 + (size_t)r * rb, b, blk);
+            load_block_s<QT>(wr + (size_t)r * rb, b, blk);
             acc[r] = fmaf(wgt, raw_block_dot<QT>(blk, ab), acc[r]);
           }
         }
@@ -573,10 +670,10 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
     __syncthreads();  // the next piece reuses the buffer
   }
   tr(a, TR_DN_LOOP, trows);
-  // each row: warp sums, then the warps' sums in warp order
+  // each row: warp sums, then its group's warp sums in warp order
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    if (r < R) {
+    if (r < RPG) {
       const float v = warp_sum(acc[r]);
       if (lane == 0) part[warp][r] = v;
     }
@@ -584,9 +681,9 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   __syncthreads();
   tr(a, TR_DN_SUMS, trows);
   if (tid < R) {
+    const int g = tid / RPG, rl = tid % RPG, w0 = g * (TPG / 32);
     float y = 0.f;
-#pragma unroll
-    for (int w = 0; w < DN_THREADS / 32; ++w) y += part[w][tid];
+    for (int w = 0; w < TPG / 32; ++w) y += part[w0 + w][rl];
     const int h = h0 + tid;
     if (a.flags & FLAG_RESIDUAL) y = __ldcg(a.x + h) + y;
     if (a.flags & FLAG_ACCUMULATE) y = __ldcg(a.out + h) + y;

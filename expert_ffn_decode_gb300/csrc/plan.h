@@ -38,6 +38,7 @@ struct DecodePlan {
   // down kernel
   int dn_rows;          // output rows per CTA (1, 2, 4 or 8)
   int dn_piece;         // activation blocks quantised at a time (all, or a multiple of 256)
+  int dn_rg;            // row groups of the down CTA's threads (1, 2, 4 or 8; divides dn_rows)
   uint32_t dn_win_f;    // bytes of a routed window (dn_rows rows rounded out)
   uint32_t dn_win_fs;   // bytes of the shared window (0 without a shared expert)
   uint32_t dn_smem;     // dynamic shared memory
@@ -52,8 +53,9 @@ MOE_HD uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
 // 16-byte bounds, so it can take up to 16 more bytes than align16(bytes).
 MOE_HD uint32_t window_bytes(uint32_t bytes) { return align16(bytes) + 16u; }
 
-// Dynamic shared memory of the selection (probabilities and keys of every expert).
-MOE_HD uint32_t select_smem(int E) { return align16((uint32_t)E * 8u); }
+// Dynamic shared memory of the selection: probabilities and keys of every expert,
+// then 256 candidate keys and 256 candidate experts.
+MOE_HD uint32_t select_smem(int E) { return align16((uint32_t)E * 8u) + 2048u; }
 
 constexpr uint32_t FLAG_ACCUMULATE = 1u;  // out = out + contribution
 constexpr uint32_t FLAG_RESIDUAL = 2u;    // out = x + contribution
