@@ -214,12 +214,21 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
     out = torch.empty(w["hidden"], device=dev)
     nc = torch.cuda.get_device_properties(dev).multi_processor_count
     rows = []
+    # the chain is captured in a CUDA graph and replayed, as the timed steps are, so the
+    # timeline shows the kernels' overlap rather than the host's launch pace
+    for i in range(chain):  # warm-up, and the kernels' attributes set outside the capture
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg, out, ws, nbytes, stream))
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chain):
+            lay = layers[i % L]
+            ffn.check(ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                             lay["shared_blocks"], cfg, out, ws, nbytes, stream))
     for rep in range(reps):
-        with torch.cuda.stream(stream):
-            for i in range(chain):
-                lay = layers[(rep * chain + i) % L]
-                ffn.check(ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
-                                                 lay["shared_blocks"], cfg, out, ws, nbytes, stream))
+        g.replay()
         stream.synchronize()
         ffn.check(ffn.moe_workspace_status(ws, stream))
         rows.append(ws[off:off + nc * ffn.TRACE_STRIDE * 8].view(torch.int64).view(nc, ffn.TRACE_STRIDE).cpu().double())

@@ -105,6 +105,7 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
 template <bool kShared = false>
 __device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float2* info,
                                              int t, int nthreads) {
+  #pragma unroll 1
   for (int base = 0; base < 4 * nb; base += 2 * nthreads) {
     float v[2][8];
     int idx[2];
@@ -131,17 +132,34 @@ struct ActBlock {
   float s, X;
 };
 
-__device__ __forceinline__ void load_act_block(ActBlock& a, const uint8_t* planes, const float2* info, int b,
-                                               int stride) {
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// Block b of a transposed activation array (chunk stride `stride` blocks) in shared
+// memory, planes and info given as shared addresses.
+__device__ __forceinline__ void load_act_block_s(ActBlock& a, uint32_t planes, uint32_t info, int b, int stride) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint4 v = *reinterpret_cast<const uint4*>(planes + ((size_t)c * stride + b) * 16);
+    const uint4 v = lds128(planes + (uint32_t)(c * stride + b) * 16u);
     a.p[4 * c + 0] = v.x;
     a.p[4 * c + 1] = v.y;
     a.p[4 * c + 2] = v.z;
     a.p[4 * c + 3] = v.w;
   }
-  const float2 f = info[b];
+  const float2 f = lds64f(info + (uint32_t)b * 8u);
   a.s = f.x;
   a.X = f.y;
 }
@@ -170,12 +188,12 @@ struct RawBlock {
   uint32_t sh;  // Q4_0: 0 or 16, the block's bit offset in w
 };
 template <int QT>
-__device__ __forceinline__ void load_block_s(const uint8_t* row, int b, RawBlock& r) {
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(row) + (uintptr_t)(QT == 3 ? 20 : 18) * (uint32_t)b;
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(addr & ~uintptr_t(3));
+__device__ __forceinline__ void load_block_s(uint32_t row, int b, RawBlock& r) {  // row: a shared address
+  const uint32_t addr = row + (uint32_t)(QT == 3 ? 20 : 18) * (uint32_t)b;
+  const uint32_t w = addr & ~3u;
 #pragma unroll
-  for (int i = 0; i < 5; ++i) r.w[i] = w[i];
-  r.sh = (uint32_t)(addr & 3u) * 8u;
+  for (int i = 0; i < 5; ++i) r.w[i] = lds32(w + 4u * i);
+  r.sh = (addr & 3u) * 8u;
 }
 template <int QT>
 __device__ __forceinline__ float raw_block_dot(const RawBlock& r, const ActBlock& a) {
@@ -311,8 +329,10 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
   __syncthreads();
   if (p.G > 1) {
     const int per = p.E / p.G;
+    #pragma unroll 1
     for (int g = warp; g < p.G; g += 8) {
       float x1 = -INFINITY, x2 = -INFINITY;
+      #pragma unroll 1
       for (int e = g * per + lane; e < (g + 1) * per; e += 32) {
         const uint32_t k = keys[e];
         const float v = __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
@@ -341,6 +361,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
       }
       sort_list(gk, gi);
       uint32_t kept_lo = 0u, kept_hi = 0u;
+      #pragma unroll 1
       for (int j = 0; j < p.Gu; ++j) {
         const uint32_t mk = __reduce_max_sync(0xffffffffu, gk[0]);
         const int win = (int)__reduce_min_sync(0xffffffffu, gk[0] == mk && mk != 0u ? (unsigned)gi[0] : 0xffffffffu);
@@ -350,6 +371,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
         }
       }
       // experts of dropped groups get key 0
+      #pragma unroll 1
       for (int e = lane; e < p.E; e += 32) {
         const int g = e / per;
         const bool kept = g < 32 ? ((kept_lo >> g) & 1u) : ((kept_hi >> (g - 32)) & 1u);
@@ -369,6 +391,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
       kv[i] = e < p.E ? keys[e] : 0u;
     }
     sort_list(kv, ki);
+    #pragma unroll 1
     for (int j = 0; j < p.K; ++j) {
       const uint32_t mk = __reduce_max_sync(0xffffffffu, kv[0]);
       const int win = (int)__reduce_min_sync(0xffffffffu, kv[0] == mk && mk != 0u ? (unsigned)ki[0] : 0xffffffffu);
@@ -392,6 +415,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
     int h = 0;
     uint32_t bk = lane < 8 ? ckey[lane * p.K] : 0u;
     int bi = lane < 8 ? cidx[lane * p.K] : 0x7fffffff;
+    #pragma unroll 1
     for (int j = 0; j < p.K; ++j) {
       const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
       int win = (int)__reduce_min_sync(0xffffffffu, bk == mk && mk != 0u ? (unsigned)bi : 0xffffffffu);
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
 #pragma unroll
   for (int i = 0; i < MAXB; ++i) {
     const int b = mh.sub + mh.lpr * i;
-    if (b < p.nbH) load_act_block(xc[i], xplanes, xinfo, b, p.nbH);
+    if (b < p.nbH) load_act_block_s(xc[i], smem_addr(xplanes), smem_addr(xinfo), b, p.nbH);
   }
   const uint8_t* rec = a.shared;
   if (!shared) {
@@ -539,8 +563,8 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
   tr(a, TR_GU_DATA, trows);
   const uint8_t* gsrc = rec + (size_t)(f0 + 8 * c) * p.rb_h;
   const uint8_t* usrc = rec + (size_t)(ff + f0 + 8 * c) * p.rb_h;
-  const uint8_t* gwin = win + (size_t)(2 * c) * p.gu_win + (reinterpret_cast<uintptr_t>(gsrc) & 15u);
-  const uint8_t* uwin = win + (size_t)(2 * c + 1) * p.gu_win + (reinterpret_cast<uintptr_t>(usrc) & 15u);
+  const uint32_t gwin = smem_addr(win) + (uint32_t)(2 * c) * p.gu_win + (uint32_t)(reinterpret_cast<uintptr_t>(gsrc) & 15u);
+  const uint32_t uwin = smem_addr(win) + (uint32_t)(2 * c + 1) * p.gu_win + (uint32_t)(reinterpret_cast<uintptr_t>(usrc) & 15u);
   const int vl = 2 * (warp & 3);  // first value of the warp within the chunk
   float dots[4] = {0.f, 0.f, 0.f, 0.f};
   if (ok) {
@@ -548,7 +572,7 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
     for (int s = 0; s < 4; ++s) {
       const int r = mh.rsub + mh.rps * s;
       if (r < 4) {
-        const uint8_t* row = ((r & 1) ? uwin : gwin) + (size_t)(vl + (r >> 1)) * p.rb_h;
+        const uint32_t row = ((r & 1) ? uwin : gwin) + (uint32_t)(vl + (r >> 1)) * p.rb_h;
 #pragma unroll
         for (int i = 0; i < MAXB; ++i) {
           const int b = mh.sub + mh.lpr * i;
@@ -635,6 +659,7 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
 #pragma unroll
   for (int r = 0; r < 8; ++r) acc[r] = 0.f;
   bool ok = true;
+  #pragma unroll 1
   for (int pb = 0; pb < nact; pb += p.dn_piece) {
     const int np = nact - pb < p.dn_piece ? nact - pb : p.dn_piece;
     quant_blocks(a.act + (size_t)pb * 32, np, p.dn_piece, aplanes, ainfo, tid, DN_THREADS);
@@ -646,22 +671,23 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
       tr(a, TR_DN_DATA, trows);
     }
     if (ok) {
+      #pragma unroll 1
       for (int i = tl; i < np; i += TPG) {
         const int cb = pb + i;
         const bool sh = cb < p.nbFs;
         const int j = sh ? 0 : (cb - p.nbFs) / p.nbF;
         const int b = sh ? cb : cb - p.nbFs - j * p.nbF;
-        const uint8_t* w0 = dsm + (sh ? (size_t)woff[32] : win_r + (size_t)j * p.dn_win_f + woff[j]);
+        const uint32_t w0 = smem_addr(dsm) + (sh ? woff[32] : (uint32_t)win_r + (uint32_t)j * p.dn_win_f + woff[j]);
         const uint32_t rb = sh ? p.rb_fs : p.rb_f;
         const float wgt = sh ? 1.f : rw[j];
         ActBlock ab;
-        load_act_block(ab, aplanes, ainfo, i, p.dn_piece);
-        const uint8_t* wr = w0 + (size_t)(grp * RPG) * rb;
+        load_act_block_s(ab, smem_addr(aplanes), smem_addr(ainfo), i, p.dn_piece);
+        const uint32_t wr = w0 + (uint32_t)(grp * RPG) * rb;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           if (r < RPG) {
             RawBlock blk;
-            load_block_s<QT>(wr + (size_t)r * rb, b, blk);
+            load_block_s<QT>(wr + (uint32_t)r * rb, b, blk);
             acc[r] = fmaf(wgt, raw_block_dot<QT>(blk, ab), acc[r]);
           }
         }
