@@ -309,6 +309,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
   uint32_t* keys = reinterpret_cast<uint32_t*>(sel + (size_t)p.E * 4);
   uint32_t* ckey = reinterpret_cast<uint32_t*>(sel + (size_t)p.E * 8);
   int* cidx = reinterpret_cast<int*>(sel + (size_t)p.E * 8 + 1024);
+  __shared__ unsigned long long kept_groups;
   {
     float l[N];
 #pragma unroll
@@ -326,6 +327,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
       }
     }
   }
+  if (tid == 0) kept_groups = ~0ull;
   __syncthreads();
   if (p.G > 1) {
     const int per = p.E / p.G;
@@ -360,35 +362,35 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
         gk[i] = gi[i] < p.G ? order_key(gscore[gi[i]]) : 0u;
       }
       sort_list(gk, gi);
-      uint32_t kept_lo = 0u, kept_hi = 0u;
-      #pragma unroll 1
+      unsigned long long kept = 0ull;
+#pragma unroll 1
       for (int j = 0; j < p.Gu; ++j) {
         const uint32_t mk = __reduce_max_sync(0xffffffffu, gk[0]);
         const int win = (int)__reduce_min_sync(0xffffffffu, gk[0] == mk && mk != 0u ? (unsigned)gi[0] : 0xffffffffu);
-        if (win < 32) kept_lo |= 1u << win; else kept_hi |= 1u << (win - 32);
+        kept |= 1ull << (win & 63);
         if (gk[0] == mk && gi[0] == win) {
           gk[0] = gk[1]; gi[0] = gi[1]; gk[1] = 0u;
         }
       }
-      // experts of dropped groups get key 0
-      #pragma unroll 1
-      for (int e = lane; e < p.E; e += 32) {
-        const int g = e / per;
-        const bool kept = g < 32 ? ((kept_lo >> g) & 1u) : ((kept_hi >> (g - 32)) & 1u);
-        if (!kept) keys[e] = 0u;
-      }
+      if (lane == 0) kept_groups = kept;
     }
     __syncthreads();
   }
   {
-    // stage 1: each warp's top k, from lane lists sorted into selection order
+    // stage 1: each warp's top k, from lane lists sorted into selection order; experts
+    // of dropped groups take key 0. The group of expert e is floor((e + 1/2) / per) in
+    // fp32: exact, since the quotient stays at least 1/(2 per) >= 1/1024 away from an
+    // integer and e < 1024.
+    const unsigned long long kg = kept_groups;
+    const float inv_per = p.G > 1 ? 1.f / (float)(p.E / p.G) : 0.f;
     uint32_t kv[N];
     int ki[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) {
       const int e = 32 * warp + lane + 256 * i;
       ki[i] = e;
-      kv[i] = e < p.E ? keys[e] : 0u;
+      const int g = (int)(((float)e + 0.5f) * inv_per);
+      kv[i] = (e < p.E && ((kg >> g) & 1ull)) ? keys[e] : 0u;
     }
     sort_list(kv, ki);
     #pragma unroll 1
