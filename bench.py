@@ -530,8 +530,9 @@ def main():
                    "l2": f"inputs larger than L2: {L} distinct layers, {L * step_bytes / 1e6:.0f} MB of "
                          f"step bytes between reuses of any weight byte (L2 {l2 / 1e6:.0f} MB)",
                    "pdl": not args.no_pdl, "graph_steps": G},
-        "arith": "4-bit weights x activations in 22-bit block fixed point: exact int32 block dots (dp4a), "
-                 "fp32 scaling and accumulation; router and routing in fp32",
+        "arith": "4-bit weights x activations in 16-bit block fixed point (15 bits and sign, power-of-two "
+                 "scale per 32 values): exact int32 block dots (dp4a), fp32 scaling and accumulation; router "
+                 "and routing in fp32",
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": H * 4 * T,

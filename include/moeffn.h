@@ -104,10 +104,12 @@ typedef struct moe_cfg {
 
 /* Two execution paths, chosen by n_tokens (both are exact restatements of the step
  * above; they differ in arithmetic only):
- *   n_tokens < 8   one fused persistent kernel per token. The router is an f32 dot;
- *                  the 4-bit blocks meet activations held in 22-bit block fixed point,
- *                  so each block dot is an exact int32 sum (dp4a), scaled and
- *                  accumulated in f32.
+ *   n_tokens < 8   three chained kernels per token (router; picks, gate/up rows and
+ *                  SwiGLU; picks, down rows and the weighted sum). The router is an
+ *                  f32 dot; the 4-bit blocks meet activations held in 16-bit block
+ *                  fixed point (a power-of-two scale per 32 values, error at most
+ *                  2^-15 of the block's largest magnitude), so each block dot is an
+ *                  exact int32 sum (dp4a), scaled and accumulated in f32.
  *   n_tokens >= 8  the batched path, in passes of at most 512 tokens. An f32 router
  *                  contraction; one warp per token for the selection; a stable
  *                  counting sort of the (token, pick) pairs by expert; grouped
