@@ -26,8 +26,11 @@ What it computes, step by step, each written from the passage named beside it
    ``routeLing``: the sum clamped at 6.103515625e-5, scale applied after the
    division).
 7. Each picked expert: gu = W_gu x (gate rows then up rows), act = silu(g) * u,
-   y = W_down act (ling_moe_ssd.js ``swiglu`` with no clamp; flint_moe_ssd.js
-   header: "SwiGLU experts (512)").
+   y = W_down act (ling_moe_ssd.js ``swiglu``; flint_moe_ssd.js header: "SwiGLU
+   experts (512)"). With a clamp limit L > 0 (ling_moe_ssd.js, the ``swiglu``
+   kernel and the comment above it; its header: some layers clamp the SwiGLU,
+   with separate per-layer limits for the routed and the shared experts), act =
+   min(silu(g), L) * clamp(u, -L, L); L = 0 means no clamp.
 8. The shared expert: the same SwiGLU on its own record with weight 1, no gate
    (flint_moe_ssd.js header: "one always-on shared SwiGLU expert (1024, no
    gate)").
@@ -68,6 +71,8 @@ class MoeConfig:
     weights_scale: float = 1.0
     norm_min: float = NORM_MIN
     flags: int = 0
+    swiglu_limit: float = 0.0         # routed experts' clamp limit L (0: none)
+    swiglu_limit_shared: float = 0.0  # the shared expert's
 
 
 # --------------------------------------------------------------------------
@@ -231,12 +236,18 @@ def route(x: np.ndarray, router_w: np.ndarray, bias, cfg: MoeConfig):
 # 7-9. Experts and combine
 # --------------------------------------------------------------------------
 
-def swiglu(x: np.ndarray, w_gu: np.ndarray, w_dn: np.ndarray) -> np.ndarray:
-    """y = W_down (silu(g) * u), with [g; u] = W_gu x and silu(g) = g / (1 + e^-g)."""
+def swiglu(x: np.ndarray, w_gu: np.ndarray, w_dn: np.ndarray, limit: float = 0.0) -> np.ndarray:
+    """y = W_down (silu(g) * u), with [g; u] = W_gu x and silu(g) = g / (1 + e^-g);
+    with limit L > 0, act = min(silu(g), L) * clamp(u, -L, L) (ling_moe_ssd.js
+    ``swiglu``)."""
     ff = w_gu.shape[0] // 2
     gu = w_gu @ np.asarray(x, np.float64)
     g, u = gu[:ff], gu[ff:]
-    act = g / (1.0 + np.exp(-g)) * u
+    sg = g / (1.0 + np.exp(-g))
+    if limit > 0.0:
+        u = np.minimum(np.maximum(u, -limit), limit)
+        sg = np.minimum(sg, limit)
+    act = sg * u
     return w_dn @ act
 
 
@@ -274,9 +285,9 @@ def moe_ffn(x, router_w, bias, expert_blocks, shared_blocks, cfg: MoeConfig, out
         acc = np.zeros(H, np.float64)
         for j in range(cfg.top_k):
             w_gu, w_dn = experts(int(ids[t, j]))
-            acc += w[t, j] * swiglu(x[t], w_gu, w_dn)
+            acc += w[t, j] * swiglu(x[t], w_gu, w_dn, cfg.swiglu_limit)
         if shared is not None:
-            acc += swiglu(x[t], shared[0], shared[1])
+            acc += swiglu(x[t], shared[0], shared[1], cfg.swiglu_limit_shared)
         if cfg.flags & ACCUMULATE:
             acc += np.asarray(out_in[t], np.float64)
         if cfg.flags & RESIDUAL:

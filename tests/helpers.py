@@ -23,7 +23,8 @@ def oracle_cfg(w: dict, flags: int = 0) -> mo.MoeConfig:
                         expert_ff=w["expert_ff"], shared_ff=w["shared_ff"], n_groups=w["n_groups"],
                         groups_used=w["groups_used"], qtype=w["qtype"],
                         weights_scale=w["weights_scale"], norm_min=w.get("norm_min", mo.NORM_MIN),
-                        flags=flags)
+                        flags=flags, swiglu_limit=w.get("swiglu_limit", 0.0),
+                        swiglu_limit_shared=w.get("swiglu_limit_shared", 0.0))
 
 
 def selection_gap(s: np.ndarray, w: dict) -> float:

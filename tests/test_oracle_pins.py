@@ -258,6 +258,42 @@ def test_swiglu_closed_form():
     check_swiglu_closed_form()
 
 
+def check_swiglu_clamp_closed_form():
+    # The same one-hot expert (y_h = act(g = x_h, u = 2 x_{h+1}) / 2) with a clamp limit
+    # L = 1 (ling_moe_ssd.js swiglu: act = min(silu(g), L) * clamp(u, -L, L)):
+    #   h = 0: g = ln 3 -> silu = 0.75 ln 3 < 1 kept; u = 4 -> 1;        y = 0.375 ln 3
+    #   h = 1: g = 2 -> silu(2) = 1.76 -> 1;       u = -2 ln 3 -> -1;   y = -0.5
+    #   h = 2: g = -ln 3 -> silu = -0.25 ln 3 kept; u = 1 -> 1 (edge);  y = -0.125 ln 3
+    # The shared expert takes its own limit: 0 (no clamp) here, on the same record.
+    H = F = 32
+    one_hot = lambda c, v: [v if i == c else 0 for i in range(32)]
+    rec = b"".join(_q4_1_block(1.0, 0.0, one_hot(f, 1)) for f in range(F))
+    rec += b"".join(_q4_1_block(1.0, 0.0, one_hot((f + 1) % 32, 2)) for f in range(F))
+    rec += b"".join(_q4_1_block(0.5, 0.0, one_hot(h, 1)) for h in range(H))
+    rec = np.frombuffer(rec, np.uint8)
+    ln3 = math.log(3.0)
+    x = np.zeros(H, np.float32)
+    x[:4] = [ln3, 2.0, -ln3, 0.5]
+    cfg = mo.MoeConfig(hidden=H, n_experts=1, top_k=1, expert_ff=F, swiglu_limit=1.0)
+    out, _, _ = mo.moe_ffn(x, np.zeros((1, H), np.float32), None, rec, None, cfg)
+    x64 = x.astype(np.float64)
+    assert math.isclose(out[0][0], 0.375 * math.log(3.0), rel_tol=1e-6)
+    assert math.isclose(out[0][1], -0.5, rel_tol=1e-12)
+    assert math.isclose(out[0][2], -0.125 * math.log(3.0), rel_tol=1e-6)
+    # limit 0: exactly the unclamped step; the shared expert ignores the routed limit
+    cfg0 = mo.MoeConfig(hidden=H, n_experts=1, top_k=1, expert_ff=F)
+    plain, _, _ = mo.moe_ffn(x, np.zeros((1, H), np.float32), None, rec, None, cfg0)
+    assert math.isclose(plain[0][1], 0.5 * (2.0 / (1.0 + math.exp(-2.0))) * (2.0 * float(x64[2])), rel_tol=1e-6)
+    cfgs = mo.MoeConfig(hidden=H, n_experts=1, top_k=1, expert_ff=F, shared_ff=F, swiglu_limit=1.0,
+                        swiglu_limit_shared=0.0)
+    both, _, _ = mo.moe_ffn(x, np.zeros((1, H), np.float32), None, rec, rec, cfgs)
+    assert np.allclose(both[0] - out[0], plain[0], rtol=1e-12, atol=1e-15)
+
+
+def test_swiglu_clamp_closed_form():
+    check_swiglu_clamp_closed_form()
+
+
 def _random_cfg_layer(seed, shared=True, groups=False):
     from expert_ffn_decode_gb300 import synth
     w = dict(hidden=64, n_experts=8, top_k=3, expert_ff=32, shared_ff=64 if shared else 0,
@@ -341,7 +377,7 @@ def test_expert_matches_textbook_dense():
 ALL_CHECKS = [check_half_decode, check_golden_blocks, check_q4_0_is_q4_1_with_offset,
               check_block_dot_identity, check_golden_routing, check_routing_brute_force,
               check_routing_reductions, check_route_weights_closed_form,
-              check_swiglu_closed_form, check_combine_invariants,
+              check_swiglu_closed_form, check_swiglu_clamp_closed_form, check_combine_invariants,
               check_expert_matches_textbook_dense]
 
 
@@ -403,18 +439,41 @@ def _mut_scale_inside(p, picks, scale, norm_min=mo.NORM_MIN):
     return pp / max(pp.sum() * scale, norm_min)
 
 
-def _mut_swiglu_swap(x, w_gu, w_dn):
+def _mut_swiglu_swap(x, w_gu, w_dn, limit=0.0):
     ff = w_gu.shape[0] // 2
     gu = w_gu @ np.asarray(x, np.float64)
     u, g = gu[:ff], gu[ff:]
     return w_dn @ (g / (1.0 + np.exp(-g)) * u)
 
 
-def _mut_silu_sign(x, w_gu, w_dn):
+def _mut_silu_sign(x, w_gu, w_dn, limit=0.0):
     ff = w_gu.shape[0] // 2
     gu = w_gu @ np.asarray(x, np.float64)
     g, u = gu[:ff], gu[ff:]
     return w_dn @ (g / (1.0 + np.exp(g)) * u)
+
+
+def _mut_clamp_gate_first(x, w_gu, w_dn, limit=0.0):
+    # the limit applied to g before the silu instead of to silu(g)
+    ff = w_gu.shape[0] // 2
+    gu = w_gu @ np.asarray(x, np.float64)
+    g, u = gu[:ff], gu[ff:]
+    if limit > 0.0:
+        g = np.minimum(g, limit)
+        u = np.minimum(np.maximum(u, -limit), limit)
+    return w_dn @ (g / (1.0 + np.exp(-g)) * u)
+
+
+def _mut_clamp_up_one_sided(x, w_gu, w_dn, limit=0.0):
+    # u clamped from above only
+    ff = w_gu.shape[0] // 2
+    gu = w_gu @ np.asarray(x, np.float64)
+    g, u = gu[:ff], gu[ff:]
+    sg = g / (1.0 + np.exp(-g))
+    if limit > 0.0:
+        u = np.minimum(u, limit)
+        sg = np.minimum(sg, limit)
+    return w_dn @ (sg * u)
 
 
 def _mut_half_no_subnormal(bits):
@@ -436,6 +495,8 @@ MUTANTS = [
     ("route_weights", _mut_scale_inside),
     ("swiglu", _mut_swiglu_swap),
     ("swiglu", _mut_silu_sign),
+    ("swiglu", _mut_clamp_gate_first),
+    ("swiglu", _mut_clamp_up_one_sided),
     ("half_to_float", _mut_half_no_subnormal),
 ]
 
