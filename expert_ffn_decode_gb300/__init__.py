@@ -58,14 +58,17 @@ class moe_cfg(ctypes.Structure):
         ("weights_scale", ctypes.c_float),
         ("norm_min", ctypes.c_float),
         ("flags", ctypes.c_uint32),
+        ("swiglu_limit", ctypes.c_float),
+        ("swiglu_limit_shared", ctypes.c_float),
     ]
 
 
 def make_cfg(hidden, n_experts, top_k, expert_ff, shared_ff=0, n_groups=1, groups_used=1,
-             n_tokens=1, qtype=MOE_Q4_1, weights_scale=1.0, norm_min=NORM_MIN, flags=0, **_ignored):
+             n_tokens=1, qtype=MOE_Q4_1, weights_scale=1.0, norm_min=NORM_MIN, flags=0,
+             swiglu_limit=0.0, swiglu_limit_shared=0.0, **_ignored):
     """A :class:`moe_cfg` from keyword arguments (extra keys are ignored)."""
     return moe_cfg(hidden, n_experts, top_k, expert_ff, shared_ff, n_groups, groups_used,
-                   n_tokens, qtype, weights_scale, norm_min, flags)
+                   n_tokens, qtype, weights_scale, norm_min, flags, swiglu_limit, swiglu_limit_shared)
 
 
 class MoeError(RuntimeError):

@@ -72,6 +72,9 @@ int check_cfg(const moe_cfg* c) {
     return fail(MOE_ERR_INVALID_CFG, "weights_scale is not finite");
   if (!(c->norm_min >= 0.f) || !std::isfinite(c->norm_min))
     return fail(MOE_ERR_INVALID_CFG, "norm_min must be finite and >= 0");
+  if (!(c->swiglu_limit >= 0.f) || !std::isfinite(c->swiglu_limit) || !(c->swiglu_limit_shared >= 0.f) ||
+      !std::isfinite(c->swiglu_limit_shared))
+    return fail(MOE_ERR_INVALID_CFG, "swiglu limits must be finite and >= 0");
   if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
@@ -360,6 +363,8 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     pa.qtype = c->qtype;
     pa.scale = c->weights_scale;
     pa.norm_min = c->norm_min;
+    pa.lim = c->swiglu_limit;
+    pa.lim_s = c->swiglu_limit_shared;
     pa.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
     pa.rb_h = pe.plan.rb_h;
     pa.rb_f = pe.plan.rb_f;
@@ -388,6 +393,8 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
+  a.lim = c->swiglu_limit;
+  a.lim_s = c->swiglu_limit_shared;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
@@ -582,6 +589,8 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
+  a.lim = c->swiglu_limit;
+  a.lim_s = c->swiglu_limit_shared;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);

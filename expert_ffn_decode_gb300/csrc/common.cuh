@@ -136,6 +136,17 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// SwiGLU of one intermediate value: silu(g) * u, or with a clamp limit L > 0,
+// min(silu(g), L) * clamp(u, -L, L) (ling_moe_ssd.js, the swiglu kernel).
+__device__ __forceinline__ float swiglu_act(float g, float u, float L) {
+  float sg = g / (1.f + expf(-g));
+  if (L > 0.f) {
+    u = fminf(fmaxf(u, -L), L);
+    sg = fminf(sg, L);
+  }
+  return sg * u;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

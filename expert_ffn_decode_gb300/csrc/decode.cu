@@ -248,7 +248,6 @@ __device__ __forceinline__ void group_sum_n(float (&v)[N], int lpr) {
 }
 
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 // Timeline points (MOE_TRACE): %globaltimer readings per CTA index (CTAs below the
 // trace's row count), written by thread 0.
@@ -598,7 +597,8 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
     }
   }
   __syncwarp();
-  if (lane < 2) a.act[v0 + 2 * warp + lane] = silu_mul(rowdot[warp][2 * lane], rowdot[warp][2 * lane + 1]);
+  if (lane < 2)
+    a.act[v0 + 2 * warp + lane] = swiglu_act(rowdot[warp][2 * lane], rowdot[warp][2 * lane + 1], shared ? a.lim_s : a.lim);
   tr(a, TR_GU_END, trows);
 }
 

@@ -75,6 +75,7 @@ struct DecodeArgs {
   float* logits;              // [E]
   float* act;                 // [K * F + Fs] SwiGLU activations, shared expert's first
   float scale, norm_min;
+  float lim, lim_s;           // SwiGLU clamp limits of the routed and shared experts (0: none)
   uint32_t flags;
   DecodePlan p;
 };

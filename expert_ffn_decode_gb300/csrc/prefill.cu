@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
             const float other = __shfl_xor_sync(0xffffffffu, v, 1);
             const int c = c0 + i;
             if (!(m & 1) && m < mrows && c < ch.n) {
-              const float act = v / (1.f + expf(-v)) * other;  // silu(gate) * up
+              const float act = swiglu_act(v, other, sh ? a.lim_s : a.lim);  // silu(gate) * up, clamped
               __half* dst = sh ? a.act16s + (size_t)(ch.row0 + c) * ff : a.act16 + (size_t)(ch.row0 + c) * ff;
               dst[kpos(f)] = __float2half_rn(act);
             }

@@ -58,6 +58,7 @@ struct PrefillArgs {
   // shape
   int T, H, E, K, F, Fs, G, Gu, qtype;
   float scale, norm_min;
+  float lim, lim_s;         // SwiGLU clamp limits of the routed and shared experts (0: none)
   uint32_t flags;
   uint32_t rb_h, rb_f, rb_fs;
   uint64_t rec_bytes;

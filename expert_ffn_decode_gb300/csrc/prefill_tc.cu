@@ -677,9 +677,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
               if (MODE == 2) {
                 if (c < t.n && t.e0 + m < a.E) a.logits[(size_t)(t.row0 + c) * a.E + t.e0 + m] = v + other;
               } else {
-                // act = silu(gate) * up for f = f0 + lane, gathered into the four 16-byte
+                // act = silu(gate) * up (clamped) for f = f0 + lane, gathered into the four 16-byte
                 // pieces of the block (slot 8w + k holds value 4w + {0,2,1,3}[k], +16 for k >= 4)
-                const float act = v / (1.f + expf(-v)) * other;
+                const float act = swiglu_act(v, other, t.shared ? a.lim_s : a.lim);
                 const uint32_t hv = (uint32_t)__half_as_ushort(__float2half_rn(act));
                 const int w = lane & 3;
                 uint32_t pk[4];

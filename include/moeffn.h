@@ -11,8 +11,9 @@
  *   picks: top_k rounds of argmax over the kept s, lowest index on ties, in
  *   selection order                                         (TOPK_SIG_BODY)
  *   w_j = p_pick_j / max(sum_j p_pick_j, norm_min) * weights_scale   (TOPK_SIG_BODY, routeLing)
- *   expert: [g; u] = W_gu x (gate rows then up rows), y = W_down (silu(g) * u)
- *                                                          (ling_moe_ssd.js, swiglu without clamp;
+ *   expert: [g; u] = W_gu x (gate rows then up rows), y = W_down (silu(g) * u), or with a
+ *   clamp limit L > 0, y = W_down (min(silu(g), L) * clamp(u, -L, L))
+ *                                                          (ling_moe_ssd.js, swiglu;
  *                                                           flint_moe_ssd.js, planLayoutFlint record)
  *   shared expert: the same SwiGLU with weight 1, no gate  (flint_moe_ssd.js, file header)
  *   out[t] = sum_j w_j y_j + shared                         (ling_moe_ssd.js, moeAccum)
@@ -100,6 +101,12 @@ typedef struct moe_cfg {
   float weights_scale; /* 1.0 unless the layer says otherwise */
   float norm_min;      /* clamp on the sum of the picked sigmoids */
   uint32_t flags;      /* MOE_* flags above */
+  /* SwiGLU clamp limits L, >= 0 (ling_moe_ssd.js, the swiglu kernel and its comment:
+   * act = min(silu(g), L) * clamp(u, -L, L); L = 0 means no clamp). The routed experts
+   * and the shared expert take separate per-layer limits, as the page's
+   * swiglu_clamp_exp / swiglu_clamp_shexp arrays do. */
+  float swiglu_limit;
+  float swiglu_limit_shared;
 } moe_cfg;
 
 /* Two execution paths, chosen by n_tokens (both are exact restatements of the step

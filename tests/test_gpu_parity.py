@@ -99,6 +99,41 @@ def test_random_shapes(w):
     compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']}")
 
 
+CLAMP = [
+    _small(30, shared_ff=64, swiglu_limit=0.8, swiglu_limit_shared=0.5),
+    _small(31, qtype=mo.Q4_0, shared_ff=128, swiglu_limit=0.6, n_groups=4, groups_used=2, top_k=3,
+           bias_std=0.1),
+    _small(32, hidden=96, expert_ff=160, shared_ff=96, swiglu_limit=0.5, swiglu_limit_shared=0.9),
+]
+
+
+@pytest.mark.parametrize("w", CLAMP, ids=[f"s{w['seed']}" for w in CLAMP])
+def test_swiglu_clamp(w):
+    # the clamped SwiGLU (ling_moe_ssd.js swiglu), with limits that clamp a good share of
+    # the gate and up values, against the oracle; the clamp must change the output
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    g = GpuLayer(layer, w)
+    out, ids, wts = g.run(x)
+    compare(out, ids, wts, ref, rid, rwt, f"clamp seed {w['seed']}")
+    plain = {**w, "swiglu_limit": 0.0, "swiglu_limit_shared": 0.0}
+    unclamped, _, _ = GpuLayer(layer, plain).run(x)
+    assert min(rel_l2(out[t], unclamped[t]) for t in range(len(x))) > 1e-2
+
+
+def test_ling_decode_with_clamp():
+    # the Ling-shaped layer with both clamp limits set
+    w0, layer = layer_of("ling_decode_t1")
+    w = {**w0, "swiglu_limit": 1.0, "swiglu_limit_shared": 0.7}
+    x, _ = margin_tokens(layer, w, 2, seed=9, stream=5)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    compare(out, ids, wts, ref, rid, rwt, "ling clamp")
+
+
 def test_flags_accumulate_residual_hostio_nopdl():
     import expert_ffn_decode_gb300 as ffn
     w, layer = layer_of("flint_decode_t1")

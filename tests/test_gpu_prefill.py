@@ -74,6 +74,25 @@ def test_prefill_shapes(w):
     print(f"seed {w['seed']} T={w['n_tokens']}: max rel-L2 {err:.3e}")
 
 
+CLAMP = [
+    _small(58, shared_ff=128, n_tokens=40, swiglu_limit=0.8, swiglu_limit_shared=0.5),   # tile path
+    _small(59, hidden=96, expert_ff=96, shared_ff=96, qtype=mo.Q4_0, n_tokens=20, swiglu_limit=0.7,
+           swiglu_limit_shared=0.3),                                                      # general path
+]
+
+
+@pytest.mark.parametrize("w", CLAMP, ids=["tile", "general"])
+def test_prefill_swiglu_clamp(w):
+    layer = synth.make_layer(w)
+    x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    compare(out, ids, wts, ref, rid, rwt, f"clamp seed {w['seed']}")
+    unclamped, _, _ = GpuLayer(layer, {**w, "swiglu_limit": 0.0, "swiglu_limit_shared": 0.0}).run(x)
+    assert min(rel_l2(out[t], unclamped[t]) for t in range(len(x))) > 1e-2
+
+
 @pytest.mark.parametrize("shared_ff", [64, 128], ids=["general", "tile"])
 def test_prefill_two_passes_and_decode_boundary(shared_ff):
     # 7 tokens decode token by token, 8 take the batched path, 600 run as passes of 512 + 88
