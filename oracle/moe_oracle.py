@@ -37,6 +37,11 @@ What it computes, step by step, each written from the passage named beside it
 9. out = sum_j w_j y_j + shared (ling_moe_ssd.js ``moeAccum``: x[h] += sum_j
    w_j out[j*H + h] + shared[h]); the oracle returns the contribution, or adds
    it to ``out_in`` when accumulating, or to x for the residual form.
+0. Optional layer prologue: the step's input is rms_norm(x) * ffn_norm, with
+   rms_norm(x) = x / sqrt(mean(x^2) + eps) (flint_moe_ssd.js and
+   lfm2_moe_ssd.js headers: "x += ffn(rms_norm(x) * ffn_norm)"; eps is the
+   model's ``attention.layer_norm_rms_epsilon``). The residual form then adds
+   the un-normalised x, which makes the whole FFN block x += ffn(...).
 
 Parity status: every step above is pinned by the not-gpu tests (golden blocks,
 closed forms, brute-force routing, invariants); none is "parity unpinned".
@@ -73,6 +78,7 @@ class MoeConfig:
     flags: int = 0
     swiglu_limit: float = 0.0         # routed experts' clamp limit L (0: none)
     swiglu_limit_shared: float = 0.0  # the shared expert's
+    rms_eps: float = 0.0              # the prologue's epsilon (used with an ffn_norm vector)
 
 
 # --------------------------------------------------------------------------
@@ -267,13 +273,22 @@ class ExpertCache:
         return self.cache[e]
 
 
-def moe_ffn(x, router_w, bias, expert_blocks, shared_blocks, cfg: MoeConfig, out_in=None):
+def rms_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * weight, per row, in float64 (step 0)."""
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
+    return x * r * np.asarray(weight, np.float64)[None, :]
+
+
+def moe_ffn(x, router_w, bias, expert_blocks, shared_blocks, cfg: MoeConfig, out_in=None, ffn_norm=None):
     """The whole step for T tokens. Returns (out [T][H] f64, ids [T][k], w [T][k]).
 
-    out[t] = sum_j w[t][j] * E_{ids[t][j]}(x[t]) + S(x[t]) (+ out_in[t] when
-    ``cfg.flags & ACCUMULATE``, + x[t] when ``cfg.flags & RESIDUAL``).
+    out[t] = sum_j w[t][j] * E_{ids[t][j]}(xn[t]) + S(xn[t]) (+ out_in[t] when
+    ``cfg.flags & ACCUMULATE``, + x[t] when ``cfg.flags & RESIDUAL``), where xn = x, or
+    rms_norm(x) * ffn_norm when a norm vector is given.
     """
-    x = np.atleast_2d(np.asarray(x, np.float32))
+    x_in = np.atleast_2d(np.asarray(x, np.float32))
+    x = x_in if ffn_norm is None else rms_norm(x_in, ffn_norm, cfg.rms_eps)
     T, H = x.shape
     ids, w, _ = route(x, router_w, bias, cfg)
     experts = ExpertCache(expert_blocks, cfg)
@@ -291,6 +306,6 @@ def moe_ffn(x, router_w, bias, expert_blocks, shared_blocks, cfg: MoeConfig, out
         if cfg.flags & ACCUMULATE:
             acc += np.asarray(out_in[t], np.float64)
         if cfg.flags & RESIDUAL:
-            acc += x[t].astype(np.float64)
+            acc += x_in[t].astype(np.float64)
         out[t] = acc
     return out, ids, w

@@ -294,6 +294,47 @@ def test_swiglu_clamp_closed_form():
     check_swiglu_clamp_closed_form()
 
 
+def check_rms_norm_prologue():
+    # rms_norm(x) * w = x / sqrt(mean(x^2) + eps) * w (flint_moe_ssd.js header:
+    # x += ffn(rms_norm(x) * ffn_norm)), in closed form on small vectors
+    H = 32
+    x = np.zeros(H, np.float32)
+    x[:2] = [3.0, 4.0]                      # mean(x^2) = 25 / 32
+    w = np.full(H, 2.0)
+    xn = mo.rms_norm(x, w, 0.0)[0]
+    assert math.isclose(xn[0], 3.0 * 2.0 * math.sqrt(32.0) / 5.0, rel_tol=1e-12)
+    assert math.isclose(xn[1], 4.0 * 2.0 * math.sqrt(32.0) / 5.0, rel_tol=1e-12)
+    assert xn[2] == 0.0
+    y = np.zeros(H, np.float32)
+    y[0] = 4.0                              # mean(y^2) = 1/2; with eps = 1/2 the scale is 1
+    assert math.isclose(mo.rms_norm(y, np.ones(H), 0.5)[0][0], 4.0, rel_tol=1e-12)
+    # the step with the prologue is the step on the normalised input; the residual form
+    # adds the raw x
+    rng = np.random.default_rng(5)
+    Hs, E, F = 64, 8, 32
+    cfg = mo.MoeConfig(hidden=Hs, n_experts=E, top_k=3, expert_ff=F, rms_eps=1e-5)
+    rec = mo.record_bytes(Hs, F, mo.Q4_1)
+    blocks = rng.integers(0, 256, E * rec, dtype=np.uint8)
+    for e in range(E):  # sane f16 scales in every block (d ~ 0.01, m ~ -0.05)
+        b = blocks[e * rec:(e + 1) * rec].reshape(-1, 20)
+        b[:, 0:2] = np.frombuffer(np.float16(0.01).tobytes(), np.uint8)
+        b[:, 2:4] = np.frombuffer(np.float16(-0.05).tobytes(), np.uint8)
+    router = rng.standard_normal((E, Hs)).astype(np.float32) * 0.2
+    xt = (rng.standard_normal((2, Hs)) * 3.0).astype(np.float32)
+    norm = rng.uniform(0.5, 1.5, Hs)
+    a, ia, wa = mo.moe_ffn(xt, router, None, blocks, None, cfg, ffn_norm=norm)
+    xn = mo.rms_norm(xt, norm, 1e-5)
+    b_, ib, wb = mo.moe_ffn(xn, router, None, blocks, None, cfg)  # xn enters as f32, hence rtol 1e-5
+    assert np.array_equal(ia, ib) and np.allclose(a, b_, rtol=1e-5, atol=1e-9)
+    cfgr = mo.MoeConfig(**{**cfg.__dict__, "flags": mo.RESIDUAL})
+    r, _, _ = mo.moe_ffn(xt, router, None, blocks, None, cfgr, ffn_norm=norm)
+    assert np.allclose(r - xt.astype(np.float64), a, rtol=1e-12, atol=1e-12)
+
+
+def test_rms_norm_prologue():
+    check_rms_norm_prologue()
+
+
 def _random_cfg_layer(seed, shared=True, groups=False):
     from expert_ffn_decode_gb300 import synth
     w = dict(hidden=64, n_experts=8, top_k=3, expert_ff=32, shared_ff=64 if shared else 0,
@@ -377,7 +418,8 @@ def test_expert_matches_textbook_dense():
 ALL_CHECKS = [check_half_decode, check_golden_blocks, check_q4_0_is_q4_1_with_offset,
               check_block_dot_identity, check_golden_routing, check_routing_brute_force,
               check_routing_reductions, check_route_weights_closed_form,
-              check_swiglu_closed_form, check_swiglu_clamp_closed_form, check_combine_invariants,
+              check_swiglu_closed_form, check_swiglu_clamp_closed_form, check_rms_norm_prologue,
+              check_combine_invariants,
               check_expert_matches_textbook_dense]
 
 
@@ -476,6 +518,16 @@ def _mut_clamp_up_one_sided(x, w_gu, w_dn, limit=0.0):
     return w_dn @ (sg * u)
 
 
+def _mut_rms_eps_outside(x, weight, eps):
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    return x / (np.sqrt(np.mean(x * x, axis=1, keepdims=True)) + eps) * np.asarray(weight, np.float64)[None, :]
+
+
+def _mut_rms_sum_not_mean(x, weight, eps):
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    return x / np.sqrt(np.sum(x * x, axis=1, keepdims=True) + eps) * np.asarray(weight, np.float64)[None, :]
+
+
 def _mut_half_no_subnormal(bits):
     v = ORIG["half_to_float"](bits)
     h = np.asarray(bits, np.int64)
@@ -483,7 +535,8 @@ def _mut_half_no_subnormal(bits):
 
 
 ORIG = {name: getattr(mo, name) for name in
-        ["dequant_rows", "select_experts", "group_scores", "route_weights", "swiglu", "half_to_float"]}
+        ["dequant_rows", "select_experts", "group_scores", "route_weights", "swiglu", "half_to_float",
+         "rms_norm"]}
 
 MUTANTS = [
     ("dequant_rows", _mut_nibble_order),
@@ -498,6 +551,8 @@ MUTANTS = [
     ("swiglu", _mut_clamp_gate_first),
     ("swiglu", _mut_clamp_up_one_sided),
     ("half_to_float", _mut_half_no_subnormal),
+    ("rms_norm", _mut_rms_eps_outside),
+    ("rms_norm", _mut_rms_sum_not_mean),
 ]
 
 
