@@ -60,15 +60,19 @@ class moe_cfg(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("swiglu_limit", ctypes.c_float),
         ("swiglu_limit_shared", ctypes.c_float),
+        ("rms_eps", ctypes.c_float),
+        ("ffn_norm", ctypes.c_void_p),
     ]
 
 
 def make_cfg(hidden, n_experts, top_k, expert_ff, shared_ff=0, n_groups=1, groups_used=1,
              n_tokens=1, qtype=MOE_Q4_1, weights_scale=1.0, norm_min=NORM_MIN, flags=0,
-             swiglu_limit=0.0, swiglu_limit_shared=0.0, **_ignored):
-    """A :class:`moe_cfg` from keyword arguments (extra keys are ignored)."""
+             swiglu_limit=0.0, swiglu_limit_shared=0.0, rms_eps=0.0, ffn_norm=None, **_ignored):
+    """A :class:`moe_cfg` from keyword arguments (extra keys are ignored). ``ffn_norm`` is
+    a device vector (a tensor or an address) or None."""
     return moe_cfg(hidden, n_experts, top_k, expert_ff, shared_ff, n_groups, groups_used,
-                   n_tokens, qtype, weights_scale, norm_min, flags, swiglu_limit, swiglu_limit_shared)
+                   n_tokens, qtype, weights_scale, norm_min, flags, swiglu_limit, swiglu_limit_shared,
+                   rms_eps, _ptr(ffn_norm))
 
 
 class MoeError(RuntimeError):

@@ -75,6 +75,8 @@ int check_cfg(const moe_cfg* c) {
   if (!(c->swiglu_limit >= 0.f) || !std::isfinite(c->swiglu_limit) || !(c->swiglu_limit_shared >= 0.f) ||
       !std::isfinite(c->swiglu_limit_shared))
     return fail(MOE_ERR_INVALID_CFG, "swiglu limits must be finite and >= 0");
+  if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps))
+    return fail(MOE_ERR_INVALID_CFG, "rms_eps must be finite and >= 0");
   if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
@@ -82,7 +84,7 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, prefill, total;
+  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
 };
 
 // SMs of the current device (the timeline keeps one row per SM); without a
@@ -132,7 +134,12 @@ WsLayout ws_layout(const moe_cfg* c) {
     o = up256(o + (size_t)device_sms() * 24 * 8);
   }
   L.prefill = 0;
+  L.xn = 0;
   if (const int tp = prefill_pass_tokens(c->n_tokens)) {
+    if (c->ffn_norm) {
+      L.xn = o;  // batched passes: the normalised tokens [pass][H] f32
+      o = up256(o + (size_t)tp * c->hidden * 4);
+    }
     L.prefill = o;
     const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype);
     o = up256(o + moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff, c->shared_ff, tile)
@@ -282,6 +289,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   if (!(c->flags & MOE_HOST_IO) && (!aligned(x, 16) || !aligned(out, 16)))
     return fail(MOE_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
   if (bias && !aligned(bias, 4)) return fail(MOE_ERR_ALIGNMENT, "router_bias must be 4-byte aligned");
+  if (c->ffn_norm && !aligned(c->ffn_norm, 16)) return fail(MOE_ERR_ALIGNMENT, "ffn_norm must be 16-byte aligned");
   if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   const size_t xbytes = (size_t)T * c->hidden * 4;
   {
@@ -365,6 +373,9 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     pa.norm_min = c->norm_min;
     pa.lim = c->swiglu_limit;
     pa.lim_s = c->swiglu_limit_shared;
+    pa.norm = c->ffn_norm;
+    pa.eps = c->rms_eps;
+    pa.xn = c->ffn_norm ? reinterpret_cast<float*>(wsb + W.xn) : nullptr;
     pa.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
     pa.rb_h = pe.plan.rb_h;
     pa.rb_f = pe.plan.rb_f;
@@ -374,6 +385,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     for (int t0 = 0; t0 < T; t0 += tp) {
       pa.T = T - t0 < tp ? T - t0 : tp;
       pa.x = dx + (size_t)t0 * c->hidden;
+      pa.xres = pa.x;
       pa.out = dout + (size_t)t0 * c->hidden;
       pa.topk_ids = dids ? dids + (size_t)t0 * c->top_k : nullptr;
       pa.topk_w = dw ? dw + (size_t)t0 * c->top_k : nullptr;
@@ -395,6 +407,8 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.norm_min = c->norm_min;
   a.lim = c->swiglu_limit;
   a.lim_s = c->swiglu_limit_shared;
+  a.norm = c->ffn_norm;
+  a.eps = c->rms_eps;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
@@ -552,7 +566,8 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     return fail(MOE_ERR_NULL_PTR, "x, router_w, expert_blocks and out must not be NULL");
   if (c->shared_ff > 0 && !shared_blocks) return fail(MOE_ERR_NULL_PTR, "shared_ff > 0 needs shared_blocks");
   if (!aligned(router_w, 16) || !aligned(expert_blocks, 16) || (shared_blocks && !aligned(shared_blocks, 16)) ||
-      !aligned(x, 16) || !aligned(out, 16) || (router_bias && !aligned(router_bias, 4)))
+      !aligned(x, 16) || !aligned(out, 16) || (router_bias && !aligned(router_bias, 4)) ||
+      (c->ffn_norm && !aligned(c->ffn_norm, 16)))
     return fail(MOE_ERR_ALIGNMENT, "x, out, router_w and the blocks must be 16-byte aligned, the bias 4-byte");
   const size_t xbytes = (size_t)T * c->hidden * 4;
   {
@@ -591,6 +606,8 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.norm_min = c->norm_min;
   a.lim = c->swiglu_limit;
   a.lim_s = c->swiglu_limit_shared;
+  a.norm = c->ffn_norm;
+  a.eps = c->rms_eps;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -152,6 +152,28 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+
+// 1 / sqrt(mean(x^2) + eps) over a row of H floats (H a multiple of 4, x 16-byte
+// aligned), by a whole CTA of blockDim.x threads (a multiple of 32, at most 1024);
+// `red` is 32 floats of shared memory. Every thread gets the result; the summation
+// order is fixed. Synchronises the CTA.
+__device__ __forceinline__ float block_rms_scale(const float* x, int H, float eps, float* red) {
+  float ss = 0.f;
+  for (int h = 4 * (int)threadIdx.x; h < H; h += 4 * (int)blockDim.x) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(x + h));
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+  __syncthreads();  // red may be reused
+  return 1.f / sqrtf(tot / (float)H + eps);
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

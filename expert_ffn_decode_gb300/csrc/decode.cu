@@ -99,12 +99,13 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
 }
 
 // Quantise blocks [0, nb) of an f32 vector (global memory, or shared memory when
-// kShared) as quant_task describes. Each thread takes two tasks a round and loads
-// both before computing; every thread runs the same number of rounds and whole
-// warps call it (the groups use shuffles).
+// kShared) as quant_task describes; with `mul`, value i is first multiplied by
+// scal * mul[i]. Each thread takes two tasks a round and loads both before
+// computing; every thread runs the same number of rounds and whole warps call it
+// (the groups use shuffles).
 template <bool kShared = false>
 __device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float2* info,
-                                             int t, int nthreads) {
+                                             int t, int nthreads, const float* mul = nullptr, float scal = 1.f) {
   #pragma unroll 1
   for (int base = 0; base < 4 * nb; base += 2 * nthreads) {
     float v[2][8];
@@ -117,6 +118,13 @@ __device__ __forceinline__ void quant_blocks(const float* src, int nb, int strid
         const float4 a = kShared ? s4[0] : __ldcg(s4), c = kShared ? s4[1] : __ldcg(s4 + 1);
         v[h][0] = a.x; v[h][1] = a.y; v[h][2] = a.z; v[h][3] = a.w;
         v[h][4] = c.x; v[h][5] = c.y; v[h][6] = c.z; v[h][7] = c.w;
+        if (mul) {
+          const float4* m4 = reinterpret_cast<const float4*>(mul + (size_t)(idx[h] >> 2) * 32 + (idx[h] & 3) * 8);
+          const float4 ma = __ldg(m4), mc = __ldg(m4 + 1);
+          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mc.x, mc.y, mc.z, mc.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[h][i] = v[h][i] * scal * mm[i];
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[h][i] = 0.f;
@@ -448,6 +456,7 @@ __device__ __forceinline__ void select_picks(const DecodeArgs& a, uint8_t* sel, 
 // ===========================================================================
 __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int trows) {
   __shared__ float part[RT_THREADS / 32];
+  __shared__ float red[32];
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   tr(a, TR_RT_START, trows);
@@ -465,12 +474,22 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   pdl_wait_prior_grids();  // x may come from the previous kernel
   pdl_launch_dependents();
   tr(a, TR_RT_X, trows);
+  // the prologue (with a norm vector): the input is x * r * norm, r = 1/rms(x); the
+  // router dot takes x * norm and the row's sum is scaled by r
+  const float r = a.norm ? block_rms_scale(a.x, p.H, a.eps, red) : 1.f;
   float acc = 0.f;
 #pragma unroll
   for (int i = 0; i < 6; ++i) {
     const int j = lane + 32 * i;
     if (has && j < nq4) {
-      const float4 xv = __ldcg(reinterpret_cast<const float4*>(a.x + q * (p.H / 4)) + j);
+      float4 xv = __ldcg(reinterpret_cast<const float4*>(a.x + q * (p.H / 4)) + j);
+      if (a.norm) {
+        const float4 nv = __ldg(reinterpret_cast<const float4*>(a.norm + q * (p.H / 4)) + j);
+        xv.x *= nv.x;
+        xv.y *= nv.y;
+        xv.z *= nv.z;
+        xv.w *= nv.w;
+      }
       acc = fmaf(wv[i].x, xv.x, acc);
       acc = fmaf(wv[i].y, xv.y, acc);
       acc = fmaf(wv[i].z, xv.z, acc);
@@ -481,8 +500,8 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   if (lane == 0) part[warp] = acc;
   __syncthreads();
   if (tid < 2) {
-    const int r = blockIdx.x * 2 + tid;
-    if (r < p.E) a.logits[r] = ((part[4 * tid] + part[4 * tid + 1]) + part[4 * tid + 2]) + part[4 * tid + 3];
+    const int row2 = blockIdx.x * 2 + tid;
+    if (row2 < p.E) a.logits[row2] = (((part[4 * tid] + part[4 * tid + 1]) + part[4 * tid + 2]) + part[4 * tid + 3]) * r;
   }
   tr(a, TR_RT_DONE, trows);
 }
@@ -530,7 +549,11 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
   if (shared && tid < 4) issue(a.shared);
   // x -> activation blocks (x is complete: the router kernel waited for it before this
   // launch was triggered)
-  quant_blocks(a.x, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS);
+  {
+    __shared__ float red[32];
+    const float r = a.norm ? block_rms_scale(a.x, p.H, a.eps, red) : 1.f;
+    quant_blocks(a.x, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, r);
+  }
   __syncthreads();
   tr(a, TR_GU_XQ, trows);
   const RowMap mh = row_map(p.nbH, lane);

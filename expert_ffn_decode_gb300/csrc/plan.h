@@ -76,6 +76,8 @@ struct DecodeArgs {
   float* act;                 // [K * F + Fs] SwiGLU activations, shared expert's first
   float scale, norm_min;
   float lim, lim_s;           // SwiGLU clamp limits of the routed and shared experts (0: none)
+  const float* norm;          // [H] prologue norm weights, or null (x enters as is)
+  float eps;                  // the prologue's epsilon
   uint32_t flags;
   DecodePlan p;
 };

@@ -522,9 +522,23 @@ __global__ void prefill_combine(const PrefillArgs a) {
   float acc = 0.f;
   for (int j = 0; j < a.K; ++j) acc += a.ybuf[(size_t)a.pos_of[(size_t)t * a.K + j] * a.H + h];
   if (a.Fs) acc += a.sbuf[i];
-  if (a.flags & FLAG_RESIDUAL) acc = a.x[i] + acc;
+  if (a.flags & FLAG_RESIDUAL) acc = a.xres[i] + acc;
   if (a.flags & FLAG_ACCUMULATE) acc = a.out[i] + acc;
   a.out[i] = acc;
+}
+
+// The layer prologue: xn[t] = x[t] / sqrt(mean(x[t]^2) + eps) * norm, one CTA per token.
+__global__ void __launch_bounds__(256) prefill_rmsnorm(const PrefillArgs a) {
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  const float* xr = a.x + (size_t)t * a.H;
+  const float r = block_rms_scale(xr, a.H, a.eps, red);
+  for (int h = 4 * threadIdx.x; h < a.H; h += 4 * blockDim.x) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(xr + h));
+    const float4 n = __ldg(reinterpret_cast<const float4*>(a.norm + h));
+    *reinterpret_cast<float4*>(a.xn + (size_t)t * a.H + h) =
+        make_float4(v.x * r * n.x, v.y * r * n.y, v.z * r * n.z, v.w * r * n.w);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -583,9 +597,17 @@ static cudaError_t launch_gemm(const PrefillArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st) {
+cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
   cudaError_t e;
+  PrefillArgs a = a_in;
   const size_t nx = (size_t)a.T * a.H;
+  if (a.norm) {
+    // the prologue: every kernel below reads the normalised tokens, the combine's
+    // residual the raw ones (a.xres)
+    prefill_rmsnorm<<<(unsigned)a.T, 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    a.x = a.xn;
+  }
   if (a.tile) {
     // token-chunk images first: the router and the shared expert read them
     if ((e = tile_images_launch(a, false, st)) != cudaSuccess) return e;

@@ -59,6 +59,10 @@ struct PrefillArgs {
   int T, H, E, K, F, Fs, G, Gu, qtype;
   float scale, norm_min;
   float lim, lim_s;         // SwiGLU clamp limits of the routed and shared experts (0: none)
+  const float* norm;        // [H] prologue norm weights, or null
+  float eps;                // the prologue's epsilon
+  const float* xres;        // [T][H] the raw tokens (the residual form adds these)
+  float* xn;                // [T][H] workspace for the normalised tokens (with a norm)
   uint32_t flags;
   uint32_t rb_h, rb_f, rb_fs;
   uint64_t rec_bytes;

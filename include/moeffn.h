@@ -107,6 +107,13 @@ typedef struct moe_cfg {
    * swiglu_clamp_exp / swiglu_clamp_shexp arrays do. */
   float swiglu_limit;
   float swiglu_limit_shared;
+  /* Optional layer prologue: with ffn_norm (a device vector [hidden] f32, 16-byte
+   * aligned) the step's input is rms_norm(x) * ffn_norm, rms_norm(x) = x /
+   * sqrt(mean(x^2) + rms_eps) (flint_moe_ssd.js / lfm2_moe_ssd.js headers: x +=
+   * ffn(rms_norm(x) * ffn_norm)); MOE_RESIDUAL then adds the raw x, giving the whole
+   * FFN block. NULL: x enters as is. */
+  float rms_eps;
+  const float* ffn_norm;
 } moe_cfg;
 
 /* Two execution paths, chosen by n_tokens (both are exact restatements of the step

@@ -24,7 +24,8 @@ def oracle_cfg(w: dict, flags: int = 0) -> mo.MoeConfig:
                         groups_used=w["groups_used"], qtype=w["qtype"],
                         weights_scale=w["weights_scale"], norm_min=w.get("norm_min", mo.NORM_MIN),
                         flags=flags, swiglu_limit=w.get("swiglu_limit", 0.0),
-                        swiglu_limit_shared=w.get("swiglu_limit_shared", 0.0))
+                        swiglu_limit_shared=w.get("swiglu_limit_shared", 0.0),
+                        rms_eps=w.get("rms_eps", 0.0))
 
 
 def selection_gap(s: np.ndarray, w: dict) -> float:
@@ -46,14 +47,16 @@ def selection_gap(s: np.ndarray, w: dict) -> float:
     return float(min(gaps)) if gaps else np.inf
 
 
-def margin_tokens(layer: dict, w: dict, n: int, seed: int, stream: int = 1):
-    """n tokens from the seeded stream, skipping draws within MARGIN of a tie."""
+def margin_tokens(layer: dict, w: dict, n: int, seed: int, stream: int = 1, norm=None, scale: float = 1.0):
+    """n tokens from the seeded stream (times `scale`), skipping draws within MARGIN of a
+    tie; with a prologue norm vector the routing is that of the normalised token."""
     cfg = oracle_cfg(w)
     it = synth.token_stream(seed, w["hidden"], stream)
     out, redraws = [], 0
     while len(out) < n:
-        x = next(it)
-        _, _, s = mo.route(x, layer["router_w"], layer["bias"], cfg)
+        x = (next(it) * np.float32(scale)).astype(np.float32)
+        xr = x if norm is None else mo.rms_norm(x, norm, cfg.rms_eps)
+        _, _, s = mo.route(xr, layer["router_w"], layer["bias"], cfg)
         if selection_gap(s[0], w) >= MARGIN:
             out.append(x)
         else:

@@ -134,6 +134,31 @@ def test_ling_decode_with_clamp():
     compare(out, ids, wts, ref, rid, rwt, "ling clamp")
 
 
+PROLOGUE = [
+    _small(33, shared_ff=64, rms_eps=1e-5),
+    _small(34, qtype=mo.Q4_0, n_experts=64, n_groups=8, groups_used=3, top_k=6, bias_std=0.1, rms_eps=1e-6),
+    # a dense SwiGLU layer: one expert, always picked with weight 1 (the router is moot)
+    _small(35, hidden=512, expert_ff=1024, n_experts=1, top_k=1, rms_eps=1e-5),
+]
+
+
+@pytest.mark.parametrize("w", PROLOGUE, ids=[f"s{w['seed']}" for w in PROLOGUE])
+def test_rms_norm_prologue(w):
+    # x += ffn(rms_norm(x) * ffn_norm): the prologue folded into the step, with the raw x
+    # added back by the residual form; tokens scaled by 3 so the norm matters
+    import expert_ffn_decode_gb300 as ffn
+    import torch
+    layer = synth.make_layer(w)
+    norm = np.random.default_rng(w["seed"] + 100).uniform(0.5, 1.5, w["hidden"]).astype(np.float32)
+    x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"], norm=norm, scale=3.0)
+    wn = {**w, "ffn_norm": torch.from_numpy(norm).cuda()}
+    for flags, oflags in ((0, 0), (ffn.MOE_RESIDUAL, mo.RESIDUAL)):
+        ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                                   layer["shared_blocks"], oracle_cfg(w, oflags), ffn_norm=norm)
+        out, ids, wts = GpuLayer(layer, wn).run(x, flags=flags)
+        compare(out, ids, wts, ref, rid, rwt, f"prologue seed {w['seed']} flags {flags}")
+
+
 def test_flags_accumulate_residual_hostio_nopdl():
     import expert_ffn_decode_gb300 as ffn
     w, layer = layer_of("flint_decode_t1")

@@ -93,6 +93,28 @@ def test_prefill_swiglu_clamp(w):
     assert min(rel_l2(out[t], unclamped[t]) for t in range(len(x))) > 1e-2
 
 
+PROLOGUE = [
+    _small(62, shared_ff=128, n_tokens=40, rms_eps=1e-5),                                 # tile path
+    _small(63, hidden=96, expert_ff=96, shared_ff=96, qtype=mo.Q4_0, n_tokens=20, rms_eps=1e-6),
+    _small(64, hidden=512, expert_ff=1024, n_experts=1, top_k=1, n_tokens=24, rms_eps=1e-5),  # dense layer
+]
+
+
+@pytest.mark.parametrize("w", PROLOGUE, ids=["tile", "general", "dense"])
+def test_prefill_rms_norm_prologue(w):
+    import expert_ffn_decode_gb300 as ffn
+    import torch
+    layer = synth.make_layer(w)
+    norm = np.random.default_rng(w["seed"] + 100).uniform(0.5, 1.5, w["hidden"]).astype(np.float32)
+    x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"], norm=norm, scale=3.0)
+    wn = {**w, "ffn_norm": torch.from_numpy(norm).cuda()}
+    for flags, oflags in ((0, 0), (ffn.MOE_RESIDUAL, mo.RESIDUAL)):
+        ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                                   layer["shared_blocks"], oracle_cfg(w, oflags), ffn_norm=norm)
+        out, ids, wts = GpuLayer(layer, wn).run(x, flags=flags)
+        compare(out, ids, wts, ref, rid, rwt, f"prologue seed {w['seed']} flags {flags}")
+
+
 @pytest.mark.parametrize("shared_ff", [64, 128], ids=["general", "tile"])
 def test_prefill_two_passes_and_decode_boundary(shared_ff):
     # 7 tokens decode token by token, 8 take the batched path, 600 run as passes of 512 + 88
