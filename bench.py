@@ -340,6 +340,60 @@ def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, 
             "h2d_bytes_per_step": T * H * 4, "d2h_bytes_per_step": T * H * 4}
 
 
+def sweep_tokens(args, ffn, synth, w, dev, layers_n=4, calls=8, reps=5):
+    """Microseconds per call for each T of --sweep-tokens: the library's own path (decode
+    below the batched threshold, the batched path from it) against T single-token calls.
+    Each is a CUDA graph of `calls` calls over `layers_n` rotated layers, replayed `reps`
+    times after a warm replay, timed with CUDA events on the replaying stream."""
+    import torch
+    layers = [synth.make_layer_torch(w, 100 + i, dev) for i in range(layers_n)]
+    H = w["hidden"]
+    st = torch.cuda.Stream(dev)
+    table = {}
+    for T in [int(v) for v in args.sweep_tokens.split(",") if v]:
+        x = torch.randn(T, H, device=dev)
+        out = torch.empty(T, H, device=dev)
+        cfg_t = ffn.make_cfg(**{**w, "n_tokens": T})
+        cfg_1 = ffn.make_cfg(**{**w, "n_tokens": 1})
+        n_t, n_1 = ffn.moe_workspace_size(cfg_t), ffn.moe_workspace_size(cfg_1)
+        ws_t = torch.zeros(n_t, dtype=torch.uint8, device=dev)
+        ws_1 = torch.zeros(n_1, dtype=torch.uint8, device=dev)
+
+        def whole(i):
+            lay = layers[i % layers_n]
+            ffn.check(ffn.moe_ffn_forward_ex(x, lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                             lay["shared_blocks"], cfg_t, out, ws_t, n_t, st))
+
+        def tokenwise(i):
+            lay = layers[i % layers_n]
+            for t in range(T):
+                ffn.check(ffn.moe_ffn_forward_ex(x[t], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                                 lay["shared_blocks"], cfg_1, out[t], ws_1, n_1, st))
+
+        row = {}
+        for name, fn in (("library", whole), ("tokenwise", tokenwise)):
+            with torch.cuda.stream(st):
+                for i in range(3):
+                    fn(i)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(calls):
+                    fn(i)
+            with torch.cuda.stream(st):
+                g.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(st)
+            st.synchronize()
+            row[name] = round(e0.elapsed_time(e1) * 1000 / (reps * calls), 1)
+        table[T] = row
+    print(json.dumps({"workload": args.workload, "us_per_call": table}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -354,6 +408,10 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=480, help="timed batched steps (0: skip)")
     ap.add_argument("--trace", action="store_true",
                     help="after timing, print the kernel's per-CTA phase timeline (stderr)")
+    ap.add_argument("--sweep-tokens", default="",
+                    help="comma-separated tokens per call: time one call of each on the workload's "
+                         "layer (the library's choice of path against token-by-token decode), print the "
+                         "table as JSON and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -373,6 +431,8 @@ def main():
         build.build()
     w = synth.WORKLOADS[args.workload]
     T, H = w["n_tokens"], w["hidden"]
+    if args.sweep_tokens:
+        return sweep_tokens(args, ffn, synth, w, dev)
     if T != 1:
         return main_prefill(args, ffn, synth, dev, rank, world, local)
     step_bytes = layer_bytes(w)

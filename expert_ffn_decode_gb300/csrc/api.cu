@@ -77,14 +77,14 @@ int check_cfg(const moe_cfg* c) {
     return fail(MOE_ERR_INVALID_CFG, "swiglu limits must be finite and >= 0");
   if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps))
     return fail(MOE_ERR_INVALID_CFG, "rms_eps must be finite and >= 0");
-  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE))
+  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE | MOE_BATCHED))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
 }
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
+  size_t ctrl, logits, act, ids, wts, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
 };
 
 // SMs of the current device (the timeline keeps one row per SM); without a
@@ -99,23 +99,40 @@ int device_sms() {
   return sms;
 }
 
-// Tokens of one prefill pass for a call of T tokens (0: the call decodes token by token).
-int prefill_pass_tokens(int T) {
-  if (T < moe::PREFILL_MIN_T) return 0;
+// Tokens of one batched pass for a call (0: the call takes the decode path). Calls of
+// at least PREFILL_MIN_T tokens, or any call with MOE_BATCHED, take the batched path.
+int prefill_pass_tokens(const moe_cfg* c) {
+  const int T = c->n_tokens;
+  if (T < 1 || (T < moe::PREFILL_MIN_T && !(c->flags & MOE_BATCHED))) return 0;
   return T < moe::PREFILL_CHUNK_T ? T : moe::PREFILL_CHUNK_T;
 }
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-WsLayout ws_layout(const moe_cfg* c) {
+// Tokens per decode call for a call on the decode path (1 otherwise).
+int decode_call_tokens(const moe_cfg* c) {
+  const int T = c->n_tokens;
+  if (prefill_pass_tokens(c) || T < 1) return 1;
+  return T < moe::DEC_TMAX ? T : moe::DEC_TMAX;
+}
+
+// decode_only: the layout of calls that always decode (moe_ffn_forward_noalloc), up
+// to DEC_TMAX tokens at a time and without the batched path's regions.
+WsLayout ws_layout(const moe_cfg* c, bool decode_only = false) {
   WsLayout L;
   size_t o = 0;
   L.ctrl = o;
   o += moe::CTRL_BYTES;
-  L.logits = o;  // decode: router logits [E] f32
-  o = up256(o + (size_t)c->n_experts * 4);
-  L.act = o;     // decode: SwiGLU activations of every slot [K * F + Fs] f32
-  o = up256(o + ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
+  const size_t td = decode_only ? (size_t)(c->n_tokens < moe::DEC_TMAX ? c->n_tokens : moe::DEC_TMAX)
+                                : (size_t)decode_call_tokens(c);  // tokens of one decode call
+  L.logits = o;  // decode: router logits [td][E] f32
+  o = up256(o + td * c->n_experts * 4);
+  L.act = o;     // decode: SwiGLU activations of every slot [td][K * F + Fs] f32
+  o = up256(o + td * ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
+  L.ids = o;     // decode: picks and weights [td][K] (calls of several tokens)
+  o = up256(o + td * c->top_k * 4);
+  L.wts = o;
+  o = up256(o + td * c->top_k * 4);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -135,7 +152,7 @@ WsLayout ws_layout(const moe_cfg* c) {
   }
   L.prefill = 0;
   L.xn = 0;
-  if (const int tp = prefill_pass_tokens(c->n_tokens)) {
+  if (const int tp = decode_only ? 0 : prefill_pass_tokens(c)) {
     if (c->ffn_norm) {
       L.xn = o;  // batched passes: the normalised tokens [pass][H] f32
       o = up256(o + (size_t)tp * c->hidden * 4);
@@ -185,6 +202,7 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.nbF = p.F / 32;
   p.nbFs = p.Fs / 32;
   p.nact = p.nbFs + p.K * p.nbF;
+  p.act_stride = p.K * p.F + p.Fs;
   const uint32_t budget = 200u * 1024u;  // dynamic shared memory of one CTA
   // gate/up: 4 windows of 8 rows, the x blocks and the selection
   p.gu_win = moe::window_bytes(8u * p.rb_h);
@@ -325,7 +343,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     }
   }
 
-  if (const int tp = prefill_pass_tokens(T)) {
+  if (const int tp = prefill_pass_tokens(c)) {
     // batched path: router, top-k, expert sort and grouped tensor-core GEMMs
     const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype);
     const moe::PrefillWs P = moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff,
@@ -402,6 +420,8 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<float*>(wsb + W.logits);
   a.act = reinterpret_cast<float*>(wsb + W.act);
+  a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
+  a.wts = reinterpret_cast<float*>(wsb + W.wts);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -412,7 +432,9 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
-  for (int t = 0; t < T && !prefill_pass_tokens(T); ++t) {
+  const int td = decode_call_tokens(c);
+  for (int t = 0; t < T && !prefill_pass_tokens(c); t += td) {
+    a.T = T - t < td ? T - t : td;
     a.x = dx + (size_t)t * c->hidden;
     a.out = dout + (size_t)t * c->hidden;
     a.topk_ids = dids ? dids + (size_t)t * c->top_k : nullptr;
@@ -575,9 +597,14 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     const char* oa = reinterpret_cast<const char*>(out);
     if (xa < oa + xbytes && oa < xa + xbytes) return fail(MOE_ERR_INVALID_CFG, "x and out overlap");
   }
-  moe_cfg c1 = *c;  // the calls decode token by token: one token's scratch
-  c1.n_tokens = 1;
-  const WsLayout W = ws_layout(&c1);
+  // the calls decode up to td tokens at a time: as many as the fixed scratch holds
+  moe_cfg c1 = *c;
+  int td = T < moe::DEC_TMAX ? T : moe::DEC_TMAX;
+  for (;; --td) {
+    c1.n_tokens = td;
+    if (td == 1 || ws_layout(&c1, true).total <= NOALLOC_SCRATCH_BYTES) break;
+  }
+  const WsLayout W = ws_layout(&c1, true);
   if (W.total > NOALLOC_SCRATCH_BYTES)
     return fail(MOE_ERR_UNSUPPORTED,
                 "this layer needs %zu bytes of scratch; the fixed scratch of moe_ffn_forward_noalloc holds %zu",
@@ -601,6 +628,8 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<float*>(wsb + W.logits);
   a.act = reinterpret_cast<float*>(wsb + W.act);
+  a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
+  a.wts = reinterpret_cast<float*>(wsb + W.wts);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -612,7 +641,8 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.p = pe.plan;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
-  for (int t = 0; t < T; ++t) {
+  for (int t = 0; t < T; t += td) {
+    a.T = T - t < td ? T - t : td;
     a.x = x + (size_t)t * c->hidden;
     a.out = out + (size_t)t * c->hidden;
     a.topk_ids = nullptr;

@@ -268,7 +268,8 @@ enum TracePoint : int {
   TR_POINTS = 24
 };
 __device__ __forceinline__ void tr(const DecodeArgs& a, int point, int rows) {
-  if (a.trace && threadIdx.x == 0 && (int)blockIdx.x < rows) a.trace[(size_t)blockIdx.x * TR_POINTS + point] = globaltimer();
+  if (a.trace && threadIdx.x == 0 && blockIdx.y == 0 && (int)blockIdx.x < rows)
+    a.trace[(size_t)blockIdx.x * TR_POINTS + point] = globaltimer();
 }
 
 __device__ __forceinline__ void report_timeout(const DecodeArgs& a) {
@@ -309,7 +310,8 @@ __device__ __forceinline__ void sort_list(uint32_t (&kv)[N], int (&ki)[N]) {
 //      the weights
 // Key 0 is below every real key (every float's key is at least that of -inf).
 template <int N>
-__device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore, int* rids, float* rw) {
+__device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* sel, float* gscore, int* rids,
+                               float* rw) {
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* probs = reinterpret_cast<float*>(sel);
@@ -322,7 +324,7 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
 #pragma unroll
     for (int i = 0; i < N; ++i) {  // loads first
       const int e = tid + 256 * i;
-      l[i] = e < p.E ? __ldcg(a.logits + e) : 0.f;
+      l[i] = e < p.E ? __ldcg(lg + e) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < N; ++i) {
@@ -444,19 +446,21 @@ __device__ void select_picks_n(const DecodeArgs& a, uint8_t* sel, float* gscore,
   }
   __syncthreads();
 }
-__device__ __forceinline__ void select_picks(const DecodeArgs& a, uint8_t* sel, float* gscore, int* rids,
-                                             float* rw) {
-  if (a.p.E <= 256) select_picks_n<1>(a, sel, gscore, rids, rw);
-  else if (a.p.E <= 512) select_picks_n<2>(a, sel, gscore, rids, rw);
-  else select_picks_n<4>(a, sel, gscore, rids, rw);
+// The picks of the token whose logits row is `lg`.
+__device__ __forceinline__ void select_picks(const DecodeArgs& a, const float* lg, uint8_t* sel, float* gscore,
+                                             int* rids, float* rw) {
+  if (a.p.E <= 256) select_picks_n<1>(a, lg, sel, gscore, rids, rw);
+  else if (a.p.E <= 512) select_picks_n<2>(a, lg, sel, gscore, rids, rw);
+  else select_picks_n<4>(a, lg, sel, gscore, rids, rw);
 }
 
 // ===========================================================================
 // Router: logits
 // ===========================================================================
 __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int trows) {
-  __shared__ float part[RT_THREADS / 32];
-  __shared__ float red[32];
+  __shared__ float part[RT_THREADS / 32][DEC_TMAX];
+  __shared__ float red[RT_THREADS / 32][DEC_TMAX];
+  __shared__ float rscale[DEC_TMAX];
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   tr(a, TR_RT_START, trows);
@@ -474,36 +478,92 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   pdl_wait_prior_grids();  // x may come from the previous kernel
   pdl_launch_dependents();
   tr(a, TR_RT_X, trows);
-  // the prologue (with a norm vector): the input is x * r * norm, r = 1/rms(x); the
-  // router dot takes x * norm and the row's sum is scaled by r
-  const float r = a.norm ? block_rms_scale(a.x, p.H, a.eps, red) : 1.f;
-  float acc = 0.f;
+  // the prologue (with a norm vector): token t's input is x_t * r_t * norm, r_t =
+  // 1/rms(x_t); the router dot takes x_t * norm and the row's sum is scaled by r_t.
+  // Every token's sum of squares in one pass (loads of all tokens in flight together).
+  if (a.norm) {
+    float ss[DEC_TMAX];
+#pragma unroll
+    for (int t = 0; t < DEC_TMAX; ++t) ss[t] = 0.f;
+    for (int h = 4 * tid; h < p.H; h += 4 * RT_THREADS) {
+#pragma unroll
+      for (int t = 0; t < DEC_TMAX; ++t) {
+        if (t < a.T) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x + (size_t)t * p.H + h));
+          ss[t] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[t]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < DEC_TMAX; ++t) {
+      if (t < a.T) {
+        const float v = warp_sum(ss[t]);
+        if (lane == 0) red[warp][t] = v;
+      }
+    }
+    __syncthreads();
+    if (tid < a.T) {
+      float tot = 0.f;
+      for (int w = 0; w < RT_THREADS / 32; ++w) tot += red[w][tid];
+      rscale[tid] = 1.f / sqrtf(tot / (float)p.H + a.eps);
+    }
+  }
+  float4 nv[6];
 #pragma unroll
   for (int i = 0; i < 6; ++i) {
     const int j = lane + 32 * i;
-    if (has && j < nq4) {
-      float4 xv = __ldcg(reinterpret_cast<const float4*>(a.x + q * (p.H / 4)) + j);
-      if (a.norm) {
-        const float4 nv = __ldg(reinterpret_cast<const float4*>(a.norm + q * (p.H / 4)) + j);
-        xv.x *= nv.x;
-        xv.y *= nv.y;
-        xv.z *= nv.z;
-        xv.w *= nv.w;
+    nv[i] = (a.norm && has && j < nq4) ? __ldg(reinterpret_cast<const float4*>(a.norm + q * (p.H / 4)) + j)
+                                       : make_float4(1.f, 1.f, 1.f, 1.f);
+  }
+#pragma unroll 1
+  for (int t = 0; t < a.T; ++t) {
+    const float* xt = a.x + (size_t)t * p.H + q * (p.H / 4);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+      const int j = lane + 32 * i;
+      if (has && j < nq4) {
+        const float4 xv = __ldcg(reinterpret_cast<const float4*>(xt) + j);
+        acc = fmaf(wv[i].x, xv.x * nv[i].x, acc);
+        acc = fmaf(wv[i].y, xv.y * nv[i].y, acc);
+        acc = fmaf(wv[i].z, xv.z * nv[i].z, acc);
+        acc = fmaf(wv[i].w, xv.w * nv[i].w, acc);
       }
-      acc = fmaf(wv[i].x, xv.x, acc);
-      acc = fmaf(wv[i].y, xv.y, acc);
-      acc = fmaf(wv[i].z, xv.z, acc);
-      acc = fmaf(wv[i].w, xv.w, acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) part[warp][t] = acc;
+  }
+  __syncthreads();
+  for (int u = tid; u < 2 * a.T; u += RT_THREADS) {
+    const int rr = u & 1, t = u >> 1;
+    const int row2 = blockIdx.x * 2 + rr;
+    if (row2 < p.E) {
+      const float v = ((part[4 * rr][t] + part[4 * rr + 1][t]) + part[4 * rr + 2][t]) + part[4 * rr + 3][t];
+      a.logits[(size_t)t * p.E + row2] = a.norm ? v * rscale[t] : v;
     }
   }
-  acc = warp_sum(acc);
-  if (lane == 0) part[warp] = acc;
-  __syncthreads();
-  if (tid < 2) {
-    const int row2 = blockIdx.x * 2 + tid;
-    if (row2 < p.E) a.logits[row2] = (((part[4 * tid] + part[4 * tid + 1]) + part[4 * tid + 2]) + part[4 * tid + 3]) * r;
-  }
   tr(a, TR_RT_DONE, trows);
+}
+
+// ===========================================================================
+// Selection of a call of several tokens: one CTA per token
+// ===========================================================================
+__global__ void __launch_bounds__(256) dec_select(const DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t ssm[];
+  __shared__ float gscore[64];
+  __shared__ int rids[32];
+  __shared__ float rw[32];
+  const int t = blockIdx.x;
+  pdl_wait_prior_grids();  // the logits
+  pdl_launch_dependents();
+  select_picks(a, a.logits + (size_t)t * a.p.E, ssm, gscore, rids, rw);
+  if (threadIdx.x < a.p.K) {
+    const size_t o = (size_t)t * a.p.K + threadIdx.x;
+    a.ids[o] = rids[threadIdx.x];
+    a.wts[o] = rw[threadIdx.x];
+    if (a.topk_ids) a.topk_ids[o] = rids[threadIdx.x];
+    if (a.topk_w) a.topk_w[o] = rw[threadIdx.x];
+  }
 }
 
 // ===========================================================================
@@ -523,6 +583,8 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int v0 = blockIdx.x * GU_VALUES;  // first activation index of the CTA
+  const int tok = blockIdx.y;             // the call's token
+  const float* xt = a.x + (size_t)tok * p.H;
   const bool shared = v0 < p.Fs;          // the shared expert's values need no routing
   const int ff = shared ? p.Fs : p.F;
   const int f0 = shared ? v0 : (v0 - p.Fs) % p.F;
@@ -551,8 +613,8 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
   // launch was triggered)
   {
     __shared__ float red[32];
-    const float r = a.norm ? block_rms_scale(a.x, p.H, a.eps, red) : 1.f;
-    quant_blocks(a.x, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, r);
+    const float r = a.norm ? block_rms_scale(xt, p.H, a.eps, red) : 1.f;
+    quant_blocks(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, r);
   }
   __syncthreads();
   tr(a, TR_GU_XQ, trows);
@@ -568,13 +630,19 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
     pdl_wait_prior_grids();  // the logits
     pdl_launch_dependents();
     tr(a, TR_GU_WAITED, trows);
-    select_picks(a, sel, gscore, rids, rw);
-    rec = a.experts + (size_t)rids[(v0 - p.Fs) / p.F] * p.rec_bytes;
-    if (tid < 4) issue(rec);
-    if (v0 == p.Fs && tid < p.K) {  // one CTA reports the picks
-      if (a.topk_ids) a.topk_ids[tid] = rids[tid];
-      if (a.topk_w) a.topk_w[tid] = rw[tid];
+    const int slot = (v0 - p.Fs) / p.F;
+    if (a.T == 1) {
+      select_picks(a, a.logits, sel, gscore, rids, rw);
+      if (v0 == p.Fs && tid < p.K) {  // one CTA reports the picks
+        if (a.topk_ids) a.topk_ids[tid] = rids[tid];
+        if (a.topk_w) a.topk_w[tid] = rw[tid];
+      }
+    } else if (tid == 0) {
+      rids[slot] = __ldcg(a.ids + (size_t)tok * p.K + slot);  // made by the selection kernel
     }
+    __syncthreads();
+    rec = a.experts + (size_t)rids[slot] * p.rec_bytes;
+    if (tid < 4) issue(rec);
   } else {
     pdl_launch_dependents();
   }
@@ -621,7 +689,8 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
   }
   __syncwarp();
   if (lane < 2)
-    a.act[v0 + 2 * warp + lane] = swiglu_act(rowdot[warp][2 * lane], rowdot[warp][2 * lane + 1], shared ? a.lim_s : a.lim);
+    a.act[(size_t)tok * p.act_stride + v0 + 2 * warp + lane] =
+        swiglu_act(rowdot[warp][2 * lane], rowdot[warp][2 * lane + 1], shared ? a.lim_s : a.lim);
   tr(a, TR_GU_END, trows);
 }
 
@@ -646,6 +715,7 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = p.dn_rows, h0 = blockIdx.x * R;
+  const int tok = blockIdx.y;  // the call's token
   const int nwin = p.K + (p.Fs ? 1 : 0);
   tr(a, TR_DN_START, trows);
   const size_t win_r = (size_t)p.dn_win_fs;  // first routed window
@@ -658,7 +728,16 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   }
   // the picks (the router is complete: every routed gate/up CTA waited for it before
   // this launch was triggered)
-  select_picks(a, sel, gscore, rids, rw);
+  if (a.T == 1) {
+    select_picks(a, a.logits, sel, gscore, rids, rw);
+  } else {
+    // made by the selection kernel, complete once every routed gate/up CTA has waited
+    if (tid < p.K) {
+      rids[tid] = __ldcg(a.ids + (size_t)tok * p.K + tid);
+      rw[tid] = __ldcg(a.wts + (size_t)tok * p.K + tid);
+    }
+    __syncthreads();
+  }
   tr(a, TR_DN_PICKED, trows);
   if (tid < nwin) {
     // this CTA's rows of slot window tid's down matrix, copied by thread tid
@@ -687,7 +766,8 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   #pragma unroll 1
   for (int pb = 0; pb < nact; pb += p.dn_piece) {
     const int np = nact - pb < p.dn_piece ? nact - pb : p.dn_piece;
-    quant_blocks(a.act + (size_t)pb * 32, np, p.dn_piece, aplanes, ainfo, tid, DN_THREADS);
+    quant_blocks(a.act + (size_t)tok * p.act_stride + (size_t)pb * 32, np, p.dn_piece, aplanes, ainfo, tid,
+                 DN_THREADS);
     __syncthreads();  // the piece; on the first pass also the window offsets
     if (pb == 0) {
       tr(a, TR_DN_QUANT, trows);
@@ -735,7 +815,7 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
     const int g = tid / RPG, rl = tid % RPG, w0 = g * (TPG / 32);
     float y = 0.f;
     for (int w = 0; w < TPG / 32; ++w) y += part[w0 + w][rl];
-    const int h = h0 + tid;
+    const size_t h = (size_t)tok * p.H + h0 + tid;
     if (a.flags & FLAG_RESIDUAL) y = __ldcg(a.x + h) + y;
     if (a.flags & FLAG_ACCUMULATE) y = __ldcg(a.out + h) + y;
     a.out[h] = y;
@@ -767,13 +847,18 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, int threads, siz
 template <int QT, int MAXB>
 static cudaError_t launch_chain(const DecodeArgs& a, cudaStream_t st, bool pdl, int trows) {
   const DecodePlan& p = a.p;
+  const unsigned T = (unsigned)a.T;
   cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)0, st, pdl, a, trows);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(dec_gate_up<QT, MAXB>, dim3((unsigned)((p.K * p.F + p.Fs) / GU_VALUES)), GU_THREADS,
+  if (T > 1) {  // one selection per token, shared by the gate/up and down CTAs
+    e = launch_pdl(dec_select, dim3(T), 256, (size_t)select_smem(p.E), st, pdl, a);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_pdl(dec_gate_up<QT, MAXB>, dim3((unsigned)((p.K * p.F + p.Fs) / GU_VALUES), T), GU_THREADS,
                  (size_t)p.gu_smem, st, pdl, a, trows);
   if (e != cudaSuccess) return e;
-  return launch_pdl(dec_down<QT>, dim3((unsigned)(p.H / p.dn_rows)), DN_THREADS, (size_t)p.dn_smem, st, pdl, a,
-                    trows);
+  return launch_pdl(dec_down<QT>, dim3((unsigned)(p.H / p.dn_rows), T), DN_THREADS, (size_t)p.dn_smem, st, pdl,
+                    a, trows);
 }
 
 cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, int trows) {

@@ -32,6 +32,7 @@ struct DecodePlan {
   // blocks
   int nbH, nbF, nbFs;   // blocks per gate/up row, routed down row, shared down row
   int nact;             // activation blocks: (K * F + Fs) / 32 (shared expert's first)
+  int act_stride;       // floats from one token's activations to the next (K * F + Fs)
   // gate/up kernel: two chunks of 8 values, each a gate and an up window of 8 rows
   uint32_t gu_win;      // bytes of one window (8 rows rounded out to 16-byte bounds)
   uint32_t gu_smem;     // dynamic shared memory
@@ -45,6 +46,7 @@ struct DecodePlan {
 };
 
 constexpr int GU_VALUES = 16;  // intermediate values per gate/up CTA
+constexpr int DEC_TMAX = 16;   // tokens per decode call (the chain takes up to this many at once)
 
 MOE_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
 MOE_HD uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -62,18 +64,21 @@ constexpr uint32_t FLAG_RESIDUAL = 2u;    // out = x + contribution
 
 // Arguments of the three decode kernels (one token).
 struct DecodeArgs {
-  const float* x;             // [H]
+  const float* x;             // [T][H]
   const float* router_w;      // [E][H]
   const float* bias;          // [E] or null
   const uint8_t* experts;     // E packed records
   const uint8_t* shared;      // shared record or null
-  float* out;                 // [H]
-  int32_t* topk_ids;          // [K] or null
-  float* topk_w;              // [K] or null
+  float* out;                 // [T][H]
+  int32_t* topk_ids;          // [T][K] or null
+  float* topk_w;              // [T][K] or null
   uint32_t* ctrl;             // control block (status word)
   unsigned long long* trace;  // timeline (MOE_TRACE) or null
-  float* logits;              // [E]
-  float* act;                 // [K * F + Fs] SwiGLU activations, shared expert's first
+  float* logits;              // [T][E]
+  float* act;                 // [T][act_stride] SwiGLU activations, shared expert's first
+  int32_t* ids;               // [T][K] picks (calls of T > 1: made by the selection kernel)
+  float* wts;                 // [T][K] their weights
+  int T;                      // tokens of this call, 1 .. DEC_TMAX
   float scale, norm_min;
   float lim, lim_s;           // SwiGLU clamp limits of the routed and shared experts (0: none)
   const float* norm;          // [H] prologue norm weights, or null (x enters as is)

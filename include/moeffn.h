@@ -65,6 +65,7 @@ extern "C" {
 #define MOE_HOST_IO 4u    /* x, out, topk_ids, topk_w are host pointers, staged       */
 #define MOE_NO_PDL 8u     /* launch without programmatic dependent launch             */
 #define MOE_TRACE 16u     /* record a per-CTA timeline in the workspace (see below)   */
+#define MOE_BATCHED 32u   /* take the batched path whatever the token count           */
 
 enum {
   MOE_OK = 0,
@@ -118,13 +119,15 @@ typedef struct moe_cfg {
 
 /* Two execution paths, chosen by n_tokens (both are exact restatements of the step
  * above; they differ in arithmetic only):
- *   n_tokens < 8   three chained kernels per token (router; picks, gate/up rows and
- *                  SwiGLU; picks, down rows and the weighted sum). The router is an
+ *   n_tokens < 44  the decode chain, up to 16 tokens per launch: a router kernel,
+ *                  (with several tokens) a selection kernel, a gate/up kernel and a
+ *                  down kernel with the weighted sum. The router is an
  *                  f32 dot; the 4-bit blocks meet activations held in 16-bit block
  *                  fixed point (a power-of-two scale per 32 values, error at most
  *                  2^-15 of the block's largest magnitude), so each block dot is an
  *                  exact int32 sum (dp4a), scaled and accumulated in f32.
- *   n_tokens >= 8  the batched path, in passes of at most 512 tokens. An f32 router
+ *   n_tokens >= 44 (or MOE_BATCHED) the batched path, in passes of at most 512
+ *                  tokens. An f32 router
  *                  contraction; one warp per token for the selection; a stable
  *                  counting sort of the (token, pick) pairs by expert; grouped
  *                  contractions on the tensor cores. The blocks are dequantised

@@ -56,7 +56,7 @@ def test_workload_parity(name):
 
 @pytest.mark.parametrize("name", DECODE[1:])
 def test_workload_more_tokens(name):
-    # eight more tokens of the decode layers, as one call of T = 8 (run token by token)
+    # eight more tokens of the decode layers, as one call of T = 8 (one launch of the decode chain)
     w, layer = layer_of(name)
     x, redraws = margin_tokens(layer, w, 8, seed=w["seed"], stream=2)
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
@@ -157,6 +157,24 @@ def test_rms_norm_prologue(w):
                                    layer["shared_blocks"], oracle_cfg(w, oflags), ffn_norm=norm)
         out, ids, wts = GpuLayer(layer, wn).run(x, flags=flags)
         compare(out, ids, wts, ref, rid, rwt, f"prologue seed {w['seed']} flags {flags}")
+
+
+@pytest.mark.parametrize("name,T", [("flint_decode_t1", 16), ("flint_decode_t1", 21),
+                                    ("ling_decode_t1", 7), ("lfm25_decode_t1", 39)])
+def test_multi_token_decode(name, T):
+    # calls of several tokens run the decode chain on up to 16 tokens per launch, with one
+    # selection per token; each token's arithmetic is that of a single-token call, so the
+    # outputs agree bit for bit with calls of one token, and with the oracle
+    w, layer = layer_of(name)
+    x, _ = margin_tokens(layer, w, T, seed=w["seed"], stream=6)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    g = GpuLayer(layer, w)
+    out, ids, wts = g.run(x)
+    compare(out, ids, wts, ref, rid, rwt, f"{name} T={T}")
+    for t in (0, T // 2, T - 1):
+        o1, i1, w1 = g.run(x[t:t + 1])
+        assert np.array_equal(o1[0], out[t]) and np.array_equal(i1[0], ids[t]) and np.array_equal(w1[0], wts[t])
 
 
 def test_flags_accumulate_residual_hostio_nopdl():

@@ -1,6 +1,7 @@
 """GPU parity of the batched (prefill) path against the float64 oracle.
 
-Calls of at least eight tokens take the batched path: a router GEMM, one warp
+Calls of at least 44 tokens take the batched path, and so does any call with
+MOE_BATCHED, which these tests set so that small shapes exercise it too: a router GEMM, one warp
 per token for the selection, a stable counting sort of the (token, pick) pairs
 by expert, and grouped GEMMs on the tensor cores over 4-bit weights dequantised
 to f16. Bars as for decode: identical ordered picks, weights within W_REL, each
@@ -17,6 +18,8 @@ from oracle import moe_oracle as mo
 from tests.helpers import GpuLayer, compare, margin_tokens, oracle_cfg, rel_l2
 
 pytestmark = pytest.mark.gpu
+
+BATCHED = 32  # MOE_BATCHED
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -69,7 +72,7 @@ def test_prefill_shapes(w):
     x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
-    out, ids, wts = GpuLayer(layer, w).run(x)
+    out, ids, wts = GpuLayer(layer, w).run(x, flags=BATCHED)
     err = compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']}")
     print(f"seed {w['seed']} T={w['n_tokens']}: max rel-L2 {err:.3e}")
 
@@ -87,9 +90,9 @@ def test_prefill_swiglu_clamp(w):
     x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
-    out, ids, wts = GpuLayer(layer, w).run(x)
+    out, ids, wts = GpuLayer(layer, w).run(x, flags=BATCHED)
     compare(out, ids, wts, ref, rid, rwt, f"clamp seed {w['seed']}")
-    unclamped, _, _ = GpuLayer(layer, {**w, "swiglu_limit": 0.0, "swiglu_limit_shared": 0.0}).run(x)
+    unclamped, _, _ = GpuLayer(layer, {**w, "swiglu_limit": 0.0, "swiglu_limit_shared": 0.0}).run(x, flags=BATCHED)
     assert min(rel_l2(out[t], unclamped[t]) for t in range(len(x))) > 1e-2
 
 
@@ -111,20 +114,21 @@ def test_prefill_rms_norm_prologue(w):
     for flags, oflags in ((0, 0), (ffn.MOE_RESIDUAL, mo.RESIDUAL)):
         ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                    layer["shared_blocks"], oracle_cfg(w, oflags), ffn_norm=norm)
-        out, ids, wts = GpuLayer(layer, wn).run(x, flags=flags)
+        out, ids, wts = GpuLayer(layer, wn).run(x, flags=flags | BATCHED)
         compare(out, ids, wts, ref, rid, rwt, f"prologue seed {w['seed']} flags {flags}")
 
 
 @pytest.mark.parametrize("shared_ff", [64, 128], ids=["general", "tile"])
 def test_prefill_two_passes_and_decode_boundary(shared_ff):
-    # 7 tokens decode token by token, 8 take the batched path, 600 run as passes of 512 + 88
+    # without the flag 43 tokens decode (16 + 16 + 11 per launch), 44 take the batched path,
+    # 600 run as passes of 512 + 88
     w = _small(60, n_experts=16, top_k=3, shared_ff=shared_ff)
     layer = synth.make_layer(w)
     x, _ = margin_tokens(layer, w, 600, seed=60)
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
     g = GpuLayer(layer, w)
-    for T in (7, 8, 513, 600):
+    for T in (43, 44, 513, 600):
         out, ids, wts = g.run(x[:T])
         compare(out, ids, wts, ref[:T], rid[:T], rwt[:T], f"T={T}")
 
@@ -136,20 +140,20 @@ def test_prefill_flags_and_determinism():
     layer = synth.make_layer(w)
     x, _ = margin_tokens(layer, w, 40, seed=61)
     g = GpuLayer(layer, w)
-    base, ids, wts = g.run(x)
+    base, ids, wts = g.run(x, flags=BATCHED)
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
     compare(base, ids, wts, ref, rid, rwt, "plain")
     init = np.random.default_rng(62).standard_normal(x.shape).astype(np.float32)
-    acc, _, _ = g.run(x, flags=ffn.MOE_ACCUMULATE, out_init=init)
+    acc, _, _ = g.run(x, flags=ffn.MOE_ACCUMULATE | BATCHED, out_init=init)
     assert rel_l2(acc - init, base) < 1e-6
-    res, _, _ = g.run(x, flags=ffn.MOE_RESIDUAL)
+    res, _, _ = g.run(x, flags=ffn.MOE_RESIDUAL | BATCHED)
     assert rel_l2(res - x, base) < 1e-6
     for _ in range(3):  # a fixed summation order: repeat calls agree bit for bit
-        again, ia, wa = g.run(x)
+        again, ia, wa = g.run(x, flags=BATCHED)
         assert np.array_equal(again, base) and np.array_equal(ia, ids) and np.array_equal(wa, wts)
     T, H = x.shape
-    cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": ffn.MOE_HOST_IO})
+    cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": ffn.MOE_HOST_IO | BATCHED})
     ws = torch.zeros(ffn.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
     xh = np.ascontiguousarray(x, np.float32)
     oh = np.full((T, H), np.nan, np.float32)
@@ -171,7 +175,7 @@ def test_flint_prefill_t512_sampled():
     x, _ = margin_tokens(layer, w, T, seed=w["seed"])
     cfg = oracle_cfg(w)
     rid, rwt, _ = mo.route(x, layer["router_w"], layer["bias"], cfg)
-    out, ids, wts = GpuLayer(layer, w).run(x)
+    out, ids, wts = GpuLayer(layer, w).run(x, flags=BATCHED)
     assert np.array_equal(ids, rid)
     assert np.max(np.abs(wts - rwt) / np.abs(rwt)) <= 1e-5
     assert np.all(np.isfinite(out))
@@ -191,7 +195,7 @@ def test_prefill_matches_decode_path():
     layer = synth.make_layer(w)
     x, _ = margin_tokens(layer, w, 8, seed=70)
     g = GpuLayer(layer, w)
-    batch, ib, wb = g.run(x)
+    batch, ib, wb = g.run(x, flags=BATCHED)
     one = [g.run(x[t:t + 1]) for t in range(8)]
     for t in range(8):
         assert np.array_equal(one[t][1][0], ib[t])
