@@ -1,19 +1,20 @@
 // Tile pipeline of the batched MoE-FFN step for sm_103a: the router, gate/up and
 // down contractions as warp-specialised persistent kernels on the tensor cores.
 //
-// One CTA per SM, 576 threads:
+// One CTA per SM, 608 threads:
 //   warp 0       weight producer: 2-D TMA tensor copies of the raw weight rows of each
 //                pipeline chunk (one box of 64 or 128 rows) into shared-memory stages
 //   warp 1       MMA issuer: tcgen05.mma with A in tensor memory, B in shared memory,
 //                f32 accumulator in tensor memory; commits release the stages
 //   warp 2       token-operand producer: one bulk copy per 128 K values of a pre-tiled
 //                image of the chunk's token rows
-//   warps 3..18  converters in four groups of four warps (one per TMEM lane quarter;
+//   warps 3..14  converters in three groups of four warps (one per TMEM lane quarter;
 //                thread = tile row = TMEM lane). Every converter warp waits for every raw
 //                chunk and releases it; 128-value A unit n of the tile stream goes to group
-//                n % 4, which owns one TMEM A slot: raw 4-bit blocks (or f32 router rows)
-//                -> f16 rows of A, written with tcgen05.st. Groups 0 and 1 then run the
-//                tile's epilogue (tcgen05.ld).
+//                n % 3, which owns one TMEM A slot: raw 4-bit blocks (or f32 router rows)
+//                -> f16 rows of A, written with tcgen05.st
+//   warps 15..18 the epilogue, one warp per TMEM lane quarter (tcgen05.ld), on one of two
+//                accumulators while the MMAs of the next tile run on the other
 //
 // Work units (one accumulator tile, M = 128 weight rows x N = chunk tokens):
 //   router   64 experts (f32 rows split into f16 hi rows 0..63 and lo rows 64..127)
@@ -38,16 +39,18 @@
 namespace moe {
 namespace {
 
-constexpr int TP_CONV_WARPS = 16;                 // four groups of four (one warp per TMEM lane quarter)
-constexpr int TP_GROUPS = TP_CONV_WARPS / 4;      // chunk k is converted by group k % TP_GROUPS
-constexpr int TP_EPI_WARPS = 8;                   // two per lane quarter run the epilogue
-constexpr int TP_THREADS = 96 + 32 * TP_CONV_WARPS;  // two producer warps, the MMA warp, converters
+constexpr int TP_CONV_WARPS = 12;                 // three groups of four (one warp per TMEM lane quarter)
+constexpr int TP_GROUPS = TP_CONV_WARPS / 4;      // A unit n is converted by group n % TP_GROUPS
+constexpr int TP_EPI_WARPS = 4;                   // one per lane quarter
+constexpr int TP_EPI_WARP0 = 3 + TP_CONV_WARPS;   // first epilogue warp
+constexpr int TP_THREADS = 96 + 32 * (TP_CONV_WARPS + TP_EPI_WARPS);  // producers, MMA, converters, epilogue
 constexpr int TP_KB = 128;                        // K values per token-operand stage
 constexpr int TP_B_STAGE = 128 * TP_KB * 2;       // up to 128 rows: 32 KB
 constexpr int TP_SCRATCH = 64 * 65 * 4;           // gate/up and router epilogue exchange
 constexpr int TP_SMEM_MAX = 227 * 1024 - 2048;    // dynamic shared memory (static arrays + alignment aside)
 constexpr uint32_t TP_TMEM_COLS = 512;
-constexpr uint32_t TP_A_COL = 128;                // A slots follow the accumulator columns [0, 128)
+constexpr uint32_t TP_A_COL = 128;                // A slots follow the first accumulator's columns [0, 128)
+constexpr uint32_t TP_ACC1_COL = 384;             // the second accumulator (router, gate/up): [384, 512)
 
 // Stage geometry per contraction. MODE 0 gate/up, 1 down, 2 router.
 template <int MODE, int QT>
@@ -65,7 +68,7 @@ struct Geo {
   static constexpr int SCR = MODE == 1 ? 0 : TP_SCRATCH;
   static constexpr int NSA0 = (TP_SMEM_MAX - NSB * TP_B_STAGE - SCR - 1024) / STAGE;
   static constexpr int NSA = NSA0 > 16 ? 16 : NSA0;                  // raw stages (one shared ring)
-  static constexpr int NACC = MODE == 1 ? 2 : 1;                     // accumulators (down tiles: N <= 64)
+  static constexpr int NACC = 2;                                     // accumulators (down tiles: N <= 64)
   static constexpr int SMEM = NSA * STAGE + NSB * TP_B_STAGE + SCR;
   static_assert(NSA >= 2 && SMEM + 1024 <= TP_SMEM_MAX, "shared memory");
 };
@@ -359,6 +362,13 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, const TileMa
   return t;
 }
 
+// First TMEM column of accumulator ab: the down tiles' two 64-column accumulators share
+// [0, 128); the router and gate/up tiles take [0, 128) and [384, 512).
+template <int MODE>
+__device__ __forceinline__ uint32_t acc_col(int ab) {
+  return MODE == 1 ? 64u * (uint32_t)ab : (ab ? TP_ACC1_COL : 0u);
+}
+
 // Independent accumulators of a tile: as many nb-column chains as fit in the tile's
 // accumulator columns (128; down tiles: 64 each of two), at most 4.
 template <int MODE>
@@ -513,7 +523,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
         const uint32_t idesc = idesc_f16_f32(128, t.nb);
         const int nch = tile_chains<MODE>(t.nb);
         const int ab = (int)(uc % G::NACC);
-        const uint32_t acc = tmem + 64u * ab;  // accumulator columns
+        const uint32_t acc = tmem + acc_col<MODE>(ab);  // accumulator columns
         if (uc >= (uint32_t)G::NACC && !tp_wait(&acc_empty[ab], ((uc / G::NACC) - 1) & 1u, abrt)) {
           ok = false;
           break;
@@ -552,13 +562,11 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
       tp_wait(&fin, 0, abrt);
     }
     __syncwarp();
-  } else {
-    // ------------------------------ converters + epilogue ------------------------------
+  } else if (warp < TP_EPI_WARP0) {
+    // ------------------------------ converters ------------------------------
     const int q = warp & 3, grp = (warp - 3) >> 2;  // lane quarter, converter group
     const int m = 32 * q + lane;                     // TMEM lane = tile row
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    const int h = grp;                               // epilogue: groups 0 and 1 take half the columns each
-    const bool epi = grp < 2;
     uint32_t ka = 0, n = 0, uc = 0;  // raw chunks, A units and tiles so far
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
@@ -626,17 +634,28 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[sa]);
       }
-      if (!ok || !epi) continue;
-      // ---- epilogue (warps h = 0, 1: half of the tile's columns each) ----
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    // one warp per lane quarter, every column of the tile; the MMAs of the next tile run
+    // on the other accumulator meanwhile
+    const int q = warp & 3;
+    const int m = 32 * q + lane;  // TMEM lane = tile row
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    uint32_t uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+      const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
+      // ---- the tile on accumulator ab ----
       const int ab = (int)(uc % G::NACC);
-      const uint32_t acc = tmem + lane_addr + 64u * ab;
+      const uint32_t acc = tmem + lane_addr + acc_col<MODE>(ab);
       if (!tp_wait_warp(&acc_full[ab], (uc / G::NACC) & 1u, abrt)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int half = t.npad >> 1;  // columns per warp (a multiple of 8)
-      const int c_lo = h * half;
+      const int half = t.npad;  // every column
+      const int c_lo = 0;
       if (MODE == 2 || MODE == 0) {
         // lanes 64..127 (router: lo rows; gate/up: up rows) hand their column sums over
         if (m >= 64) {
