@@ -516,15 +516,43 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
 // combine: out[t][h] = sum_j ybuf[pos(t, j)][h] + sbuf[t][h] (+ x | + out)
 // ---------------------------------------------------------------------------
 __global__ void prefill_combine(const PrefillArgs a) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (size_t)a.T * a.H) return;
+  // four consecutive outputs a thread (H is a multiple of 32); the sum order per output is
+  // unchanged: the picks in order, then the shared row, then the residual or out
+  const size_t i4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i4 * 4 >= (size_t)a.T * a.H) return;
+  const size_t i = i4 * 4;
   const int t = (int)(i / a.H), h = (int)(i % a.H);
-  float acc = 0.f;
-  for (int j = 0; j < a.K; ++j) acc += a.ybuf[(size_t)a.pos_of[(size_t)t * a.K + j] * a.H + h];
-  if (a.Fs) acc += a.sbuf[i];
-  if (a.flags & FLAG_RESIDUAL) acc = a.xres[i] + acc;
-  if (a.flags & FLAG_ACCUMULATE) acc = a.out[i] + acc;
-  a.out[i] = acc;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < a.K; ++j) {
+    const uint32_t pj = __ldg(a.pos_of + (size_t)t * a.K + j);
+    const float4 y = __ldcs(reinterpret_cast<const float4*>(a.ybuf + (size_t)pj * a.H + h));
+    acc.x += y.x;
+    acc.y += y.y;
+    acc.z += y.z;
+    acc.w += y.w;
+  }
+  if (a.Fs) {
+    const float4 sv = __ldcs(reinterpret_cast<const float4*>(a.sbuf + i));
+    acc.x += sv.x;
+    acc.y += sv.y;
+    acc.z += sv.z;
+    acc.w += sv.w;
+  }
+  if (a.flags & FLAG_RESIDUAL) {
+    const float4 xv = *reinterpret_cast<const float4*>(a.xres + i);
+    acc.x = xv.x + acc.x;
+    acc.y = xv.y + acc.y;
+    acc.z = xv.z + acc.z;
+    acc.w = xv.w + acc.w;
+  }
+  if (a.flags & FLAG_ACCUMULATE) {
+    const float4 ov = *reinterpret_cast<const float4*>(a.out + i);
+    acc.x = ov.x + acc.x;
+    acc.y = ov.y + acc.y;
+    acc.z = ov.z + acc.z;
+    acc.w = ov.w + acc.w;
+  }
+  *reinterpret_cast<float4*>(a.out + i) = acc;
 }
 
 // The layer prologue: xn[t] = x[t] / sqrt(mean(x[t]^2) + eps) * norm, one CTA per token.
@@ -635,7 +663,7 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
     e = a.qtype == 3 ? launch_gemm<3, 1>(a, st) : launch_gemm<2, 1>(a, st);
     if (e != cudaSuccess) return e;
   }
-  prefill_combine<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
+  prefill_combine<<<(unsigned)((nx / 4 + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
