@@ -653,8 +653,11 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.tile) {
     if ((e = tile_images_launch(a, true, st)) != cudaSuccess) return e;
+    // gate/up runs weights-as-A; the down contraction runs tokens-as-A when its
+    // 256-row weight tiles cover H exactly (the faster of the two layouts for each)
     if ((e = tile_gemm_launch(a, 0, st)) != cudaSuccess) return e;
-    if ((e = tile_gemm_launch(a, 1, st)) != cudaSuccess) return e;
+    const bool swap = a.H % 256 == 0;
+    if ((e = swap ? swap_down_launch(a, st) : tile_gemm_launch(a, 1, st)) != cudaSuccess) return e;
   } else {
     prefill_x16<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

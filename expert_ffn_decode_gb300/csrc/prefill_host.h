@@ -88,6 +88,8 @@ bool prefill_tile_ok(int H, int F, int Fs, int qtype);
 cudaError_t tile_router_launch(const PrefillArgs& a, cudaStream_t st);
 cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t st);
 cudaError_t tile_gemm_launch(const PrefillArgs& a, int mode, cudaStream_t st);
+// The down contraction with tokens as A and 256 down rows per tile (needs H % 256 == 0).
+cudaError_t swap_down_launch(const PrefillArgs& a, cudaStream_t st);
 
 // Enqueues the whole prefill pass on `st`. Returns the first launch error.
 cudaError_t prefill_launch(const PrefillArgs& a, cudaStream_t st);

@@ -859,6 +859,426 @@ cudaError_t make_maps(const PrefillArgs& a, TileMaps* m) {
   return encode_2d(&m->rt, a.router_w, true, (uint64_t)a.H, (uint64_t)a.E, 32, 64, true);
 }
 
+// =============================================================================================
+// Swapped down contraction: tokens as A (M = 128 operand rows), weights as B (N = 256 rows)
+// =============================================================================================
+// One MMA then covers 256 down rows x 16 K values, twice what the weights-as-A layout covers,
+// so the contraction issues half the MMAs. A tile is 256 down rows of one expert (or of the
+// shared expert) x one chunk of <= 64 token rows; the activation image holds plain token rows.
+//
+// One CTA per SM, 480 threads:
+//   warp 0       weight producer: 2-D TMA boxes of 128 raw rows x KR K values into raw stages
+//   warp 1       MMA issuer: A (token image) and B (converted weights) from shared memory,
+//                accumulators in TMEM (two of 256 columns); commits release the stages
+//   warp 2       token-operand producer: one bulk copy per 64 K values of the chunk's image
+//                (half of a 128-value image block: its pieces are contiguous)
+//   warps 3..10  converters, thread = weight row: each 32-value block of the raw stage ->
+//                one B unit (256 rows x 32 K, f16, K-major core matrices) in shared memory
+//   warps 11..14 the epilogue, one warp per TMEM lane quarter (lane = token row): weighted
+//                rows into the routed or shared output buffer
+// The same layout for gate/up (each 128-row image holding 64 tokens' hi and lo parts) measured
+// slower than the weights-as-A kernel: its converters and epilogue, not the MMAs, set the pace.
+constexpr int SW_CONV_WARPS = 8;
+constexpr int SW_EPI_WARPS = 4;
+constexpr int SW_EPI_WARP0 = 3 + SW_CONV_WARPS;
+constexpr int SW_THREADS = 32 * (3 + SW_CONV_WARPS + SW_EPI_WARPS);
+constexpr int SW_N = 256;                       // weight rows per tile (MMA N)
+constexpr int SW_KU = 32;                       // K values per B unit (one 4-bit block per row)
+constexpr int SW_BU = SW_N * SW_KU * 2;         // 16 KB
+constexpr int SW_NBU = 4;                       // B unit slots: converters run up to four units ahead
+constexpr int SW_KA = 64;                       // K values per token-operand stage (half an image block)
+constexpr int SW_A_STAGE = 128 * SW_KA * 2;     // 16 KB (up to 128 image rows)
+constexpr int SW_NA = 2;                        // token-operand stages
+constexpr uint32_t SW_TMEM_COLS = 512;          // two 256-column accumulators
+
+template <int QT>
+struct SwGeo {
+  static constexpr int BLK = QT == 3 ? 20 : 18;
+  static constexpr int KR = 256;                       // K values per raw stage
+  static constexpr int SEG = KR / 32 * BLK;            // 160 / 144 bytes
+  static constexpr int STAGE = SW_N * SEG;
+  static constexpr int NBR = KR / SW_KU;               // B units per raw stage
+  static constexpr int NSA = 3;                        // raw stages
+  static constexpr int SMEM = NSA * STAGE + SW_NBU * SW_BU + SW_NA * SW_A_STAGE;
+  static_assert(SMEM + 1024 <= TP_SMEM_MAX, "shared memory");
+};
+
+struct SwMaps {
+  CUtensorMap dn, dn_s;  // boxes of 128 rows x SEG bytes
+};
+
+struct SwUnit {
+  const CUtensorMap* map;
+  int y0, y1;        // map rows of B rows 0..127 and 128..255
+  const uint8_t* a;  // the chunk's activation image (first 128-value block)
+  int kdim;          // reduction length (F or Fs)
+  int n, npad;       // chunk tokens, rounded to 16 (= image rows)
+  int row0, prow, mt;
+  bool shared;
+};
+
+// Tiles: routed chunks x H/256 row tiles, then token chunks x H/256 for the shared expert.
+__device__ __forceinline__ int sw_units(const PrefillArgs& a) {
+  const int ntok = (a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX;
+  const int nr = (int)a.nchunks[0];
+  const int nsh = a.Fs ? ntok : 0;
+  return (nr + nsh) * (a.H / SW_N);
+}
+
+__device__ __forceinline__ SwUnit sw_unit(const PrefillArgs& a, const SwMaps& maps, int u) {
+  SwUnit t;
+  const int nr = (int)a.nchunks[0];
+  const int mt_r = a.H / SW_N, mt_s = a.H / SW_N;
+  int slot, mt;
+  if (u < nr * mt_r) {
+    const GemmChunk ch = a.chunks[u / mt_r];
+    mt = u % mt_r;
+    slot = ch.slot;
+    t.row0 = ch.row0;
+    t.n = ch.n;
+    t.prow = ch.prow;
+    t.shared = false;
+  } else {
+    const int v = u - nr * mt_r;
+    mt = v % mt_s;
+    slot = 0;
+    t.row0 = (v / mt_s) * PREFILL_TILE_NMAX;
+    t.n = min(PREFILL_TILE_NMAX, a.T - t.row0);
+    t.prow = t.row0;
+    t.shared = true;
+  }
+  t.mt = mt;
+  t.npad = (t.n + 15) & ~15;
+  const int ff = t.shared ? a.Fs : a.F;
+  t.map = t.shared ? &maps.dn_s : &maps.dn;
+  t.y0 = slot * 3 * a.H + 2 * a.H + SW_N * mt;  // down rows of the expert's packed matrix
+  t.y1 = t.y0 + 128;
+  t.kdim = ff;
+  const uint8_t* img = t.shared ? a.aimg_s : a.aimg;
+  t.a = img + (size_t)t.prow * (ff / TP_KB) * 256;
+  return t;
+}
+
+// Block J (compile-time) of a raw row segment -> its 32 values as f16 in the permuted slot
+// order: o[4 p + i] is piece p (slots 8p .. 8p + 7) word i. The block is read as the two
+// 16-byte words that cover it.
+template <int QT, int J>
+__device__ __forceinline__ void sw_convert(const uint8_t* row, uint32_t (&o)[16]) {
+  constexpr int BLK = QT == 3 ? 20 : 18;
+  constexpr int off = J * BLK;
+  constexpr int q0 = off >> 4, rel = off - 16 * q0;  // byte offset in the two words
+  const uint4* p = reinterpret_cast<const uint4*>(row) + q0;
+  const uint4 x = p[0], y = p[1];
+  const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+  if constexpr (QT == 3) {
+    constexpr int wi = rel >> 2;
+    const __half2 dmh = u2h(w[wi]);
+    const __half2 d2 = __low2half2(dmh), m2 = __high2half2(dmh);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dequant4<3>(w[wi + 1 + k], d2, m2, o + 4 * k);
+  } else {
+    constexpr int wi = rel >> 2;
+    uint32_t dw, q[4];
+    if constexpr ((rel & 2) != 0) {  // d in the high half of w[wi]; nibble words aligned
+      dw = w[wi] >> 16;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) q[k] = w[wi + 1 + k];
+    } else {  // d in the low half; each nibble word straddles two words
+      dw = w[wi] & 0xFFFFu;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) q[k] = __byte_perm(w[wi + k], w[wi + 1 + k], 0x5432);
+    }
+    const __half2 d2 = u2h(dw | (dw << 16));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dequant4<2>(q[k], d2, d2, o + 4 * k);
+  }
+}
+
+// Block j (0 .. 11, a compile-time value once the caller's loop is unrolled) of a raw row.
+template <int QT>
+__device__ __forceinline__ void sw_convert_j(const uint8_t* row, int j, uint32_t (&o)[16]) {
+  switch (j) {
+    case 0: sw_convert<QT, 0>(row, o); break;
+    case 1: sw_convert<QT, 1>(row, o); break;
+    case 2: sw_convert<QT, 2>(row, o); break;
+    case 3: sw_convert<QT, 3>(row, o); break;
+    case 4: sw_convert<QT, 4>(row, o); break;
+    case 5: sw_convert<QT, 5>(row, o); break;
+    case 6: sw_convert<QT, 6>(row, o); break;
+    case 7: sw_convert<QT, 7>(row, o); break;
+    case 8: sw_convert<QT, 8>(row, o); break;
+    case 9: sw_convert<QT, 9>(row, o); break;
+    case 10: sw_convert<QT, 10>(row, o); break;
+    default: sw_convert<QT, 11>(row, o); break;
+  }
+}
+
+template <int QT>
+__global__ void __launch_bounds__(SW_THREADS, 1) swap_down(const PrefillArgs a, const __grid_constant__ SwMaps maps) {
+  using G = SwGeo<QT>;
+  extern __shared__ __align__(1024) uint8_t ssm_dyn[];
+  uint8_t* raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ssm_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* bunits = raw + G::NSA * G::STAGE;       // [SW_NBU][SW_BU]
+  uint8_t* astage = bunits + SW_NBU * SW_BU;       // [SW_NA][SW_A_STAGE]
+  __shared__ __align__(8) uint64_t raw_full[G::NSA], raw_empty[G::NSA];
+  __shared__ __align__(8) uint64_t bu_full[SW_NBU], bu_empty[SW_NBU], a_full[SW_NA], a_empty[SW_NA];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  volatile int* abrt = &abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < G::NSA; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], SW_CONV_WARPS);
+    }
+    for (int i = 0; i < SW_NBU; ++i) {
+      mbar_init(&bu_full[i], SW_CONV_WARPS);
+      mbar_init(&bu_empty[i], 1);
+    }
+    for (int i = 0; i < SW_NA; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], SW_EPI_WARPS);
+    }
+    mbar_init(&fin, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_base, SW_TMEM_COLS);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const int units = sw_units(a);
+
+  if (warp == 0) {
+    // ------------------------------ weight producer ------------------------------
+    const uint64_t pol = policy_evict_first();
+    uint32_t ka = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const SwUnit t = sw_unit(a, maps, u);
+      const int nk = (t.kdim + G::KR - 1) / G::KR;
+      for (int kc = 0; kc < nk; ++kc, ++ka) {
+        const int sa = (int)(ka % G::NSA);
+        if (ka >= (uint32_t)G::NSA && !tp_wait_warp(&raw_empty[sa], ((ka / G::NSA) - 1) & 1u, abrt)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* dst = raw + sa * G::STAGE;
+          mbar_arrive_expect_tx(&raw_full[sa], (uint32_t)G::STAGE);
+          tma_load_2d(dst, t.map, kc * G::SEG, t.y0, &raw_full[sa], pol);
+          tma_load_2d(dst + 128 * G::SEG, t.map, kc * G::SEG, t.y1, &raw_full[sa], pol);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {  // every copy issued has landed before the CTA may exit
+      for (int sa = 0; sa < G::NSA; ++sa) {
+        const uint32_t f = ka > (uint32_t)sa ? (ka - sa - 1) / G::NSA + 1 : 0u;
+        if (f) mbar_wait(&raw_full[sa], (f - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------ token-operand producer ------------------------------
+    uint32_t rb = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const SwUnit t = sw_unit(a, maps, u);
+      const uint32_t bytes = (uint32_t)t.npad * 16u * (SW_KA / 8);  // 8 pieces of npad rows
+      for (int kk = 0; kk < t.kdim / SW_KA; ++kk, ++rb) {
+        const int s2 = (int)(rb % SW_NA);
+        if (rb >= (uint32_t)SW_NA && !tp_wait_warp(&a_empty[s2], ((rb / SW_NA) - 1) & 1u, abrt)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&a_full[s2], bytes);
+          asm volatile(
+              "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  smem_addr(astage + s2 * SW_A_STAGE)),
+              "l"(t.a + (size_t)kk * bytes), "r"(bytes), "r"(smem_addr(&a_full[s2]))
+              : "memory");
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      for (int s2 = 0; s2 < SW_NA; ++s2) {
+        const uint32_t f = rb > (uint32_t)s2 ? (rb - s2 - 1) / SW_NA + 1 : 0u;
+        if (f) mbar_wait(&a_full[s2], (f - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(128, SW_N);
+      uint32_t nbu = 0, rb = 0, uc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+        const SwUnit t = sw_unit(a, maps, u);
+        const int ab = (int)(uc & 1u);
+        const uint32_t acc = tmem + 256u * ab;
+        if (uc >= 2u && !tp_wait(&acc_empty[ab], ((uc >> 1) - 1) & 1u, abrt)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        for (int kk = 0; kk < t.kdim / SW_KA && ok; ++kk, ++rb) {
+          const int s2 = (int)(rb % SW_NA);
+          if (!tp_wait(&a_full[s2], (rb / SW_NA) & 1u, abrt)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* A = astage + s2 * SW_A_STAGE;
+          for (int q = 0; q < SW_KA / SW_KU; ++q, ++nbu) {  // the stage's two B units
+            const int sb = (int)(nbu % SW_NBU);
+            if (!tp_wait(&bu_full[sb], (nbu / SW_NBU) & 1u, abrt)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint8_t* B = bunits + sb * SW_BU;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              // K values 32 q + 16 j .. + 15: token-image pieces 4 q + 2 j, + 1; B unit pieces 2 j, 2 j + 1
+              const uint64_t ad = smem_desc(A + (size_t)(4 * q + 2 * j) * 16 * t.npad, 16u * t.npad, 128);
+              const uint64_t bd = smem_desc(B + 2 * j * 4096, 4096, 128);
+              mma_f16(acc, ad, bd, idesc, kk > 0 || q > 0 || j > 0);
+            }
+            mma_commit(&bu_empty[sb]);
+          }
+          if (!ok) break;
+          mma_commit(&a_empty[s2]);
+        }
+        if (ok) mma_commit(&acc_full[ab]);
+      }
+      mma_commit(&fin);
+      tp_wait(&fin, 0, abrt);
+    }
+    __syncwarp();
+  } else if (warp < SW_EPI_WARP0) {
+    // ------------------------------ converters ------------------------------
+    const int r = tid - 96;  // weight row of the tile (0..255)
+    uint32_t ka = 0, nbu = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const SwUnit t = sw_unit(a, maps, u);
+      const int nk = (t.kdim + G::KR - 1) / G::KR;
+      for (int kc = 0; kc < nk && ok; ++kc, ++ka) {
+        const int sa = (int)(ka % G::NSA);
+        if (!tp_wait_warp(&raw_full[sa], (ka / G::NSA) & 1u, abrt)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* row = raw + sa * G::STAGE + r * G::SEG;
+        const int nvalid = min(G::NBR, (t.kdim - kc * G::KR) / SW_KU);
+#pragma unroll
+        for (int j = 0; j < G::NBR; ++j) {
+          if (j < nvalid && ok) {
+            const int sb = (int)(nbu % SW_NBU);
+            if (nbu >= (uint32_t)SW_NBU && !tp_wait_warp(&bu_empty[sb], ((nbu / SW_NBU) - 1) & 1u, abrt)) {
+              ok = false;
+            } else {
+              uint32_t o[16];
+              sw_convert_j<QT>(row, j, o);
+              uint8_t* dst = bunits + sb * SW_BU + r * 16;
+#pragma unroll
+              for (int pc = 0; pc < 4; ++pc)
+                *reinterpret_cast<uint4*>(dst + pc * 4096) = make_uint4(o[4 * pc], o[4 * pc + 1], o[4 * pc + 2], o[4 * pc + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bu_full[sb]);
+              ++nbu;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[sa]);
+      }
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    uint32_t uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+      const SwUnit t = sw_unit(a, maps, u);
+      const int ab = (int)(uc & 1u);
+      const uint32_t acc = tmem + lane_addr + 256u * ab;
+      if (!tp_wait_warp(&acc_full[ab], (uc >> 1) & 1u, abrt)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int tr = 32 * q + lane;  // token row of the chunk
+      if (32 * q < t.npad) {
+        const int h0 = SW_N * t.mt;
+        float* dst = nullptr;
+        float wgt = 1.f;
+        if (tr < t.n) {
+          if (t.shared) dst = a.sbuf + (size_t)(t.row0 + tr) * a.H + h0;
+          else {
+            dst = a.ybuf + (size_t)(t.row0 + tr) * a.H + h0;
+            wgt = a.wsorted[t.row0 + tr];
+          }
+        }
+        for (int c0 = 0; c0 < SW_N; c0 += 8) {
+          uint32_t v[8];
+          tmem_ld8(acc + (uint32_t)c0, v);
+          tmem_ld_wait();
+          if (dst) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c0);
+            d4[0] = make_float4(wgt * __uint_as_float(v[0]), wgt * __uint_as_float(v[1]), wgt * __uint_as_float(v[2]),
+                                wgt * __uint_as_float(v[3]));
+            d4[1] = make_float4(wgt * __uint_as_float(v[4]), wgt * __uint_as_float(v[5]), wgt * __uint_as_float(v[6]),
+                                wgt * __uint_as_float(v[7]));
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && *abrt) atomicOr(a.status, DEV_ERR_MBAR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, SW_TMEM_COLS);
+  }
+}
+
+template <int QT>
+cudaError_t launch_swap(const PrefillArgs& a, const SwMaps& maps, cudaStream_t st) {
+  using G = SwGeo<QT>;
+  auto kern = swap_down<QT>;
+  const int smem = G::SMEM + 1024;  // + alignment slack
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<a.nc, SW_THREADS, smem, st>>>(a, maps);
+  return cudaGetLastError();
+}
+
+cudaError_t make_sw_maps(const PrefillArgs& a, SwMaps* m) {
+  std::memset(m, 0, sizeof *m);
+  const uint32_t seg = a.qtype == 3 ? SwGeo<3>::SEG : SwGeo<2>::SEG;
+  cudaError_t e;
+  if ((e = encode_2d(&m->dn, a.experts, false, a.rb_f, (uint64_t)a.E * 3 * a.H, seg, 128, false)) != cudaSuccess)
+    return e;
+  if (a.Fs && (e = encode_2d(&m->dn_s, a.shared, false, a.rb_fs, (uint64_t)3 * a.H, seg, 128, false)) != cudaSuccess)
+    return e;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t tile_router_launch(const PrefillArgs& a, cudaStream_t st) {
@@ -878,6 +1298,13 @@ cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t s
   }
   tile_images<<<dim3(grid, PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
   return cudaGetLastError();
+}
+
+cudaError_t swap_down_launch(const PrefillArgs& a, cudaStream_t st) {
+  SwMaps maps;
+  cudaError_t e = make_sw_maps(a, &maps);
+  if (e != cudaSuccess) return e;
+  return a.qtype == 3 ? launch_swap<3>(a, maps, st) : launch_swap<2>(a, maps, st);
 }
 
 cudaError_t tile_gemm_launch(const PrefillArgs& a, int mode, cudaStream_t st) {
