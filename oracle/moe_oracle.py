@@ -13,6 +13,10 @@ What it computes, step by step, each written from the passage named beside it
    nibbles = values 0..15, high nibbles = values 16..31, value = d*q + m). Q4_0:
    f16 d followed by 16 nibble bytes, value = d*(q - 8) (the pages name the
    format only; the value rule is the plain ggml reading, listed as a reading).
+   K-quant super-blocks of 256 values (ling_moe_ssd.js header and
+   ``planLayoutLing``: the Ling store keeps Q4_K gate/up rows and Q6_K or Q4_K
+   down rows; the block layouts themselves are not on the pages, so they are
+   the public ggml layouts, restated in ``dequant_q4k`` and ``dequant_q6k``).
 2. Router logits = router matrix (F32 ``ffn_gate_inp``, row e = expert e) times
    x (lfm2_moe_ssd.js, ``matmulF32`` router binding in ``initBuffers``).
 3. p = sigmoid(logit); selection score s = p + bias; the bias only selects
@@ -44,7 +48,9 @@ What it computes, step by step, each written from the passage named beside it
    the un-normalised x, which makes the whole FFN block x += ffn(...).
 
 Parity status: every step above is pinned by the not-gpu tests (golden blocks,
-closed forms, brute-force routing, invariants); none is "parity unpinned".
+closed forms, brute-force routing, invariants); none is "parity unpinned". The
+K-quant layouts are pinned to hand-built super-blocks and to the Q4_1 rule,
+not to the pages, which do not print them.
 """
 
 from __future__ import annotations
@@ -56,7 +62,10 @@ import numpy as np
 
 Q4_0 = 2
 Q4_1 = 3
-BLOCK_BYTES = {Q4_0: 18, Q4_1: 20}
+Q4_K = 12
+Q6_K = 14
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q4_K: 144, Q6_K: 210}
+BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q4_K: 256, Q6_K: 256}
 NORM_MIN = 6.103515625e-05  # 2^-14, the clamp on the sum of the picked sigmoids
 
 ACCUMULATE = 1  # out = out_in + contribution
@@ -73,6 +82,7 @@ class MoeConfig:
     n_groups: int = 1
     groups_used: int = 1
     qtype: int = Q4_1
+    qtype_down: int = 0               # block type of the down matrices (0: qtype)
     weights_scale: float = 1.0
     norm_min: float = NORM_MIN
     flags: int = 0
@@ -108,6 +118,10 @@ def dequant_rows(blocks: np.ndarray, n_rows: int, n_cols: int, qtype: int) -> np
     16 nibble bytes give value i (i < 16) from the low nibble of byte i and value
     16 + i from its high nibble.
     """
+    if qtype == Q4_K:
+        return dequant_q4k(blocks, n_rows, n_cols)
+    if qtype == Q6_K:
+        return dequant_q6k(blocks, n_rows, n_cols)
     bb = BLOCK_BYTES[qtype]
     nb = n_cols // 32
     b = np.asarray(blocks, dtype=np.uint8).reshape(n_rows, nb, bb).astype(np.int64)
@@ -127,22 +141,91 @@ def dequant_rows(blocks: np.ndarray, n_rows: int, n_cols: int, qtype: int) -> np
     return v.reshape(n_rows, nb * 32)
 
 
-def record_bytes(hidden: int, ff: int, qtype: int) -> int:
-    return 3 * ff * (hidden // 32) * BLOCK_BYTES[qtype]
+def dequant_q4k(blocks: np.ndarray, n_rows: int, n_cols: int) -> np.ndarray:
+    """Q4_K rows: super-blocks of 256 values, 144 bytes each.
+
+    Bytes 0-1 f16 d, 2-3 f16 dmin, 4-15 the packed 6-bit scale sc_j and min mn_j of
+    the eight 32-value sub-blocks, 16-143 the nibbles. With S the 12 packed bytes:
+    sub-block j < 4 takes sc_j = low 6 bits of S[j] and mn_j = low 6 bits of S[j+4];
+    j >= 4 takes its low 4 bits from S[j+4] (sc: low nibble, mn: high nibble) and
+    its top 2 bits from the top 2 bits of S[j-4] (sc) and S[j] (mn). Nibble bytes
+    come in four runs of 32: run c holds values 64c .. 64c+31 in its low nibbles and
+    64c+32 .. 64c+63 in its high nibbles. Value = d * sc_j * q - dmin * mn_j.
+    """
+    nsb = n_cols // 256
+    b = np.asarray(blocks, dtype=np.uint8).reshape(n_rows, nsb, 144).astype(np.int64)
+    d = half_to_float(b[..., 0] | (b[..., 1] << 8))
+    dmin = half_to_float(b[..., 2] | (b[..., 3] << 8))
+    S = b[..., 4:16]
+    sc = np.zeros((n_rows, nsb, 8))
+    mn = np.zeros((n_rows, nsb, 8))
+    for j in range(8):
+        if j < 4:
+            sc[..., j] = S[..., j] & 63
+            mn[..., j] = S[..., j + 4] & 63
+        else:
+            sc[..., j] = (S[..., j + 4] & 15) | ((S[..., j - 4] >> 6) << 4)
+            mn[..., j] = (S[..., j + 4] >> 4) | ((S[..., j] >> 6) << 4)
+    qs = b[..., 16:144]
+    v = np.zeros((n_rows, nsb, 256))
+    for c in range(4):
+        run = qs[..., 32 * c:32 * c + 32]
+        for half, q in ((0, run & 15), (1, run >> 4)):
+            j = 2 * c + half
+            v[..., 32 * j:32 * j + 32] = (d * sc[..., j])[..., None] * q - (dmin * mn[..., j])[..., None]
+    return v.reshape(n_rows, n_cols)
 
 
-def expert_matrices(record: np.ndarray, hidden: int, ff: int, qtype: int):
+def dequant_q6k(blocks: np.ndarray, n_rows: int, n_cols: int) -> np.ndarray:
+    """Q6_K rows: super-blocks of 256 values, 210 bytes each.
+
+    Bytes 0-127 ql (low 4 bits), 128-191 qh (high 2 bits), 192-207 sixteen int8
+    scales (one per 16 values), 208-209 f16 d. Each half n (values 128n ..
+    128n+127) reads ql[64n ..] and qh[32n ..]: its value 32r + i (r < 4, i < 32)
+    takes its low 4 bits from ql[64n + 32 (r % 2) + i] (the low nibble for r < 2,
+    the high nibble for r >= 2) and its high 2 bits from bits 2r, 2r+1 of
+    qh[32n + i]; q = low + 16 high. Value = d * scale[8n + 2r + i // 16] * (q - 32).
+    """
+    nsb = n_cols // 256
+    b = np.asarray(blocks, dtype=np.uint8).reshape(n_rows, nsb, 210).astype(np.int64)
+    ql, qh = b[..., 0:128], b[..., 128:192]
+    scale = b[..., 192:208]
+    scale = np.where(scale >= 128, scale - 256, scale).astype(np.float64)
+    d = half_to_float(b[..., 208] | (b[..., 209] << 8))
+    v = np.zeros((n_rows, nsb, 256))
+    for n in range(2):
+        for r in range(4):
+            i = np.arange(32)
+            low = (ql[..., 64 * n + 32 * (r % 2) + i] >> (4 * (r // 2))) & 15
+            high = (qh[..., 32 * n + i] >> (2 * r)) & 3
+            q = low + 16 * high
+            s = scale[..., 8 * n + 2 * r + i // 16]
+            v[..., 128 * n + 32 * r + i] = d[..., None] * s * (q - 32)
+    return v.reshape(n_rows, n_cols)
+
+
+def row_bytes(n_values: int, qtype: int) -> int:
+    return n_values // BLOCK_VALUES[qtype] * BLOCK_BYTES[qtype]
+
+
+def record_bytes(hidden: int, ff: int, qtype: int, qtype_down: int = 0) -> int:
+    return 2 * ff * row_bytes(hidden, qtype) + hidden * row_bytes(ff, qtype_down or qtype)
+
+
+def expert_matrices(record: np.ndarray, hidden: int, ff: int, qtype: int, qtype_down: int = 0):
     """Split one expert record into dequantised W_gu [2F][H] and W_down [H][F].
 
-    Record = gate rows [F][H/32 blocks], up rows [F][H/32 blocks], down rows
-    [H][F/32 blocks] (the Flint store keeps "gate rows then up rows (guQ), down
-    rows (dQ)", flint_moe_ssd.js ``planLayoutFlint``).
+    Record = gate rows [F], up rows [F] (rows of H values in ``qtype``), down rows
+    [H] (rows of F values in ``qtype_down``, default ``qtype``). The Flint store
+    keeps "gate rows then up rows (guQ), down rows (dQ)" (flint_moe_ssd.js
+    ``planLayoutFlint``); the Ling store types its down rows separately from its
+    gate/up rows (ling_moe_ssd.js ``planLayoutLing``).
     """
-    bb = BLOCK_BYTES[qtype]
-    gu_bytes = 2 * ff * (hidden // 32) * bb
+    qd = qtype_down or qtype
+    gu_bytes = 2 * ff * row_bytes(hidden, qtype)
     rec = np.asarray(record, dtype=np.uint8)
     w_gu = dequant_rows(rec[:gu_bytes], 2 * ff, hidden, qtype)
-    w_dn = dequant_rows(rec[gu_bytes:], hidden, ff, qtype)
+    w_dn = dequant_rows(rec[gu_bytes:gu_bytes + hidden * row_bytes(ff, qd)], hidden, ff, qd)
     return w_gu, w_dn
 
 
@@ -263,13 +346,14 @@ class ExpertCache:
     def __init__(self, expert_blocks, cfg: MoeConfig):
         self.blocks = np.asarray(expert_blocks, np.uint8)
         self.cfg = cfg
-        self.rb = record_bytes(cfg.hidden, cfg.expert_ff, cfg.qtype)
+        self.rb = record_bytes(cfg.hidden, cfg.expert_ff, cfg.qtype, cfg.qtype_down)
         self.cache = {}
 
     def __call__(self, e: int):
         if e not in self.cache:
             rec = self.blocks[e * self.rb:(e + 1) * self.rb]
-            self.cache[e] = expert_matrices(rec, self.cfg.hidden, self.cfg.expert_ff, self.cfg.qtype)
+            self.cache[e] = expert_matrices(rec, self.cfg.hidden, self.cfg.expert_ff, self.cfg.qtype,
+                                            self.cfg.qtype_down)
         return self.cache[e]
 
 
@@ -294,7 +378,7 @@ def moe_ffn(x, router_w, bias, expert_blocks, shared_blocks, cfg: MoeConfig, out
     experts = ExpertCache(expert_blocks, cfg)
     shared = None
     if cfg.shared_ff:
-        shared = expert_matrices(shared_blocks, H, cfg.shared_ff, cfg.qtype)
+        shared = expert_matrices(shared_blocks, H, cfg.shared_ff, cfg.qtype, cfg.qtype_down)
     out = np.zeros((T, H), np.float64)
     for t in range(T):
         acc = np.zeros(H, np.float64)

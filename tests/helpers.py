@@ -21,7 +21,7 @@ W_REL = 1e-5
 def oracle_cfg(w: dict, flags: int = 0) -> mo.MoeConfig:
     return mo.MoeConfig(hidden=w["hidden"], n_experts=w["n_experts"], top_k=w["top_k"],
                         expert_ff=w["expert_ff"], shared_ff=w["shared_ff"], n_groups=w["n_groups"],
-                        groups_used=w["groups_used"], qtype=w["qtype"],
+                        groups_used=w["groups_used"], qtype=w["qtype"], qtype_down=w.get("qtype_down", 0),
                         weights_scale=w["weights_scale"], norm_min=w.get("norm_min", mo.NORM_MIN),
                         flags=flags, swiglu_limit=w.get("swiglu_limit", 0.0),
                         swiglu_limit_shared=w.get("swiglu_limit_shared", 0.0),

@@ -106,6 +106,119 @@ def test_block_dot_identity():
     check_block_dot_identity()
 
 
+# ---------------------------------------------------------------- K-quant super-blocks
+
+def check_kquant_golden():
+    n = 0
+    for name, qt, hexbytes, pairs in _golden_lines("kquant_blocks.txt"):
+        qt = int(qt)
+        raw = np.array([int(h, 16) for h in hexbytes.split()], np.uint8)
+        assert len(raw) == mo.BLOCK_BYTES[qt], name
+        got = mo.dequant_rows(raw, 1, 256, qt)[0]
+        for pair in pairs.split():
+            i, v = pair.split("=")
+            assert got[int(i)] == float(v), (name, i, got[int(i)], v)
+        n += 1
+    assert n >= 5
+
+
+def test_kquant_golden():
+    check_kquant_golden()
+
+
+def _q4_1_block(d, m, vals):
+    """A Q4_1 block from f16 d, m and its 32 nibble values, in the pinned Q4_1 byte order."""
+    qs = [int(vals[i]) | (int(vals[16 + i]) << 4) for i in range(16)]
+    return (list(np.frombuffer(np.float16(d).tobytes(), np.uint8)) +
+            list(np.frombuffer(np.float16(m).tobytes(), np.uint8)) + qs)
+
+
+def check_q4k_is_eight_q4_1():
+    # A Q4_K sub-block j is a Q4_1 block with d_j = d * sc_j and m_j = -dmin * mn_j. With d and
+    # dmin powers of two both products are exact in f16, so the two decodes agree exactly. The
+    # scales are random (every packed bit used) and the nibbles are read here with plain shifts.
+    rng = np.random.default_rng(21)
+    for _ in range(8):
+        d, dmin = 2.0 ** rng.integers(-12, -6), 2.0 ** rng.integers(-12, -6)
+        S = rng.integers(0, 256, 12)
+        qs = rng.integers(0, 256, 128)
+        raw = np.concatenate([np.frombuffer(np.float16(d).tobytes(), np.uint8),
+                              np.frombuffer(np.float16(dmin).tobytes(), np.uint8),
+                              S.astype(np.uint8), qs.astype(np.uint8)])
+        sc = [S[0] & 63, S[1] & 63, S[2] & 63, S[3] & 63,
+              (S[8] & 15) | ((S[0] >> 6) << 4), (S[9] & 15) | ((S[1] >> 6) << 4),
+              (S[10] & 15) | ((S[2] >> 6) << 4), (S[11] & 15) | ((S[3] >> 6) << 4)]
+        mn = [S[4] & 63, S[5] & 63, S[6] & 63, S[7] & 63,
+              (S[8] >> 4) | ((S[4] >> 6) << 4), (S[9] >> 4) | ((S[5] >> 6) << 4),
+              (S[10] >> 4) | ((S[6] >> 6) << 4), (S[11] >> 4) | ((S[7] >> 6) << 4)]
+        blocks = []
+        for j in range(8):
+            run = qs[32 * (j // 2):32 * (j // 2) + 32]
+            vals = (run >> 4) if j % 2 else (run & 15)
+            blocks += _q4_1_block(d * sc[j], -dmin * mn[j], vals)
+        want = mo.dequant_rows(np.array(blocks, np.uint8), 1, 256, mo.Q4_1)[0]
+        got = mo.dequant_rows(raw, 1, 256, mo.Q4_K)[0]
+        assert np.array_equal(got, want)
+
+
+def test_q4k_is_eight_q4_1():
+    check_q4k_is_eight_q4_1()
+
+
+def check_q6k_is_eight_q4_1():
+    # With the two scales of each 32-value quarter equal, a Q6_K quarter (n, r) is a Q4_1 block:
+    # d_j = d * scale, nibbles from the quarter's ql run, and m_j = (16 * field - 32) * d * scale
+    # where every 2-bit field of qh is the same number (a qh byte of four equal fields). Each
+    # field value 0..3 is taken in turn; all products are exact in f16 (d a power of two).
+    rng = np.random.default_rng(22)
+    for field in range(4):
+        d = 2.0 ** rng.integers(-10, -5)
+        pair = rng.integers(-128, 128, 8)
+        scales = np.repeat(pair, 2)
+        ql = rng.integers(0, 256, 128)
+        qh = np.full(64, field * 0x55)
+        raw = np.concatenate([ql.astype(np.uint8), qh.astype(np.uint8), scales.astype(np.int8).view(np.uint8),
+                              np.frombuffer(np.float16(d).tobytes(), np.uint8)])
+        blocks = []
+        for j in range(8):
+            n, r = j // 4, j % 4
+            run = ql[64 * n + 32 * (r % 2):64 * n + 32 * (r % 2) + 32]
+            vals = (run >> 4) if r >= 2 else (run & 15)
+            s = float(pair[j])
+            blocks += _q4_1_block(d * s, (16 * field - 32) * d * s, vals)
+        want = mo.dequant_rows(np.array(blocks, np.uint8), 1, 256, mo.Q4_1)[0]
+        got = mo.dequant_rows(raw, 1, 256, mo.Q6_K)[0]
+        assert np.array_equal(got, want), field
+
+
+def test_q6k_is_eight_q4_1():
+    check_q6k_is_eight_q4_1()
+
+
+def check_kquant_record_split():
+    # A mixed record (Q4_K gate/up, Q6_K down) splits at 2F rows of H/256 * 144 bytes; the
+    # down part decodes as Q6_K rows of F/256 * 210 bytes.
+    H, F = 256, 512
+    assert mo.record_bytes(H, F, mo.Q4_K, mo.Q6_K) == 2 * F * 144 + H * 2 * 210
+    rng = np.random.default_rng(23)
+    rec = rng.integers(0, 256, mo.record_bytes(H, F, mo.Q4_K, mo.Q6_K)).astype(np.uint8)
+    rec[2 * F * 144:][208::210] = 0x00   # keep every Q6_K d finite: f16 bits 0x3C00 (1.0)
+    rec[2 * F * 144:][209::210] = 0x3C
+    rec[:2 * F * 144][0::144] = 0x00     # and every Q4_K d, dmin: 1.0
+    rec[:2 * F * 144][1::144] = 0x3C
+    rec[:2 * F * 144][2::144] = 0x00
+    rec[:2 * F * 144][3::144] = 0x3C
+    w_gu, w_dn = mo.expert_matrices(rec, H, F, mo.Q4_K, mo.Q6_K)
+    assert w_gu.shape == (2 * F, H) and w_dn.shape == (H, F)
+    assert np.array_equal(w_gu[F + 3], mo.dequant_rows(rec[(F + 3) * 144:(F + 4) * 144], 1, H, mo.Q4_K)[0])
+    dn = rec[2 * F * 144:]
+    assert np.array_equal(w_dn[7], mo.dequant_rows(dn[7 * 420:8 * 420], 1, F, mo.Q6_K)[0])
+
+
+def test_kquant_record_split():
+    check_kquant_record_split()
+
+
 # ---------------------------------------------------------------- routing
 
 def check_golden_routing():
@@ -416,7 +529,8 @@ def test_expert_matches_textbook_dense():
 
 
 ALL_CHECKS = [check_half_decode, check_golden_blocks, check_q4_0_is_q4_1_with_offset,
-              check_block_dot_identity, check_golden_routing, check_routing_brute_force,
+              check_block_dot_identity, check_kquant_golden, check_q4k_is_eight_q4_1,
+              check_q6k_is_eight_q4_1, check_kquant_record_split, check_golden_routing, check_routing_brute_force,
               check_routing_reductions, check_route_weights_closed_form,
               check_swiglu_closed_form, check_swiglu_clamp_closed_form, check_rms_norm_prologue,
               check_combine_invariants,
@@ -455,6 +569,72 @@ def _mut_q4_0_no_offset(blocks, n_rows, n_cols, qtype):
         d = mo.half_to_float(b[..., 0] | (b[..., 1] << 8))
         v = v + 8.0 * np.repeat(d, 32, axis=-1).reshape(v.shape)
     return v
+
+
+def _q4k_variant(blocks, n_rows, n_cols, hi_from=-4, min_sign=-1.0, runs_swapped=False):
+    # a Q4_K decode with one knob turned away from the layout
+    nsb = n_cols // 256
+    b = np.asarray(blocks, np.uint8).reshape(n_rows, nsb, 144).astype(np.int64)
+    d = mo.half_to_float(b[..., 0] | (b[..., 1] << 8))
+    dmin = mo.half_to_float(b[..., 2] | (b[..., 3] << 8))
+    S = b[..., 4:16]
+    v = np.zeros((n_rows, nsb, 256))
+    for j in range(8):
+        if j < 4:
+            sc, mn = S[..., j] & 63, S[..., j + 4] & 63
+        else:
+            sc = (S[..., j + 4] & 15) | ((S[..., j + hi_from] >> 6) << 4)
+            mn = (S[..., j + 4] >> 4) | ((S[..., j] >> 6) << 4)
+        run = b[..., 16 + 32 * (j // 2):16 + 32 * (j // 2) + 32]
+        q = (run & 15) if (j % 2 == 0) != runs_swapped else (run >> 4)
+        v[..., 32 * j:32 * j + 32] = (d * sc)[..., None] * q + min_sign * (dmin * mn)[..., None]
+    return v.reshape(n_rows, n_cols)
+
+
+def _mut_q4k_high_bits(blocks, n_rows, n_cols):
+    return _q4k_variant(blocks, n_rows, n_cols, hi_from=0)
+
+
+def _mut_q4k_min_added(blocks, n_rows, n_cols):
+    return _q4k_variant(blocks, n_rows, n_cols, min_sign=1.0)
+
+
+def _mut_q4k_runs_swapped(blocks, n_rows, n_cols):
+    return _q4k_variant(blocks, n_rows, n_cols, runs_swapped=True)
+
+
+def _q6k_variant(blocks, n_rows, n_cols, qh_step=2, scale_step=2, unsigned=False, ql_roles=False):
+    nsb = n_cols // 256
+    b = np.asarray(blocks, np.uint8).reshape(n_rows, nsb, 210).astype(np.int64)
+    ql, qh, scale = b[..., 0:128], b[..., 128:192], b[..., 192:208]
+    if not unsigned:
+        scale = np.where(scale >= 128, scale - 256, scale)
+    d = mo.half_to_float(b[..., 208] | (b[..., 209] << 8))
+    v = np.zeros((n_rows, nsb, 256))
+    i = np.arange(32)
+    for n in range(2):
+        for r in range(4):
+            run, sh = (r // 2, 4 * (r % 2)) if ql_roles else (r % 2, 4 * (r // 2))
+            q = ((ql[..., 64 * n + 32 * run + i] >> sh) & 15) + 16 * ((qh[..., 32 * n + i] >> (qh_step * r)) & 3)
+            sidx = np.minimum(8 * n + scale_step * r + i // 16, 15)
+            v[..., 128 * n + 32 * r + i] = d[..., None] * scale[..., sidx] * (q - 32)
+    return v.reshape(n_rows, n_cols)
+
+
+def _mut_q6k_qh_shift(blocks, n_rows, n_cols):
+    return _q6k_variant(blocks, n_rows, n_cols, qh_step=1)
+
+
+def _mut_q6k_scale_index(blocks, n_rows, n_cols):
+    return _q6k_variant(blocks, n_rows, n_cols, scale_step=1)
+
+
+def _mut_q6k_unsigned_scale(blocks, n_rows, n_cols):
+    return _q6k_variant(blocks, n_rows, n_cols, unsigned=True)
+
+
+def _mut_q6k_ql_roles(blocks, n_rows, n_cols):
+    return _q6k_variant(blocks, n_rows, n_cols, ql_roles=True)
 
 
 def _mut_ties_highest(s, top_k, n_groups=1, groups_used=1):
@@ -536,7 +716,7 @@ def _mut_half_no_subnormal(bits):
 
 ORIG = {name: getattr(mo, name) for name in
         ["dequant_rows", "select_experts", "group_scores", "route_weights", "swiglu", "half_to_float",
-         "rms_norm"]}
+         "rms_norm", "dequant_q4k", "dequant_q6k"]}
 
 MUTANTS = [
     ("dequant_rows", _mut_nibble_order),
@@ -551,6 +731,13 @@ MUTANTS = [
     ("swiglu", _mut_clamp_gate_first),
     ("swiglu", _mut_clamp_up_one_sided),
     ("half_to_float", _mut_half_no_subnormal),
+    ("dequant_q4k", _mut_q4k_high_bits),
+    ("dequant_q4k", _mut_q4k_min_added),
+    ("dequant_q4k", _mut_q4k_runs_swapped),
+    ("dequant_q6k", _mut_q6k_qh_shift),
+    ("dequant_q6k", _mut_q6k_scale_index),
+    ("dequant_q6k", _mut_q6k_unsigned_scale),
+    ("dequant_q6k", _mut_q6k_ql_roles),
     ("rms_norm", _mut_rms_eps_outside),
     ("rms_norm", _mut_rms_sum_not_mean),
 ]
