@@ -37,12 +37,26 @@ METRIC = "MoE-FFN tokens/s (decode T=1, prefill T=512); % of HBM/tensor roofline
 UNIT = "tokens/s"
 
 
+QTYPE_NAMES = {2: "Q4_0", 3: "Q4_1", 12: "Q4_K", 14: "Q6_K"}
+
+
+def record_bytes(w, ff):
+    """Bytes of one expert record of intermediate size ff (gate/up and down rows in
+    their own block types)."""
+    from expert_ffn_decode_gb300 import synth
+    return synth.record_bytes(w["hidden"], ff, w["qtype"], w.get("qtype_down", 0))
+
+
+def qtype_label(w):
+    qd = w.get("qtype_down") or w["qtype"]
+    return QTYPE_NAMES[w["qtype"]] + ("" if qd == w["qtype"] else "/" + QTYPE_NAMES[qd])
+
+
 def layer_bytes(w):
     """Algorithmic bytes of one token's step: router, the k picked experts, the
     shared expert, x and out (the experts not picked are never read)."""
-    bb = 18 if w["qtype"] == 2 else 20
     H, E, K, F, Fs = w["hidden"], w["n_experts"], w["top_k"], w["expert_ff"], w["shared_ff"]
-    rec = lambda ff: 3 * ff * (H // 32) * bb
+    rec = lambda ff: record_bytes(w, ff)
     router = E * H * 4 + (E * 4 if w.get("bias_std") is not None else 0)
     return router + K * rec(F) + (rec(Fs) if Fs else 0) + 2 * H * 4
 
@@ -146,7 +160,7 @@ w = synth.WORKLOADS[{workload!r}]
 layer = synth.make_layer(w)
 cfg = mo.MoeConfig(hidden=w["hidden"], n_experts=w["n_experts"], top_k=w["top_k"], expert_ff=w["expert_ff"],
                    shared_ff=w["shared_ff"], n_groups=w["n_groups"], groups_used=w["groups_used"],
-                   qtype=w["qtype"], weights_scale=w["weights_scale"])
+                   qtype=w["qtype"], qtype_down=w.get("qtype_down", 0), weights_scale=w["weights_scale"])
 it = synth.token_stream(w["seed"], w["hidden"], 9)
 call = lambda x: mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                             layer["shared_blocks"], cfg)
@@ -254,9 +268,8 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
 def prefill_bytes(w, distinct):
     """Algorithmic bytes of one batched step: the router, every expert some token
     picked (`distinct` of them, each read once), the shared expert, x and out."""
-    bb = 18 if w["qtype"] == 2 else 20
     H, E, T, F, Fs = w["hidden"], w["n_experts"], w["n_tokens"], w["expert_ff"], w["shared_ff"]
-    rec = lambda ff: 3 * ff * (H // 32) * bb
+    rec = lambda ff: record_bytes(w, ff)
     router = E * H * 4 + (E * 4 if w.get("bias_std") is not None else 0)
     return router + distinct * rec(F) + (rec(Fs) if Fs else 0) + 2 * T * H * 4
 
@@ -585,7 +598,7 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "T": T, "hidden": H, "n_experts": w["n_experts"],
                    "top_k": w["top_k"], "expert_ff": w["expert_ff"], "shared_ff": w["shared_ff"],
-                   "qtype": "Q4_1" if w["qtype"] == 3 else "Q4_0", "parallelism": f"replicas{world}",
+                   "qtype": qtype_label(w), "parallelism": f"replicas{world}",
                    "layers_rotated": L,
                    "l2": f"inputs larger than L2: {L} distinct layers, {L * step_bytes / 1e6:.0f} MB of "
                          f"step bytes between reuses of any weight byte (L2 {l2 / 1e6:.0f} MB)",
@@ -641,7 +654,7 @@ def main_prefill(args, ffn, synth, dev, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32", "data": "synthetic",
         "config": {"workload": args.workload, "T": T, "hidden": w["hidden"], "n_experts": w["n_experts"],
                    "top_k": w["top_k"], "expert_ff": w["expert_ff"], "shared_ff": w["shared_ff"],
-                   "qtype": "Q4_1" if w["qtype"] == 3 else "Q4_0", "parallelism": f"replicas{world}",
+                   "qtype": qtype_label(w), "parallelism": f"replicas{world}",
                    "layers_rotated": pre["layers_rotated"],
                    "l2": "inputs larger than L2: every step reads over 400 MB of weights"},
         "roofline": {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s", "frac": round(a / peak, 4),

@@ -1,4 +1,4 @@
-"""Routed MoE-FFN step (sigmoid router, top-k, Q4_0/Q4_1 SwiGLU experts) on GB300.
+"""Routed MoE-FFN step (sigmoid router, top-k, 4-bit block-quantised SwiGLU experts) on GB300.
 
 Thin Python binding of the C ABI in ``include/moeffn.h`` (``libmoeffn.so``,
 built next to this file by :mod:`expert_ffn_decode_gb300.build`). The
@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libmoeffn.so")
 
 MOE_Q4_0 = 2
 MOE_Q4_1 = 3
+MOE_Q4_K = 12
+MOE_Q6_K = 14
 
 MOE_ACCUMULATE = 1
 MOE_RESIDUAL = 2
@@ -63,17 +65,19 @@ class moe_cfg(ctypes.Structure):
         ("swiglu_limit_shared", ctypes.c_float),
         ("rms_eps", ctypes.c_float),
         ("ffn_norm", ctypes.c_void_p),
+        ("qtype_down", ctypes.c_int32),
     ]
 
 
 def make_cfg(hidden, n_experts, top_k, expert_ff, shared_ff=0, n_groups=1, groups_used=1,
              n_tokens=1, qtype=MOE_Q4_1, weights_scale=1.0, norm_min=NORM_MIN, flags=0,
-             swiglu_limit=0.0, swiglu_limit_shared=0.0, rms_eps=0.0, ffn_norm=None, **_ignored):
+             swiglu_limit=0.0, swiglu_limit_shared=0.0, rms_eps=0.0, ffn_norm=None, qtype_down=0,
+             **_ignored):
     """A :class:`moe_cfg` from keyword arguments (extra keys are ignored). ``ffn_norm`` is
-    a device vector (a tensor or an address) or None."""
+    a device vector (a tensor or an address) or None; ``qtype_down`` 0 means ``qtype``."""
     return moe_cfg(hidden, n_experts, top_k, expert_ff, shared_ff, n_groups, groups_used,
                    n_tokens, qtype, weights_scale, norm_min, flags, swiglu_limit, swiglu_limit_shared,
-                   rms_eps, _ptr(ffn_norm))
+                   rms_eps, _ptr(ffn_norm), qtype_down or 0)
 
 
 class MoeError(RuntimeError):

@@ -36,13 +36,29 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int block_bytes(int qtype) { return qtype == MOE_Q4_0 ? 18 : 20; }
+// Bytes of a weight row of n values: 32-value blocks of 18 (Q4_0) or 20 (Q4_1) bytes, or
+// 256-value super-blocks of 144 (Q4_K) or 210 (Q6_K) bytes.
+uint32_t row_bytes(int n, int qtype) {
+  switch (qtype) {
+    case MOE_Q4_0: return (uint32_t)(n / 32) * 18u;
+    case MOE_Q4_1: return (uint32_t)(n / 32) * 20u;
+    case MOE_Q4_K: return (uint32_t)(n / 256) * 144u;
+    default: return (uint32_t)(n / 256) * 210u;
+  }
+}
+bool kquant(int qtype) { return qtype == MOE_Q4_K || qtype == MOE_Q6_K; }
+// The down rows' block type.
+int down_type(const moe_cfg* c) { return c->qtype_down ? c->qtype_down : c->qtype; }
 
 // ---- configuration checks ------------------------------------------------------
 int check_cfg(const moe_cfg* c) {
   if (!c) return fail(MOE_ERR_NULL_PTR, "cfg is NULL");
-  if (c->qtype != MOE_Q4_0 && c->qtype != MOE_Q4_1)
-    return fail(MOE_ERR_INVALID_CFG, "qtype %d: expected MOE_Q4_0 (2) or MOE_Q4_1 (3)", c->qtype);
+  if (c->qtype != MOE_Q4_0 && c->qtype != MOE_Q4_1 && c->qtype != MOE_Q4_K)
+    return fail(MOE_ERR_INVALID_CFG, "qtype %d: expected MOE_Q4_0 (2), MOE_Q4_1 (3) or MOE_Q4_K (12)", c->qtype);
+  if (c->qtype_down != 0 && c->qtype_down != MOE_Q4_0 && c->qtype_down != MOE_Q4_1 && c->qtype_down != MOE_Q4_K &&
+      c->qtype_down != MOE_Q6_K)
+    return fail(MOE_ERR_INVALID_CFG, "qtype_down %d: expected 0, MOE_Q4_0, MOE_Q4_1, MOE_Q4_K or MOE_Q6_K",
+                c->qtype_down);
   if (c->hidden <= 0 || c->hidden % 32 || c->hidden > 3072)
     return fail(MOE_ERR_INVALID_CFG, "hidden %d: must be a positive multiple of 32, at most 3072", c->hidden);
   if (c->expert_ff <= 0 || c->expert_ff % 32 || c->expert_ff > 3072)
@@ -51,6 +67,11 @@ int check_cfg(const moe_cfg* c) {
   if (c->shared_ff < 0 || c->shared_ff % 32 || c->shared_ff > 3072)
     return fail(MOE_ERR_INVALID_CFG, "shared_ff %d: must be 0 or a multiple of 32, at most 3072",
                 c->shared_ff);
+  if (kquant(c->qtype) && c->hidden % 256)
+    return fail(MOE_ERR_INVALID_CFG, "hidden %d: K-quant gate/up rows need a multiple of 256", c->hidden);
+  if (kquant(down_type(c)) && (c->expert_ff % 256 || c->shared_ff % 256))
+    return fail(MOE_ERR_INVALID_CFG, "expert_ff %d, shared_ff %d: K-quant down rows need multiples of 256",
+                c->expert_ff, c->shared_ff);
   if (c->n_experts < 1 || c->n_experts > 1024)
     return fail(MOE_ERR_INVALID_CFG, "n_experts %d: must be in [1, 1024]", c->n_experts);
   if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts)
@@ -158,7 +179,7 @@ WsLayout ws_layout(const moe_cfg* c, bool decode_only = false) {
       o = up256(o + (size_t)tp * c->hidden * 4);
     }
     L.prefill = o;
-    const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype);
+    const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype, down_type(c));
     o = up256(o + moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff, c->shared_ff, tile)
                       .total);
   }
@@ -180,7 +201,8 @@ std::vector<PlanEntry> g_plans;
 bool same_shape(const moe_cfg& a, const moe_cfg& b) {
   return a.hidden == b.hidden && a.n_experts == b.n_experts && a.top_k == b.top_k &&
          a.expert_ff == b.expert_ff && a.shared_ff == b.shared_ff && a.n_groups == b.n_groups &&
-         (a.n_groups == 1 || a.groups_used == b.groups_used) && a.qtype == b.qtype;
+         (a.n_groups == 1 || a.groups_used == b.groups_used) && a.qtype == b.qtype &&
+         down_type(&a) == down_type(&b);
 }
 
 int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
@@ -193,11 +215,11 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.G = c->n_groups;
   p.Gu = c->n_groups > 1 ? c->groups_used : 1;
   p.qtype = c->qtype;
-  p.blk = (uint32_t)block_bytes(c->qtype);
-  p.rb_h = (uint32_t)(p.H / 32) * p.blk;
-  p.rb_f = (uint32_t)(p.F / 32) * p.blk;
-  p.rb_fs = p.Fs ? (uint32_t)(p.Fs / 32) * p.blk : p.rb_f;
-  p.rec_bytes = (uint64_t)3 * p.F * (p.H / 32) * p.blk;
+  p.qtype_dn = down_type(c);
+  p.rb_h = row_bytes(p.H, p.qtype);
+  p.rb_f = row_bytes(p.F, p.qtype_dn);
+  p.rb_fs = p.Fs ? row_bytes(p.Fs, p.qtype_dn) : p.rb_f;
+  p.rec_bytes = (uint64_t)2 * p.F * p.rb_h + (uint64_t)p.H * p.rb_f;
   p.nbH = p.H / 32;
   p.nbF = p.F / 32;
   p.nbFs = p.Fs / 32;
@@ -345,7 +367,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
 
   if (const int tp = prefill_pass_tokens(c)) {
     // batched path: router, top-k, expert sort and grouped tensor-core GEMMs
-    const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype);
+    const bool tile = moe::prefill_tile_ok(c->hidden, c->expert_ff, c->shared_ff, c->qtype, down_type(c));
     const moe::PrefillWs P = moe::prefill_ws_layout(tp, c->hidden, c->n_experts, c->top_k, c->expert_ff,
                                                     c->shared_ff, tile);
     uint8_t* pb = wsb + W.prefill;
@@ -387,6 +409,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     pa.G = c->n_groups;
     pa.Gu = c->n_groups > 1 ? c->groups_used : 1;
     pa.qtype = c->qtype;
+    pa.qtype_dn = down_type(c);
     pa.scale = c->weights_scale;
     pa.norm_min = c->norm_min;
     pa.lim = c->swiglu_limit;

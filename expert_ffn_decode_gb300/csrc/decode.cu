@@ -31,7 +31,11 @@
 // exactly in int32, and the block result d * s * sum(q v) (+ m * s * sum(v) for
 // Q4_1, - 8 d s sum(v) for Q4_0) is accumulated in fp32. The block formats and the
 // per-block dot identity follow flint_moe_ssd.js (WGSL section, Q41DOT and its
-// comment).
+// comment). K-quant rows (256-value super-blocks: Q4_K gate/up, Q6_K or Q4_K down, as
+// the Ling store holds them) are walked in the same 32-value blocks: a Q4_K sub-block
+// dots like a Q4_1 block with d*sc and -dmin*mn, a Q6_K sub-block as two 16-value halves
+// of signed 6-bit values, each with its own int8 scale. The gate/up kernel takes the
+// gate/up rows' type and the down kernel the down rows' type.
 #include <cstdint>
 #include <cuda_fp16.h>
 
@@ -217,6 +221,98 @@ __device__ __forceinline__ float raw_block_dot(const RawBlock& r, const ActBlock
     const float S = nibble_dot(qw, a);
     const float d = __half2float(__ushort_as_half((unsigned short)dbits));
     return a.s * d * fmaf(-8.f, a.X, S);
+  }
+}
+
+// ---- K-quant super-blocks (256 values). Each 32-value sub-block meets one activation
+// block, so a row is still walked in 32-value blocks b: super-block b / 8, sub-block b % 8.
+// The layouts are ggml's (the Ling store's Q4_K gate/up and Q6_K down rows, ling_moe_ssd.js
+// header; the pages name the types only).
+
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// Q4_K, 144 bytes: f16 d, f16 dmin, 12 bytes S of packed 6-bit scales and mins, four runs
+// of 32 nibble bytes (run c: sub-block 2c in the low nibbles, 2c + 1 in the high nibbles).
+// Sub-block j < 4: sc = S[j] & 63, mn = S[j + 4] & 63; j >= 4: the low 4 bits of both from
+// S[j + 4], the top 2 bits from S[j - 4] (sc) and S[j] (mn). Value = d sc q - dmin mn.
+// Q4_K rows are whole 16-byte multiples and start on 16-byte bounds, here and in shared memory.
+__device__ __forceinline__ float q4k_sub_dot(uint32_t row, int b, const ActBlock& a) {
+  const uint32_t sb = row + 144u * (uint32_t)(b >> 3);
+  const int j = b & 7, sh = 8 * (j & 3);
+  const uint4 hd = lds128(sb);
+  const uint4 n0 = lds128(sb + 16u + 32u * (uint32_t)(j >> 1));
+  const uint4 n1 = lds128(sb + 32u + 32u * (uint32_t)(j >> 1));
+  const uint32_t by = (hd.y >> sh) & 0xFFu, bz = (hd.z >> sh) & 0xFFu, bw = (hd.w >> sh) & 0xFFu;
+  const uint32_t sc = j < 4 ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4));
+  const uint32_t mn = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
+  const int ns = 4 * (j & 1);  // the run's low or high nibbles
+  const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+  int s0 = 0, s1 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t q = (w[i] >> ns) & 0x0F0F0F0Fu;  // values 4i .. 4i + 3
+    s0 = dp4a_uu(q, a.p[i], s0);
+    s1 = dp4a_us(q, a.p[8 + i], s1);
+  }
+  const float S = (float)(s1 * 256 + s0);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));  // d, dmin
+  return a.s * fmaf(f.x * (float)sc, S, -(f.y * (float)mn) * a.X);
+}
+
+// 32 bytes from a 2-byte aligned shared address as 8 words (9 aligned words read; the run
+// ends at least 4 bytes before its super-block does, so the ninth word stays inside it).
+__device__ __forceinline__ void lds_run32(uint32_t addr, uint32_t (&w)[8]) {
+  const uint32_t base = addr & ~3u, sh = (addr & 3u) * 8u;
+  uint32_t t[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) t[i] = lds32(base + 4u * i);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
+// Q6_K, 210 bytes: ql[128], qh[64], 16 int8 scales, f16 d. Sub-block j = (half n = j / 4,
+// quarter r = j % 4): value i takes its low 4 bits from ql[64n + 32 (r % 2) + i] (the low
+// nibble for r < 2, the high one for r >= 2) and its high 2 bits from bits 2r, 2r + 1 of
+// qh[32n + i]; value = d * scale[8n + 2r + i / 16] * (q - 32). Rows start on 2-byte bounds.
+__device__ __forceinline__ float q6k_sub_dot(uint32_t row, int b, const ActBlock& a) {
+  const uint32_t sb = row + 210u * (uint32_t)(b >> 3);
+  const int j = b & 7, n = j >> 2, r = j & 3;
+  uint32_t L[8], Hh[8];
+  lds_run32(sb + 64u * n + 32u * (r & 1), L);
+  lds_run32(sb + 128u + 32u * n, Hh);
+  const uint32_t scp = lds16(sb + 192u + 8u * n + 2u * r);  // the quarter's two scales
+  const float d = __half2float(__ushort_as_half((unsigned short)lds16(sb + 208u)));
+  const int ls = 4 * (r >> 1), hs = 2 * r;
+  int s0[2] = {0, 0}, s1[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = ((L[i] >> ls) & 0x0F0F0F0Fu) | (((Hh[i] >> hs) & 0x03030303u) << 4);  // 0..63
+    // q - 32 as signed bytes: flip bit 5, and set bits 6, 7 where bit 5 was clear (q < 32)
+    const uint32_t t = ~u & 0x20202020u;
+    const uint32_t q = (u ^ 0x20202020u) | (t << 1) | (t << 2);
+    s0[i >> 2] = dp4a_su(q, a.p[i], s0[i >> 2]);
+    s1[i >> 2] = dp4a_ss(q, a.p[8 + i], s1[i >> 2]);
+  }
+  const float sc0 = (float)(int)(int8_t)(scp & 0xFFu), sc1 = (float)(int)(int8_t)(scp >> 8);
+  const float S0 = (float)(s1[0] * 256 + s0[0]), S1 = (float)(s1[1] * 256 + s0[1]);
+  return a.s * d * fmaf(sc1, S1, sc0 * S0);
+}
+
+// Block b of a row in shared memory times activation block a.
+template <int QT>
+__device__ __forceinline__ float row_block_dot(uint32_t row, int b, const ActBlock& a) {
+  if constexpr (QT == 12) {
+    return q4k_sub_dot(row, b, a);
+  } else if constexpr (QT == 14) {
+    return q6k_sub_dot(row, b, a);
+  } else {
+    RawBlock r;
+    load_block_s<QT>(row, b, r);
+    return raw_block_dot<QT>(r, a);
   }
 }
 
@@ -669,9 +765,7 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
         for (int i = 0; i < MAXB; ++i) {
           const int b = mh.sub + mh.lpr * i;
           if (b < p.nbH) {
-            RawBlock rb;
-            load_block_s<QT>(row, b, rb);
-            dots[s] += raw_block_dot<QT>(rb, xc[i]);
+            dots[s] += row_block_dot<QT>(row, b, xc[i]);
           }
         }
       }
@@ -791,9 +885,7 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           if (r < RPG) {
-            RawBlock blk;
-            load_block_s<QT>(wr + (uint32_t)r * rb, b, blk);
-            acc[r] = fmaf(wgt, raw_block_dot<QT>(blk, ab), acc[r]);
+            acc[r] = fmaf(wgt, row_block_dot<QT>(wr + (uint32_t)r * rb, b, ab), acc[r]);
           }
         }
       }
@@ -845,30 +937,47 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, int threads, siz
 }
 
 template <int QT, int MAXB>
-static cudaError_t launch_chain(const DecodeArgs& a, cudaStream_t st, bool pdl, int trows) {
+static cudaError_t launch_gate_up(const DecodeArgs& a, cudaStream_t st, bool pdl, int trows) {
   const DecodePlan& p = a.p;
-  const unsigned T = (unsigned)a.T;
-  cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)0, st, pdl, a, trows);
-  if (e != cudaSuccess) return e;
-  if (T > 1) {  // one selection per token, shared by the gate/up and down CTAs
-    e = launch_pdl(dec_select, dim3(T), 256, (size_t)select_smem(p.E), st, pdl, a);
-    if (e != cudaSuccess) return e;
-  }
-  e = launch_pdl(dec_gate_up<QT, MAXB>, dim3((unsigned)((p.K * p.F + p.Fs) / GU_VALUES), T), GU_THREADS,
-                 (size_t)p.gu_smem, st, pdl, a, trows);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(dec_down<QT>, dim3((unsigned)(p.H / p.dn_rows), T), DN_THREADS, (size_t)p.dn_smem, st, pdl,
-                    a, trows);
+  return launch_pdl(dec_gate_up<QT, MAXB>, dim3((unsigned)((p.K * p.F + p.Fs) / GU_VALUES), (unsigned)a.T),
+                    GU_THREADS, (size_t)p.gu_smem, st, pdl, a, trows);
 }
 
+template <int QT>
+static cudaError_t launch_down(const DecodeArgs& a, cudaStream_t st, bool pdl, int trows) {
+  const DecodePlan& p = a.p;
+  return launch_pdl(dec_down<QT>, dim3((unsigned)(p.H / p.dn_rows), (unsigned)a.T), DN_THREADS, (size_t)p.dn_smem,
+                    st, pdl, a, trows);
+}
+
+// The chain: router, (several tokens) selection, gate/up in the gate/up rows' block type,
+// down in the down rows' block type.
 cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, int trows) {
-  switch (a.p.qtype * 8 + maxb) {
-    case 2 * 8 + 1: return launch_chain<2, 1>(a, st, pdl, trows);
-    case 2 * 8 + 2: return launch_chain<2, 2>(a, st, pdl, trows);
-    case 2 * 8 + 3: return launch_chain<2, 3>(a, st, pdl, trows);
-    case 3 * 8 + 1: return launch_chain<3, 1>(a, st, pdl, trows);
-    case 3 * 8 + 2: return launch_chain<3, 2>(a, st, pdl, trows);
-    case 3 * 8 + 3: return launch_chain<3, 3>(a, st, pdl, trows);
+  const DecodePlan& p = a.p;
+  cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)0, st, pdl, a, trows);
+  if (e != cudaSuccess) return e;
+  if (a.T > 1) {  // one selection per token, shared by the gate/up and down CTAs
+    e = launch_pdl(dec_select, dim3((unsigned)a.T), 256, (size_t)select_smem(p.E), st, pdl, a);
+    if (e != cudaSuccess) return e;
+  }
+  switch (p.qtype * 8 + maxb) {
+    case 2 * 8 + 1: e = launch_gate_up<2, 1>(a, st, pdl, trows); break;
+    case 2 * 8 + 2: e = launch_gate_up<2, 2>(a, st, pdl, trows); break;
+    case 2 * 8 + 3: e = launch_gate_up<2, 3>(a, st, pdl, trows); break;
+    case 3 * 8 + 1: e = launch_gate_up<3, 1>(a, st, pdl, trows); break;
+    case 3 * 8 + 2: e = launch_gate_up<3, 2>(a, st, pdl, trows); break;
+    case 3 * 8 + 3: e = launch_gate_up<3, 3>(a, st, pdl, trows); break;
+    case 12 * 8 + 1: e = launch_gate_up<12, 1>(a, st, pdl, trows); break;
+    case 12 * 8 + 2: e = launch_gate_up<12, 2>(a, st, pdl, trows); break;
+    case 12 * 8 + 3: e = launch_gate_up<12, 3>(a, st, pdl, trows); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  switch (p.qtype_dn) {
+    case 2: return launch_down<2>(a, st, pdl, trows);
+    case 3: return launch_down<3>(a, st, pdl, trows);
+    case 12: return launch_down<12>(a, st, pdl, trows);
+    case 14: return launch_down<14>(a, st, pdl, trows);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -22,9 +22,9 @@ namespace moe {
 
 struct DecodePlan {
   // layer shape
-  int H, E, K, F, Fs, G, Gu, qtype;
+  int H, E, K, F, Fs, G, Gu;
+  int qtype, qtype_dn;  // block types of the gate/up rows and of the down rows (ggml ids)
   // bytes
-  uint32_t blk;         // bytes per 32-value block (18 or 20)
   uint32_t rb_h;        // bytes per gate/up row (H values)
   uint32_t rb_f;        // bytes per routed down row (F values)
   uint32_t rb_fs;       // bytes per shared down row (Fs values)

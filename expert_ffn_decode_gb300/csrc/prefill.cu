@@ -324,6 +324,82 @@ __device__ __forceinline__ void load_block(const uint8_t* row, int blk, __half2&
   }
 }
 
+// Values 4w .. 4w + 3 (bytes of qa) and 16 + 4w .. 16 + 4w + 3 (bytes of qb) of a 32-value
+// block, each v = df * q + mf in f32 (exact for the K-quant scales) and rounded once to f16,
+// as the core-matrix row of slots 8w .. 8w + 7 (slot order: kslot).
+__device__ __forceinline__ uint4 core_row_f32(uint32_t qa, uint32_t qb, float df, float mf) {
+  float v[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[k] = fmaf(df, (float)((qa >> (8 * k)) & 0xFFu), mf);
+    v[4 + k] = fmaf(df, (float)((qb >> (8 * k)) & 0xFFu), mf);
+  }
+  return make_uint4(h2bits(__floats2half2_rn(v[0], v[2])), h2bits(__floats2half2_rn(v[1], v[3])),
+                    h2bits(__floats2half2_rn(v[4], v[6])), h2bits(__floats2half2_rn(v[5], v[7])));
+}
+
+// Block `blk` (32 values) of a weight row in global memory, dequantised into the four core
+// rows of its slots. Q4_0/Q4_1: one block. K-quants (ggml layouts, as the Ling store keeps
+// them; the pages name the types only): sub-block blk % 8 of super-block blk / 8.
+//   Q4_K (144 bytes, rows on 16-byte bounds): f16 d, f16 dmin, 12 packed scale bytes S,
+//   four runs of 32 nibble bytes (run c: sub-block 2c low nibbles, 2c + 1 high nibbles);
+//   sub-block j < 4: sc = S[j] & 63, mn = S[j + 4] & 63; j >= 4: low 4 bits from S[j + 4],
+//   top 2 bits from S[j - 4] (sc) and S[j] (mn); value = d sc q - dmin mn.
+//   Q6_K (210 bytes, rows on 2-byte bounds): ql[128], qh[64], 16 int8 scales, f16 d;
+//   sub-block j = (n = j / 4, r = j % 4), value i: nibble (low for r < 2) of
+//   ql[64n + 32 (r % 2) + i], high bits 2r, 2r + 1 of qh[32n + i], scale[8n + 2r + i / 16];
+//   value = d * scale * (q - 32).
+template <int QT>
+__device__ __forceinline__ void load_dequant(const uint8_t* row, int blk, uint4 (&o)[4]) {
+  if constexpr (QT == 12) {
+    const uint8_t* sb = row + 144 * (blk >> 3);
+    const int j = blk & 7, sh = 8 * (j & 3);
+    const uint4 hd = __ldg(reinterpret_cast<const uint4*>(sb));
+    const uint4 n0 = __ldg(reinterpret_cast<const uint4*>(sb + 16 + 32 * (j >> 1)));
+    const uint4 n1 = __ldg(reinterpret_cast<const uint4*>(sb + 32 + 32 * (j >> 1)));
+    const uint32_t by = (hd.y >> sh) & 0xFFu, bz = (hd.z >> sh) & 0xFFu, bw = (hd.w >> sh) & 0xFFu;
+    const uint32_t sc = j < 4 ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4));
+    const uint32_t mn = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
+    const float2 f = __half22float2(bits2h(hd.x));
+    const float df = f.x * (float)sc, mf = -(f.y * (float)mn);
+    const int ns = 4 * (j & 1);
+    const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      o[c] = core_row_f32((w[c] >> ns) & 0x0F0F0F0Fu, (w[4 + c] >> ns) & 0x0F0F0F0Fu, df, mf);
+  } else if constexpr (QT == 14) {
+    const uint8_t* sb = row + 210 * (blk >> 3);
+    const int j = blk & 7, n = j >> 2, r = j & 3;
+    const unsigned short* ql = reinterpret_cast<const unsigned short*>(sb + 64 * n + 32 * (r & 1));
+    const unsigned short* qh = reinterpret_cast<const unsigned short*>(sb + 128 + 32 * n);
+    const uint32_t scp = __ldg(reinterpret_cast<const unsigned short*>(sb + 192 + 8 * n + 2 * r));
+    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(sb + 208))));
+    const float df0 = d * (float)(int)(int8_t)(scp & 0xFFu), df1 = d * (float)(int)(int8_t)(scp >> 8);
+    const int ls = 4 * (r >> 1), hs = 2 * r;
+    uint32_t u[8];  // q of values 4i .. 4i + 3, 0 .. 63
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t L = (uint32_t)__ldg(ql + 2 * i) | ((uint32_t)__ldg(ql + 2 * i + 1) << 16);
+      const uint32_t Hb = (uint32_t)__ldg(qh + 2 * i) | ((uint32_t)__ldg(qh + 2 * i + 1) << 16);
+      u[i] = ((L >> ls) & 0x0F0F0F0Fu) | (((Hb >> hs) & 0x03030303u) << 4);
+    }
+    // values 0 .. 15 take scale 0 and 16 .. 31 scale 1: core row c holds 4c .. (first half)
+    // and 16 + 4c .. (second half), so each half has its own scale; q - 32 enters as the offset
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 lo = core_row_f32(u[c], 0u, df0, -32.f * df0);
+      const uint4 hi = core_row_f32(u[4 + c], 0u, df1, -32.f * df1);
+      o[c] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  } else {
+    __half2 d2, m2;
+    uint32_t qw[4];
+    load_block<QT>(row, blk, d2, m2, qw);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) o[w] = dequant_word<QT>(qw[w], d2, m2);
+  }
+}
+
 // L2 prefetch of the 16-byte-aligned part of [p, p + bytes).
 __device__ __forceinline__ void prefetch_span(const void* p, uint32_t bytes) {
   const uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15);
@@ -416,13 +492,12 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
       for (int pass = 0; pass < 2; ++pass) {
         const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
         if (m < mrows && b < kb) {
-          __half2 d2, m2;
-          uint32_t qw[4];
-          load_block<QT>(wrow(m), kc * (KC / 32) + b, d2, m2, qw);
+          uint4 o[4];
+          load_dequant<QT>(wrow(m), kc * (KC / 32) + b, o);
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const int kcore = 4 * b + w, mcore = m >> 3;
-            *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = dequant_word<QT>(qw[w], d2, m2);
+            *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = o[w];
           }
         }
       }
@@ -574,7 +649,8 @@ __global__ void __launch_bounds__(256) prefill_rmsnorm(const PrefillArgs a) {
 // ---------------------------------------------------------------------------
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-bool prefill_tile_ok(int H, int F, int Fs, int qtype) {
+bool prefill_tile_ok(int H, int F, int Fs, int qtype, int qtype_dn) {
+  if (qtype != qtype_dn || (qtype != 2 && qtype != 3)) return false;
   const int kc = qtype == 3 ? 128 : 256;
   return H % kc == 0 && F % kc == 0 && Fs % kc == 0;
 }
@@ -661,9 +737,20 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
   } else {
     prefill_x16<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    e = a.qtype == 3 ? launch_gemm<3, 0>(a, st) : launch_gemm<2, 0>(a, st);
+    switch (a.qtype) {  // gate/up in the gate/up rows' block type
+      case 2: e = launch_gemm<2, 0>(a, st); break;
+      case 3: e = launch_gemm<3, 0>(a, st); break;
+      case 12: e = launch_gemm<12, 0>(a, st); break;
+      default: return cudaErrorInvalidValue;
+    }
     if (e != cudaSuccess) return e;
-    e = a.qtype == 3 ? launch_gemm<3, 1>(a, st) : launch_gemm<2, 1>(a, st);
+    switch (a.qtype_dn) {  // down in the down rows' block type
+      case 2: e = launch_gemm<2, 1>(a, st); break;
+      case 3: e = launch_gemm<3, 1>(a, st); break;
+      case 12: e = launch_gemm<12, 1>(a, st); break;
+      case 14: e = launch_gemm<14, 1>(a, st); break;
+      default: return cudaErrorInvalidValue;
+    }
     if (e != cudaSuccess) return e;
   }
   prefill_combine<<<(unsigned)((nx / 4 + 255) / 256), 256, 0, st>>>(a);

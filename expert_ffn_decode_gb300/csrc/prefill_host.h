@@ -57,7 +57,8 @@ struct PrefillArgs {
   float* sbuf;              // [T][H] shared-expert down outputs
   uint32_t* status;         // device error bits
   // shape
-  int T, H, E, K, F, Fs, G, Gu, qtype;
+  int T, H, E, K, F, Fs, G, Gu;
+  int qtype, qtype_dn;      // block types of the gate/up rows and of the down rows (ggml ids)
   float scale, norm_min;
   float lim, lim_s;         // SwiGLU clamp limits of the routed and shared experts (0: none)
   const float* norm;        // [H] prologue norm weights, or null
@@ -79,10 +80,11 @@ struct PrefillWs {
 };
 PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile);
 
-// True when the layer's K dimensions are whole pipeline chunks (128 values for Q4_1,
-// 256 for Q4_0): every weight-row segment a chunk copies then starts and ends on a
-// 16-byte boundary, which the bulk copies of the tile pipeline need.
-bool prefill_tile_ok(int H, int F, int Fs, int qtype);
+// True when all three matrices are Q4_0 or all Q4_1 and the layer's K dimensions are whole
+// pipeline chunks (128 values for Q4_1, 256 for Q4_0): every weight-row segment a chunk
+// copies then starts and ends on a 16-byte boundary, which the bulk copies of the tile
+// pipeline need. Other layers (K-quants among them) take the general contractions.
+bool prefill_tile_ok(int H, int F, int Fs, int qtype, int qtype_dn);
 
 // Tile pipeline launches (prefill_tc.cu).
 cudaError_t tile_router_launch(const PrefillArgs& a, cudaStream_t st);

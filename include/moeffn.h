@@ -21,14 +21,24 @@
  * comment above Q41DOT): Q4_1 = f16 d, f16 m, 16 nibble bytes, value d*q + m;
  * Q4_0 = f16 d, 16 nibble bytes, value d*(q - 8). In a block the low nibble of
  * byte i is value i and its high nibble is value 16 + i.
+ * K-quant super-blocks of 256 values, the types the Ling store keeps (ling_moe_ssd.js,
+ * file header and planLayoutLing: Q4_K gate/up rows, Q6_K or Q4_K down rows); the pages
+ * name these types without their layouts, which are ggml's:
+ *   Q4_K, 144 bytes: f16 d, f16 dmin, 12 bytes of packed 6-bit scales sc_j and mins mn_j
+ *     of the eight 32-value sub-blocks, then four runs of 32 nibble bytes (run c: values
+ *     64c .. in the low nibbles, 64c + 32 .. in the high nibbles); value = d sc_j q - dmin mn_j.
+ *   Q6_K, 210 bytes: 128 bytes of low nibbles, 64 bytes of 2-bit high parts, 16 int8
+ *     scales (one per 16 values), f16 d; value = d * scale * (q - 32).
  *
  * Layouts (all row-major, little-endian):
  *   x, out         [n_tokens][hidden] f32
  *   router_w       [n_experts][hidden] f32 (row e = expert e)
  *   router_bias    [n_experts] f32, or NULL for no selection bias
- *   expert_blocks  n_experts records back to back; record = gate [expert_ff][hidden/32 blocks],
- *                  up [expert_ff][hidden/32 blocks], down [hidden][expert_ff/32 blocks];
- *                  record bytes = 3 * expert_ff * hidden / 32 * block_bytes (18 or 20)
+ *   expert_blocks  n_experts records back to back; record = gate [expert_ff rows of hidden
+ *                  values], up [expert_ff rows], both in qtype, then down [hidden rows of
+ *                  expert_ff values] in the down type (qtype_down, or qtype when it is 0);
+ *                  a row of n values takes n/32 blocks (Q4_0 18, Q4_1 20 bytes) or n/256
+ *                  super-blocks (Q4_K 144, Q6_K 210 bytes)
  *   shared_blocks  one record of the same form with shared_ff, or NULL when shared_ff == 0
  *   topk_ids       [n_tokens][top_k] int32 picks in selection order (optional output)
  *   topk_w         [n_tokens][top_k] f32 weights (optional output)
@@ -58,6 +68,8 @@ extern "C" {
 /* ggml block type ids (flint_moe_ssd.js: GGML_Q4_1 = 3). */
 #define MOE_Q4_0 2
 #define MOE_Q4_1 3
+#define MOE_Q4_K 12
+#define MOE_Q6_K 14
 
 /* moe_cfg.flags */
 #define MOE_ACCUMULATE 1u /* out = out + contribution (the pages' x += ...)          */
@@ -87,7 +99,10 @@ enum {
  *   1 <= top_k <= min(n_experts, 32); n_experts <= 1024;
  *   n_groups divides n_experts; n_groups > 1 needs n_experts / n_groups >= 2,
  *   n_groups <= 64, 1 <= groups_used <= n_groups, top_k <= groups_used * n_experts / n_groups;
- *   n_tokens >= 0 (0: nothing is launched); qtype MOE_Q4_0 or MOE_Q4_1;
+ *   n_tokens >= 0 (0: nothing is launched); qtype MOE_Q4_0, MOE_Q4_1 or MOE_Q4_K;
+ *   qtype_down 0 (the same as qtype), MOE_Q4_0, MOE_Q4_1, MOE_Q4_K or MOE_Q6_K;
+ *   K-quant gate/up rows need hidden % 256 == 0, K-quant down rows expert_ff and
+ *   shared_ff multiples of 256;
  *   norm_min >= 0 (the pages use 2^-14 = 6.103515625e-5). */
 typedef struct moe_cfg {
   int32_t hidden;
@@ -115,6 +130,10 @@ typedef struct moe_cfg {
    * FFN block. NULL: x enters as is. */
   float rms_eps;
   const float* ffn_norm;
+  /* Block type of the down rows (routed and shared), or 0 for qtype: the Ling store
+   * types its down rows per layer, apart from the gate/up rows (ling_moe_ssd.js,
+   * planLayoutLing). */
+  int32_t qtype_down;
 } moe_cfg;
 
 /* Two execution paths, chosen by n_tokens (both are exact restatements of the step
@@ -135,9 +154,10 @@ typedef struct moe_cfg {
  *                  pair (22 bits). The SwiGLU activations are rounded once to f16.
  *                  Products accumulate in f32. Requires |x| and every activation to
  *                  stay below 65504 (the f16 range).
- *   Layers whose hidden, expert_ff and shared_ff are whole multiples of 128 (Q4_1) or
- *   256 (Q4_0) run the batched contractions as warp-specialised TMA/TMEM pipelines;
- *   other shapes run a general form of the same contractions.
+ *   Layers whose three matrices are all Q4_1 (or all Q4_0) and whose hidden, expert_ff
+ *   and shared_ff are whole multiples of 128 (Q4_1) or 256 (Q4_0) run the batched
+ *   contractions as warp-specialised TMA/TMEM pipelines; other layers (K-quant ones
+ *   among them) run a general form of the same contractions.
  * Both paths give the same picks; outputs agree to the tolerance of their arithmetic
  * (relative L2 well under 2e-3 against a float64 evaluation). */
 

@@ -50,6 +50,10 @@ BAD = [
     dict(n_tokens=-1), dict(qtype=8), dict(weights_scale=float("inf")), dict(norm_min=-1.0),
     dict(flags=64), dict(swiglu_limit=-1.0), dict(swiglu_limit_shared=float("nan")),
     dict(swiglu_limit=float("inf")), dict(rms_eps=-1.0), dict(rms_eps=float("nan")),
+    dict(qtype=14), dict(qtype_down=13), dict(qtype_down=-1),
+    dict(qtype=12, hidden=96),                      # K-quant gate/up rows: hidden % 256
+    dict(qtype_down=14, expert_ff=128),             # K-quant down rows: expert_ff % 256
+    dict(qtype_down=12, expert_ff=256, shared_ff=96),
 ]
 
 
@@ -60,6 +64,13 @@ def test_invalid_cfg_rejected(built, kw):
     rc = ffn.moe_ffn_forward_ex(16, 16, None, 16, 16, cfg, 4096, 256, 1 << 20, None)
     assert rc == ffn.MOE_ERR_INVALID_CFG, (rc, ffn.moe_last_error())
     assert ffn.moe_last_error()
+
+
+@pytest.mark.parametrize("kw", [dict(qtype=12, hidden=256, expert_ff=256), dict(qtype=12, qtype_down=14,
+                                hidden=512, expert_ff=768, shared_ff=256), dict(qtype_down=14, expert_ff=512),
+                                dict(qtype=12, qtype_down=2, hidden=256, expert_ff=96)])
+def test_kquant_cfg_accepted(built, kw):
+    assert ffn.moe_workspace_size(_cfg(**kw)) > 0, ffn.moe_last_error()
 
 
 def test_valid_cfg_workspace_size(built):
