@@ -158,11 +158,12 @@ def moe_trace_offset(cfg):
 
 
 # Names of the MOE_TRACE timeline points, in order.
-TRACE_POINTS = ("router_start", "router_x_ready", "router_done", "",
+TRACE_POINTS = ("router_start", "router_x_ready", "router_done", "gate_up_sel_keys",
                 "gate_up_start", "gate_up_x_quantised", "gate_up_waited", "gate_up_picked", "gate_up_rows_landed",
                 "gate_up_end", "gate_up_dots", "gate_up_sums",
                 "down_start", "down_picked", "down_rows_requested", "down_waited", "down_act_staged",
-                "down_rows_landed", "down_end", "", "down_loop_done", "down_sums")
+                "down_rows_landed", "down_end", "gate_up_sel_cands", "down_loop_done", "down_sums",
+                "gate_up_sel_ranked")
 TRACE_STRIDE = 24  # u64 words per CTA
 
 

@@ -105,7 +105,7 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, ids, wts, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
+  size_t ctrl, logits, act, ids, wts, pub, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
 };
 
 // SMs of the current device (the timeline keeps one row per SM); without a
@@ -154,6 +154,8 @@ WsLayout ws_layout(const moe_cfg* c, bool decode_only = false) {
   o = up256(o + td * c->top_k * 4);
   L.wts = o;
   o = up256(o + td * c->top_k * 4);
+  L.pub = o;     // decode: the picks a single-token call publishes for its down kernel [K] u64
+  o = up256(o + (size_t)c->top_k * 8);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -445,6 +447,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.act = reinterpret_cast<float*>(wsb + W.act);
   a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
   a.wts = reinterpret_cast<float*>(wsb + W.wts);
+  a.pub = reinterpret_cast<unsigned long long*>(wsb + W.pub);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -653,6 +656,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.act = reinterpret_cast<float*>(wsb + W.act);
   a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
   a.wts = reinterpret_cast<float*>(wsb + W.wts);
+  a.pub = reinterpret_cast<unsigned long long*>(wsb + W.pub);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;

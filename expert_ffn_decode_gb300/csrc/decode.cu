@@ -356,7 +356,7 @@ __device__ __forceinline__ void group_sum_n(float (&v)[N], int lpr) {
 // Timeline points (MOE_TRACE): %globaltimer readings per CTA index (CTAs below the
 // trace's row count), written by thread 0.
 enum TracePoint : int {
-  TR_RT_START = 0, TR_RT_X = 1, TR_RT_DONE = 2,
+  TR_RT_START = 0, TR_RT_X = 1, TR_RT_DONE = 2, TR_SEL_KEYS = 3, TR_SEL_CANDS = 19, TR_SEL_RANKED = 22,
   TR_GU_START = 4, TR_GU_XQ = 5, TR_GU_WAITED = 6, TR_GU_PICKED = 7, TR_GU_DATA = 8, TR_GU_END = 9,
   TR_DN_START = 12, TR_DN_PICKED = 13, TR_DN_REQUESTED = 14, TR_DN_WAITED = 15, TR_DN_QUANT = 16,
   TR_DN_DATA = 17, TR_DN_END = 18, TR_GU_DOTS = 10, TR_GU_SUMS = 11, TR_DN_LOOP = 20,
@@ -404,10 +404,11 @@ __device__ __forceinline__ void sort_list(uint32_t (&kv)[N], int (&ki)[N]) {
 //      k rounds over the lanes' sorted lists (the winning lane drops its head)
 //   4. warp 0: the top k of the 8 sorted candidate lists (lane l walks list l), then
 //      the weights
-// Key 0 is below every real key (every float's key is at least that of -inf).
+// Key 0 is below every real key (every float's key is at least that of -inf). With
+// trows > 0 thread 0 records the timeline points of the selection's phases.
 template <int N>
 __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* sel, float* gscore, int* rids,
-                               float* rw) {
+                               float* rw, int trows) {
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* probs = reinterpret_cast<float*>(sel);
@@ -434,6 +435,7 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
   }
   if (tid == 0) kept_groups = ~0ull;
   __syncthreads();
+  tr(a, TR_SEL_KEYS, trows);
   if (p.G > 1) {
     const int per = p.E / p.G;
     #pragma unroll 1
@@ -517,6 +519,7 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
     }
   }
   __syncthreads();
+  tr(a, TR_SEL_CANDS, trows);
   if (warp == 0) {
     // stage 2: lane l < 8 walks warp l's sorted candidates
     int h = 0;
@@ -535,6 +538,7 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
       }
     }
     __syncwarp();
+    tr(a, TR_SEL_RANKED, trows);
     // weights from the picked sigmoids
     const float pj = lane < p.K ? probs[rids[lane]] : 0.f;
     const float wsum = fmaxf(warp_sum(pj), a.norm_min);
@@ -544,10 +548,10 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
 }
 // The picks of the token whose logits row is `lg`.
 __device__ __forceinline__ void select_picks(const DecodeArgs& a, const float* lg, uint8_t* sel, float* gscore,
-                                             int* rids, float* rw) {
-  if (a.p.E <= 256) select_picks_n<1>(a, lg, sel, gscore, rids, rw);
-  else if (a.p.E <= 512) select_picks_n<2>(a, lg, sel, gscore, rids, rw);
-  else select_picks_n<4>(a, lg, sel, gscore, rids, rw);
+                                             int* rids, float* rw, int trows = 0) {
+  if (a.p.E <= 256) select_picks_n<1>(a, lg, sel, gscore, rids, rw, trows);
+  else if (a.p.E <= 512) select_picks_n<2>(a, lg, sel, gscore, rids, rw, trows);
+  else select_picks_n<4>(a, lg, sel, gscore, rids, rw, trows);
 }
 
 // ===========================================================================
@@ -574,6 +578,9 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   pdl_wait_prior_grids();  // x may come from the previous kernel
   pdl_launch_dependents();
   tr(a, TR_RT_X, trows);
+  // this call's published picks start empty (the previous call's kernels are complete:
+  // the wait above covers them, and every reader of this call starts after this grid)
+  if (a.T == 1 && blockIdx.x == 0 && tid < p.K) st_relaxed_u64(a.pub + tid, PUB_EMPTY);
   // the prologue (with a norm vector): token t's input is x_t * r_t * norm, r_t =
   // 1/rms(x_t); the router dot takes x_t * norm and the row's sum is scaled by r_t.
   // Every token's sum of squares in one pass (loads of all tokens in flight together).
@@ -669,7 +676,7 @@ __global__ void __launch_bounds__(256) dec_select(const DecodeArgs a) {
 // 8 rows), then the x planes [nbH][64] and x info [nbH], then the selection's probs
 // and keys.
 template <int QT, int MAXB>
-__global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, int trows) {
+__global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a, int trows) {
   extern __shared__ __align__(128) uint8_t gsm[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ float rowdot[GU_THREADS / 32][4];
@@ -728,10 +735,13 @@ __global__ void __launch_bounds__(GU_THREADS) dec_gate_up(const DecodeArgs a, in
     tr(a, TR_GU_WAITED, trows);
     const int slot = (v0 - p.Fs) / p.F;
     if (a.T == 1) {
-      select_picks(a, a.logits, sel, gscore, rids, rw);
+      select_picks(a, a.logits, sel, gscore, rids, rw, trows);
       if (v0 == p.Fs && tid < p.K) {  // one CTA reports the picks
         if (a.topk_ids) a.topk_ids[tid] = rids[tid];
         if (a.topk_w) a.topk_w[tid] = rw[tid];
+        // for down CTAs that start after this point: one 64-bit store per pick
+        st_relaxed_u64(a.pub + tid, (unsigned long long)(uint32_t)rids[tid] |
+                                        ((unsigned long long)__float_as_uint(rw[tid]) << 32));
       }
     } else if (tid == 0) {
       rids[slot] = __ldcg(a.ids + (size_t)tok * p.K + slot);  // made by the selection kernel
@@ -823,7 +833,17 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   // the picks (the router is complete: every routed gate/up CTA waited for it before
   // this launch was triggered)
   if (a.T == 1) {
-    select_picks(a, a.logits, sel, gscore, rids, rw);
+    // The picks: those the gate/up kernel has published if all k are there (a down CTA
+    // that could not start before the gate/up CTAs left finds them), else made here.
+    // Nothing waits on them: an entry is either empty or this call's pick.
+    bool mine = true;
+    if (tid < p.K) {
+      const unsigned long long v = ld_relaxed_u64(a.pub + tid);
+      mine = v != PUB_EMPTY;
+      rids[tid] = (int)(uint32_t)v;
+      rw[tid] = __uint_as_float((uint32_t)(v >> 32));
+    }
+    if (!__syncthreads_and(mine)) select_picks(a, a.logits, sel, gscore, rids, rw);
   } else {
     // made by the selection kernel, complete once every routed gate/up CTA has waited
     if (tid < p.K) {

@@ -59,6 +59,8 @@ MOE_HD uint32_t window_bytes(uint32_t bytes) { return align16(bytes) + 16u; }
 // then 256 candidate keys and 256 candidate experts.
 MOE_HD uint32_t select_smem(int E) { return align16((uint32_t)E * 8u) + 2048u; }
 
+constexpr unsigned long long PUB_EMPTY = ~0ull;  // an entry not (yet) published in this call
+
 constexpr uint32_t FLAG_ACCUMULATE = 1u;  // out = out + contribution
 constexpr uint32_t FLAG_RESIDUAL = 2u;    // out = x + contribution
 
@@ -78,6 +80,8 @@ struct DecodeArgs {
   float* act;                 // [T][act_stride] SwiGLU activations, shared expert's first
   int32_t* ids;               // [T][K] picks (calls of T > 1: made by the selection kernel)
   float* wts;                 // [T][K] their weights
+  unsigned long long* pub;    // [K] a single-token call's picks as the gate/up kernel publishes
+                              // them: id | weight bits << 32, or PUB_EMPTY
   int T;                      // tokens of this call, 1 .. DEC_TMAX
   float scale, norm_min;
   float lim, lim_s;           // SwiGLU clamp limits of the routed and shared experts (0: none)

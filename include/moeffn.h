@@ -192,7 +192,8 @@ size_t moe_workspace_size(const moe_cfg* cfg);
  * the CTA with that index in each of the three decode kernels of the last token:
  * router kernel 0 start, 1 x ready (previous kernel done), 2 logits written;
  * gate/up kernel 4 start, 5 x quantised, 6 logits ready, 7 picks made, 8 the CTA's
- * first rows in shared memory, 9 activation block written; down kernel 12 start,
+ * first rows in shared memory, 9 activation block written, and within its selection
+ * (single-token calls) 3 keys made, 19 candidates gathered, 22 picks ranked; down kernel 12 start,
  * 13 picks made, 14 row copies issued, 15 activation blocks ready, 16 activation
  * blocks staged, 17 rows in shared memory, 18 output rows written. Unused words
  * stay 0. */

@@ -253,3 +253,33 @@ def test_weight_clamp_case():
     assert list(rid[0]) == [0, 1, 2]
     out, ids, wts = GpuLayer(layer, w).run(x)
     compare(out, ids, wts, ref, rid, rwt, "clamp")
+
+
+TIES = [
+    # (experts, picks, groups, groups used, distinct router rows): the top class holds about
+    # E / rows experts that tie exactly; up to 64 candidates take the pruned ranking, more
+    # take the sorted-list rounds
+    (256, 6, 1, 1, 5),
+    (256, 8, 1, 1, 3),
+    (512, 8, 8, 4, 6),
+    (64, 6, 8, 3, 4),
+    (1000, 7, 1, 1, 40),
+]
+
+
+@pytest.mark.parametrize("E,K,G,Gu,rows", TIES, ids=[f"E{t[0]}k{t[1]}g{t[2]}r{t[4]}" for t in TIES])
+def test_selection_exact_ties(E, K, G, Gu, rows):
+    # duplicated router rows give bit-identical logits on both sides: the picks are the
+    # lowest experts of the best tie classes, in index order within a class
+    w = _small(90 + rows, n_experts=E, top_k=K, n_groups=G, groups_used=Gu, hidden=128, expert_ff=64,
+               router_std=0.1)
+    layer = synth.make_layer(w)
+    base = layer["router_w"][:rows].copy()
+    layer["router_w"] = base[(np.arange(E) * 37) % rows]
+    x = synth.make_tokens(5, w["hidden"], 2)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], None, layer["expert_blocks"], None, oracle_cfg(w))
+    out, ids, wts = GpuLayer(layer, w).run(x)
+    compare(out, ids, wts, ref, rid, rwt, "ties")
+    for t in range(2):  # and one token per call (the selection inside the gate/up and down CTAs)
+        o1, i1, w1 = GpuLayer(layer, w).run(x[t:t + 1])
+        compare(o1, i1, w1, ref[t:t + 1], rid[t:t + 1], rwt[t:t + 1], f"ties token {t}")
