@@ -265,6 +265,17 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
           file=sys.stderr)
 
 
+def prefill_launches(w):
+    """Kernel launches of one batched pass of at most 512 tokens. The tile path (all three
+    matrices Q4_1, or all Q4_0, with H, F and Fs whole multiples of 128 (Q4_1) or 256 (Q4_0)):
+    token images, router, top-k, sort, routed images, gate/up, down, combine. The general
+    path: router, top-k, sort, x operand, gate/up, down, combine."""
+    qt, qd = w["qtype"], w.get("qtype_down") or w["qtype"]
+    kc = 128 if qt == 3 else 256
+    tile = qt == qd and qt in (2, 3) and all(v % kc == 0 for v in (w["hidden"], w["expert_ff"], w["shared_ff"]))
+    return 8 if tile else 7
+
+
 def prefill_bytes(w, distinct):
     """Algorithmic bytes of one batched step: the router, every expert some token
     picked (`distinct` of them, each read once), the shared expert, x and out."""
@@ -349,7 +360,7 @@ def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, 
     ffn.check(ffn.moe_workspace_status(wsh, stream))
     return {"workload": workload, "T": T, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": ms, "steps": n, "layers_rotated": L, "distinct_experts_per_step": statistics.mean(distinct),
-            "bytes_per_step": step_bytes, "launches_per_step": 7, "e2e": round(e2e, 1), "e2e_steps": e2e_steps,
+            "bytes_per_step": step_bytes, "launches_per_step": prefill_launches(w) * -(-T // 512), "e2e": round(e2e, 1), "e2e_steps": e2e_steps,
             "h2d_bytes_per_step": T * H * 4, "d2h_bytes_per_step": T * H * 4}
 
 

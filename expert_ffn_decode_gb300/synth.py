@@ -63,6 +63,10 @@ WORKLOADS = {
     "ling_kq_decode_t1": dict(hidden=2560, n_experts=512, top_k=8, expert_ff=768, shared_ff=768,
                               n_groups=8, groups_used=4, qtype=Q4_K, qtype_down=Q6_K, weights_scale=2.5,
                               n_tokens=1, router_std=0.02, bias_std=0.1, seed=5),
+    # The same K-quant layer over T=512 tokens (the batched path's general contractions).
+    "ling_kq_prefill_t512": dict(hidden=2560, n_experts=512, top_k=8, expert_ff=768, shared_ff=768,
+                                 n_groups=8, groups_used=4, qtype=Q4_K, qtype_down=Q6_K, weights_scale=2.5,
+                                 n_tokens=512, router_std=0.02, bias_std=0.1, seed=8),
     # Small K-quant layers for the parity tests: H=256, 16 experts, top-2, F=256,
     # shared F=256, Q4_K gate/up with Q6_K (or Q4_K) down, T=4.
     "tiny_kq_t4": dict(hidden=256, n_experts=16, top_k=2, expert_ff=256, shared_ff=256,
