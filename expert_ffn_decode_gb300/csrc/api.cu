@@ -36,6 +36,17 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The device address of page-locked host memory mapped into the current device's address
+// space, or null for any other pointer (pageable host memory, device memory).
+void* mapped_host(const void* p) {
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return pa.type == cudaMemoryTypeHost ? pa.devicePointer : nullptr;
+}
+
 // Bytes of a weight row of n values: 32-value blocks of 18 (Q4_0) or 20 (Q4_1) bytes, or
 // 256-value super-blocks of 144 (Q4_K) or 210 (Q6_K) bytes.
 uint32_t row_bytes(int n, int qtype) {
@@ -354,14 +365,29 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   int32_t* dids = ids;
   float* dw = wts;
   cudaError_t e;
+  // Host outputs in page-locked memory mapped into the device's address space are written
+  // in place by the kernels (one pass of stores, no copy back); other host outputs are staged.
+  bool out_direct = false, ids_direct = false, w_direct = false;
   if (host) {
     dx = reinterpret_cast<const float*>(wsb + W.x_stage);
     dout = reinterpret_cast<float*>(wsb + W.out_stage);
     dids = ids ? reinterpret_cast<int32_t*>(wsb + W.ids_stage) : nullptr;
     dw = wts ? reinterpret_cast<float*>(wsb + W.w_stage) : nullptr;
+    if (void* m = mapped_host(out)) {
+      dout = static_cast<float*>(m);
+      out_direct = true;
+    }
+    if (void* m = ids ? mapped_host(ids) : nullptr) {
+      dids = static_cast<int32_t*>(m);
+      ids_direct = true;
+    }
+    if (void* m = wts ? mapped_host(wts) : nullptr) {
+      dw = static_cast<float*>(m);
+      w_direct = true;
+    }
     e = cudaMemcpyAsync(const_cast<float*>(dx), x, xbytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "copy of x to the device");
-    if (c->flags & MOE_ACCUMULATE) {
+    if ((c->flags & MOE_ACCUMULATE) && !out_direct) {
       e = cudaMemcpyAsync(dout, out, xbytes, cudaMemcpyHostToDevice, st);
       if (e != cudaSuccess) return cuda_fail(e, "copy of out to the device");
     }
@@ -469,13 +495,15 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   if (host) {
-    e = cudaMemcpyAsync(out, dout, xbytes, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return cuda_fail(e, "copy of out to the host");
-    if (ids) {
+    if (!out_direct) {
+      e = cudaMemcpyAsync(out, dout, xbytes, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess) return cuda_fail(e, "copy of out to the host");
+    }
+    if (ids && !ids_direct) {
       e = cudaMemcpyAsync(ids, dids, (size_t)T * c->top_k * 4, cudaMemcpyDeviceToHost, st);
       if (e != cudaSuccess) return cuda_fail(e, "copy of topk_ids to the host");
     }
-    if (wts) {
+    if (wts && !w_direct) {
       e = cudaMemcpyAsync(wts, dw, (size_t)T * c->top_k * 4, cudaMemcpyDeviceToHost, st);
       if (e != cudaSuccess) return cuda_fail(e, "copy of topk_w to the host");
     }

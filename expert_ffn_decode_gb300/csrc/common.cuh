@@ -5,15 +5,16 @@
 
 #include <cstdint>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
 
 namespace moe {
 
 // ---- control block (first 512 bytes of every workspace) ---------------------
-// A workspace starts zeroed. The decode router kernel counts its finished CTAs in
-// CTRL_ROUTER; the last one selects and sets the counter back to zero. The status
-// word is sticky until the host clears it.
+// A workspace starts zeroed. The status word is sticky until the host clears it.
 enum CtrlWord : int {
-  CTRL_ROUTER = 1,   // router CTAs of the running decode call that finished
   CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
 };
 constexpr int CTRL_BYTES = 512;
@@ -21,6 +22,33 @@ constexpr int CTRL_BYTES = 512;
 enum DevErr : uint32_t {
   DEV_ERR_MBAR_TIMEOUT = 2u,   // a copy or a slot release never arrived
 };
+
+// Raises a kernel's dynamic shared memory limit on the current device when a launch needs
+// more than any earlier one did. The attribute persists, so later launches skip the
+// driver call (it is on every call's host path).
+inline cudaError_t ensure_smem(const void* kern, int bytes) {
+  struct Entry {
+    int dev;
+    const void* kern;
+    int bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto& d : done)
+    if (d.dev == dev && d.kern == kern) {
+      if (d.bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) d.bytes = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back(Entry{dev, kern, bytes});
+  return e;
+}
 
 // Spin limit, measured on %globaltimer: an mbarrier wait gives up after this many
 // nanoseconds.

@@ -695,7 +695,7 @@ template <int QT, int MODE>
 static cudaError_t launch_gemm(const PrefillArgs& a, cudaStream_t st) {
   auto kern = prefill_gemm<QT, MODE>;
   const int smem = 2 * A_STAGE + 2 * (MODE == 0 ? B_STAGE_GU : B_STAGE_DN);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   kern<<<a.nc, PREFILL_THREADS, smem, st>>>(a);
   return cudaGetLastError();
@@ -721,7 +721,7 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t topk_smem = (size_t)8 * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
-  e = cudaFuncSetAttribute(prefill_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem);
+  e = ensure_smem(reinterpret_cast<const void*>(prefill_topk), (int)topk_smem);
   if (e != cudaSuccess) return e;
   prefill_topk<<<(a.T + 7) / 8, 256, topk_smem, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

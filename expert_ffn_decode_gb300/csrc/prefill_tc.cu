@@ -836,7 +836,7 @@ cudaError_t launch_tile(const PrefillArgs& a, const TileMaps& maps, cudaStream_t
   using G = Geo<MODE, QT>;
   auto kern = tile_gemm<MODE, QT>;
   const int smem = G::SMEM + 1024;  // + alignment slack
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   kern<<<a.nc, TP_THREADS, smem, st>>>(a, maps);
   return cudaGetLastError();
@@ -1262,7 +1262,7 @@ cudaError_t launch_swap(const PrefillArgs& a, const SwMaps& maps, cudaStream_t s
   using G = SwGeo<QT>;
   auto kern = swap_down<QT>;
   const int smem = G::SMEM + 1024;  // + alignment slack
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   kern<<<a.nc, SW_THREADS, smem, st>>>(a, maps);
   return cudaGetLastError();

@@ -74,7 +74,9 @@ extern "C" {
 /* moe_cfg.flags */
 #define MOE_ACCUMULATE 1u /* out = out + contribution (the pages' x += ...)          */
 #define MOE_RESIDUAL 2u   /* out = x + contribution                                 */
-#define MOE_HOST_IO 4u    /* x, out, topk_ids, topk_w are host pointers, staged       */
+#define MOE_HOST_IO 4u    /* x, out, topk_ids, topk_w are host pointers: x is copied in;
+                           * outputs in page-locked memory mapped into the device's address
+                           * space are written in place, other outputs are staged */
 #define MOE_NO_PDL 8u     /* launch without programmatic dependent launch             */
 #define MOE_TRACE 16u     /* record a per-CTA timeline in the workspace (see below)   */
 #define MOE_BATCHED 32u   /* take the batched path whatever the token count           */

@@ -207,6 +207,21 @@ def test_flags_accumulate_residual_hostio_nopdl():
                                      st, ih, wh))
     ffn.check(ffn.moe_workspace_status(ws, st))
     assert np.array_equal(oh, base) and np.array_equal(ih, ids) and np.array_equal(wh, wts)
+    # page-locked outputs are written in place by the kernels (no staging copy), also when
+    # accumulating into them
+    po = torch.full((T, H), float("nan")).pin_memory()
+    pi = torch.full((T, w["top_k"]), -1, dtype=torch.int32).pin_memory()
+    pw = torch.full((T, w["top_k"]), float("nan")).pin_memory()
+    ffn.check(ffn.moe_ffn_forward_ex(xh, g.router_w, g.bias, g.experts, g.shared, cfg, po, ws, ws.numel(),
+                                     st, pi, pw))
+    st.synchronize()
+    assert np.array_equal(po.numpy(), base) and np.array_equal(pi.numpy(), ids) and np.array_equal(pw.numpy(), wts)
+    cfg_acc = ffn.make_cfg(**{**w, "n_tokens": T, "flags": ffn.MOE_HOST_IO | ffn.MOE_ACCUMULATE})
+    po.copy_(torch.from_numpy(init))
+    ffn.check(ffn.moe_ffn_forward_ex(xh, g.router_w, g.bias, g.experts, g.shared, cfg_acc, po, ws, ws.numel(),
+                                     st, None, None))
+    ffn.check(ffn.moe_workspace_status(ws, st))
+    assert np.array_equal(po.numpy(), acc)
 
 
 def test_plain_entry_point_and_repeat_determinism():
