@@ -181,14 +181,44 @@ print(json.dumps({{"tokens": n, "seconds": dt}}))
     return d, None
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend="nccl"):
+    """(rank, world, local rank) from the launcher's environment; with more than one rank,
+    joins the process group (one process per GPU: NCCL; the CPU tests use gloo)."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
     return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, dev):
+    """The largest of every rank's v (the slowest rank's time)."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, seconds, world, dev):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time
+    (every rank processes the same number of units)."""
+    return units_per_rank * world / max_over_ranks(seconds, world, dev)
+
+
+def layer_seed(rank, i, base=1000):
+    """Seed of a rank's i-th benchmark layer: every rank draws its own layers."""
+    return base + 7919 * rank + i
 
 
 def run_reference(args, rank, world):
@@ -294,7 +324,7 @@ def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     full = prefill_bytes(w, w["n_experts"])
     L = layers or max(2, math.ceil(2 * l2 / full) + 1)
-    layers = [synth.make_layer_torch(w, seed=5000 + 7919 * rank + i, device=dev) for i in range(L)]
+    layers = [synth.make_layer_torch(w, seed=layer_seed(rank, i, 5000), device=dev) for i in range(L)]
     NX = 3
     xs = [synth.make_tokens_torch(300 + 17 * rank + j, H, T, dev) for j in range(NX)]
     out = torch.zeros((T, H), device=dev)
@@ -462,7 +492,7 @@ def main():
     step_bytes = layer_bytes(w)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     L = args.layers or max(8, math.ceil(4 * l2 / step_bytes) + 1)
-    layers = [synth.make_layer_torch(w, seed=1000 + 7919 * rank + i, device=dev) for i in range(L)]
+    layers = [synth.make_layer_torch(w, seed=layer_seed(rank, i), device=dev) for i in range(L)]
     NX = 64
     xs = synth.make_tokens_torch(77 + rank, H, NX, dev)
     outs = torch.zeros((2, H), device=dev)
@@ -506,9 +536,7 @@ def main():
             wg.replay()
     stream.synchronize()
     ffn.check(ffn.moe_workspace_status(ws, stream))
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    barrier(world)
 
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -524,11 +552,7 @@ def main():
         torch.cuda.synchronize()
     elapsed_ms = ev0.elapsed_time(ev1)
     ffn.check(ffn.moe_workspace_status(ws, stream))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     sec = elapsed_ms / 1e3
     value = args.steps * T * world / sec
     ms_per_step = elapsed_ms / args.steps
@@ -560,22 +584,12 @@ def main():
         stream.synchronize()  # the step's result is on the host
     e2e_sec = time.perf_counter() - t0
     ffn.check(ffn.moe_workspace_status(wsh, stream))
-    e2e_val = n_e2e * T / e2e_sec
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_sec], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_val = n_e2e * T * world / float(t.item())
+    e2e_val = job_rate(n_e2e * T, e2e_sec, world, dev)
 
     pre = None
     if args.prefill_steps > 0:
         pre = bench_prefill(ffn, synth, "flint_prefill_t512", dev, rank, args.prefill_steps, 24)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([pre["ms_per_step"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            pre["ms_per_step"] = float(t.item())
-            pre["value"] = round(pre["T"] * world / (pre["ms_per_step"] * 1e-3), 1)
+        reduce_prefill(pre, world, dev)
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
@@ -630,22 +644,24 @@ def main():
     print(json.dumps(line))
 
 
+def reduce_prefill(pre, world, dev):
+    """A batched result over all ranks: the slowest rank's step time and e2e time, the
+    tokens of every rank."""
+    pre["ms_per_step"] = max_over_ranks(pre["ms_per_step"], world, dev)
+    pre["value"] = round(pre["T"] * world / (pre["ms_per_step"] * 1e-3), 1)
+    pre["e2e"] = round(job_rate(pre["T"], pre["T"] / pre["e2e"], world, dev), 1)
+
+
 def main_prefill(args, ffn, synth, dev, rank, world, local):
     """The batched workload as the headline line."""
     import torch
     w = synth.WORKLOADS[args.workload]
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    barrier(world)
     with ClockSampler(local) as clk:
         pre = bench_prefill(ffn, synth, args.workload, dev, rank, args.steps, args.warmup,
                             e2e_steps=min(args.e2e_steps, 50), layers=args.layers)
+    reduce_prefill(pre, world, dev)
     ms = pre["ms_per_step"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
