@@ -295,6 +295,59 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
           file=sys.stderr)
 
 
+def active_bytes(w):
+    """The second numerator: the bytes of the k picked experts and the shared expert only."""
+    K, F, Fs = w["top_k"], w["expert_ff"], w["shared_ff"]
+    return K * record_bytes(w, F) + (record_bytes(w, Fs) if Fs else 0)
+
+
+def bench_chained(ffn, w, layers, L, dev, stream, reps=10):
+    """Per-layer latency with a real dependence between layers: x_{l+1} = x_l +
+    FFN(rms_norm(x_l) * norm) (the residual form with the norm prologue, which keeps the
+    layer's input bounded), rotating through the L distinct layers. One CUDA graph of G
+    steps, replayed `reps` times; returns ms per step."""
+    import torch
+    H = w["hidden"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    norm = torch.empty(H, device=dev).uniform_(0.5, 1.5, generator=gen)
+    x0 = torch.empty(H, device=dev).normal_(0.0, 1.0, generator=gen)
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": ffn.MOE_RESIDUAL, "rms_eps": 1e-6, "ffn_norm": norm})
+    ws_bytes = ffn.moe_workspace_size(cfg)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    bufs = torch.empty((2, H), device=dev)
+
+    def step(i):
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(bufs[i % 2], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg, bufs[(i + 1) % 2], ws, ws_bytes, stream))
+
+    G = L * max(1, 320 // L)
+    G += G % 2
+    with torch.cuda.stream(stream):
+        bufs[0].copy_(x0)
+        for i in range(2 * L):
+            step(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):  # G is even: the graph starts and ends with x in bufs[0]
+            step(i)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        bufs[0].copy_(x0)
+        g.replay()
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    if not bool(torch.isfinite(bufs[0]).all()):
+        raise RuntimeError("chained layers left the f32 range")
+    return ev0.elapsed_time(ev1) / (reps * G)
+
+
 def prefill_launches(w):
     """Kernel launches of one batched pass of at most 512 tokens. The tile path (all three
     matrices Q4_1, or all Q4_0, with H, F and Fs whole multiples of 128 (Q4_1) or 256 (Q4_0)):
@@ -559,6 +612,7 @@ def main():
 
     if args.trace:
         print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream)
+    chained_ms = max_over_ranks(bench_chained(ffn, w, layers, L, dev, stream), world, dev)
 
     # ---- end to end through the C ABI with host buffers (pinned) ----
     cfg_h = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags | ffn.MOE_HOST_IO})
@@ -606,7 +660,8 @@ def main():
             "frac": round(achieved / peak, 4), "traffic": prof["dram_bytes_per_step"] if prof else None,
             "peak_kind": peak_kind, "kernel": "decode chain: dec_router -> dec_gate_up -> dec_down",
             "over": "the whole step (three kernels overlapped by programmatic dependent launch)",
-            "bytes_per_step": step_bytes}
+            "bytes_per_step": step_bytes, "active_bytes_per_step": active_bytes(w),
+            "active_frac": round(active_bytes(w) / (ms_per_step * 1e-3) / 1e9 / peak, 4)}
     cpu = None
     if not args.no_cpu_baseline:
         d, err = cpu_baseline(args.workload)
@@ -632,6 +687,9 @@ def main():
                  "scale per 32 values): exact int32 block dots (dp4a), fp32 scaling and accumulation; router "
                  "and routing in fp32",
         "roofline": roof,
+        "chained": {"ms_per_step": chained_ms, "value": round(T * world / (chained_ms * 1e-3), 1), "unit": UNIT,
+                    "how": "x of layer l+1 = x_l + FFN(rms_norm(x_l) * norm): the residual form with the "
+                           "norm prologue, each layer waiting on the last, same rotated layers, one CUDA graph"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": H * 4 * T,
                 "d2h_bytes_per_step": H * 4 * T, "steps": n_e2e,
