@@ -104,12 +104,14 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
 
 // Quantise blocks [0, nb) of an f32 vector (global memory, or shared memory when
 // kShared) as quant_task describes; with `mul`, value i is first multiplied by
-// scal * mul[i]. Each thread takes two tasks a round and loads both before
+// scal * mul[i]. With `ss`, the thread adds the squares of the values it loaded (before
+// any multiplication) to *ss. Each thread takes two tasks a round and loads both before
 // computing; every thread runs the same number of rounds and whole warps call it
 // (the groups use shuffles).
 template <bool kShared = false>
 __device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float2* info,
-                                             int t, int nthreads, const float* mul = nullptr, float scal = 1.f) {
+                                             int t, int nthreads, const float* mul = nullptr, float scal = 1.f,
+                                             float* ss = nullptr) {
   #pragma unroll 1
   for (int base = 0; base < 4 * nb; base += 2 * nthreads) {
     float v[2][8];
@@ -122,6 +124,10 @@ __device__ __forceinline__ void quant_blocks(const float* src, int nb, int strid
         const float4 a = kShared ? s4[0] : __ldcg(s4), c = kShared ? s4[1] : __ldcg(s4 + 1);
         v[h][0] = a.x; v[h][1] = a.y; v[h][2] = a.z; v[h][3] = a.w;
         v[h][4] = c.x; v[h][5] = c.y; v[h][6] = c.z; v[h][7] = c.w;
+        if (ss) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) *ss = fmaf(v[h][i], v[h][i], *ss);
+        }
         if (mul) {
           const float4* m4 = reinterpret_cast<const float4*>(mul + (size_t)(idx[h] >> 2) * 32 + (idx[h] & 3) * 8);
           const float4 ma = __ldg(m4), mc = __ldg(m4 + 1);
@@ -559,8 +565,7 @@ __device__ __forceinline__ void select_picks(const DecodeArgs& a, const float* l
 // ===========================================================================
 __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int trows) {
   __shared__ float part[RT_THREADS / 32][DEC_TMAX];
-  __shared__ float red[RT_THREADS / 32][DEC_TMAX];
-  __shared__ float rscale[DEC_TMAX];
+  __shared__ float red[RT_THREADS / 32][DEC_TMAX];  // sums of squares (with a norm vector)
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   tr(a, TR_RT_START, trows);
@@ -575,6 +580,13 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
     wv[i] = (has && j < nq4) ? __ldg(reinterpret_cast<const float4*>(a.router_w + (size_t)row * p.H + q * (p.H / 4)) + j)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  float4 nv[6];  // the norm vector's quarter (with a prologue)
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    const int j = lane + 32 * i;
+    nv[i] = (a.norm && has && j < nq4) ? __ldg(reinterpret_cast<const float4*>(a.norm + q * (p.H / 4)) + j)
+                                       : make_float4(1.f, 1.f, 1.f, 1.f);
+  }
   pdl_wait_prior_grids();  // x may come from the previous kernel
   pdl_launch_dependents();
   tr(a, TR_RT_X, trows);
@@ -582,46 +594,12 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   // the wait above covers them, and every reader of this call starts after this grid)
   if (a.T == 1 && blockIdx.x == 0 && tid < p.K) st_relaxed_u64(a.pub + tid, PUB_EMPTY);
   // the prologue (with a norm vector): token t's input is x_t * r_t * norm, r_t =
-  // 1/rms(x_t); the router dot takes x_t * norm and the row's sum is scaled by r_t.
-  // Every token's sum of squares in one pass (loads of all tokens in flight together).
-  if (a.norm) {
-    float ss[DEC_TMAX];
-#pragma unroll
-    for (int t = 0; t < DEC_TMAX; ++t) ss[t] = 0.f;
-    for (int h = 4 * tid; h < p.H; h += 4 * RT_THREADS) {
-#pragma unroll
-      for (int t = 0; t < DEC_TMAX; ++t) {
-        if (t < a.T) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x + (size_t)t * p.H + h));
-          ss[t] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[t]))));
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < DEC_TMAX; ++t) {
-      if (t < a.T) {
-        const float v = warp_sum(ss[t]);
-        if (lane == 0) red[warp][t] = v;
-      }
-    }
-    __syncthreads();
-    if (tid < a.T) {
-      float tot = 0.f;
-      for (int w = 0; w < RT_THREADS / 32; ++w) tot += red[w][tid];
-      rscale[tid] = 1.f / sqrtf(tot / (float)p.H + a.eps);
-    }
-  }
-  float4 nv[6];
-#pragma unroll
-  for (int i = 0; i < 6; ++i) {
-    const int j = lane + 32 * i;
-    nv[i] = (a.norm && has && j < nq4) ? __ldg(reinterpret_cast<const float4*>(a.norm + q * (p.H / 4)) + j)
-                                       : make_float4(1.f, 1.f, 1.f, 1.f);
-  }
+  // 1/rms(x_t). The dot takes x_t * norm and its sum is scaled by r_t; the sum of squares
+  // comes from the same loads (a row's four quarter warps cover x_t once).
 #pragma unroll 1
   for (int t = 0; t < a.T; ++t) {
     const float* xt = a.x + (size_t)t * p.H + q * (p.H / 4);
-    float acc = 0.f;
+    float acc = 0.f, ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 6; ++i) {
       const int j = lane + 32 * i;
@@ -631,18 +609,27 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
         acc = fmaf(wv[i].y, xv.y * nv[i].y, acc);
         acc = fmaf(wv[i].z, xv.z * nv[i].z, acc);
         acc = fmaf(wv[i].w, xv.w * nv[i].w, acc);
+        ss = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, fmaf(xv.z, xv.z, fmaf(xv.w, xv.w, ss))));
       }
     }
     acc = warp_sum(acc);
-    if (lane == 0) part[warp][t] = acc;
+    if (a.norm) ss = warp_sum(ss);
+    if (lane == 0) {
+      part[warp][t] = acc;
+      red[warp][t] = ss;
+    }
   }
   __syncthreads();
   for (int u = tid; u < 2 * a.T; u += RT_THREADS) {
     const int rr = u & 1, t = u >> 1;
     const int row2 = blockIdx.x * 2 + rr;
     if (row2 < p.E) {
-      const float v = ((part[4 * rr][t] + part[4 * rr + 1][t]) + part[4 * rr + 2][t]) + part[4 * rr + 3][t];
-      a.logits[(size_t)t * p.E + row2] = a.norm ? v * rscale[t] : v;
+      float v = ((part[4 * rr][t] + part[4 * rr + 1][t]) + part[4 * rr + 2][t]) + part[4 * rr + 3][t];
+      if (a.norm) {
+        const float sq = ((red[4 * rr][t] + red[4 * rr + 1][t]) + red[4 * rr + 2][t]) + red[4 * rr + 3][t];
+        v *= 1.f / sqrtf(sq / (float)p.H + a.eps);
+      }
+      a.logits[(size_t)t * p.E + row2] = v;
     }
   }
   tr(a, TR_RT_DONE, trows);
@@ -714,12 +701,25 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   if (shared && tid < 4) issue(a.shared);
   // x -> activation blocks (x is complete: the router kernel waited for it before this
   // launch was triggered)
+  // With a norm vector the blocks hold x * norm; r = 1/rms(x) comes from the same loads
+  // and scales the row dots (every dot is linear in x).
+  __shared__ float red[GU_THREADS / 32];
   {
-    __shared__ float red[32];
-    const float r = a.norm ? block_rms_scale(xt, p.H, a.eps, red) : 1.f;
-    quant_blocks(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, r);
+    float ss = 0.f;
+    quant_blocks(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, 1.f, a.norm ? &ss : nullptr);
+    if (a.norm) {
+      ss = warp_sum(ss);
+      if (lane == 0) red[warp] = ss;
+    }
   }
   __syncthreads();
+  float r = 1.f;
+  if (a.norm) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < GU_THREADS / 32; ++w) tot += red[w];
+    r = 1.f / sqrtf(tot / (float)p.H + a.eps);
+  }
   tr(a, TR_GU_XQ, trows);
   const RowMap mh = row_map(p.nbH, lane);
   ActBlock xc[MAXB];
@@ -794,7 +794,7 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   __syncwarp();
   if (lane < 2)
     a.act[(size_t)tok * p.act_stride + v0 + 2 * warp + lane] =
-        swiglu_act(rowdot[warp][2 * lane], rowdot[warp][2 * lane + 1], shared ? a.lim_s : a.lim);
+        swiglu_act(rowdot[warp][2 * lane] * r, rowdot[warp][2 * lane + 1] * r, shared ? a.lim_s : a.lim);
   tr(a, TR_GU_END, trows);
 }
 
@@ -866,6 +866,14 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
     woff[sh ? 32 : j] = (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u);
   }
   tr(a, TR_DN_REQUESTED, trows);
+  // the residual and accumulate inputs: complete before this call's first kernel started,
+  // so they are read ahead of the wait
+  float xres = 0.f, oin = 0.f;
+  if (tid < R) {
+    const size_t h = (size_t)tok * p.H + h0 + tid;
+    if (a.flags & FLAG_RESIDUAL) xres = __ldcg(a.x + h);
+    if (a.flags & FLAG_ACCUMULATE) oin = __ldcg(a.out + h);
+  }
   pdl_wait_prior_grids();  // the activations
   pdl_launch_dependents();
   tr(a, TR_DN_WAITED, trows);
@@ -928,8 +936,8 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
     float y = 0.f;
     for (int w = 0; w < TPG / 32; ++w) y += part[w0 + w][rl];
     const size_t h = (size_t)tok * p.H + h0 + tid;
-    if (a.flags & FLAG_RESIDUAL) y = __ldcg(a.x + h) + y;
-    if (a.flags & FLAG_ACCUMULATE) y = __ldcg(a.out + h) + y;
+    if (a.flags & FLAG_RESIDUAL) y = xres + y;
+    if (a.flags & FLAG_ACCUMULATE) y = oin + y;
     a.out[h] = y;
   }
   tr(a, TR_DN_END, trows);
