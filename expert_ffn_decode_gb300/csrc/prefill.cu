@@ -297,33 +297,6 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t qw, __half2 d2, __half2 m
   return make_uint4(h2bits(lo02), h2bits(lo13), h2bits(hi02), h2bits(hi13));
 }
 
-// Loads block `blk` of a weight row from global memory: d, m and the four nibble words.
-template <int QT>
-__device__ __forceinline__ void load_block(const uint8_t* row, int blk, __half2& d2, __half2& m2, uint32_t (&qw)[4]) {
-  if constexpr (QT == 3) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 20 * blk);
-    const uint32_t dm = __ldg(w);
-    qw[0] = __ldg(w + 1);
-    qw[1] = __ldg(w + 2);
-    qw[2] = __ldg(w + 3);
-    qw[3] = __ldg(w + 4);
-    const __half2 h = bits2h(dm);
-    d2 = __low2half2(h);
-    m2 = __high2half2(h);
-  } else {
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(row + 18 * blk);
-    unsigned short u[9];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) u[i] = __ldg(h + i);
-    qw[0] = (uint32_t)u[1] | ((uint32_t)u[2] << 16);
-    qw[1] = (uint32_t)u[3] | ((uint32_t)u[4] << 16);
-    qw[2] = (uint32_t)u[5] | ((uint32_t)u[6] << 16);
-    qw[3] = (uint32_t)u[7] | ((uint32_t)u[8] << 16);
-    d2 = __half2half2(__ushort_as_half(u[0]));
-    m2 = d2;
-  }
-}
-
 // Values 4w .. 4w + 3 (bytes of qa) and 16 + 4w .. 16 + 4w + 3 (bytes of qb) of a 32-value
 // block, each v = df * q + mf in f32 (exact for the K-quant scales) and rounded once to f16,
 // as the core-matrix row of slots 8w .. 8w + 7 (slot order: kslot).
@@ -339,8 +312,10 @@ __device__ __forceinline__ uint4 core_row_f32(uint32_t qa, uint32_t qb, float df
 }
 
 // Block `blk` (32 values) of a weight row in global memory, dequantised into the four core
-// rows of its slots. Q4_0/Q4_1: one block. K-quants (ggml layouts, as the Ling store keeps
-// them; the pages name the types only): sub-block blk % 8 of super-block blk / 8.
+// rows of its slots, in two steps so that a thread can have several blocks' loads in
+// flight before it uses them: load_raw issues the loads, dequant_raw does the arithmetic.
+// Q4_0/Q4_1: one block. K-quants (ggml layouts, as the Ling store keeps them; the pages name
+// the types only): sub-block blk % 8 of super-block blk / 8.
 //   Q4_K (144 bytes, rows on 16-byte bounds): f16 d, f16 dmin, 12 packed scale bytes S,
 //   four runs of 32 nibble bytes (run c: sub-block 2c low nibbles, 2c + 1 high nibbles);
 //   sub-block j < 4: sc = S[j] & 63, mn = S[j + 4] & 63; j >= 4: low 4 bits from S[j + 4],
@@ -349,40 +324,81 @@ __device__ __forceinline__ uint4 core_row_f32(uint32_t qa, uint32_t qb, float df
 //   sub-block j = (n = j / 4, r = j % 4), value i: nibble (low for r < 2) of
 //   ql[64n + 32 (r % 2) + i], high bits 2r, 2r + 1 of qh[32n + i], scale[8n + 2r + i / 16];
 //   value = d * scale * (q - 32).
+struct RawBlk {
+  uint32_t w[18];
+};
+
 template <int QT>
-__device__ __forceinline__ void load_dequant(const uint8_t* row, int blk, uint4 (&o)[4]) {
+__device__ __forceinline__ void load_raw(const uint8_t* row, int blk, RawBlk& r) {
   if constexpr (QT == 12) {
     const uint8_t* sb = row + 144 * (blk >> 3);
-    const int j = blk & 7, sh = 8 * (j & 3);
+    const int j = blk & 7;
     const uint4 hd = __ldg(reinterpret_cast<const uint4*>(sb));
     const uint4 n0 = __ldg(reinterpret_cast<const uint4*>(sb + 16 + 32 * (j >> 1)));
     const uint4 n1 = __ldg(reinterpret_cast<const uint4*>(sb + 32 + 32 * (j >> 1)));
-    const uint32_t by = (hd.y >> sh) & 0xFFu, bz = (hd.z >> sh) & 0xFFu, bw = (hd.w >> sh) & 0xFFu;
-    const uint32_t sc = j < 4 ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4));
-    const uint32_t mn = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
-    const float2 f = __half22float2(bits2h(hd.x));
-    const float df = f.x * (float)sc, mf = -(f.y * (float)mn);
-    const int ns = 4 * (j & 1);
-    const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      o[c] = core_row_f32((w[c] >> ns) & 0x0F0F0F0Fu, (w[4 + c] >> ns) & 0x0F0F0F0Fu, df, mf);
+    r.w[0] = hd.x; r.w[1] = hd.y; r.w[2] = hd.z; r.w[3] = hd.w;
+    r.w[4] = n0.x; r.w[5] = n0.y; r.w[6] = n0.z; r.w[7] = n0.w;
+    r.w[8] = n1.x; r.w[9] = n1.y; r.w[10] = n1.z; r.w[11] = n1.w;
   } else if constexpr (QT == 14) {
     const uint8_t* sb = row + 210 * (blk >> 3);
-    const int j = blk & 7, n = j >> 2, r = j & 3;
-    const unsigned short* ql = reinterpret_cast<const unsigned short*>(sb + 64 * n + 32 * (r & 1));
-    const unsigned short* qh = reinterpret_cast<const unsigned short*>(sb + 128 + 32 * n);
-    const uint32_t scp = __ldg(reinterpret_cast<const unsigned short*>(sb + 192 + 8 * n + 2 * r));
-    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(sb + 208))));
-    const float df0 = d * (float)(int)(int8_t)(scp & 0xFFu), df1 = d * (float)(int)(int8_t)(scp >> 8);
-    const int ls = 4 * (r >> 1), hs = 2 * r;
-    uint32_t u[8];  // q of values 4i .. 4i + 3, 0 .. 63
+    const int j = blk & 7, n = j >> 2, q = j & 3;
+    // each 32-byte run as nine aligned words, shifted by the run's 2-byte offset (the run ends
+    // at least 4 bytes before its super-block does, so the ninth word stays inside it)
+    const uint8_t* ql = sb + 64 * n + 32 * (q & 1);
+    const uint8_t* qh = sb + 128 + 32 * n;
+    const uint32_t* wl = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(ql) & ~uintptr_t(3));
+    const uint32_t* wh = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(qh) & ~uintptr_t(3));
+    const uint32_t sl = (uint32_t)(reinterpret_cast<uintptr_t>(ql) & 3u) * 8u;  // 0 or 16
+    uint32_t tl[9], th[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      tl[i] = __ldg(wl + i);
+      th[i] = __ldg(wh + i);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t L = (uint32_t)__ldg(ql + 2 * i) | ((uint32_t)__ldg(ql + 2 * i + 1) << 16);
-      const uint32_t Hb = (uint32_t)__ldg(qh + 2 * i) | ((uint32_t)__ldg(qh + 2 * i + 1) << 16);
-      u[i] = ((L >> ls) & 0x0F0F0F0Fu) | (((Hb >> hs) & 0x03030303u) << 4);
+      r.w[i] = __funnelshift_r(tl[i], tl[i + 1], sl);
+      r.w[8 + i] = __funnelshift_r(th[i], th[i + 1], sl);
     }
+    r.w[16] = __ldg(reinterpret_cast<const unsigned short*>(sb + 192 + 8 * n + 2 * q));
+    r.w[17] = __ldg(reinterpret_cast<const unsigned short*>(sb + 208));
+  } else if constexpr (QT == 3) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(row + 20 * blk);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) r.w[i] = __ldg(w + i);
+  } else {
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(row + 18 * blk);
+    unsigned short u[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) u[i] = __ldg(h + i);
+    r.w[0] = u[0];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.w[1 + i] = (uint32_t)u[1 + 2 * i] | ((uint32_t)u[2 + 2 * i] << 16);
+  }
+}
+
+template <int QT>
+__device__ __forceinline__ void dequant_raw(const RawBlk& r, int blk, uint4 (&o)[4]) {
+  if constexpr (QT == 12) {
+    const int j = blk & 7, sh = 8 * (j & 3);
+    const uint32_t by = (r.w[1] >> sh) & 0xFFu, bz = (r.w[2] >> sh) & 0xFFu, bw = (r.w[3] >> sh) & 0xFFu;
+    const uint32_t sc = j < 4 ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4));
+    const uint32_t mn = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
+    const float2 f = __half22float2(bits2h(r.w[0]));
+    const float df = f.x * (float)sc, mf = -(f.y * (float)mn);
+    const int ns = 4 * (j & 1);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      o[c] = core_row_f32((r.w[4 + c] >> ns) & 0x0F0F0F0Fu, (r.w[8 + c] >> ns) & 0x0F0F0F0Fu, df, mf);
+  } else if constexpr (QT == 14) {
+    const int q = blk & 3;
+    const float d = __half2float(__ushort_as_half((unsigned short)r.w[17]));
+    const uint32_t scp = r.w[16];
+    const float df0 = d * (float)(int)(int8_t)(scp & 0xFFu), df1 = d * (float)(int)(int8_t)(scp >> 8);
+    const int ls = 4 * (q >> 1), hs = 2 * q;
+    uint32_t u[8];  // q of values 4i .. 4i + 3, 0 .. 63
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = ((r.w[i] >> ls) & 0x0F0F0F0Fu) | (((r.w[8 + i] >> hs) & 0x03030303u) << 4);
     // values 0 .. 15 take scale 0 and 16 .. 31 scale 1: core row c holds 4c .. (first half)
     // and 16 + 4c .. (second half), so each half has its own scale; q - 32 enters as the offset
 #pragma unroll
@@ -393,11 +409,42 @@ __device__ __forceinline__ void load_dequant(const uint8_t* row, int blk, uint4 
     }
   } else {
     __half2 d2, m2;
-    uint32_t qw[4];
-    load_block<QT>(row, blk, d2, m2, qw);
+    if constexpr (QT == 3) {
+      const __half2 h = bits2h(r.w[0]);
+      d2 = __low2half2(h);
+      m2 = __high2half2(h);
+    } else {
+      d2 = __half2half2(__ushort_as_half((unsigned short)r.w[0]));
+      m2 = d2;
+    }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) o[w] = dequant_word<QT>(qw[w], d2, m2);
+    for (int w = 0; w < 4; ++w) o[w] = dequant_word<QT>(r.w[1 + w], d2, m2);
   }
+}
+
+// The two blocks (rows m = i % 128, blocks b = i / 128 of the chunk, i = tid and
+// tid + 256) that thread `tid` dequantises for pipeline chunk kc: their loads are issued.
+template <int QT, typename RowFn>
+__device__ __forceinline__ void issue_raw(RawBlk (&r)[2], bool (&v)[2], int kc, int nbk, int mrows, int tid,
+                                          const RowFn& wrow) {
+  const int kb = min(KC / 32, nbk - kc * (KC / 32));
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
+    v[pass] = m < mrows && b < kb;
+    if (v[pass]) load_raw<QT>(wrow(m), kc * (KC / 32) + b, r[pass]);
+  }
+}
+
+// 16 bytes from global to shared memory without a register round trip; with !valid the
+// destination is zero-filled (nothing is read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // L2 prefetch of the 16-byte-aligned part of [p, p + bytes).
@@ -479,6 +526,9 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
     __syncthreads();
     const __half* bsrc = MODE == 0 ? a.x16 : (sh ? a.act16s : a.act16);
     const int bld = MODE == 0 ? a.H : ff;  // B row length (values)
+    RawBlk cur[2], nxt[2];
+    bool vcur[2], vnxt[2] = {false, false};
+    issue_raw<QT>(cur, vcur, 0, nbk, mrows, tid, wrow);
 
     for (int kc = 0; kc < nkc; ++kc, ++g) {
       const int s = g & 1;
@@ -489,31 +539,44 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
       const int kb = min(KC / 32, nbk - kc * (KC / 32));  // blocks in this chunk
       // A: 128 rows x 4 blocks; a warp takes 32 consecutive rows of one block, so its
       // 16-byte shared stores of one core row cover all banks
-      for (int pass = 0; pass < 2; ++pass) {
-        const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
-        if (m < mrows && b < kb) {
-          uint4 o[4];
-          load_dequant<QT>(wrow(m), kc * (KC / 32) + b, o);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int kcore = 4 * b + w, mcore = m >> 3;
-            *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = o[w];
-          }
-        }
-      }
-      // B: rows x (16-byte pieces of this chunk's K slice)
+      // B: rows x (16-byte pieces of this chunk's K slice), copied asynchronously (rows
+      // past the chunk are zero-filled) while the A blocks load and dequantise
       {
         const int pieces = kb * 4;  // 8 values a piece
         for (int i = tid; i < nb * pieces; i += PREFILL_THREADS) {
           const int r = i / pieces, pc = i % pieces;
           const int rr = r < npad ? r : r - npad;  // chunk row (lo rows: second half)
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (rr < ch.n) {
-            const size_t src = MODE == 0 ? 2 * (size_t)rowsrc[rr] + (r >= npad) : (size_t)rowsrc[rr];
-            v = __ldg(reinterpret_cast<const uint4*>(bsrc + src * bld + kc * KC + pc * 8));
-          }
-          *reinterpret_cast<uint4*>(B + (pc * (nb / 8) + (r >> 3)) * 128 + 16 * (r & 7)) = v;
+          const bool valid = rr < ch.n;
+          const size_t src = !valid ? 0 : MODE == 0 ? 2 * (size_t)rowsrc[rr] + (r >= npad) : (size_t)rowsrc[rr];
+          cp_async16(B + (pc * (nb / 8) + (r >> 3)) * 128 + 16 * (r & 7), bsrc + src * bld + kc * KC + pc * 8,
+                     valid);
         }
+      }
+      // A: 128 rows x 4 blocks, two per thread. The next chunk's blocks are requested before
+      // this chunk's are dequantised, so two chunks' loads overlap; a warp takes 32
+      // consecutive rows of one block, so its 16-byte shared stores of one core row cover
+      // all banks
+      {
+        if (kc + 1 < nkc) issue_raw<QT>(nxt, vnxt, kc + 1, nbk, mrows, tid, wrow);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
+          if (vcur[pass]) {
+            uint4 o[4];
+            dequant_raw<QT>(cur[pass], kc * (KC / 32) + b, o);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int kcore = 4 * b + w, mcore = m >> 3;
+              *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = o[w];
+            }
+          }
+        }
+      }
+      cp_async_wait_all();
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        cur[pass] = nxt[pass];
+        vcur[pass] = vnxt[pass];
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
