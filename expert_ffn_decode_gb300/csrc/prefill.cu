@@ -1,4 +1,8 @@
-// Batched MoE-FFN step (prefill: T tokens at once) for sm_103a.
+// Batched MoE-FFN step (prefill: T tokens at once) for sm_103a: the general form of its
+// contractions, for every shape and block type, and the passes both forms share. Layers
+// whose three matrices are all Q4_1 (or all Q4_0), with K dimensions in whole 128 (256)
+// value chunks, run the contractions and the router as the TMA/TMEM tile pipeline in
+// prefill_tc.cu instead.
 //
 // Passes, each a kernel on the caller's stream:
 //   router      logits[T][E] = X Wr^T                       (f32, tiled SIMT)
@@ -23,7 +27,11 @@
 // carries x to 22 bits. The activations (one rounding per value, independent
 // across rows) and the weights go in as single f16 values. The 4-bit blocks are dequantised
 // exactly (nibble -> f16 integer, then d*q + m rounded once) into f16; the
-// products are summed in f32 in TMEM. Inside each 32-value block the K order is
+// products are summed in f32 in TMEM. K-quant sub-blocks (Q4_K, Q6_K) are dequantised in
+// f32, where their scale products are exact, and rounded once to f16. Each 128-value K
+// step copies the token rows by cp.async and has its weight loads issued one step ahead,
+// so a step waits on one round trip rather than one per operand piece. Inside each
+// 32-value block the K order is
 // permuted so that one 32-bit nibble word fills one 16-byte row of a core matrix:
 // slot 8w + (0..7) holds values 4w, 4w+2, 4w+1, 4w+3, 16+4w, 16+4w+2, 16+4w+1,
 // 16+4w+3. Every operand uses the same order, so the dot products are unchanged.
