@@ -173,7 +173,8 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(workload: str, seconds: float = 12.0, warmup: int = 0, max_tokens: int = 10 ** 9):
+def cpu_baseline(workload: str, seconds: float = 12.0, warmup: int = 0, max_tokens: int = 10 ** 9,
+                 threads: int = 1):
     """The oracle, as it stands, on one thread, on a bounded sample of the workload:
     single-token calls on one synthetic layer until `seconds` or `max_tokens` is reached."""
     code = f"""
@@ -199,7 +200,8 @@ while n < {max_tokens} and (n == 0 or time.perf_counter() - t0 < {seconds}):
 dt = time.perf_counter() - t0
 print(json.dumps({{"tokens": n, "seconds": dt}}))
 """
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         return None, r.stderr[-400:]
@@ -702,6 +704,12 @@ def main():
             cpu = {"value": d["tokens"] / d["seconds"] * T, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{d['tokens']} single-token oracle calls in {d['seconds']:.1f} s on one "
                              f"layer of the workload (numpy float64, one thread)"}
+            # the same oracle with its numpy BLAS on every host core
+            nproc = os.cpu_count() or 1
+            d2, _ = cpu_baseline(args.workload, seconds=6.0, threads=nproc)
+            if d2 is not None:
+                cpu["all_cores"] = {"value": d2["tokens"] / d2["seconds"] * T, "cores": nproc,
+                                    "sample": f"{d2['tokens']} calls in {d2['seconds']:.1f} s"}
         else:
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {err}"}
     clocks = clk.summary()

@@ -58,30 +58,67 @@ __host__ __device__ __forceinline__ int kpos(int k) { return (k & ~31) | kslot(k
 // ---------------------------------------------------------------------------
 // router: logits[t][e] = sum_h x[t][h] * Wr[e][h]
 // ---------------------------------------------------------------------------
+// CTA tile: 64 tokens x 64 experts, thread (ty, tx) = (tid / 16, tid % 16) owns tokens
+// 4 ty .. 4 ty + 3 and experts 4 tx .. 4 tx + 3. K goes in slices of 32 staged in shared
+// memory K-major (row stride RT_LD floats, 16-byte aligned), so each k costs two 16-byte
+// shared loads for 16 FMAs; the next slice's global loads are held in registers while the
+// current slice is multiplied. Each logit is one f32 sum in a fixed order.
+constexpr int RT_TILE = 64, RT_KS = 32, RT_LD = 68;
 __global__ void __launch_bounds__(256) prefill_router(const PrefillArgs a) {
-  __shared__ float xs[32][33], ws[32][33];
-  const int t0 = blockIdx.y * 32, e0 = blockIdx.x * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int k0 = 0; k0 < a.H; k0 += 32) {
-    for (int i = ty; i < 32; i += 8) {
-      const int t = t0 + i, e = e0 + i;
-      xs[i][tx] = t < a.T ? __ldg(a.x + (size_t)t * a.H + k0 + tx) : 0.f;
-      ws[i][tx] = e < a.E ? __ldg(a.router_w + (size_t)e * a.H + k0 + tx) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float wv = ws[tx][k];
+  __shared__ __align__(16) float xs[RT_KS][RT_LD], ws[RT_KS][RT_LD];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.y * RT_TILE, e0 = blockIdx.x * RT_TILE;
+  // global loads of a slice: 64 rows x 8 float4 of each matrix, two of each per thread
+  float4 gx[2], gw[2];
+  auto load = [&](int k0) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j] = fmaf(xs[ty + 8 * j][k], wv, acc[j]);
+    for (int q = 0; q < 2; ++q) {
+      const int idx = tid + 256 * q, row = idx >> 3, c4 = idx & 7;
+      const int t = t0 + row, e = e0 + row;
+      gx[q] = t < a.T ? __ldg(reinterpret_cast<const float4*>(a.x + (size_t)t * a.H + k0) + c4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      gw[q] = e < a.E ? __ldg(reinterpret_cast<const float4*>(a.router_w + (size_t)e * a.H + k0) + c4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int idx = tid + 256 * q, row = idx >> 3, k = 4 * (idx & 7);
+      xs[k][row] = gx[q].x; xs[k + 1][row] = gx[q].y; xs[k + 2][row] = gx[q].z; xs[k + 3][row] = gx[q].w;
+      ws[k][row] = gw[q].x; ws[k + 1][row] = gw[q].y; ws[k + 2][row] = gw[q].z; ws[k + 3][row] = gw[q].w;
+    }
+  };
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  load(0);
+  for (int k0 = 0; k0 < a.H; k0 += RT_KS) {
+    stash();
+    __syncthreads();
+    if (k0 + RT_KS < a.H) load(k0 + RT_KS);
+#pragma unroll 8
+    for (int k = 0; k < RT_KS; ++k) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[k][4 * ty]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][4 * tx]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wa[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int t = t0 + ty + 8 * j, e = e0 + tx;
-    if (t < a.T && e < a.E) a.logits[(size_t)t * a.E + e] = acc[j];
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + 4 * ty + i;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + 4 * tx + j;
+      if (t < a.T && e < a.E) a.logits[(size_t)t * a.E + e] = acc[i][j];
+    }
   }
 }
 
@@ -791,7 +828,7 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
     if ((e = tile_images_launch(a, false, st)) != cudaSuccess) return e;
     if ((e = tile_router_launch(a, st)) != cudaSuccess) return e;
   } else {
-    prefill_router<<<dim3((a.E + 31) / 32, (a.T + 31) / 32), 256, 0, st>>>(a);
+    prefill_router<<<dim3((a.E + RT_TILE - 1) / RT_TILE, (a.T + RT_TILE - 1) / RT_TILE), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t topk_smem = (size_t)8 * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
