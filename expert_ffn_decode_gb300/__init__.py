@@ -44,7 +44,8 @@ NORM_MIN = 6.103515625e-05  # 2^-14
 
 # Every symbol include/moeffn.h declares.
 EXPORTS = ("moe_ffn_forward", "moe_ffn_forward_ex", "moe_workspace_size", "moe_trace_offset",
-           "moe_workspace_status", "moe_ffn_forward_noalloc", "moe_last_error", "moe_shutdown")
+           "moe_workspace_status", "moe_selftest_timeout", "moe_ffn_forward_noalloc", "moe_last_error",
+           "moe_shutdown")
 
 
 class moe_cfg(ctypes.Structure):
@@ -107,6 +108,8 @@ def lib():
         L.moe_trace_offset.restype = ctypes.c_size_t
         L.moe_workspace_status.argtypes = [vp, vp]
         L.moe_workspace_status.restype = ctypes.c_int
+        L.moe_selftest_timeout.argtypes = [vp, vp]
+        L.moe_selftest_timeout.restype = ctypes.c_int
         L.moe_ffn_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, cp, vp, vp]
         L.moe_ffn_forward_noalloc.restype = ctypes.c_int
         L.moe_last_error.argtypes = []
@@ -169,6 +172,10 @@ TRACE_STRIDE = 24  # u64 words per CTA
 
 def moe_workspace_status(workspace, stream=None):
     return lib().moe_workspace_status(_ptr(workspace), _stream(stream))
+
+
+def moe_selftest_timeout(workspace, stream=None):
+    return lib().moe_selftest_timeout(_ptr(workspace), _stream(stream))
 
 
 def moe_ffn_forward_noalloc(x, router_w, router_bias, expert_blocks, shared_blocks, cfg, out, stream=None):

@@ -529,6 +529,18 @@ int read_status(void* ws, cudaStream_t st) {
 
 }  // namespace
 
+// One thread waits on a fresh mbarrier (one arrival expected, none made) through the
+// bounded wait; when it gives up it sets the timeout bit, as a stalled copy's wait would.
+__global__ void selftest_timeout_kernel(uint32_t* ctrl) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    moe::mbar_init(&bar, 1);
+    moe::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !moe::mbar_wait(&bar, 0)) atomicOr(ctrl + moe::CTRL_STATUS, moe::DEV_ERR_MBAR_TIMEOUT);
+}
+
 extern "C" {
 
 int moe_ffn_forward(const float* x, const float* router_w, const float* router_bias,
@@ -570,6 +582,14 @@ int moe_workspace_status(void* workspace, void* stream) {
   g_err.clear();
   if (!workspace) return fail(MOE_ERR_NULL_PTR, "workspace is NULL");
   return read_status(workspace, static_cast<cudaStream_t>(stream));
+}
+
+int moe_selftest_timeout(void* workspace, void* stream) {
+  g_err.clear();
+  if (!workspace) return fail(MOE_ERR_NULL_PTR, "workspace is NULL");
+  selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(workspace));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "self-test launch");
 }
 
 const char* moe_last_error(void) { return g_err.c_str(); }

@@ -206,6 +206,14 @@ size_t moe_trace_offset(const moe_cfg* cfg);
  * workspace's control block is zeroed again so it can be reused). */
 int moe_workspace_status(void* workspace, void* stream);
 
+/* Exercises the error path above without a fault: one kernel waits on an mbarrier that
+ * nothing completes, through the same bounded wait the step's kernels use, gives up after
+ * its time limit (0.5 s) and sets the timeout bit in the workspace's status word, as a
+ * stalled copy would. A following moe_workspace_status reports MOE_ERR_TIMEOUT and clears
+ * it; the context stays usable. `workspace` is any workspace of at least 512 bytes;
+ * asynchronous on `stream`. Returns MOE_OK or MOE_ERR_NULL_PTR / MOE_ERR_CUDA. */
+int moe_selftest_timeout(void* workspace, void* stream);
+
 /* The step for callers that cannot allocate memory: no cudaMalloc, cudaFree or
  * other allocating call is made, on the device or on the host. Such callers
  * include code that runs where an allocator may not be entered (inside another

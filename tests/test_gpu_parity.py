@@ -298,3 +298,22 @@ def test_selection_exact_ties(E, K, G, Gu, rows):
     for t in range(2):  # and one token per call (the selection inside the gate/up and down CTAs)
         o1, i1, w1 = GpuLayer(layer, w).run(x[t:t + 1])
         compare(o1, i1, w1, ref[t:t + 1], rid[t:t + 1], rwt[t:t + 1], f"ties token {t}")
+
+
+def test_device_wait_timeout_is_reported_and_cleared():
+    # a bounded device wait that nothing completes gives up, the status word says so, reading
+    # it clears it, and the context keeps working (no fault, trap or unbounded loop involved)
+    import expert_ffn_decode_gb300 as ffn
+    import torch
+    w, layer = layer_of("tiny_q4_0_t4")
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1})
+    ws = torch.zeros(ffn.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    assert ffn.moe_selftest_timeout(ws, st) == ffn.MOE_OK
+    assert ffn.moe_workspace_status(ws, st) == ffn.MOE_ERR_TIMEOUT
+    assert b"timed out" in ffn.moe_last_error()
+    assert ffn.moe_workspace_status(ws, st) == ffn.MOE_OK
+    x, _ = margin_tokens(layer, w, 1, seed=w["seed"], stream=7)
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    compare(*GpuLayer(layer, w).run(x, workspace=ws), ref, rid, rwt, "after the timeout")
