@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
 // chunks when `routed`), 8 K values a lane per step.
 __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int routed) {
   const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = 8 * blockIdx.y + warp;
+  const int r0 = 8 * blockIdx.y + warp;
   int n, row0, prow;
   uint8_t* base;
   const int nkh = a.H / TP_KB;
@@ -773,31 +773,49 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
     prow = row0;
     base = a.ximg;
   }
-  if (r >= n) return;
   const int npad = (n + 15) & ~15, nb = 2 * npad;
   base += (size_t)2 * prow * nkh * 256;
-  const int tok = routed ? (int)(a.perm[row0 + r] / (uint32_t)a.K) : row0 + r;
-  const float* xrow = a.x + (size_t)tok * a.H;
-  const int rl = npad + r;
-  const uint32_t hi_off = (uint32_t)((r >> 3) * 128 + (r & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
-  for (int p = lane; p < a.H / 8; p += 32) {
-    const int kk = p >> 4, kc8 = p & 15;
-    const int g = kk * TP_KB + 8 * kc8;  // first slot of the piece
-    const int b = g >> 5, w = (g & 31) >> 3;
-    const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * b);
-    const float4 x0 = __ldg(xr + w), x1 = __ldg(xr + 4 + w);
-    uint4 hi, lo;
-    hi.x = pack_h2(x0.x, x0.z);
-    hi.y = pack_h2(x0.y, x0.w);
-    hi.z = pack_h2(x1.x, x1.z);
-    hi.w = pack_h2(x1.y, x1.w);
-    lo.x = pack_lo(x0.x, x0.z, hi.x);
-    lo.y = pack_lo(x0.y, x0.w, hi.y);
-    lo.z = pack_lo(x1.x, x1.z, hi.z);
-    lo.w = pack_lo(x1.y, x1.w, hi.w);
-    uint8_t* blk = base + (size_t)kk * nb * 256 + (size_t)kc8 * (nb >> 3) * 128;
-    *reinterpret_cast<uint4*>(blk + hi_off) = hi;
-    *reinterpret_cast<uint4*>(blk + lo_off) = lo;
+  // warp w of row group y takes rows 8 y + w, then 8 gridDim.y further on
+  for (int r = r0; r < n; r += 8 * (int)gridDim.y) {
+    const int tok = routed ? (int)(a.perm[row0 + r] / (uint32_t)a.K) : row0 + r;
+    const float* xrow = a.x + (size_t)tok * a.H;
+    const int rl = npad + r;
+    const uint32_t hi_off = (uint32_t)((r >> 3) * 128 + (r & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
+    // four pieces a lane at a time: their loads are all issued before any store (the stores
+    // could alias x as far as the compiler knows, so it would not hoist the loads itself)
+    const int np = a.H / 8;
+    for (int p0 = lane; p0 < np; p0 += 4 * 32) {
+      float4 x0[4], x1[4];
+  #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = p0 + 32 * u;
+        if (p < np) {
+          const int g = (p >> 4) * TP_KB + 8 * (p & 15);  // first slot of the piece
+          const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * (g >> 5));
+          x0[u] = __ldg(xr + ((g & 31) >> 3));
+          x1[u] = __ldg(xr + 4 + ((g & 31) >> 3));
+        }
+      }
+  #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int p = p0 + 32 * u;
+        if (p < np) {
+          const int kk = p >> 4, kc8 = p & 15;
+          uint4 hi, lo;
+          hi.x = pack_h2(x0[u].x, x0[u].z);
+          hi.y = pack_h2(x0[u].y, x0[u].w);
+          hi.z = pack_h2(x1[u].x, x1[u].z);
+          hi.w = pack_h2(x1[u].y, x1[u].w);
+          lo.x = pack_lo(x0[u].x, x0[u].z, hi.x);
+          lo.y = pack_lo(x0[u].y, x0[u].w, hi.y);
+          lo.z = pack_lo(x1[u].x, x1[u].z, hi.z);
+          lo.w = pack_lo(x1[u].y, x1[u].w, hi.w);
+          uint8_t* blk = base + (size_t)kk * nb * 256 + (size_t)kc8 * (nb >> 3) * 128;
+          *reinterpret_cast<uint4*>(blk + hi_off) = hi;
+          *reinterpret_cast<uint4*>(blk + lo_off) = lo;
+        }
+      }
+    }
   }
 }
 
@@ -1296,7 +1314,9 @@ cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t s
   } else {
     grid = (a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX;
   }
-  tile_images<<<dim3(grid, PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
+  // routed chunks hold about P / E rows (a dozen for the Flint batch): two row groups, looping
+  // over any further rows, launch far fewer CTAs that would exit at once
+  tile_images<<<dim3(grid, routed ? 2 : PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
   return cudaGetLastError();
 }
 
