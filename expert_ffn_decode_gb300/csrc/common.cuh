@@ -133,12 +133,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Named barriers (bar.sync / bar.arrive are warp-aligned: the warp reconverges first).
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  __syncwarp();
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---- integer dot products ---------------------------------------------------------
 // dp4a with unsigned bytes in a and unsigned (uu) or signed (us) bytes in b.
 __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
@@ -222,11 +216,6 @@ __device__ __forceinline__ float block_rms_scale(const float* x, int H, float ep
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
   __syncthreads();  // red may be reused
   return 1.f / sqrtf(tot / (float)H + eps);
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
 }
 
 }  // namespace moe

@@ -55,40 +55,3 @@ __device__ __forceinline__ void topk_rounds(const uint32_t* keys, int E, int k, 
 }
 
 }  // namespace moe
-
-namespace moe {
-
-// The same selection with the keys left in shared memory: each lane keeps the best
-// of its experts (l, l + 32, ...), scanning in ascending order so the lowest index
-// wins among equal keys; after each round the winner's lane zeroes the winner's key
-// and rescans. Few registers for any E. `keys` is modified.
-__device__ __forceinline__ void lane_scan(const uint32_t* keys, int E, int lane, uint32_t& bk, int& bi) {
-  bk = 0u;
-  bi = lane;
-  for (int e = lane; e < E; e += 32) {
-    const uint32_t k = keys[e];
-    if (k > bk) {
-      bk = k;
-      bi = e;
-    }
-  }
-}
-__device__ __forceinline__ void topk_scan(uint32_t* keys, int E, int k, int* ids, int lane) {
-  uint32_t bk;
-  int bi;
-  lane_scan(keys, E, lane, bk, bi);
-  for (int j = 0; j < k; ++j) {
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-    const unsigned cand = (bk == mk && mk != 0u) ? (unsigned)bi : 0xffffffffu;
-    int win = (int)__reduce_min_sync(0xffffffffu, cand);
-    if (win < 0 || win >= E) win = j % E;  // unreachable for a valid configuration
-    if (lane == 0) ids[j] = win;
-    if ((win & 31) == lane) {
-      keys[win] = 0u;
-      lane_scan(keys, E, lane, bk, bi);
-    }
-    __syncwarp();
-  }
-}
-
-}  // namespace moe
