@@ -39,6 +39,17 @@ UNIT = "tokens/s"
 
 QTYPE_NAMES = {2: "Q4_0", 3: "Q4_1", 12: "Q4_K", 14: "Q6_K"}
 
+# The decode chain's two activation arithmetics (MOE_FIXED_POINT selects the second).
+ARITH_DTYPE = {False: "f32", True: "q4 x i16 block fixed point -> f32"}
+ARITH_TEXT = {
+    False: "4-bit weights dequantised exactly to f32 (d*q + m), f32 activations, f32 FMA accumulation "
+           "(d * sum(q x) + m * sum(x) per block); router and routing in f32",
+    True: "4-bit weights x activations in 16-bit block fixed point (15 bits and sign, power-of-two scale per "
+          "32 values): exact int32 block dots (dp4a), f32 scaling and accumulation; router and routing in f32",
+}
+# Decode workloads timed beside the headline, each in a sub-object of the line.
+OTHER_DECODE = ("flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1", "ling_kq_decode_t1")
+
 
 def record_bytes(w, ff):
     """Bytes of one expert record of intermediate size ff (gate/up and down rows in
@@ -329,7 +340,98 @@ def active_bytes(w):
     return K * record_bytes(w, F) + (record_bytes(w, Fs) if Fs else 0)
 
 
-def bench_chained(ffn, w, layers, L, dev, stream, reps=10):
+def rotation_graphs(step, K, L, stream):
+    """CUDA graphs of exactly K consecutive steps each, that together close the rotation over
+    L layers: graph j runs steps jK .. jK + K - 1 (step i uses layer i % L), and L / gcd(K, L)
+    graphs bring the rotation back to its start."""
+    import torch
+    graphs = []
+    for j in range(L // math.gcd(K, L)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(j * K, (j + 1) * K):
+                step(i, stream)
+        graphs.append(g)
+    return graphs
+
+
+def timed_repeats(graphs, stream, warm, min_ms, max_repeats=20000):
+    """Replays the graphs in rotation order: `warm` untimed replays, then timed repeats (one
+    graph each, a pair of CUDA events on the replaying stream around every one) until at
+    least `min_ms` of device time has passed. Returns the milliseconds of every repeat."""
+    import torch
+    n = len(graphs)
+    with torch.cuda.stream(stream):
+        for r in range(warm):
+            graphs[r % n].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for r in range(warm, warm + 3):
+            graphs[r % n].replay()
+        e1.record(stream)
+    e1.synchronize()
+    est = max(e0.elapsed_time(e1) / 3, 1e-3)
+    R = int(min(max_repeats, max(5, math.ceil(min_ms / est))))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(R + 1)]
+    start = warm + 3
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for r in range(R):
+            graphs[(start + r) % n].replay()
+            evs[r + 1].record(stream)
+    evs[-1].synchronize()
+    return [evs[r].elapsed_time(evs[r + 1]) for r in range(R)]
+
+
+def decode_timing(ffn, w, layers, xs, flags, dev, stream, K, warmup, min_ms):
+    """The decode step of workload `w` (one token per step, step i on layer i % L and token
+    i % NX): timed repeats of exactly K steps each, until at least `min_ms` of device time,
+    after at least `warmup` warm-up steps and one whole rotation of the layers. Returns the
+    median milliseconds per step over the repeats and how they were taken."""
+    import torch
+    L, NX, H = len(layers), len(xs), w["hidden"]
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags})
+    ws_bytes = ffn.moe_workspace_size(cfg)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    outs = torch.zeros((2, H), device=dev)
+
+    def step(i, st):
+        lay = layers[i % L]
+        ffn.check(ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
+                                         lay["shared_blocks"], cfg, outs[i % 2], ws, ws_bytes, st))
+
+    with torch.cuda.stream(stream):
+        for i in range(2 * L):  # eager warm-up (plans, lazy module loading, shared-memory limits)
+            step(i, stream)
+    stream.synchronize()
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    graphs = rotation_graphs(step, K, L, stream)
+    warm = max(1, math.ceil(max(warmup, L) / K))
+    per = timed_repeats(graphs, stream, warm, min_ms)
+    ffn.check(ffn.moe_workspace_status(ws, stream))
+    med = statistics.median(per)
+    return {"ms_per_step": med / K, "steps": K, "repeats": len(per), "timed_ms": round(sum(per), 3),
+            "warmup_steps": warm * K, "layers_rotated": L, "graphs": len(graphs),
+            "repeat_ms_min": round(min(per), 5), "repeat_ms_max": round(max(per), 5)}
+
+
+def decode_layers(synth, w, dev, rank, l2, layers=0):
+    """Distinct device-resident layers of `w`, enough that 4 x L2 of step bytes pass between
+    reuses of any weight byte, and 64 tokens."""
+    L = layers or max(8, math.ceil(4 * l2 / layer_bytes(w)) + 1)
+    lay = [synth.make_layer_torch(w, seed=layer_seed(rank, i), device=dev) for i in range(L)]
+    return lay, synth.make_tokens_torch(77 + rank, w["hidden"], 64, dev)
+
+
+def decode_roofline(w, ms, peak, peak_kind):
+    achieved = layer_bytes(w) / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "bytes_per_step": layer_bytes(w),
+            "active_bytes_per_step": active_bytes(w),
+            "active_frac": round(active_bytes(w) / (ms * 1e-3) / 1e9 / peak, 4)}
+
+
+def bench_chained(ffn, w, layers, L, dev, stream, reps=10, flags=0):
     """Per-layer latency with a real dependence between layers: x_{l+1} = x_l +
     FFN(rms_norm(x_l) * norm) (the residual form with the norm prologue, which keeps the
     layer's input bounded), rotating through the L distinct layers. One CUDA graph of G
@@ -340,7 +442,7 @@ def bench_chained(ffn, w, layers, L, dev, stream, reps=10):
     gen.manual_seed(4242)
     norm = torch.empty(H, device=dev).uniform_(0.5, 1.5, generator=gen)
     x0 = torch.empty(H, device=dev).normal_(0.0, 1.0, generator=gen)
-    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": ffn.MOE_RESIDUAL, "rms_eps": 1e-6, "ffn_norm": norm})
+    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": ffn.MOE_RESIDUAL | flags, "rms_eps": 1e-6, "ffn_norm": norm})
     ws_bytes = ffn.moe_workspace_size(cfg)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     bufs = torch.empty((2, H), device=dev)
@@ -539,14 +641,19 @@ def sweep_tokens(args, ffn, synth, w, dev, layers_n=4, calls=8, reps=5):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=320, help="steps per timed repeat")
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--min-ms", type=float, default=1500.0,
+                    help="device time the headline's timed repeats add up to at least")
+    ap.add_argument("--no-other-decode", action="store_true", help="skip the other decode workloads")
     ap.add_argument("--workload", default="flint_decode_t1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="distinct layers to rotate (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--fixed-point", action="store_true",
+                    help="decode with the 16-bit block fixed-point activations (MOE_FIXED_POINT)")
     ap.add_argument("--prefill-steps", type=int, default=480, help="timed batched steps (0: skip)")
     ap.add_argument("--trace", action="store_true",
                     help="after timing, print the kernel's per-CTA phase timeline (stderr)")
@@ -579,75 +686,43 @@ def main():
         return main_prefill(args, ffn, synth, dev, rank, world, local)
     step_bytes = layer_bytes(w)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    L = args.layers or max(8, math.ceil(4 * l2 / step_bytes) + 1)
-    layers = [synth.make_layer_torch(w, seed=layer_seed(rank, i), device=dev) for i in range(L)]
-    NX = 64
-    xs = synth.make_tokens_torch(77 + rank, H, NX, dev)
-    outs = torch.zeros((2, H), device=dev)
-    flags = ffn.MOE_NO_PDL if args.no_pdl else 0
-    cfg = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags})
-    ws_bytes = ffn.moe_workspace_size(cfg)
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    layers, xs = decode_layers(synth, w, dev, rank, l2, args.layers)
+    L, NX = len(layers), len(xs)
+    base_flags = ffn.MOE_NO_PDL if args.no_pdl else 0
+    flags = base_flags | (ffn.MOE_FIXED_POINT if args.fixed_point else 0)
     stream = torch.cuda.Stream(dev)
-
-    def step(i, st):
-        lay = layers[i % L]
-        rc = ffn.moe_ffn_forward_ex(xs[i % NX], lay["router_w"], lay["bias"], lay["expert_blocks"],
-                                    lay["shared_blocks"], cfg, outs[i % 2], ws, ws_bytes, st)
-        if rc != 0:
-            raise RuntimeError(ffn.moe_last_error())
-
-    # one graph of G steps (a whole number of layer sweeps), replayed
-    G = L * max(1, 320 // L)
-    with torch.cuda.stream(stream):
-        for i in range(2 * L):  # eager warm-up (plans, lazy module loading)
-            step(i, stream)
-    stream.synchronize()
-    ffn.check(ffn.moe_workspace_status(ws, stream))
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                step(i, stream)
-        return g
-
-    g_main = capture(G)
-    tail = args.steps % G
-    g_tail = capture(tail) if tail else None
-    wg = capture(args.warmup % G) if args.warmup % G else None
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup // G):
-            g_main.replay()
-        if wg is not None:
-            wg.replay()
-    stream.synchronize()
-    ffn.check(ffn.moe_workspace_status(ws, stream))
     barrier(world)
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps // G):
-                g_main.replay()
-            if g_tail is not None:
-                g_tail.replay()
-            ev1.record(stream)
-        ev1.synchronize()
+        head = decode_timing(ffn, w, layers, xs, flags, dev, stream, args.steps, args.warmup, args.min_ms)
+        # the other arithmetic of the decode chain, timed the same way (A/B)
+        ab = decode_timing(ffn, w, layers, xs, flags ^ ffn.MOE_FIXED_POINT, dev, stream, args.steps,
+                           args.warmup, args.min_ms / 4)
         torch.cuda.synchronize()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    ffn.check(ffn.moe_workspace_status(ws, stream))
-    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    sec = elapsed_ms / 1e3
-    value = args.steps * T * world / sec
-    ms_per_step = elapsed_ms / args.steps
+    ms_per_step = max_over_ranks(head["ms_per_step"], world, dev)
+    value = T * world / (ms_per_step * 1e-3)
+    ab_ms = max_over_ranks(ab["ms_per_step"], world, dev)
+    others = {}
+    if not args.no_other_decode:
+        for name in OTHER_DECODE:
+            if name == args.workload:
+                continue
+            wo = synth.WORKLOADS[name]
+            lo, xo = decode_layers(synth, wo, dev, rank, l2)
+            with ClockSampler(local) as clk_o:
+                r = decode_timing(ffn, wo, lo, xo, flags, dev, stream, args.steps, args.warmup, args.min_ms / 4)
+            r["ms_per_step"] = max_over_ranks(r["ms_per_step"], world, dev)
+            r["value"] = round(wo["n_tokens"] * world / (r["ms_per_step"] * 1e-3), 1)
+            r["unit"] = UNIT
+            r["qtype"] = qtype_label(wo)
+            r["clocks"] = clk_o.summary()
+            others[name] = r
+            del lo, xo
+            torch.cuda.empty_cache()
 
     if args.trace:
         print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream)
-    chained_ms = max_over_ranks(bench_chained(ffn, w, layers, L, dev, stream), world, dev)
+    chained_ms = max_over_ranks(bench_chained(ffn, w, layers, L, dev, stream, flags=flags), world, dev)
 
     # ---- end to end through the C ABI with host buffers (pinned) ----
     cfg_h = ffn.make_cfg(**{**w, "n_tokens": 1, "flags": flags | ffn.MOE_HOST_IO})
@@ -689,14 +764,15 @@ def main():
                            "frac": round(a / peak, 4), "peak_kind": peak_kind, "over": "the whole batched step",
                            "traffic": pp["dram_bytes_per_step"] if pp else None,
                            "tensor_pipe_active": pp["tensor_pipe_active"] if pp else None}
-    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
     prof = profile_counters(f"decode_chain_{args.workload}", "decode_chain")
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": prof["dram_bytes_per_step"] if prof else None,
-            "peak_kind": peak_kind, "kernel": "decode chain: dec_router -> dec_gate_up -> dec_down",
-            "over": "the whole step (three kernels overlapped by programmatic dependent launch)",
-            "bytes_per_step": step_bytes, "active_bytes_per_step": active_bytes(w),
-            "active_frac": round(active_bytes(w) / (ms_per_step * 1e-3) / 1e9 / peak, 4)}
+    roof = decode_roofline(w, ms_per_step, peak, peak_kind)
+    roof.update({"traffic": prof["dram_bytes_per_step"] if prof else None,
+                 "kernel": "decode chain: dec_router -> dec_gate_up -> dec_down",
+                 "over": "the whole step (three kernels overlapped by programmatic dependent launch)"})
+    for name, r in others.items():
+        r["roofline"] = decode_roofline(synth.WORKLOADS[name], r["ms_per_step"], peak, peak_kind)
+        pr = profile_counters(f"decode_chain_{name}", "decode_chain")
+        r["roofline"]["traffic"] = pr["dram_bytes_per_step"] if pr else None
     cpu = None
     if not args.no_cpu_baseline:
         d, err = cpu_baseline(args.workload)
@@ -713,21 +789,29 @@ def main():
         else:
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {err}"}
     clocks = clk.summary()
+    fixed = bool(flags & ffn.MOE_FIXED_POINT)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": ARITH_DTYPE[fixed], "data": "synthetic",
         "config": {"workload": args.workload, "T": T, "hidden": H, "n_experts": w["n_experts"],
                    "top_k": w["top_k"], "expert_ff": w["expert_ff"], "shared_ff": w["shared_ff"],
                    "qtype": qtype_label(w), "parallelism": f"replicas{world}",
                    "layers_rotated": L,
                    "l2": f"inputs larger than L2: {L} distinct layers, {L * step_bytes / 1e6:.0f} MB of "
                          f"step bytes between reuses of any weight byte (L2 {l2 / 1e6:.0f} MB)",
-                   "pdl": not args.no_pdl, "graph_steps": G},
-        "arith": "4-bit weights x activations in 16-bit block fixed point (15 bits and sign, power-of-two "
-                 "scale per 32 values): exact int32 block dots (dp4a), fp32 scaling and accumulation; router "
-                 "and routing in fp32",
+                   "pdl": not args.no_pdl},
+        "timing": dict(head, how=f"{head['repeats']} timed repeats of exactly {args.steps} steps (each a CUDA "
+                                 f"graph replay between two CUDA events on the replaying stream), the layer "
+                                 f"rotation continuing from repeat to repeat; ms_per_step is the median repeat "
+                                 f"over the steps"),
+        "arith": ARITH_TEXT[fixed],
         "roofline": roof,
+        "ab_arith": {"dtype": ARITH_DTYPE[not fixed], "arith": ARITH_TEXT[not fixed], "ms_per_step": ab_ms,
+                     "value": round(T * world / (ab_ms * 1e-3), 1), "unit": UNIT, "repeats": ab["repeats"],
+                     "how": "the same steps with the decode chain's other activation arithmetic, timed the "
+                            "same way right after the headline"},
+        "decode_configs": others,
         "chained": {"ms_per_step": chained_ms, "value": round(T * world / (chained_ms * 1e-3), 1), "unit": UNIT,
                     "how": "x of layer l+1 = x_l + FFN(rms_norm(x_l) * norm): the residual form with the "
                            "norm prologue, each layer waiting on the last, same rotated layers, one CUDA graph"},
@@ -736,7 +820,7 @@ def main():
                 "d2h_bytes_per_step": H * 4 * T, "steps": n_e2e,
                 "how": "moe_ffn_forward_ex with MOE_HOST_IO from pinned host memory, stream synchronised "
                        "every step"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 3 * args.steps * head["repeats"],
         "clocks": clocks,
         "prefill": pre,
     }

@@ -6,7 +6,6 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
-#include <string>
 #include <vector>
 
 #include "../../include/moeffn.h"
@@ -17,15 +16,14 @@
 
 namespace {
 
-thread_local std::string g_err;
+// The calling thread's last error text, formatted in place (no allocation).
+thread_local char g_err[512];
 
 int fail(int code, const char* fmt, ...) {
-  char buf[512];
   va_list ap;
   va_start(ap, fmt);
-  vsnprintf(buf, sizeof buf, fmt, ap);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
   va_end(ap);
-  g_err = buf;
   return code;
 }
 
@@ -109,14 +107,15 @@ int check_cfg(const moe_cfg* c) {
     return fail(MOE_ERR_INVALID_CFG, "swiglu limits must be finite and >= 0");
   if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps))
     return fail(MOE_ERR_INVALID_CFG, "rms_eps must be finite and >= 0");
-  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE | MOE_BATCHED))
+  if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE | MOE_BATCHED |
+                   MOE_FIXED_POINT))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
 }
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, ids, wts, pub, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
+  size_t ctrl, logits, act, ids, wts, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
 };
 
 // SMs of the current device (the timeline keeps one row per SM); without a
@@ -161,12 +160,10 @@ WsLayout ws_layout(const moe_cfg* c, bool decode_only = false) {
   o = up256(o + td * c->n_experts * 4);
   L.act = o;     // decode: SwiGLU activations of every slot [td][K * F + Fs] f32
   o = up256(o + td * ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
-  L.ids = o;     // decode: picks and weights [td][K] (calls of several tokens)
+  L.ids = o;     // decode: picks and weights [td][K]
   o = up256(o + td * c->top_k * 4);
   L.wts = o;
   o = up256(o + td * c->top_k * 4);
-  L.pub = o;     // decode: the picks a single-token call publishes for its down kernel [K] u64
-  o = up256(o + (size_t)c->top_k * 8);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -241,15 +238,15 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   const uint32_t budget = 200u * 1024u;  // dynamic shared memory of one CTA
   // gate/up: 4 windows of 8 rows, the x blocks and the selection
   p.gu_win = moe::window_bytes(8u * p.rb_h);
-  p.gu_smem = 4u * p.gu_win + (uint32_t)p.nbH * 72u + moe::select_smem(p.E);
+  p.gu_smem = 4u * p.gu_win + (uint32_t)p.nbH * moe::ACT_BLOCK_SMEM;
   if (p.gu_smem > budget) return fail(MOE_ERR_UNSUPPORTED, "gate/up rows too long for shared memory");
   // down: the activation blocks in one piece when they fit in 40 KiB, else pieces of
-  // 512; then as many rows per CTA (8, 4, 2, 1) as the windows allow
-  p.dn_piece = (size_t)p.nact * 72 <= 40 * 1024 ? p.nact : 512;
+  // 256; then as many rows per CTA (8, 4, 2, 1) as the windows allow
+  p.dn_piece = (size_t)p.nact * moe::ACT_BLOCK_SMEM <= 40 * 1024 ? p.nact : 256;
   for (p.dn_rows = 8; p.dn_rows >= 1; p.dn_rows /= 2) {
     p.dn_win_f = moe::window_bytes((uint32_t)p.dn_rows * p.rb_f);
     p.dn_win_fs = p.Fs ? moe::window_bytes((uint32_t)p.dn_rows * p.rb_fs) : 0u;
-    p.dn_smem = p.dn_win_fs + (uint32_t)p.K * p.dn_win_f + (uint32_t)p.dn_piece * 72u + moe::select_smem(p.E);
+    p.dn_smem = p.dn_win_fs + (uint32_t)p.K * p.dn_win_f + (uint32_t)p.dn_piece * moe::ACT_BLOCK_SMEM;
     if (p.dn_smem <= budget) break;
   }
   if (p.dn_rows < 1) return fail(MOE_ERR_UNSUPPORTED, "down rows too long for shared memory");
@@ -473,7 +470,6 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.act = reinterpret_cast<float*>(wsb + W.act);
   a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
   a.wts = reinterpret_cast<float*>(wsb + W.wts);
-  a.pub = reinterpret_cast<unsigned long long*>(wsb + W.pub);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -491,7 +487,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     a.out = dout + (size_t)t * c->hidden;
     a.topk_ids = dids ? dids + (size_t)t * c->top_k : nullptr;
     a.topk_w = dw ? dw + (size_t)t * c->top_k : nullptr;
-    e = moe::decode_launch(a, pe.maxb, st, pdl, pe.sms);
+    e = moe::decode_launch(a, pe.maxb, st, pdl, (c->flags & MOE_FIXED_POINT) != 0, pe.sms);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   if (host) {
@@ -511,6 +507,15 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   return MOE_OK;
 }
 
+// The error a nonzero status word reports.
+int status_error(uint32_t bits) {
+  if (bits & moe::DEV_ERR_MBAR_TIMEOUT)
+    return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out (status bits 0x%x); control block reset", bits);
+  return fail(MOE_ERR_WORKSPACE,
+              "a decode pick in the workspace was out of range (status bits 0x%x): the workspace was not "
+              "zero-filled before its first use; control block reset", bits);
+}
+
 int read_status(void* ws, cudaStream_t st) {
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
@@ -522,7 +527,7 @@ int read_status(void* ws, cudaStream_t st) {
     const uint32_t bits = ctrl[moe::CTRL_STATUS];
     e = cudaMemset(ws, 0, moe::CTRL_BYTES);
     if (e != cudaSuccess) return cuda_fail(e, "control block reset");
-    return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out (status bits 0x%x); control block reset", bits);
+    return status_error(bits);
   }
   return MOE_OK;
 }
@@ -545,7 +550,7 @@ extern "C" {
 
 int moe_ffn_forward(const float* x, const float* router_w, const float* router_bias,
                     const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg, float* out) {
-  g_err.clear();
+  g_err[0] = 0;
   int rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
   if (cfg->n_tokens == 0) return MOE_OK;
@@ -563,7 +568,7 @@ int moe_ffn_forward_ex(const float* x, const float* router_w, const float* route
                        const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg, float* out,
                        void* workspace, size_t workspace_bytes, void* stream, int32_t* topk_ids,
                        float* topk_w) {
-  g_err.clear();
+  g_err[0] = 0;
   return run(x, router_w, router_bias, expert_blocks, shared_blocks, cfg, out, workspace, workspace_bytes,
              static_cast<cudaStream_t>(stream), topk_ids, topk_w);
 }
@@ -579,20 +584,20 @@ size_t moe_trace_offset(const moe_cfg* cfg) {
 }
 
 int moe_workspace_status(void* workspace, void* stream) {
-  g_err.clear();
+  g_err[0] = 0;
   if (!workspace) return fail(MOE_ERR_NULL_PTR, "workspace is NULL");
   return read_status(workspace, static_cast<cudaStream_t>(stream));
 }
 
 int moe_selftest_timeout(void* workspace, void* stream) {
-  g_err.clear();
+  g_err[0] = 0;
   if (!workspace) return fail(MOE_ERR_NULL_PTR, "workspace is NULL");
   selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(workspace));
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "self-test launch");
 }
 
-const char* moe_last_error(void) { return g_err.c_str(); }
+const char* moe_last_error(void) { return g_err; }
 
 int moe_shutdown(void) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -619,30 +624,22 @@ int moe_shutdown(void) {
 namespace {
 
 // Fixed scratch for moe_ffn_forward_noalloc: the control block, the logits and the
-// SwiGLU activations of one token (at most 405 KiB for the largest layer the checks
-// admit: 32 picks of 3072 values plus a shared expert of 3072). It is device memory that exists from the moment the
-// library's code is loaded on a device until the process exits; every call on
-// that device shares it.
+// SwiGLU activations of the tokens of one launch (one token of the largest layer the
+// checks admit, 32 picks of 3072 values plus a shared expert of 3072, needs about 401 KiB).
+// It is device memory that exists from the moment the library's code is loaded on a
+// device until the process exits; every call on that device shares it.
 constexpr size_t NOALLOC_SCRATCH_BYTES = 512 * 1024;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
-// Device address of the scratch per device, looked up on the first call there.
-// In host code the array's name only stands in for the symbol; the address the
-// kernel needs comes from cudaGetSymbolAddress with that device current.
-constexpr int NOALLOC_MAX_DEVICES = 64;
-void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
-std::mutex g_noalloc_mu;
-
-int noalloc_scratch(int dev, void** ptr) {
-  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return fail(MOE_ERR_UNSUPPORTED, "device %d out of range", dev);
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch");
-    g_noalloc_ptr[dev] = p;
-  }
-  *ptr = g_noalloc_ptr[dev];
+// The scratch's device address on the current device. In host code the array's name only
+// stands in for the symbol; the address a kernel needs comes from cudaGetSymbolAddress with
+// that device current. It is looked up on every call (cheap once the library's module is
+// loaded on the device), so no address outlives the context it came from.
+int noalloc_scratch(void** ptr) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch");
+  *ptr = p;
   return MOE_OK;
 }
 
@@ -651,7 +648,7 @@ int noalloc_scratch(int dev, void** ptr) {
 extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, const float* router_bias,
                                        const void* expert_blocks, const void* shared_blocks,
                                        const moe_cfg* c, float* out, void* stream) {
-  g_err.clear();
+  g_err[0] = 0;
   int rc = check_cfg(c);
   if (rc != MOE_OK) return rc;
   if (c->flags & (MOE_HOST_IO | MOE_TRACE))
@@ -687,7 +684,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   void* scratch = nullptr;
-  rc = noalloc_scratch(dev, &scratch);
+  rc = noalloc_scratch(&scratch);
   if (rc != MOE_OK) return rc;
   PlanEntry pe;  // planned on every call: the plan cache of the other entry points would grow
   rc = make_plan(c, dev, &pe);
@@ -704,7 +701,6 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.act = reinterpret_cast<float*>(wsb + W.act);
   a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
   a.wts = reinterpret_cast<float*>(wsb + W.wts);
-  a.pub = reinterpret_cast<unsigned long long*>(wsb + W.pub);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -722,7 +718,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     a.out = out + (size_t)t * c->hidden;
     a.topk_ids = nullptr;
     a.topk_w = nullptr;
-    e = moe::decode_launch(a, pe.maxb, st, pdl, 0);
+    e = moe::decode_launch(a, pe.maxb, st, pdl, (c->flags & MOE_FIXED_POINT) != 0, 0);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   // wait, then read the status word; after a device-side timeout the control block
@@ -735,7 +731,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   if (status != 0) {
     e = cudaMemset(wsb + W.ctrl, 0, moe::CTRL_BYTES);
     if (e != cudaSuccess) return cuda_fail(e, "control block reset");
-    return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out (status bits 0x%x); control block reset", status);
+    return status_error(status);
   }
   return MOE_OK;
 }

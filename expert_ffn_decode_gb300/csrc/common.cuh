@@ -8,7 +8,6 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
-#include <vector>
 
 namespace moe {
 
@@ -16,37 +15,45 @@ namespace moe {
 // A workspace starts zeroed. The status word is sticky until the host clears it.
 enum CtrlWord : int {
   CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
+  CTRL_TICKET = 16,  // decode router: CTAs that have written their logits in this call
 };
 constexpr int CTRL_BYTES = 512;
 
 enum DevErr : uint32_t {
   DEV_ERR_MBAR_TIMEOUT = 2u,   // a copy or a slot release never arrived
+  DEV_ERR_BAD_PICK = 4u,       // a decode pick read from the workspace was out of range
 };
 
 // Raises a kernel's dynamic shared memory limit on the current device when a launch needs
 // more than any earlier one did. The attribute persists, so later launches skip the
-// driver call (it is on every call's host path).
+// driver call (it is on every call's host path). The table of raised limits is a fixed
+// array (no allocation); once it is full, launches of further kernels set the attribute
+// every time.
 inline cudaError_t ensure_smem(const void* kern, int bytes) {
   struct Entry {
     int dev;
     const void* kern;
     int bytes;
   };
+  constexpr int kMax = 512;
   static std::mutex mu;
-  static std::vector<Entry> done;
+  static Entry done[kMax];
+  static int n = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(mu);
-  for (auto& d : done)
+  for (int i = 0; i < n; ++i) {
+    Entry& d = done[i];
     if (d.dev == dev && d.kern == kern) {
       if (d.bytes >= bytes) return cudaSuccess;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
       if (e == cudaSuccess) d.bytes = bytes;
       return e;
     }
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.push_back(Entry{dev, kern, bytes});
+  if (e == cudaSuccess && n < kMax) done[n++] = Entry{dev, kern, bytes};
   return e;
 }
 
@@ -165,6 +172,35 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
+}
+
+// ---- f32 block dots ------------------------------------------------------------
+// A small unsigned integer q (a byte holding 0..63) becomes the f32 number 2^23 + q when it
+// is placed in the low mantissa byte of 2^23 (bit pattern 0x4B000000); subtracting 2^23 (or
+// 2^23 + c) then leaves q (or q - c) exactly. Byte j (0..3) of w:
+__device__ __forceinline__ float magic_byte(uint32_t w, int j) {
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)j));
+}
+constexpr float MAGIC_2P23 = 8388608.0f;  // 2^23
+
+// Packed pairs of f32 (two lanes of one 64-bit register pair): a - c on both lanes, and
+// a + q * x on both lanes, each rounded as the scalar f32 operation is.
+__device__ __forceinline__ void sub2_f32(float& q0, float& q1, float c) {
+  asm("{.reg .b64 q, c;\n mov.b64 q, {%0, %1};\n mov.b64 c, {%2, %2};\n sub.rn.f32x2 q, q, c;\n"
+      " mov.b64 {%0, %1}, q;}" : "+f"(q0), "+f"(q1) : "f"(c));
+}
+__device__ __forceinline__ void fma2_f32(float& a0, float& a1, float q0, float q1, float x0, float x1) {
+  asm("{.reg .b64 q, x, a;\n mov.b64 q, {%2, %3};\n mov.b64 x, {%4, %5};\n mov.b64 a, {%0, %1};\n"
+      " fma.rn.f32x2 a, q, x, a;\n mov.b64 {%0, %1}, a;}"
+      : "+f"(a0), "+f"(a1) : "f"(q0), "f"(q1), "f"(x0), "f"(x1));
+}
+// a0/a1 += (q_j - off) * x_j for the four byte values q_j of w and the four floats of x.
+__device__ __forceinline__ void word_dot_f32(uint32_t w, const float4& x, float off, float& a0, float& a1) {
+  float q0 = magic_byte(w, 0), q1 = magic_byte(w, 1), q2 = magic_byte(w, 2), q3 = magic_byte(w, 3);
+  sub2_f32(q0, q1, off);
+  sub2_f32(q2, q3, off);
+  fma2_f32(a0, a1, q0, q1, x.x, x.y);
+  fma2_f32(a0, a1, q2, q3, x.z, x.w);
 }
 
 // Round-to-nearest-even of |y| <= 2^22 to an integer by the add-and-subtract of

@@ -105,43 +105,44 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
 // Quantise blocks [0, nb) of an f32 vector (global memory, or shared memory when
 // kShared) as quant_task describes; with `mul`, value i is first multiplied by
 // scal * mul[i]. With `ss`, the thread adds the squares of the values it loaded (before
-// any multiplication) to *ss. Each thread takes two tasks a round and loads both before
-// computing; every thread runs the same number of rounds and whole warps call it
+// any multiplication) to *ss. Each thread takes four tasks a round and loads all of them
+// before computing; every thread runs the same number of rounds and whole warps call it
 // (the groups use shuffles).
 template <bool kShared = false>
 __device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float2* info,
                                              int t, int nthreads, const float* mul = nullptr, float scal = 1.f,
                                              float* ss = nullptr) {
+  constexpr int TPR = 4;  // tasks per thread and round
   #pragma unroll 1
-  for (int base = 0; base < 4 * nb; base += 2 * nthreads) {
-    float v[2][8];
-    int idx[2];
+  for (int base = 0; base < 4 * nb; base += TPR * nthreads) {
+    float4 va[TPR], vc[TPR], ma[TPR], mc[TPR];
+    int idx[TPR];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < TPR; ++h) {
       idx[h] = base + h * nthreads + t;
-      if (idx[h] < 4 * nb) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)(idx[h] >> 2) * 32 + (idx[h] & 3) * 8);
-        const float4 a = kShared ? s4[0] : __ldcg(s4), c = kShared ? s4[1] : __ldcg(s4 + 1);
-        v[h][0] = a.x; v[h][1] = a.y; v[h][2] = a.z; v[h][3] = a.w;
-        v[h][4] = c.x; v[h][5] = c.y; v[h][6] = c.z; v[h][7] = c.w;
-        if (ss) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) *ss = fmaf(v[h][i], v[h][i], *ss);
-        }
-        if (mul) {
-          const float4* m4 = reinterpret_cast<const float4*>(mul + (size_t)(idx[h] >> 2) * 32 + (idx[h] & 3) * 8);
-          const float4 ma = __ldg(m4), mc = __ldg(m4 + 1);
-          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mc.x, mc.y, mc.z, mc.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[h][i] = v[h][i] * scal * mm[i];
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[h][i] = 0.f;
-      }
+      const bool ok = idx[h] < 4 * nb;
+      const size_t off = (size_t)(idx[h] >> 2) * 32 + (idx[h] & 3) * 8;
+      const float4* s4 = reinterpret_cast<const float4*>(src + off);
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f), one = make_float4(1.f, 1.f, 1.f, 1.f);
+      va[h] = ok ? (kShared ? s4[0] : __ldcg(s4)) : z;
+      vc[h] = ok ? (kShared ? s4[1] : __ldcg(s4 + 1)) : z;
+      ma[h] = (mul && ok) ? __ldg(reinterpret_cast<const float4*>(mul + off)) : one;
+      mc[h] = (mul && ok) ? __ldg(reinterpret_cast<const float4*>(mul + off) + 1) : one;
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) quant_task(v[h], idx[h] < 4 * nb, idx[h] >> 2, idx[h] & 3, stride, planes, info);
+    for (int h = 0; h < TPR; ++h) {
+      float v[8] = {va[h].x, va[h].y, va[h].z, va[h].w, vc[h].x, vc[h].y, vc[h].z, vc[h].w};
+      if (ss) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) *ss = fmaf(v[i], v[i], *ss);
+      }
+      if (mul) {
+        const float mm[8] = {ma[h].x, ma[h].y, ma[h].z, ma[h].w, mc[h].x, mc[h].y, mc[h].z, mc[h].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = v[i] * scal * mm[i];
+      }
+      quant_task(v, idx[h] < 4 * nb, idx[h] >> 2, idx[h] & 3, stride, planes, info);
+    }
   }
 }
 
@@ -308,6 +309,152 @@ __device__ __forceinline__ float q6k_sub_dot(uint32_t row, int b, const ActBlock
   return a.s * d * fmaf(sc1, S1, sc0 * S0);
 }
 
+// ---- f32 activations (the default) -------------------------------------------------
+// Activations stay f32, the pages' arithmetic (flint_moe_ssd.js, WGSL section, Q41DOT and its
+// comment: a Q4_1 block contributes d * sum(q x) + m * sum(x), in f32). In shared memory an
+// activation array of nb blocks is stored as 8 chunks of 4 floats per block, chunk c (values
+// 4c .. 4c+3) of block b at (c * nb + b) * 16 bytes, so that lanes reading consecutive blocks
+// hit consecutive 16-byte words; the block sums sum(x) sit in a float array [nb].
+
+// Stores blocks [0, nb) of an f32 vector (global memory) as above, with chunk stride `stride`
+// blocks (>= nb); with `mul`, value i is first multiplied by mul[i]. With `ss`, the thread
+// adds the squares of the values it loaded (before any multiplication) to *ss. Each thread
+// takes U chunks a round and loads all of them (and their `mul` chunks) before storing any;
+// every thread runs the same number of rounds and whole warps call it (the block sums use
+// shuffles over the 8 lanes of a block).
+template <int U>
+__device__ __forceinline__ void store_blocks_f32(const float* src, int nb, int stride, float4* xs, float* xsum,
+                                                 int t, int nthreads, const float* mul = nullptr,
+                                                 float* ss = nullptr) {
+  #pragma unroll 1
+  for (int base = 0; base < 8 * nb; base += U * nthreads) {
+    float4 v[U], m[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int u = base + j * nthreads + t;  // chunk u & 7 of block u >> 3
+      const bool ok = u < 8 * nb;
+      v[j] = ok ? __ldcg(reinterpret_cast<const float4*>(src) + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      m[j] = (mul && ok) ? __ldg(reinterpret_cast<const float4*>(mul) + u) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int u = base + j * nthreads + t;
+      float4 w = v[j];
+      if (ss) *ss = fmaf(w.x, w.x, fmaf(w.y, w.y, fmaf(w.z, w.z, fmaf(w.w, w.w, *ss))));
+      if (mul) {
+        w.x *= m[j].x; w.y *= m[j].y; w.z *= m[j].z; w.w *= m[j].w;
+      }
+      float s = (w.x + w.y) + (w.z + w.w);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      if (u < 8 * nb) {
+        xs[(size_t)(u & 7) * stride + (u >> 3)] = w;
+        if ((u & 7) == 0) xsum[u >> 3] = s;
+      }
+    }
+  }
+}
+
+struct XBlock {
+  float4 c[8];  // values 4k .. 4k+3 in c[k]
+  float s;      // their sum
+};
+__device__ __forceinline__ void load_xblock(XBlock& x, uint32_t xs, uint32_t xsum, int b, int nb) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = lds128(xs + (uint32_t)(k * nb + b) * 16u);
+    x.c[k] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  x.s = __uint_as_float(lds32(xsum + (uint32_t)b * 4u));
+}
+
+// sum over the block of (q_i - off) x_i for the four nibble words of a Q4_0/Q4_1 block (word k:
+// low nibbles = values 4k .. 4k+3, high nibbles = values 16+4k ..), in f32
+__device__ __forceinline__ float nibble_dot_f32(const uint32_t (&qw)[4], const XBlock& x, float off) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    word_dot_f32(qw[k] & 0x0F0F0F0Fu, x.c[k], off, a0, a1);
+    word_dot_f32((qw[k] >> 4) & 0x0F0F0F0Fu, x.c[4 + k], off, a2, a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+// Q4_1: d * sum(q x) + m * sum(x); Q4_0: d * sum((q - 8) x), the 8 taken off each q exactly.
+template <int QT>
+__device__ __forceinline__ float raw_block_dot_f32(const RawBlock& r, const XBlock& x) {
+  if constexpr (QT == 3) {
+    const uint32_t qw[4] = {r.w[1], r.w[2], r.w[3], r.w[4]};
+    const float S = nibble_dot_f32(qw, x, MAGIC_2P23);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r.w[0]));
+    return fmaf(f.x, S, f.y * x.s);
+  } else {
+    const uint32_t dbits = __funnelshift_rc(r.w[0], r.w[1], r.sh) & 0xFFFFu;
+    const uint32_t qw[4] = {__funnelshift_rc(r.w[0], r.w[1], 16 + r.sh), __funnelshift_rc(r.w[1], r.w[2], 16 + r.sh),
+                            __funnelshift_rc(r.w[2], r.w[3], 16 + r.sh), __funnelshift_rc(r.w[3], r.w[4], 16 + r.sh)};
+    const float S = nibble_dot_f32(qw, x, MAGIC_2P23 + 8.f);
+    return __half2float(__ushort_as_half((unsigned short)dbits)) * S;
+  }
+}
+
+// Q4_K sub-block b % 8 of super-block b / 8 (layout as q4k_sub_dot): d sc sum(q x) - dmin mn sum(x).
+__device__ __forceinline__ float q4k_sub_dot_f32(uint32_t row, int b, const XBlock& x) {
+  const uint32_t sb = row + 144u * (uint32_t)(b >> 3);
+  const int j = b & 7, sh = 8 * (j & 3);
+  const uint4 hd = lds128(sb);
+  const uint4 n0 = lds128(sb + 16u + 32u * (uint32_t)(j >> 1));
+  const uint4 n1 = lds128(sb + 32u + 32u * (uint32_t)(j >> 1));
+  const uint32_t by = (hd.y >> sh) & 0xFFu, bz = (hd.z >> sh) & 0xFFu, bw = (hd.w >> sh) & 0xFFu;
+  const uint32_t sc = j < 4 ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4));
+  const uint32_t mn = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
+  const int ns = 4 * (j & 1);
+  const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    word_dot_f32((w[i] >> ns) & 0x0F0F0F0Fu, x.c[i], MAGIC_2P23, a0, a1);
+    word_dot_f32((w[i + 1] >> ns) & 0x0F0F0F0Fu, x.c[i + 1], MAGIC_2P23, a2, a3);
+  }
+  const float S = (a0 + a1) + (a2 + a3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));  // d, dmin
+  return fmaf(f.x * (float)sc, S, -(f.y * (float)mn) * x.s);
+}
+
+// Q6_K sub-block (layout as q6k_sub_dot): d (sc0 sum_{i<16} (q_i - 32) x_i + sc1 sum_{i>=16} ...).
+__device__ __forceinline__ float q6k_sub_dot_f32(uint32_t row, int b, const XBlock& x) {
+  const uint32_t sb = row + 210u * (uint32_t)(b >> 3);
+  const int j = b & 7, n = j >> 2, r = j & 3;
+  uint32_t L[8], Hh[8];
+  lds_run32(sb + 64u * n + 32u * (r & 1), L);
+  lds_run32(sb + 128u + 32u * n, Hh);
+  const uint32_t scp = lds16(sb + 192u + 8u * n + 2u * r);
+  const float d = __half2float(__ushort_as_half((unsigned short)lds16(sb + 208u)));
+  const int ls = 4 * (r >> 1), hs = 2 * r;
+  float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = ((L[i] >> ls) & 0x0F0F0F0Fu) | (((Hh[i] >> hs) & 0x03030303u) << 4);  // 0..63
+    word_dot_f32(u, x.c[i], MAGIC_2P23 + 32.f, a[i >> 2][0], a[i >> 2][1]);
+  }
+  const float sc0 = (float)(int)(int8_t)(scp & 0xFFu), sc1 = (float)(int)(int8_t)(scp >> 8);
+  return d * fmaf(sc1, a[1][0] + a[1][1], sc0 * (a[0][0] + a[0][1]));
+}
+
+// Block b of a row in shared memory times f32 activation block x.
+template <int QT>
+__device__ __forceinline__ float row_block_dot_f32(uint32_t row, int b, const XBlock& x) {
+  if constexpr (QT == 12) {
+    return q4k_sub_dot_f32(row, b, x);
+  } else if constexpr (QT == 14) {
+    return q6k_sub_dot_f32(row, b, x);
+  } else {
+    RawBlock r;
+    load_block_s<QT>(row, b, r);
+    return raw_block_dot_f32<QT>(r, x);
+  }
+}
+
 // Block b of a row in shared memory times activation block a.
 template <int QT>
 __device__ __forceinline__ float row_block_dot(uint32_t row, int b, const ActBlock& a) {
@@ -406,10 +553,13 @@ __device__ __forceinline__ void sort_list(uint32_t (&kv)[N], int (&ki)[N]) {
 //   2. groups (n_groups > 1): each warp scores groups (the two largest s, summed);
 //      warp 0 keeps groups_used of them, the largest score first, the lowest group
 //      on ties; the keys of the other groups' experts become 0
-//   3. each warp: the top k of its experts (warp w: experts 32 w + lane + 256 i), as
-//      k rounds over the lanes' sorted lists (the winning lane drops its head)
-//   4. warp 0: the top k of the 8 sorted candidate lists (lane l walks list l), then
-//      the weights
+//   3. k <= 8: tau = the k-th largest of the 8 warps' largest keys. At least k keys reach
+//      tau, so every pick does: the keys >= tau are gathered (typically little more than
+//      k of them) and each takes its rank among them; ranks below k are the picks.
+//   4. otherwise (or when more than 256 keys reach tau, i.e. many exact ties): each warp
+//      takes its top k in k rounds over the lanes' sorted lists, then warp 0 merges the 8
+//      sorted candidate lists in k rounds
+//   5. warp 0: the weights from the picked sigmoids
 // Key 0 is below every real key (every float's key is at least that of -inf). With
 // trows > 0 thread 0 records the timeline points of the selection's phases.
 template <int N>
@@ -422,6 +572,9 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
   uint32_t* ckey = reinterpret_cast<uint32_t*>(sel + (size_t)p.E * 8);
   int* cidx = reinterpret_cast<int*>(sel + (size_t)p.E * 8 + 1024);
   __shared__ unsigned long long kept_groups;
+  __shared__ uint32_t wmax[8];
+  __shared__ int wcnt[8];
+  uint32_t kv[N];  // this thread's keys: experts tid + 256 i
   {
     float l[N];
 #pragma unroll
@@ -432,17 +585,19 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
 #pragma unroll
     for (int i = 0; i < N; ++i) {
       const int e = tid + 256 * i;
+      kv[i] = 0u;
       if (e < p.E) {
         const float pr = 1.f / (1.f + expf(-l[i]));
         probs[e] = pr;
-        keys[e] = order_key(pr + (a.bias ? __ldg(a.bias + e) : 0.f));
+        kv[i] = order_key(pr + (a.bias ? __ldg(a.bias + e) : 0.f));
+        if (p.G > 1) keys[e] = kv[i];
       }
     }
   }
-  if (tid == 0) kept_groups = ~0ull;
-  __syncthreads();
   tr(a, TR_SEL_KEYS, trows);
   if (p.G > 1) {
+    if (tid == 0) kept_groups = ~0ull;
+    __syncthreads();
     const int per = p.E / p.G;
     #pragma unroll 1
     for (int g = warp; g < p.G; g += 8) {
@@ -488,23 +643,86 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
       if (lane == 0) kept_groups = kept;
     }
     __syncthreads();
-  }
-  {
-    // stage 1: each warp's top k, from lane lists sorted into selection order; experts
-    // of dropped groups take key 0. The group of expert e is floor((e + 1/2) / per) in
-    // fp32: exact, since the quotient stays at least 1/(2 per) >= 1/1024 away from an
+    // experts of dropped groups take key 0. The group of expert e is floor((e + 1/2) / per)
+    // in fp32: exact, since the quotient stays at least 1/(2 per) >= 1/1024 away from an
     // integer and e < 1024.
     const unsigned long long kg = kept_groups;
-    const float inv_per = p.G > 1 ? 1.f / (float)(p.E / p.G) : 0.f;
-    uint32_t kv[N];
-    int ki[N];
+    const float inv_per = 1.f / (float)per;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-      const int e = 32 * warp + lane + 256 * i;
-      ki[i] = e;
+      const int e = tid + 256 * i;
       const int g = (int)(((float)e + 0.5f) * inv_per);
-      kv[i] = (e < p.E && ((kg >> g) & 1ull)) ? keys[e] : 0u;
+      if (e < p.E && !((kg >> g) & 1ull)) kv[i] = 0u;
     }
+  }
+  uint32_t m = 0u;
+#pragma unroll
+  for (int i = 0; i < N; ++i) m = kv[i] > m ? kv[i] : m;
+  m = __reduce_max_sync(0xffffffffu, m);
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  bool pruned = p.K <= 8;
+  if (pruned) {
+    uint32_t wm[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) wm[w] = wmax[w];
+    uint32_t tau = 0u;  // the k-th largest warp maximum
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int rank = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rank += (wm[i] > wm[j] || (wm[i] == wm[j] && i < j)) ? 1 : 0;
+      if (rank == p.K - 1) tau = wm[j];
+    }
+    unsigned bal[N];
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      bal[i] = __ballot_sync(0xffffffffu, kv[i] != 0u && kv[i] >= tau);
+      cnt += __popc(bal[i]);
+    }
+    if (lane == 0) wcnt[warp] = cnt;
+    __syncthreads();
+    int off = 0, C = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = wcnt[w];
+      off += w < warp ? c : 0;
+      C += c;
+    }
+    if (C <= 256) {
+      const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        if ((bal[i] >> lane) & 1u) {
+          const int pos = off + __popc(bal[i] & below);
+          ckey[pos] = kv[i];
+          cidx[pos] = tid + 256 * i;
+        }
+        off += __popc(bal[i]);
+      }
+    }
+    __syncthreads();
+    tr(a, TR_SEL_CANDS, trows);
+    if (C <= 256) {
+      #pragma unroll 1
+      for (int j = tid; j < C; j += 256) {
+        const uint32_t kj = ckey[j];
+        const int ij = cidx[j];
+        int rank = 0;
+        #pragma unroll 4
+        for (int c = 0; c < C; ++c) rank += before(ckey[c], cidx[c], kj, ij) ? 1 : 0;
+        if (rank < p.K) rids[rank] = ij;
+      }
+    } else {
+      pruned = false;
+    }
+  }
+  if (!pruned) {
+    // stage 1: each warp's top k, from lane lists sorted into selection order
+    int ki[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) ki[i] = tid + 256 * i;
     sort_list(kv, ki);
     #pragma unroll 1
     for (int j = 0; j < p.K; ++j) {
@@ -523,28 +741,30 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
         kv[N - 1] = 0u;
       }
     }
-  }
-  __syncthreads();
-  tr(a, TR_SEL_CANDS, trows);
-  if (warp == 0) {
-    // stage 2: lane l < 8 walks warp l's sorted candidates
-    int h = 0;
-    uint32_t bk = lane < 8 ? ckey[lane * p.K] : 0u;
-    int bi = lane < 8 ? cidx[lane * p.K] : 0x7fffffff;
-    #pragma unroll 1
-    for (int j = 0; j < p.K; ++j) {
-      const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-      int win = (int)__reduce_min_sync(0xffffffffu, bk == mk && mk != 0u ? (unsigned)bi : 0xffffffffu);
-      if (win < 0 || win >= p.E) win = j % p.E;  // unreachable for a valid configuration
-      if (lane == 0) rids[j] = win;
-      if (lane < 8 && bk == mk && bi == win) {
-        ++h;
-        bk = h < p.K ? ckey[lane * p.K + h] : 0u;
-        bi = h < p.K ? cidx[lane * p.K + h] : 0x7fffffff;
+    __syncthreads();
+    tr(a, TR_SEL_CANDS, trows);
+    if (warp == 0) {
+      // stage 2: lane l < 8 walks warp l's sorted candidates
+      int h = 0;
+      uint32_t bk = lane < 8 ? ckey[lane * p.K] : 0u;
+      int bi = lane < 8 ? cidx[lane * p.K] : 0x7fffffff;
+      #pragma unroll 1
+      for (int j = 0; j < p.K; ++j) {
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        int win = (int)__reduce_min_sync(0xffffffffu, bk == mk && mk != 0u ? (unsigned)bi : 0xffffffffu);
+        if (win < 0 || win >= p.E) win = j % p.E;  // unreachable for a valid configuration
+        if (lane == 0) rids[j] = win;
+        if (lane < 8 && bk == mk && bi == win) {
+          ++h;
+          bk = h < p.K ? ckey[lane * p.K + h] : 0u;
+          bi = h < p.K ? cidx[lane * p.K + h] : 0x7fffffff;
+        }
       }
     }
-    __syncwarp();
-    tr(a, TR_SEL_RANKED, trows);
+  }
+  __syncthreads();
+  tr(a, TR_SEL_RANKED, trows);
+  if (warp == 0) {
     // weights from the picked sigmoids
     const float pj = lane < p.K ? probs[rids[lane]] : 0.f;
     const float wsum = fmaxf(warp_sum(pj), a.norm_min);
@@ -563,9 +783,19 @@ __device__ __forceinline__ void select_picks(const DecodeArgs& a, const float* l
 // ===========================================================================
 // Router: logits
 // ===========================================================================
+// A single-token call also makes the token's picks here, once: every CTA writes its logits
+// and then takes a ticket (an atomic count in the control block); the CTA that takes the
+// last ticket sees every logit, selects, writes the picks and weights for the gate/up and
+// down kernels, and returns the count to 0 for the next call. Nothing waits on the count.
+// Dynamic shared memory: the selection's (select_smem).
 __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int trows) {
+  extern __shared__ __align__(16) uint8_t rsm[];
   __shared__ float part[RT_THREADS / 32][DEC_TMAX];
   __shared__ float red[RT_THREADS / 32][DEC_TMAX];  // sums of squares (with a norm vector)
+  __shared__ float gscore[64];
+  __shared__ int rids[32];
+  __shared__ float rw[32];
+  __shared__ int last;
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   tr(a, TR_RT_START, trows);
@@ -590,9 +820,6 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   pdl_wait_prior_grids();  // x may come from the previous kernel
   pdl_launch_dependents();
   tr(a, TR_RT_X, trows);
-  // this call's published picks start empty (the previous call's kernels are complete:
-  // the wait above covers them, and every reader of this call starts after this grid)
-  if (a.T == 1 && blockIdx.x == 0 && tid < p.K) st_relaxed_u64(a.pub + tid, PUB_EMPTY);
   // the prologue (with a norm vector): token t's input is x_t * r_t * norm, r_t =
   // 1/rms(x_t). The dot takes x_t * norm and its sum is scaled by r_t; the sum of squares
   // comes from the same loads (a row's four quarter warps cover x_t once).
@@ -630,9 +857,26 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
         v *= 1.f / sqrtf(sq / (float)p.H + a.eps);
       }
       a.logits[(size_t)t * p.E + row2] = v;
+      if (a.T == 1) __threadfence();  // the logit is visible before this CTA's ticket
     }
   }
   tr(a, TR_RT_DONE, trows);
+  if (a.T == 1) {
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(a.ctrl + CTRL_TICKET, 1u) == gridDim.x - 1u;
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      select_picks(a, a.logits, rsm, gscore, rids, rw, trows);
+      if (tid < p.K) {
+        a.ids[tid] = rids[tid];
+        a.wts[tid] = rw[tid];
+        if (a.topk_ids) a.topk_ids[tid] = rids[tid];
+        if (a.topk_w) a.topk_w[tid] = rw[tid];
+      }
+      if (tid == 0) a.ctrl[CTRL_TICKET] = 0u;  // the next call's routers count after this grid ends
+    }
+  }
 }
 
 // ===========================================================================
@@ -660,16 +904,13 @@ __global__ void __launch_bounds__(256) dec_select(const DecodeArgs a) {
 // Gate/up: 16 intermediate values of a slot per CTA
 // ===========================================================================
 // Dynamic shared memory: 4 windows (chunk c: gate window 2c, up window 2c + 1, each
-// 8 rows), then the x planes [nbH][64] and x info [nbH], then the selection's probs
-// and keys.
-template <int QT, int MAXB>
+// 8 rows), then x: f32 chunks [8][nbH] and block sums [nbH], or (fixed point) the planes
+// [nbH][64] and info [nbH].
+template <int QT, int MAXB, bool FX>
 __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a, int trows) {
   extern __shared__ __align__(128) uint8_t gsm[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ float rowdot[GU_THREADS / 32][4];
-  __shared__ float gscore[64];
-  __shared__ int rids[32];
-  __shared__ float rw[32];
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int v0 = blockIdx.x * GU_VALUES;  // first activation index of the CTA
@@ -680,9 +921,10 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   const int f0 = shared ? v0 : (v0 - p.Fs) % p.F;
   tr(a, TR_GU_START, trows);
   uint8_t* win = gsm;
-  uint8_t* xplanes = gsm + (size_t)4 * p.gu_win;
+  uint8_t* xplanes = gsm + (size_t)4 * p.gu_win;  // x: fixed-point planes, or f32 chunks
   float2* xinfo = reinterpret_cast<float2*>(xplanes + (size_t)p.nbH * 64);
-  uint8_t* sel = xplanes + (size_t)p.nbH * 72;
+  float4* xs = reinterpret_cast<float4*>(xplanes);
+  float* xsum = reinterpret_cast<float*>(xplanes + (size_t)p.nbH * 128);
   const uint32_t rows8 = 8u * p.rb_h;
   if (tid == 0) {
     mbar_init(&bars[0], 2);
@@ -698,15 +940,34 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
     mbar_arrive_expect_tx(&bars[c], window_span(src, rows8));
     copy_window(win + (size_t)tid * p.gu_win, src, rows8, &bars[c], policy_evict_first());
   };
-  if (shared && tid < 4) issue(a.shared);
-  // x -> activation blocks (x is complete: the router kernel waited for it before this
-  // launch was triggered)
-  // With a norm vector the blocks hold x * norm; r = 1/rms(x) comes from the same loads
-  // and scales the row dots (every dot is linear in x).
+  const uint8_t* rec = a.shared;
+  if (shared) {
+    if (tid < 4) issue(a.shared);
+    pdl_launch_dependents();
+  } else {
+    // the picks: made by the router kernel (one token) or by the selection kernel
+    pdl_wait_prior_grids();
+    pdl_launch_dependents();
+    tr(a, TR_GU_WAITED, trows);
+    const int slot = (v0 - p.Fs) / p.F;
+    int e = __ldcg(a.ids + (size_t)tok * p.K + slot);
+    if ((unsigned)e >= (unsigned)p.E) {  // only a workspace that was not zeroed before its first use
+      if (tid == 0) atomicOr(a.ctrl + CTRL_STATUS, DEV_ERR_BAD_PICK);
+      e = 0;
+    }
+    rec = a.experts + (size_t)e * p.rec_bytes;
+    if (tid < 4) issue(rec);
+  }
+  tr(a, TR_GU_PICKED, trows);
+  // x -> activation blocks while the rows are copied in (x is complete: the router kernel
+  // waited for it before this launch was triggered). With a norm vector the blocks hold
+  // x * norm; r = 1/rms(x) comes from the same loads and scales the row dots (every dot is
+  // linear in x).
   __shared__ float red[GU_THREADS / 32];
   {
     float ss = 0.f;
-    quant_blocks(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, 1.f, a.norm ? &ss : nullptr);
+    if constexpr (FX) quant_blocks(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, 1.f, a.norm ? &ss : nullptr);
+    else store_blocks_f32<4>(xt, p.nbH, p.nbH, xs, xsum, tid, GU_THREADS, a.norm, a.norm ? &ss : nullptr);
     if (a.norm) {
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
@@ -722,37 +983,14 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   }
   tr(a, TR_GU_XQ, trows);
   const RowMap mh = row_map(p.nbH, lane);
-  ActBlock xc[MAXB];
+  ActBlock xc[FX ? MAXB : 1];
+  if constexpr (FX) {
 #pragma unroll
-  for (int i = 0; i < MAXB; ++i) {
-    const int b = mh.sub + mh.lpr * i;
-    if (b < p.nbH) load_act_block_s(xc[i], smem_addr(xplanes), smem_addr(xinfo), b, p.nbH);
-  }
-  const uint8_t* rec = a.shared;
-  if (!shared) {
-    pdl_wait_prior_grids();  // the logits
-    pdl_launch_dependents();
-    tr(a, TR_GU_WAITED, trows);
-    const int slot = (v0 - p.Fs) / p.F;
-    if (a.T == 1) {
-      select_picks(a, a.logits, sel, gscore, rids, rw, trows);
-      if (v0 == p.Fs && tid < p.K) {  // one CTA reports the picks
-        if (a.topk_ids) a.topk_ids[tid] = rids[tid];
-        if (a.topk_w) a.topk_w[tid] = rw[tid];
-        // for down CTAs that start after this point: one 64-bit store per pick
-        st_relaxed_u64(a.pub + tid, (unsigned long long)(uint32_t)rids[tid] |
-                                        ((unsigned long long)__float_as_uint(rw[tid]) << 32));
-      }
-    } else if (tid == 0) {
-      rids[slot] = __ldcg(a.ids + (size_t)tok * p.K + slot);  // made by the selection kernel
+    for (int i = 0; i < MAXB; ++i) {
+      const int b = mh.sub + mh.lpr * i;
+      if (b < p.nbH) load_act_block_s(xc[i], smem_addr(xplanes), smem_addr(xinfo), b, p.nbH);
     }
-    __syncthreads();
-    rec = a.experts + (size_t)rids[slot] * p.rec_bytes;
-    if (tid < 4) issue(rec);
-  } else {
-    pdl_launch_dependents();
   }
-  tr(a, TR_GU_PICKED, trows);
   // warp w: values 2w, 2w + 1 of the CTA (chunk w / 4); its rows r = 0..3 are gate
   // (r even) and up (r odd) of value 2w + r / 2
   const int c = warp >> 2;
@@ -766,16 +1004,36 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   const int vl = 2 * (warp & 3);  // first value of the warp within the chunk
   float dots[4] = {0.f, 0.f, 0.f, 0.f};
   if (ok) {
+    if constexpr (FX) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int r = mh.rsub + mh.rps * s;
-      if (r < 4) {
-        const uint32_t row = ((r & 1) ? uwin : gwin) + (uint32_t)(vl + (r >> 1)) * p.rb_h;
+      for (int s = 0; s < 4; ++s) {
+        const int r = mh.rsub + mh.rps * s;
+        if (r < 4) {
+          const uint32_t row = ((r & 1) ? uwin : gwin) + (uint32_t)(vl + (r >> 1)) * p.rb_h;
 #pragma unroll
-        for (int i = 0; i < MAXB; ++i) {
-          const int b = mh.sub + mh.lpr * i;
-          if (b < p.nbH) {
-            dots[s] += row_block_dot<QT>(row, b, xc[i]);
+          for (int i = 0; i < MAXB; ++i) {
+            const int b = mh.sub + mh.lpr * i;
+            if (b < p.nbH) {
+              dots[s] += row_block_dot<QT>(row, b, xc[i]);
+            }
+          }
+        }
+      }
+    } else {
+      // each x block is loaded once for the warp's rows
+#pragma unroll
+      for (int i = 0; i < MAXB; ++i) {
+        const int b = mh.sub + mh.lpr * i;
+        if (b < p.nbH) {
+          XBlock xb;
+          load_xblock(xb, smem_addr(xs), smem_addr(xsum), b, p.nbH);
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const int r = mh.rsub + mh.rps * s;
+            if (r < 4) {
+              const uint32_t row = ((r & 1) ? uwin : gwin) + (uint32_t)(vl + (r >> 1)) * p.rb_h;
+              dots[s] += row_block_dot_f32<QT>(row, b, xb);
+            }
           }
         }
       }
@@ -802,16 +1060,15 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
 // Down: R output rows per CTA over every slot, weighted, in a fixed order
 // ===========================================================================
 // Dynamic shared memory: the shared window, then K routed windows, then one piece of
-// quantised activation blocks (planes [4][piece][16 B], info [piece]), then the
-// selection's probs and keys. The threads form RG row groups of 256 / RG threads;
+// activation blocks: f32 chunks [8][piece] and block sums [piece], or (fixed point)
+// planes [4][piece][16 B] and info [piece]. The threads form RG row groups of 256 / RG threads;
 // group g owns rows g R / RG .. (g + 1) R / RG - 1, and its thread t takes blocks t,
 // t + 256 / RG, ... of each piece with all of the group's rows: an activation block
 // is read once for R / RG block dots.
-template <int QT>
+template <int QT, bool FX>
 __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int trows) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ float gscore[64];
   __shared__ int rids[32];
   __shared__ float rw[32];
   __shared__ uint32_t woff[33];  // offset of each window's first row in the window
@@ -823,35 +1080,26 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   const int nwin = p.K + (p.Fs ? 1 : 0);
   tr(a, TR_DN_START, trows);
   const size_t win_r = (size_t)p.dn_win_fs;  // first routed window
-  uint8_t* aplanes = dsm + win_r + (size_t)p.K * p.dn_win_f;
+  uint8_t* aplanes = dsm + win_r + (size_t)p.K * p.dn_win_f;  // activations: fixed-point planes, or f32 chunks
   float2* ainfo = reinterpret_cast<float2*>(aplanes + (size_t)p.dn_piece * 64);
-  uint8_t* sel = aplanes + (size_t)p.dn_piece * 72;
+  float4* axs = reinterpret_cast<float4*>(aplanes);
+  float* axsum = reinterpret_cast<float*>(aplanes + (size_t)p.dn_piece * 128);
   if (tid == 0) {
     mbar_init(&bar, (uint32_t)nwin);
     fence_mbar_init();
   }
-  // the picks (the router is complete: every routed gate/up CTA waited for it before
-  // this launch was triggered)
-  if (a.T == 1) {
-    // The picks: those the gate/up kernel has published if all k are there (a down CTA
-    // that could not start before the gate/up CTAs left finds them), else made here.
-    // Nothing waits on them: an entry is either empty or this call's pick.
-    bool mine = true;
-    if (tid < p.K) {
-      const unsigned long long v = ld_relaxed_u64(a.pub + tid);
-      mine = v != PUB_EMPTY;
-      rids[tid] = (int)(uint32_t)v;
-      rw[tid] = __uint_as_float((uint32_t)(v >> 32));
+  // the picks, made by the router kernel (one token) or by the selection kernel: complete,
+  // since every routed gate/up CTA waited for that kernel before this launch was triggered
+  if (tid < p.K) {
+    int e = __ldcg(a.ids + (size_t)tok * p.K + tid);
+    if ((unsigned)e >= (unsigned)p.E) {  // only a workspace that was not zeroed before its first use
+      atomicOr(a.ctrl + CTRL_STATUS, DEV_ERR_BAD_PICK);
+      e = 0;
     }
-    if (!__syncthreads_and(mine)) select_picks(a, a.logits, sel, gscore, rids, rw);
-  } else {
-    // made by the selection kernel, complete once every routed gate/up CTA has waited
-    if (tid < p.K) {
-      rids[tid] = __ldcg(a.ids + (size_t)tok * p.K + tid);
-      rw[tid] = __ldcg(a.wts + (size_t)tok * p.K + tid);
-    }
-    __syncthreads();
+    rids[tid] = e;
+    rw[tid] = __ldcg(a.wts + (size_t)tok * p.K + tid);
   }
+  __syncthreads();
   tr(a, TR_DN_PICKED, trows);
   if (tid < nwin) {
     // this CTA's rows of slot window tid's down matrix, copied by thread tid
@@ -888,8 +1136,12 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   #pragma unroll 1
   for (int pb = 0; pb < nact; pb += p.dn_piece) {
     const int np = nact - pb < p.dn_piece ? nact - pb : p.dn_piece;
-    quant_blocks(a.act + (size_t)tok * p.act_stride + (size_t)pb * 32, np, p.dn_piece, aplanes, ainfo, tid,
-                 DN_THREADS);
+    if constexpr (FX)
+      quant_blocks(a.act + (size_t)tok * p.act_stride + (size_t)pb * 32, np, p.dn_piece, aplanes, ainfo, tid,
+                   DN_THREADS);
+    else
+      store_blocks_f32<8>(a.act + (size_t)tok * p.act_stride + (size_t)pb * 32, np, p.dn_piece, axs, axsum, tid,
+                          DN_THREADS);
     __syncthreads();  // the piece; on the first pass also the window offsets
     if (pb == 0) {
       tr(a, TR_DN_QUANT, trows);
@@ -907,13 +1159,24 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
         const uint32_t w0 = smem_addr(dsm) + (sh ? woff[32] : (uint32_t)win_r + (uint32_t)j * p.dn_win_f + woff[j]);
         const uint32_t rb = sh ? p.rb_fs : p.rb_f;
         const float wgt = sh ? 1.f : rw[j];
-        ActBlock ab;
-        load_act_block_s(ab, smem_addr(aplanes), smem_addr(ainfo), i, p.dn_piece);
         const uint32_t wr = w0 + (uint32_t)(grp * RPG) * rb;
+        if constexpr (FX) {
+          ActBlock ab;
+          load_act_block_s(ab, smem_addr(aplanes), smem_addr(ainfo), i, p.dn_piece);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          if (r < RPG) {
-            acc[r] = fmaf(wgt, row_block_dot<QT>(wr + (uint32_t)r * rb, b, ab), acc[r]);
+          for (int r = 0; r < 8; ++r) {
+            if (r < RPG) {
+              acc[r] = fmaf(wgt, row_block_dot<QT>(wr + (uint32_t)r * rb, b, ab), acc[r]);
+            }
+          }
+        } else {
+          XBlock xb;
+          load_xblock(xb, smem_addr(axs), smem_addr(axsum), i, p.dn_piece);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r < RPG) {
+              acc[r] = fmaf(wgt, row_block_dot_f32<QT>(wr + (uint32_t)r * rb, b, xb), acc[r]);
+            }
           }
         }
       }
@@ -965,47 +1228,50 @@ static cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, int threads, siz
 }
 
 template <int QT, int MAXB>
-static cudaError_t launch_gate_up(const DecodeArgs& a, cudaStream_t st, bool pdl, int trows) {
+static cudaError_t launch_gate_up(const DecodeArgs& a, cudaStream_t st, bool pdl, bool fx, int trows) {
   const DecodePlan& p = a.p;
-  return launch_pdl(dec_gate_up<QT, MAXB>, dim3((unsigned)((p.K * p.F + p.Fs) / GU_VALUES), (unsigned)a.T),
-                    GU_THREADS, (size_t)p.gu_smem, st, pdl, a, trows);
+  const dim3 grid((unsigned)((p.K * p.F + p.Fs) / GU_VALUES), (unsigned)a.T);
+  if (fx) return launch_pdl(dec_gate_up<QT, MAXB, true>, grid, GU_THREADS, (size_t)p.gu_smem, st, pdl, a, trows);
+  return launch_pdl(dec_gate_up<QT, MAXB, false>, grid, GU_THREADS, (size_t)p.gu_smem, st, pdl, a, trows);
 }
 
 template <int QT>
-static cudaError_t launch_down(const DecodeArgs& a, cudaStream_t st, bool pdl, int trows) {
+static cudaError_t launch_down(const DecodeArgs& a, cudaStream_t st, bool pdl, bool fx, int trows) {
   const DecodePlan& p = a.p;
-  return launch_pdl(dec_down<QT>, dim3((unsigned)(p.H / p.dn_rows), (unsigned)a.T), DN_THREADS, (size_t)p.dn_smem,
-                    st, pdl, a, trows);
+  const dim3 grid((unsigned)(p.H / p.dn_rows), (unsigned)a.T);
+  if (fx) return launch_pdl(dec_down<QT, true>, grid, DN_THREADS, (size_t)p.dn_smem, st, pdl, a, trows);
+  return launch_pdl(dec_down<QT, false>, grid, DN_THREADS, (size_t)p.dn_smem, st, pdl, a, trows);
 }
 
 // The chain: router, (several tokens) selection, gate/up in the gate/up rows' block type,
-// down in the down rows' block type.
-cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, int trows) {
+// down in the down rows' block type; `fx` selects the 16-bit fixed-point activations.
+cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, bool fx, int trows) {
   const DecodePlan& p = a.p;
-  cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)0, st, pdl, a, trows);
+  cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)select_smem(p.E), st,
+                             pdl, a, trows);
   if (e != cudaSuccess) return e;
   if (a.T > 1) {  // one selection per token, shared by the gate/up and down CTAs
     e = launch_pdl(dec_select, dim3((unsigned)a.T), 256, (size_t)select_smem(p.E), st, pdl, a);
     if (e != cudaSuccess) return e;
   }
   switch (p.qtype * 8 + maxb) {
-    case 2 * 8 + 1: e = launch_gate_up<2, 1>(a, st, pdl, trows); break;
-    case 2 * 8 + 2: e = launch_gate_up<2, 2>(a, st, pdl, trows); break;
-    case 2 * 8 + 3: e = launch_gate_up<2, 3>(a, st, pdl, trows); break;
-    case 3 * 8 + 1: e = launch_gate_up<3, 1>(a, st, pdl, trows); break;
-    case 3 * 8 + 2: e = launch_gate_up<3, 2>(a, st, pdl, trows); break;
-    case 3 * 8 + 3: e = launch_gate_up<3, 3>(a, st, pdl, trows); break;
-    case 12 * 8 + 1: e = launch_gate_up<12, 1>(a, st, pdl, trows); break;
-    case 12 * 8 + 2: e = launch_gate_up<12, 2>(a, st, pdl, trows); break;
-    case 12 * 8 + 3: e = launch_gate_up<12, 3>(a, st, pdl, trows); break;
+    case 2 * 8 + 1: e = launch_gate_up<2, 1>(a, st, pdl, fx, trows); break;
+    case 2 * 8 + 2: e = launch_gate_up<2, 2>(a, st, pdl, fx, trows); break;
+    case 2 * 8 + 3: e = launch_gate_up<2, 3>(a, st, pdl, fx, trows); break;
+    case 3 * 8 + 1: e = launch_gate_up<3, 1>(a, st, pdl, fx, trows); break;
+    case 3 * 8 + 2: e = launch_gate_up<3, 2>(a, st, pdl, fx, trows); break;
+    case 3 * 8 + 3: e = launch_gate_up<3, 3>(a, st, pdl, fx, trows); break;
+    case 12 * 8 + 1: e = launch_gate_up<12, 1>(a, st, pdl, fx, trows); break;
+    case 12 * 8 + 2: e = launch_gate_up<12, 2>(a, st, pdl, fx, trows); break;
+    case 12 * 8 + 3: e = launch_gate_up<12, 3>(a, st, pdl, fx, trows); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   switch (p.qtype_dn) {
-    case 2: return launch_down<2>(a, st, pdl, trows);
-    case 3: return launch_down<3>(a, st, pdl, trows);
-    case 12: return launch_down<12>(a, st, pdl, trows);
-    case 14: return launch_down<14>(a, st, pdl, trows);
+    case 2: return launch_down<2>(a, st, pdl, fx, trows);
+    case 3: return launch_down<3>(a, st, pdl, fx, trows);
+    case 12: return launch_down<12>(a, st, pdl, fx, trows);
+    case 14: return launch_down<14>(a, st, pdl, fx, trows);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -7,10 +7,11 @@
 
 namespace moe {
 
-// Enqueues the three kernels for one token on `st` (with programmatic dependent
-// launch when `pdl`). `maxb` = blocks per lane of a gate/up row: ceil(H / 1024).
+// Enqueues the decode chain for up to DEC_TMAX tokens on `st` (with programmatic dependent
+// launch when `pdl`). `maxb` = blocks per lane of a gate/up row: ceil(H / 1024). `fx`: the
+// block dots take 16-bit block fixed-point activations instead of f32.
 // The plan's shared-memory sizes and rows per CTA must come from the host planner.
 // With a trace, CTAs with index below `trows` record their timeline.
-cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, int trows);
+cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, bool fx, int trows);
 
 }  // namespace moe

@@ -195,6 +195,24 @@ def token_stream(seed: int, hidden: int, stream: int = 1):
         yield rng.standard_normal(hidden).astype(np.float32)
 
 
+def outlier_channels(hidden: int, seed: int) -> np.ndarray:
+    """One channel index per 32-value block: the channel a heavy-tailed token scales.
+
+    Drawn once from ``default_rng([seed, 999])``, uniform over the block's 32 positions,
+    so every token of a test shares the same outlier channels, as trained models'
+    activations do.
+    """
+    rng = np.random.default_rng([seed, 999])
+    return np.arange(0, hidden, 32) + rng.integers(0, 32, hidden // 32)
+
+
+def with_outliers(x: np.ndarray, factor: float, channels: np.ndarray) -> np.ndarray:
+    """``x`` (f32 [..., H]) with the given channels multiplied by ``factor`` (rounded to f32)."""
+    y = np.array(x, np.float32, copy=True)
+    y[..., channels] *= np.float32(factor)
+    return y
+
+
 def make_tokens(seed: int, hidden: int, n_tokens: int, stream: int = 1) -> np.ndarray:
     """The first ``n_tokens`` draws of :func:`token_stream` as [T][H] f32."""
     it = token_stream(seed, hidden, stream)

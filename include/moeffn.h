@@ -80,6 +80,8 @@ extern "C" {
 #define MOE_NO_PDL 8u     /* launch without programmatic dependent launch             */
 #define MOE_TRACE 16u     /* record a per-CTA timeline in the workspace (see below)   */
 #define MOE_BATCHED 32u   /* take the batched path whatever the token count           */
+#define MOE_FIXED_POINT 64u /* decode chain: block dots on 16-bit block fixed-point
+                             * activations (dp4a) instead of f32 (see below)           */
 
 enum {
   MOE_OK = 0,
@@ -214,23 +216,25 @@ int moe_workspace_status(void* workspace, void* stream);
  * asynchronous on `stream`. Returns MOE_OK or MOE_ERR_NULL_PTR / MOE_ERR_CUDA. */
 int moe_selftest_timeout(void* workspace, void* stream);
 
-/* The step for callers that cannot allocate memory: no cudaMalloc, cudaFree or
- * other allocating call is made, on the device or on the host. Such callers
- * include code that runs where an allocator may not be entered (inside another
- * allocator's hooks, in a real-time or signal context, under a memory budget
- * that has already been handed out) or that has no allocator of its own to lend
- * a workspace. The pages have no counterpart: their engines own every buffer.
- * The scratch lives in a fixed device array of 512 KiB compiled into the
- * library; every device that loads the library holds it until the process
- * exits, and every call on a device shares it, so calls whose work overlaps on
- * the GPU (other streams, other threads) race and must not be made. The first
- * call on a device looks the array's address up once (make it before any stream
- * capture). Tokens are decoded one at a time; a token's scratch (control block,
- * logits and SwiGLU activations) is at most 405 KiB for every
- * layer the configuration checks admit, and a layer that needed more would be
- * rejected with MOE_ERR_UNSUPPORTED. Device buffers only: MOE_HOST_IO
- * and MOE_TRACE are rejected. Blocking: returns after the step has finished on
- * `stream` (a cudaStream_t, NULL = legacy default stream), with device-side
+/* The step for callers that cannot allocate memory: the call makes no cudaMalloc,
+ * cudaFree or other allocating call, on the device or on the host. Such callers include
+ * code that runs where an allocator may not be entered (inside another allocator's hooks,
+ * in a real-time or signal context, under a memory budget that has already been handed
+ * out) or that has no allocator of its own to lend a workspace. The pages have no
+ * counterpart: their engines own every buffer.
+ * The scratch lives in a fixed device array of 512 KiB compiled into the library; every
+ * device that loads the library holds it until the process exits, and every call on a
+ * device shares it, so calls whose work overlaps on the GPU (other streams, other
+ * threads) race and must not be made. Each call looks the array's device address up
+ * afresh. CUDA loads the library's kernels and this array onto a device on first use,
+ * and that loading may itself allocate device memory: make the first call on each device
+ * before the stretch in which nothing may be allocated, and before any stream capture.
+ * Up to 16 tokens are decoded per launch, as many as the array holds the scratch of
+ * (control block, logits and SwiGLU activations); one token of the largest layer the
+ * configuration checks admit needs about 401 KiB, so every admitted layer runs, and a
+ * layer that needed more would be rejected with MOE_ERR_UNSUPPORTED. Device buffers
+ * only: MOE_HOST_IO and MOE_TRACE are rejected. Blocking: returns after the step has
+ * finished on `stream` (a cudaStream_t, NULL = legacy default stream), with device-side
  * errors reported directly. Arguments otherwise as moe_ffn_forward. */
 int moe_ffn_forward_noalloc(const float* x, const float* router_w, const float* router_bias,
                             const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg,

@@ -47,14 +47,18 @@ def selection_gap(s: np.ndarray, w: dict) -> float:
     return float(min(gaps)) if gaps else np.inf
 
 
-def margin_tokens(layer: dict, w: dict, n: int, seed: int, stream: int = 1, norm=None, scale: float = 1.0):
-    """n tokens from the seeded stream (times `scale`), skipping draws within MARGIN of a
-    tie; with a prologue norm vector the routing is that of the normalised token."""
+def margin_tokens(layer: dict, w: dict, n: int, seed: int, stream: int = 1, norm=None, scale: float = 1.0,
+                  transform=None):
+    """n tokens from the seeded stream (times `scale`, then through `transform` if given),
+    skipping draws within MARGIN of a tie; with a prologue norm vector the routing is that
+    of the normalised token."""
     cfg = oracle_cfg(w)
     it = synth.token_stream(seed, w["hidden"], stream)
     out, redraws = [], 0
     while len(out) < n:
         x = (next(it) * np.float32(scale)).astype(np.float32)
+        if transform is not None:
+            x = transform(x)
         xr = x if norm is None else mo.rms_norm(x, norm, cfg.rms_eps)
         _, _, s = mo.route(xr, layer["router_w"], layer["bias"], cfg)
         if selection_gap(s[0], w) >= MARGIN:

@@ -41,17 +41,23 @@ def layer_of(name):
 DECODE = ["tiny_q4_0_t4", "flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1"]
 
 
+FIXED = 64  # MOE_FIXED_POINT: the decode chain's 16-bit block fixed-point activations
+
+
+@pytest.mark.parametrize("flags", [0, FIXED], ids=["f32", "fixed"])
 @pytest.mark.parametrize("name", DECODE)
-def test_workload_parity(name):
+def test_workload_parity(name, flags):
     w, layer = layer_of(name)
     T = w["n_tokens"]
     x, _ = margin_tokens(layer, w, T, seed=w["seed"])
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
     g = GpuLayer(layer, w)
-    out, ids, wts = g.run(x)
+    out, ids, wts = g.run(x, flags=flags)
     err = compare(out, ids, wts, ref, rid, rwt, name)
-    print(f"{name}: max rel-L2 {err:.3e}")
+    for t in range(T):  # and one token per call
+        compare(*g.run(x[t:t + 1], flags=flags), ref[t:t + 1], rid[t:t + 1], rwt[t:t + 1], f"{name} token {t}")
+    print(f"{name} ({'fixed point' if flags else 'f32'}): max rel-L2 {err:.3e}")
 
 
 @pytest.mark.parametrize("name", DECODE[1:])
@@ -95,8 +101,12 @@ def test_random_shapes(w):
     x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
-    out, ids, wts = GpuLayer(layer, w).run(x)
-    compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']}")
+    g = GpuLayer(layer, w)
+    for flags in (0, FIXED):
+        out, ids, wts = g.run(x, flags=flags)
+        compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']} flags {flags}")
+        o1, i1, w1 = g.run(x[:1], flags=flags)
+        compare(o1, i1, w1, ref[:1], rid[:1], rwt[:1], f"seed {w['seed']} flags {flags} one token")
 
 
 CLAMP = [

@@ -181,25 +181,18 @@ def test_prefill_flags_and_determinism():
     assert np.array_equal(po.numpy(), acc)
 
 
-def test_flint_prefill_t512_sampled():
-    # the full Flint-shaped batch: every token's picks and weights against the oracle's
-    # routing, and the outputs of a spread of sampled tokens against the oracle's step
+def test_flint_prefill_t512_all_tokens():
+    # the full Flint-shaped batch, every token against the oracle: its picks and weights, and
+    # its output element by element (relative L2 per token), as every parity test does
     w = synth.WORKLOADS["flint_prefill_t512"]
     layer = synth.make_layer(w)
     T = w["n_tokens"]
     x, _ = margin_tokens(layer, w, T, seed=w["seed"])
-    cfg = oracle_cfg(w)
-    rid, rwt, _ = mo.route(x, layer["router_w"], layer["bias"], cfg)
     out, ids, wts = GpuLayer(layer, w).run(x, flags=BATCHED)
-    assert np.array_equal(ids, rid)
-    assert np.max(np.abs(wts - rwt) / np.abs(rwt)) <= 1e-5
-    assert np.all(np.isfinite(out))
-    sample = [0, 1, 63, 127, 128, 200, 255, 256, 383, 400, 510, 511]
-    for t in sample:
-        ref, _, _ = mo.moe_ffn(x[t:t + 1], layer["router_w"], layer["bias"], layer["expert_blocks"],
-                               layer["shared_blocks"], cfg)
-        e = rel_l2(out[t], ref[0])
-        assert e <= 2e-3, f"token {t}: rel-L2 {e}"
+    ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                               layer["shared_blocks"], oracle_cfg(w))
+    err = compare(out, ids, wts, ref, rid, rwt, "flint T=512")
+    print(f"flint_prefill_t512: all {T} tokens, max rel-L2 {err:.3e}")
 
 
 def test_prefill_matches_decode_path():

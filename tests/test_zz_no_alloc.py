@@ -3,9 +3,11 @@
 Some callers may not enter any allocator (for example code running inside another
 allocator's hooks, in a real-time path, or under a memory budget already handed
 out), so they cannot provide a workspace. This entry point runs the same decode
-kernels on a fixed scratch array compiled into the library. These tests check it
-against the workspace entry point through the C ABI, on two calls in a row (the
-second call reuses the scratch the first left behind).
+kernels on a fixed scratch array compiled into the library. These tests call it
+through the C ABI on two calls in a row (the second call reuses the scratch the
+first left behind) and check each call against the float64 oracle and, bit for bit,
+against the workspace entry point, which runs the same kernels with the same
+arithmetic.
 
 This file is collected last on purpose: a run that stops at the first failure has
 then already run every other test.
@@ -18,7 +20,8 @@ import pytest
 
 import expert_ffn_decode_gb300 as ffn
 from expert_ffn_decode_gb300 import synth
-from tests.helpers import OUT_REL_L2, GpuLayer, margin_tokens, rel_l2
+from oracle import moe_oracle as mo
+from tests.helpers import OUT_REL_L2, GpuLayer, compare, margin_tokens, oracle_cfg, rel_l2
 
 
 def _built():
@@ -47,22 +50,27 @@ def test_noalloc_scratch_holds_the_largest_layer_and_rejects_workspace_flags():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("flags", [0, ffn.MOE_FIXED_POINT], ids=["f32", "fixed"])
 @pytest.mark.parametrize("name", ["flint_decode_t1", "tiny_q4_0_t4"])
-def test_noalloc_matches_workspace_entry_point_twice(name):
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name, flags):
     import torch
     _built()
     w = synth.WORKLOADS[name]
     layer = synth.make_layer(w)
     g = GpuLayer(layer, w)
     T = max(2, w["n_tokens"])
+    cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": flags})
     for call in range(2):
         x, _ = margin_tokens(layer, w, T, seed=w["seed"], stream=20 + call)
-        want, _, _ = g.run(x)  # moe_ffn_forward_ex with a workspace
-        cfg = ffn.make_cfg(**{**w, "n_tokens": T})
+        ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
+                                   layer["shared_blocks"], oracle_cfg(w))
+        want, ids, wts = g.run(x, flags=flags)  # moe_ffn_forward_ex with a workspace
+        compare(want, ids, wts, ref, rid, rwt, f"{name} workspace call {call}")
         xd = torch.from_numpy(x).cuda()
         out = torch.full_like(xd, float("nan"))
         ffn.check(ffn.moe_ffn_forward_noalloc(xd, g.router_w, g.bias, g.experts, g.shared, cfg, out,
                                               torch.cuda.current_stream()))
         got = out.cpu().numpy()
         for t in range(T):
-            assert rel_l2(got[t], want[t]) <= OUT_REL_L2, (name, call, t)
+            assert rel_l2(got[t], ref[t]) <= OUT_REL_L2, (name, call, t)
+        assert np.array_equal(got, want), (name, call)
