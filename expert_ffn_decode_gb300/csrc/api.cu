@@ -115,7 +115,9 @@ int check_cfg(const moe_cfg* c) {
 
 // ---- workspace layout -----------------------------------------------------------
 struct WsLayout {
-  size_t ctrl, logits, act, ids, wts, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
+  size_t ctrl, logits, act, ids, wts, pub, x_stage, out_stage, ids_stage, w_stage, trace, xn, prefill, total;
+  int rep;                    // copies of the decode chain's broadcast arrays
+  size_t lg_copy, act_copy;   // floats from one copy to the next
 };
 
 // SMs of the current device (the timeline keeps one row per SM); without a
@@ -148,22 +150,29 @@ int decode_call_tokens(const moe_cfg* c) {
 }
 
 // decode_only: the layout of calls that always decode (moe_ffn_forward_noalloc), up
-// to DEC_TMAX tokens at a time and without the batched path's regions.
-WsLayout ws_layout(const moe_cfg* c, bool decode_only = false) {
+// to DEC_TMAX tokens at a time and without the batched path's regions. `rep`: copies of
+// the decode chain's broadcast arrays.
+WsLayout ws_layout(const moe_cfg* c, bool decode_only = false, int rep = moe::DEC_REP) {
   WsLayout L;
   size_t o = 0;
   L.ctrl = o;
   o += moe::CTRL_BYTES;
   const size_t td = decode_only ? (size_t)(c->n_tokens < moe::DEC_TMAX ? c->n_tokens : moe::DEC_TMAX)
                                 : (size_t)decode_call_tokens(c);  // tokens of one decode call
-  L.logits = o;  // decode: router logits [td][E] f32
-  o = up256(o + td * c->n_experts * 4);
-  L.act = o;     // decode: SwiGLU activations of every slot [td][K * F + Fs] f32
-  o = up256(o + td * ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4);
-  L.ids = o;     // decode: picks and weights [td][K]
+  // decode: `rep` copies of the arrays every CTA reads, each copy 256-byte aligned
+  L.rep = rep;
+  L.lg_copy = up256(td * c->n_experts * 4) / 4;
+  L.act_copy = up256(td * ((size_t)c->top_k * c->expert_ff + c->shared_ff) * 4) / 4;
+  L.logits = o;  // router logits [rep][td][E] f32
+  o += (size_t)rep * L.lg_copy * 4;
+  L.act = o;     // SwiGLU activations of every slot [rep][td][K * F + Fs] f32
+  o += (size_t)rep * L.act_copy * 4;
+  L.ids = o;     // decode: picks and weights [td][K] (calls of several tokens)
   o = up256(o + td * c->top_k * 4);
   L.wts = o;
   o = up256(o + td * c->top_k * 4);
+  L.pub = o;     // decode: the picks a single-token call publishes for its down kernel [K] u64
+  o = up256(o + (size_t)c->top_k * 8);
   const size_t T = (size_t)c->n_tokens;
   L.x_stage = L.out_stage = L.ids_stage = L.w_stage = 0;
   if (c->flags & MOE_HOST_IO) {
@@ -212,7 +221,7 @@ bool same_shape(const moe_cfg& a, const moe_cfg& b) {
   return a.hidden == b.hidden && a.n_experts == b.n_experts && a.top_k == b.top_k &&
          a.expert_ff == b.expert_ff && a.shared_ff == b.shared_ff && a.n_groups == b.n_groups &&
          (a.n_groups == 1 || a.groups_used == b.groups_used) && a.qtype == b.qtype &&
-         down_type(&a) == down_type(&b);
+         down_type(&a) == down_type(&b) && (a.flags & MOE_FIXED_POINT) == (b.flags & MOE_FIXED_POINT);
 }
 
 int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
@@ -235,18 +244,21 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.nbFs = p.Fs / 32;
   p.nact = p.nbFs + p.K * p.nbF;
   p.act_stride = p.K * p.F + p.Fs;
+  p.rep = moe::DEC_REP;
   const uint32_t budget = 200u * 1024u;  // dynamic shared memory of one CTA
+  // shared bytes per 32-value activation block: f32 chunks and sum, or fixed-point planes and info
+  const uint32_t blk = (c->flags & MOE_FIXED_POINT) ? moe::ACT_BLOCK_SMEM_FX : moe::ACT_BLOCK_SMEM;
   // gate/up: 4 windows of 8 rows, the x blocks and the selection
   p.gu_win = moe::window_bytes(8u * p.rb_h);
-  p.gu_smem = 4u * p.gu_win + (uint32_t)p.nbH * moe::ACT_BLOCK_SMEM;
+  p.gu_smem = 4u * p.gu_win + (uint32_t)p.nbH * blk + moe::select_smem(p.E);
   if (p.gu_smem > budget) return fail(MOE_ERR_UNSUPPORTED, "gate/up rows too long for shared memory");
   // down: the activation blocks in one piece when they fit in 40 KiB, else pieces of
   // 256; then as many rows per CTA (8, 4, 2, 1) as the windows allow
-  p.dn_piece = (size_t)p.nact * moe::ACT_BLOCK_SMEM <= 40 * 1024 ? p.nact : 256;
+  p.dn_piece = (size_t)p.nact * blk <= 40 * 1024 ? p.nact : 256;
   for (p.dn_rows = 8; p.dn_rows >= 1; p.dn_rows /= 2) {
     p.dn_win_f = moe::window_bytes((uint32_t)p.dn_rows * p.rb_f);
     p.dn_win_fs = p.Fs ? moe::window_bytes((uint32_t)p.dn_rows * p.rb_fs) : 0u;
-    p.dn_smem = p.dn_win_fs + (uint32_t)p.K * p.dn_win_f + (uint32_t)p.dn_piece * moe::ACT_BLOCK_SMEM;
+    p.dn_smem = p.dn_win_fs + (uint32_t)p.K * p.dn_win_f + (uint32_t)p.dn_piece * blk + moe::select_smem(p.E);
     if (p.dn_smem <= budget) break;
   }
   if (p.dn_rows < 1) return fail(MOE_ERR_UNSUPPORTED, "down rows too long for shared memory");
@@ -468,8 +480,11 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<float*>(wsb + W.logits);
   a.act = reinterpret_cast<float*>(wsb + W.act);
+  a.lg_copy = W.lg_copy;
+  a.act_copy = W.act_copy;
   a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
   a.wts = reinterpret_cast<float*>(wsb + W.wts);
+  a.pub = reinterpret_cast<unsigned long long*>(wsb + W.pub);
   a.trace = (c->flags & MOE_TRACE) ? reinterpret_cast<unsigned long long*>(wsb + W.trace) : nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -479,6 +494,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   a.eps = c->rms_eps;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
+  a.p.rep = W.rep;
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
   const int td = decode_call_tokens(c);
   for (int t = 0; t < T && !prefill_pass_tokens(c); t += td) {
@@ -668,14 +684,18 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     const char* oa = reinterpret_cast<const char*>(out);
     if (xa < oa + xbytes && oa < xa + xbytes) return fail(MOE_ERR_INVALID_CFG, "x and out overlap");
   }
-  // the calls decode up to td tokens at a time: as many as the fixed scratch holds
+  // the calls decode up to td tokens at a time with `rep` copies of the broadcast arrays:
+  // the most copies for which one token's scratch fits, then as many tokens as fit
   moe_cfg c1 = *c;
-  int td = T < moe::DEC_TMAX ? T : moe::DEC_TMAX;
-  for (;; --td) {
+  int td = 1, rep = moe::DEC_REP;
+  c1.n_tokens = 1;
+  while (rep > 1 && ws_layout(&c1, true, rep).total > NOALLOC_SCRATCH_BYTES) --rep;
+  for (td = T < moe::DEC_TMAX ? T : moe::DEC_TMAX; td > 1; --td) {
     c1.n_tokens = td;
-    if (td == 1 || ws_layout(&c1, true).total <= NOALLOC_SCRATCH_BYTES) break;
+    if (ws_layout(&c1, true, rep).total <= NOALLOC_SCRATCH_BYTES) break;
   }
-  const WsLayout W = ws_layout(&c1, true);
+  c1.n_tokens = td;
+  const WsLayout W = ws_layout(&c1, true, rep);
   if (W.total > NOALLOC_SCRATCH_BYTES)
     return fail(MOE_ERR_UNSUPPORTED,
                 "this layer needs %zu bytes of scratch; the fixed scratch of moe_ffn_forward_noalloc holds %zu",
@@ -699,8 +719,11 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.ctrl = reinterpret_cast<uint32_t*>(wsb + W.ctrl);
   a.logits = reinterpret_cast<float*>(wsb + W.logits);
   a.act = reinterpret_cast<float*>(wsb + W.act);
+  a.lg_copy = W.lg_copy;
+  a.act_copy = W.act_copy;
   a.ids = reinterpret_cast<int32_t*>(wsb + W.ids);
   a.wts = reinterpret_cast<float*>(wsb + W.wts);
+  a.pub = reinterpret_cast<unsigned long long*>(wsb + W.pub);
   a.trace = nullptr;
   a.scale = c->weights_scale;
   a.norm_min = c->norm_min;
@@ -710,6 +733,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
   a.eps = c->rms_eps;
   a.flags = c->flags & (MOE_ACCUMULATE | MOE_RESIDUAL);
   a.p = pe.plan;
+  a.p.rep = W.rep;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool pdl = (c->flags & MOE_NO_PDL) == 0;
   for (int t = 0; t < T; t += td) {

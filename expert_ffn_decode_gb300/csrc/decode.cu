@@ -105,14 +105,13 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
 // Quantise blocks [0, nb) of an f32 vector (global memory, or shared memory when
 // kShared) as quant_task describes; with `mul`, value i is first multiplied by
 // scal * mul[i]. With `ss`, the thread adds the squares of the values it loaded (before
-// any multiplication) to *ss. Each thread takes four tasks a round and loads all of them
+// any multiplication) to *ss. Each thread takes TPR tasks a round and loads all of them
 // before computing; every thread runs the same number of rounds and whole warps call it
-// (the groups use shuffles).
-template <bool kShared = false>
+// (the groups use shuffles). TPR: tasks a thread loads per round.
+template <int TPR, bool kShared = false>
 __device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float2* info,
                                              int t, int nthreads, const float* mul = nullptr, float scal = 1.f,
                                              float* ss = nullptr) {
-  constexpr int TPR = 4;  // tasks per thread and round
   #pragma unroll 1
   for (int base = 0; base < 4 * nb; base += TPR * nthreads) {
     float4 va[TPR], vc[TPR], ma[TPR], mc[TPR];
@@ -129,19 +128,28 @@ __device__ __forceinline__ void quant_blocks(const float* src, int nb, int strid
       ma[h] = (mul && ok) ? __ldg(reinterpret_cast<const float4*>(mul + off)) : one;
       mc[h] = (mul && ok) ? __ldg(reinterpret_cast<const float4*>(mul + off) + 1) : one;
     }
-#pragma unroll
+    // one task a pass, the rest moved down a slot: a single copy of the task's code
+    #pragma unroll 1
     for (int h = 0; h < TPR; ++h) {
-      float v[8] = {va[h].x, va[h].y, va[h].z, va[h].w, vc[h].x, vc[h].y, vc[h].z, vc[h].w};
+      float v[8] = {va[0].x, va[0].y, va[0].z, va[0].w, vc[0].x, vc[0].y, vc[0].z, vc[0].w};
       if (ss) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) *ss = fmaf(v[i], v[i], *ss);
       }
       if (mul) {
-        const float mm[8] = {ma[h].x, ma[h].y, ma[h].z, ma[h].w, mc[h].x, mc[h].y, mc[h].z, mc[h].w};
+        const float mm[8] = {ma[0].x, ma[0].y, ma[0].z, ma[0].w, mc[0].x, mc[0].y, mc[0].z, mc[0].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = v[i] * scal * mm[i];
       }
-      quant_task(v, idx[h] < 4 * nb, idx[h] >> 2, idx[h] & 3, stride, planes, info);
+      quant_task(v, idx[0] < 4 * nb, idx[0] >> 2, idx[0] & 3, stride, planes, info);
+#pragma unroll
+      for (int k = 0; k + 1 < TPR; ++k) {
+        va[k] = va[k + 1];
+        vc[k] = vc[k + 1];
+        ma[k] = ma[k + 1];
+        mc[k] = mc[k + 1];
+        idx[k] = idx[k + 1];
+      }
     }
   }
 }
@@ -553,9 +561,10 @@ __device__ __forceinline__ void sort_list(uint32_t (&kv)[N], int (&ki)[N]) {
 //   2. groups (n_groups > 1): each warp scores groups (the two largest s, summed);
 //      warp 0 keeps groups_used of them, the largest score first, the lowest group
 //      on ties; the keys of the other groups' experts become 0
-//   3. k <= 8: tau = the k-th largest of the 8 warps' largest keys. At least k keys reach
-//      tau, so every pick does: the keys >= tau are gathered (typically little more than
-//      k of them) and each takes its rank among them; ranks below k are the picks.
+//   3. k <= 8: tau = the k-th largest of the 16 keys that are some warp's largest or second
+//      largest. At least k keys reach tau, so every pick does: the keys >= tau are gathered
+//      (typically little more than k of them) and each takes its rank among them; ranks
+//      below k are the picks.
 //   4. otherwise (or when more than 256 keys reach tau, i.e. many exact ties): each warp
 //      takes its top k in k rounds over the lanes' sorted lists, then warp 0 merges the 8
 //      sorted candidate lists in k rounds
@@ -572,7 +581,8 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
   uint32_t* ckey = reinterpret_cast<uint32_t*>(sel + (size_t)p.E * 8);
   int* cidx = reinterpret_cast<int*>(sel + (size_t)p.E * 8 + 1024);
   __shared__ unsigned long long kept_groups;
-  __shared__ uint32_t wmax[8];
+  __shared__ uint32_t wtop[16];
+  __shared__ uint32_t tau_s;
   __shared__ int wcnt[8];
   uint32_t kv[N];  // this thread's keys: experts tid + 256 i
   {
@@ -655,25 +665,43 @@ __device__ void select_picks_n(const DecodeArgs& a, const float* lg, uint8_t* se
       if (e < p.E && !((kg >> g) & 1ull)) kv[i] = 0u;
     }
   }
-  uint32_t m = 0u;
+  // each warp's two largest keys (as a multiset: the lane holding the largest offers its
+  // next one)
+  {
+    uint32_t m1 = 0u, m2 = 0u;
 #pragma unroll
-  for (int i = 0; i < N; ++i) m = kv[i] > m ? kv[i] : m;
-  m = __reduce_max_sync(0xffffffffu, m);
-  if (lane == 0) wmax[warp] = m;
+    for (int i = 0; i < N; ++i) {
+      if (kv[i] > m1) {
+        m2 = m1;
+        m1 = kv[i];
+      } else if (kv[i] > m2) {
+        m2 = kv[i];
+      }
+    }
+    const uint32_t w1 = __reduce_max_sync(0xffffffffu, m1);
+    const int hl = __ffs(__ballot_sync(0xffffffffu, m1 == w1)) - 1;
+    const uint32_t w2 = __reduce_max_sync(0xffffffffu, lane == hl ? m2 : m1);
+    if (lane == 0) {
+      wtop[2 * warp] = w1;
+      wtop[2 * warp + 1] = w2;
+    }
+  }
   __syncthreads();
   bool pruned = p.K <= 8;
   if (pruned) {
-    uint32_t wm[8];
-#pragma unroll
-    for (int w = 0; w < 8; ++w) wm[w] = wmax[w];
-    uint32_t tau = 0u;  // the k-th largest warp maximum
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    // tau: the k-th largest of the 16 warp top-two keys (lane l < 16 ranks entry l)
+    if (warp == 0) {
+      const uint32_t v = lane < 16 ? wtop[lane] : 0u;
       int rank = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rank += (wm[i] > wm[j] || (wm[i] == wm[j] && i < j)) ? 1 : 0;
-      if (rank == p.K - 1) tau = wm[j];
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t o = __shfl_sync(0xffffffffu, v, i);
+        rank += (o > v || (o == v && i < lane)) ? 1 : 0;
+      }
+      if (lane < 16 && rank == p.K - 1) tau_s = v;
     }
+    __syncthreads();
+    const uint32_t tau = tau_s;
     unsigned bal[N];
     int cnt = 0;
 #pragma unroll
@@ -783,19 +811,10 @@ __device__ __forceinline__ void select_picks(const DecodeArgs& a, const float* l
 // ===========================================================================
 // Router: logits
 // ===========================================================================
-// A single-token call also makes the token's picks here, once: every CTA writes its logits
-// and then takes a ticket (an atomic count in the control block); the CTA that takes the
-// last ticket sees every logit, selects, writes the picks and weights for the gate/up and
-// down kernels, and returns the count to 0 for the next call. Nothing waits on the count.
-// Dynamic shared memory: the selection's (select_smem).
+// The logits go to every copy of the logits array (the consumers read copy blockIdx.x % rep).
 __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int trows) {
-  extern __shared__ __align__(16) uint8_t rsm[];
   __shared__ float part[RT_THREADS / 32][DEC_TMAX];
   __shared__ float red[RT_THREADS / 32][DEC_TMAX];  // sums of squares (with a norm vector)
-  __shared__ float gscore[64];
-  __shared__ int rids[32];
-  __shared__ float rw[32];
-  __shared__ int last;
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   tr(a, TR_RT_START, trows);
@@ -820,6 +839,9 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
   pdl_wait_prior_grids();  // x may come from the previous kernel
   pdl_launch_dependents();
   tr(a, TR_RT_X, trows);
+  // this call's published picks start empty (the previous call's kernels are complete:
+  // the wait above covers them, and every reader of this call starts after this grid)
+  if (a.T == 1 && blockIdx.x == 0 && tid < p.K) st_relaxed_u64(a.pub + tid, PUB_EMPTY);
   // the prologue (with a norm vector): token t's input is x_t * r_t * norm, r_t =
   // 1/rms(x_t). The dot takes x_t * norm and its sum is scaled by r_t; the sum of squares
   // comes from the same loads (a row's four quarter warps cover x_t once).
@@ -856,27 +878,10 @@ __global__ void __launch_bounds__(RT_THREADS) dec_router(const DecodeArgs a, int
         const float sq = ((red[4 * rr][t] + red[4 * rr + 1][t]) + red[4 * rr + 2][t]) + red[4 * rr + 3][t];
         v *= 1.f / sqrtf(sq / (float)p.H + a.eps);
       }
-      a.logits[(size_t)t * p.E + row2] = v;
-      if (a.T == 1) __threadfence();  // the logit is visible before this CTA's ticket
+      for (int c = 0; c < p.rep; ++c) a.logits[(size_t)c * a.lg_copy + (size_t)t * p.E + row2] = v;
     }
   }
   tr(a, TR_RT_DONE, trows);
-  if (a.T == 1) {
-    __syncthreads();
-    if (tid == 0) last = atomicAdd(a.ctrl + CTRL_TICKET, 1u) == gridDim.x - 1u;
-    __syncthreads();
-    if (last) {
-      __threadfence();
-      select_picks(a, a.logits, rsm, gscore, rids, rw, trows);
-      if (tid < p.K) {
-        a.ids[tid] = rids[tid];
-        a.wts[tid] = rw[tid];
-        if (a.topk_ids) a.topk_ids[tid] = rids[tid];
-        if (a.topk_w) a.topk_w[tid] = rw[tid];
-      }
-      if (tid == 0) a.ctrl[CTRL_TICKET] = 0u;  // the next call's routers count after this grid ends
-    }
-  }
 }
 
 // ===========================================================================
@@ -890,7 +895,7 @@ __global__ void __launch_bounds__(256) dec_select(const DecodeArgs a) {
   const int t = blockIdx.x;
   pdl_wait_prior_grids();  // the logits
   pdl_launch_dependents();
-  select_picks(a, a.logits + (size_t)t * a.p.E, ssm, gscore, rids, rw);
+  select_picks(a, a.logits + (size_t)(t % a.p.rep) * a.lg_copy + (size_t)t * a.p.E, ssm, gscore, rids, rw);
   if (threadIdx.x < a.p.K) {
     const size_t o = (size_t)t * a.p.K + threadIdx.x;
     a.ids[o] = rids[threadIdx.x];
@@ -911,11 +916,14 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   extern __shared__ __align__(128) uint8_t gsm[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ float rowdot[GU_THREADS / 32][4];
+  __shared__ float gscore[64];
+  __shared__ int rids[32];
+  __shared__ float rw[32];
   const DecodePlan& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int v0 = blockIdx.x * GU_VALUES;  // first activation index of the CTA
   const int tok = blockIdx.y;             // the call's token
-  const float* xt = a.x + (size_t)tok * p.H;
+  const int cp = blockIdx.x % p.rep;      // the copy of the logits this CTA reads
   const bool shared = v0 < p.Fs;          // the shared expert's values need no routing
   const int ff = shared ? p.Fs : p.F;
   const int f0 = shared ? v0 : (v0 - p.Fs) % p.F;
@@ -925,6 +933,7 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   float2* xinfo = reinterpret_cast<float2*>(xplanes + (size_t)p.nbH * 64);
   float4* xs = reinterpret_cast<float4*>(xplanes);
   float* xsum = reinterpret_cast<float*>(xplanes + (size_t)p.nbH * 128);
+  uint8_t* sel = xplanes + (size_t)p.nbH * (FX ? ACT_BLOCK_SMEM_FX : ACT_BLOCK_SMEM);
   const uint32_t rows8 = 8u * p.rb_h;
   if (tid == 0) {
     mbar_init(&bars[0], 2);
@@ -940,33 +949,16 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
     mbar_arrive_expect_tx(&bars[c], window_span(src, rows8));
     copy_window(win + (size_t)tid * p.gu_win, src, rows8, &bars[c], policy_evict_first());
   };
-  const uint8_t* rec = a.shared;
-  if (shared) {
-    if (tid < 4) issue(a.shared);
-    pdl_launch_dependents();
-  } else {
-    // the picks: made by the router kernel (one token) or by the selection kernel
-    pdl_wait_prior_grids();
-    pdl_launch_dependents();
-    tr(a, TR_GU_WAITED, trows);
-    const int slot = (v0 - p.Fs) / p.F;
-    int e = __ldcg(a.ids + (size_t)tok * p.K + slot);
-    if ((unsigned)e >= (unsigned)p.E) {  // only a workspace that was not zeroed before its first use
-      if (tid == 0) atomicOr(a.ctrl + CTRL_STATUS, DEV_ERR_BAD_PICK);
-      e = 0;
-    }
-    rec = a.experts + (size_t)e * p.rec_bytes;
-    if (tid < 4) issue(rec);
-  }
-  tr(a, TR_GU_PICKED, trows);
-  // x -> activation blocks while the rows are copied in (x is complete: the router kernel
-  // waited for it before this launch was triggered). With a norm vector the blocks hold
-  // x * norm; r = 1/rms(x) comes from the same loads and scales the row dots (every dot is
-  // linear in x).
+  if (shared && tid < 4) issue(a.shared);
+  // x -> activation blocks (x is complete: the router kernel waited for it before this
+  // launch was triggered); routed CTAs do this while the router kernel runs. With a norm
+  // vector the blocks hold x * norm; r = 1/rms(x) comes from the same loads and scales the
+  // row dots (every dot is linear in x).
+  const float* xt = a.x + (size_t)tok * p.H;
   __shared__ float red[GU_THREADS / 32];
   {
     float ss = 0.f;
-    if constexpr (FX) quant_blocks(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, 1.f, a.norm ? &ss : nullptr);
+    if constexpr (FX) quant_blocks<2>(xt, p.nbH, p.nbH, xplanes, xinfo, tid, GU_THREADS, a.norm, 1.f, a.norm ? &ss : nullptr);
     else store_blocks_f32<4>(xt, p.nbH, p.nbH, xs, xsum, tid, GU_THREADS, a.norm, a.norm ? &ss : nullptr);
     if (a.norm) {
       ss = warp_sum(ss);
@@ -982,6 +974,37 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
     r = 1.f / sqrtf(tot / (float)p.H + a.eps);
   }
   tr(a, TR_GU_XQ, trows);
+  const uint8_t* rec = a.shared;
+  if (shared) {
+    pdl_launch_dependents();
+  } else {
+    pdl_wait_prior_grids();  // the logits
+    tr(a, TR_GU_WAITED, trows);
+    const int slot = (v0 - p.Fs) / p.F;
+    if (a.T == 1) {
+      select_picks(a, a.logits + (size_t)cp * a.lg_copy, sel, gscore, rids, rw, trows);
+      if (v0 == p.Fs && tid < p.K) {  // one CTA reports the picks
+        if (a.topk_ids) a.topk_ids[tid] = rids[tid];
+        if (a.topk_w) a.topk_w[tid] = rw[tid];
+        // for down CTAs that start after this point: one 64-bit store per pick
+        st_relaxed_u64(a.pub + tid, (unsigned long long)(uint32_t)rids[tid] |
+                                        ((unsigned long long)__float_as_uint(rw[tid]) << 32));
+      }
+      rec = a.experts + (size_t)rids[slot] * p.rec_bytes;
+    } else {
+      int e = __ldcg(a.ids + (size_t)tok * p.K + slot);  // made by the selection kernel
+      if ((unsigned)e >= (unsigned)p.E) {  // only a workspace that was not zeroed before its first use
+        if (tid == 0) atomicOr(a.ctrl + CTRL_STATUS, DEV_ERR_BAD_PICK);
+        e = 0;
+      }
+      rec = a.experts + (size_t)e * p.rec_bytes;
+    }
+    if (tid < 4) issue(rec);
+    // the down kernel may start once every CTA is here: by then the picks are published
+    // (its CTAs that still find them missing select for themselves)
+    pdl_launch_dependents();
+  }
+  tr(a, TR_GU_PICKED, trows);
   const RowMap mh = row_map(p.nbH, lane);
   ActBlock xc[FX ? MAXB : 1];
   if constexpr (FX) {
@@ -1050,9 +1073,11 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
     }
   }
   __syncwarp();
-  if (lane < 2)
-    a.act[(size_t)tok * p.act_stride + v0 + 2 * warp + lane] =
+  if (lane < 2) {
+    const float act =
         swiglu_act(rowdot[warp][2 * lane] * r, rowdot[warp][2 * lane + 1] * r, shared ? a.lim_s : a.lim);
+    for (int c = 0; c < p.rep; ++c) a.act[(size_t)c * a.act_copy + (size_t)tok * p.act_stride + v0 + 2 * warp + lane] = act;
+  }
   tr(a, TR_GU_END, trows);
 }
 
@@ -1069,6 +1094,7 @@ template <int QT, bool FX>
 __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int trows) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ __align__(8) uint64_t bar;
+  __shared__ float gscore[64];
   __shared__ int rids[32];
   __shared__ float rw[32];
   __shared__ uint32_t woff[33];  // offset of each window's first row in the window
@@ -1084,22 +1110,39 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   float2* ainfo = reinterpret_cast<float2*>(aplanes + (size_t)p.dn_piece * 64);
   float4* axs = reinterpret_cast<float4*>(aplanes);
   float* axsum = reinterpret_cast<float*>(aplanes + (size_t)p.dn_piece * 128);
+  uint8_t* sel = aplanes + (size_t)p.dn_piece * (FX ? ACT_BLOCK_SMEM_FX : ACT_BLOCK_SMEM);
   if (tid == 0) {
     mbar_init(&bar, (uint32_t)nwin);
     fence_mbar_init();
   }
-  // the picks, made by the router kernel (one token) or by the selection kernel: complete,
-  // since every routed gate/up CTA waited for that kernel before this launch was triggered
-  if (tid < p.K) {
-    int e = __ldcg(a.ids + (size_t)tok * p.K + tid);
-    if ((unsigned)e >= (unsigned)p.E) {  // only a workspace that was not zeroed before its first use
-      atomicOr(a.ctrl + CTRL_STATUS, DEV_ERR_BAD_PICK);
-      e = 0;
+  const int cp = blockIdx.x % p.rep;  // the copy of the logits and activations this CTA reads
+  // the picks (the router is complete: every routed gate/up CTA waited for it before
+  // this launch was triggered)
+  if (a.T == 1) {
+    // The picks: those the gate/up kernel has published if all k are there (a down CTA
+    // that could not start before the gate/up CTAs left finds them), else made here.
+    // Nothing waits on them: an entry is either empty or this call's pick.
+    bool mine = true;
+    if (tid < p.K) {
+      const unsigned long long v = ld_relaxed_u64(a.pub + tid);
+      mine = v != PUB_EMPTY;
+      rids[tid] = (int)(uint32_t)v;
+      rw[tid] = __uint_as_float((uint32_t)(v >> 32));
     }
-    rids[tid] = e;
-    rw[tid] = __ldcg(a.wts + (size_t)tok * p.K + tid);
+    if (!__syncthreads_and(mine)) select_picks(a, a.logits + (size_t)cp * a.lg_copy, sel, gscore, rids, rw);
+  } else {
+    // made by the selection kernel, complete once every routed gate/up CTA has waited
+    if (tid < p.K) {
+      int e = __ldcg(a.ids + (size_t)tok * p.K + tid);
+      if ((unsigned)e >= (unsigned)p.E) {  // only a workspace that was not zeroed before its first use
+        atomicOr(a.ctrl + CTRL_STATUS, DEV_ERR_BAD_PICK);
+        e = 0;
+      }
+      rids[tid] = e;
+      rw[tid] = __ldcg(a.wts + (size_t)tok * p.K + tid);
+    }
+    __syncthreads();
   }
-  __syncthreads();
   tr(a, TR_DN_PICKED, trows);
   if (tid < nwin) {
     // this CTA's rows of slot window tid's down matrix, copied by thread tid
@@ -1136,12 +1179,11 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   #pragma unroll 1
   for (int pb = 0; pb < nact; pb += p.dn_piece) {
     const int np = nact - pb < p.dn_piece ? nact - pb : p.dn_piece;
+    const float* act = a.act + (size_t)cp * a.act_copy + (size_t)tok * p.act_stride + (size_t)pb * 32;
     if constexpr (FX)
-      quant_blocks(a.act + (size_t)tok * p.act_stride + (size_t)pb * 32, np, p.dn_piece, aplanes, ainfo, tid,
-                   DN_THREADS);
+      quant_blocks<4>(act, np, p.dn_piece, aplanes, ainfo, tid, DN_THREADS);
     else
-      store_blocks_f32<8>(a.act + (size_t)tok * p.act_stride + (size_t)pb * 32, np, p.dn_piece, axs, axsum, tid,
-                          DN_THREADS);
+      store_blocks_f32<4>(act, np, p.dn_piece, axs, axsum, tid, DN_THREADS);
     __syncthreads();  // the piece; on the first pass also the window offsets
     if (pb == 0) {
       tr(a, TR_DN_QUANT, trows);
@@ -1247,8 +1289,7 @@ static cudaError_t launch_down(const DecodeArgs& a, cudaStream_t st, bool pdl, b
 // down in the down rows' block type; `fx` selects the 16-bit fixed-point activations.
 cudaError_t decode_launch(const DecodeArgs& a, int maxb, cudaStream_t st, bool pdl, bool fx, int trows) {
   const DecodePlan& p = a.p;
-  cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)select_smem(p.E), st,
-                             pdl, a, trows);
+  cudaError_t e = launch_pdl(dec_router, dim3((unsigned)ceil_div(p.E, 2)), RT_THREADS, (size_t)0, st, pdl, a, trows);
   if (e != cudaSuccess) return e;
   if (a.T > 1) {  // one selection per token, shared by the gate/up and down CTAs
     e = launch_pdl(dec_select, dim3((unsigned)a.T), 256, (size_t)select_smem(p.E), st, pdl, a);

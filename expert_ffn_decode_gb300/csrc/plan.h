@@ -33,6 +33,8 @@ struct DecodePlan {
   int nbH, nbF, nbFs;   // blocks per gate/up row, routed down row, shared down row
   int nact;             // activation blocks: (K * F + Fs) / 32 (shared expert's first)
   int act_stride;       // floats from one token's activations to the next (K * F + Fs)
+  int rep;              // copies of the arrays many CTAs read (logits, activations); a CTA
+                        // reads copy blockIdx.x % rep, so no L2 line serves every CTA
   // gate/up kernel: two chunks of 8 values, each a gate and an up window of 8 rows
   uint32_t gu_win;      // bytes of one window (8 rows rounded out to 16-byte bounds)
   uint32_t gu_smem;     // dynamic shared memory
@@ -46,9 +48,10 @@ struct DecodePlan {
 };
 
 constexpr int GU_VALUES = 16;  // intermediate values per gate/up CTA
-// Shared-memory bytes per 32-value activation block: f32 chunks (128) and the block sum (4);
-// the 16-bit fixed-point form takes 72 and fits the same space.
+// Shared-memory bytes per 32-value activation block: f32 chunks (128) and the block sum (4),
+// or the 16-bit fixed-point form: planes (64) and the scale and sum (8).
 constexpr uint32_t ACT_BLOCK_SMEM = 132;
+constexpr uint32_t ACT_BLOCK_SMEM_FX = 72;
 constexpr int DEC_TMAX = 16;   // tokens per decode call (the chain takes up to this many at once)
 
 MOE_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -62,6 +65,9 @@ MOE_HD uint32_t window_bytes(uint32_t bytes) { return align16(bytes) + 16u; }
 // then 256 candidate keys and 256 candidate experts.
 MOE_HD uint32_t select_smem(int E) { return align16((uint32_t)E * 8u) + 2048u; }
 
+
+constexpr unsigned long long PUB_EMPTY = ~0ull;  // an entry not (yet) published in this call
+constexpr int DEC_REP = 8;                        // copies of the broadcast arrays (at most)
 
 constexpr uint32_t FLAG_ACCUMULATE = 1u;  // out = out + contribution
 constexpr uint32_t FLAG_RESIDUAL = 2u;    // out = x + contribution
@@ -78,11 +84,13 @@ struct DecodeArgs {
   float* topk_w;              // [T][K] or null
   uint32_t* ctrl;             // control block (status word)
   unsigned long long* trace;  // timeline (MOE_TRACE) or null
-  float* logits;              // [T][E]
-  float* act;                 // [T][act_stride] SwiGLU activations, shared expert's first
-  int32_t* ids;               // [T][K] picks (one token: made by the router kernel's last CTA;
-                              // several: by the selection kernel)
+  float* logits;              // [rep][T][E]
+  float* act;                 // [rep][T][act_stride] SwiGLU activations, shared expert's first
+  size_t lg_copy, act_copy;   // floats from one copy of the logits (activations) to the next
+  int32_t* ids;               // [T][K] picks (calls of T > 1: made by the selection kernel)
   float* wts;                 // [T][K] their weights
+  unsigned long long* pub;    // [K] a single-token call's picks as the gate/up kernel publishes
+                              // them: id | weight bits << 32, or PUB_EMPTY
   int T;                      // tokens of this call, 1 .. DEC_TMAX
   float scale, norm_min;
   float lim, lim_s;           // SwiGLU clamp limits of the routed and shared experts (0: none)
