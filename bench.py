@@ -39,7 +39,7 @@ UNIT = "tokens/s"
 
 QTYPE_NAMES = {2: "Q4_0", 3: "Q4_1", 12: "Q4_K", 14: "Q6_K"}
 
-# The decode chain's two activation arithmetics (MOE_FIXED_POINT selects the second).
+# The decode chain's two activation arithmetics (the default, and MOE_F32_ACT).
 ARITH_DTYPE = {False: "f32", True: "q4 x i16 block fixed point -> f32"}
 ARITH_TEXT = {
     False: "4-bit weights dequantised exactly to f32 (d*q + m), f32 activations, f32 FMA accumulation "
@@ -340,47 +340,43 @@ def active_bytes(w):
     return K * record_bytes(w, F) + (record_bytes(w, Fs) if Fs else 0)
 
 
-def rotation_graphs(step, K, L, stream):
-    """CUDA graphs of exactly K consecutive steps each, that together close the rotation over
-    L layers: graph j runs steps jK .. jK + K - 1 (step i uses layer i % L), and L / gcd(K, L)
-    graphs bring the rotation back to its start."""
+def repeat_graph(step, K, L, stream, target_steps=1280, max_repeats=2048):
+    """One CUDA graph of NR back-to-back repeats of exactly K consecutive steps (step i uses
+    layer i % L). NR is a multiple of L / gcd(K, L), so the rotation over the layers
+    continues from one replay to the next, and NR K is about `target_steps`, so a graph
+    launch falls once in that many steps. Returns (graph, NR)."""
     import torch
-    graphs = []
-    for j in range(L // math.gcd(K, L)):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(j * K, (j + 1) * K):
-                step(i, stream)
-        graphs.append(g)
-    return graphs
+    base = L // math.gcd(K, L)
+    nr = base * max(1, math.ceil(math.ceil(target_steps / K) / base))
+    nr = max(base, min(nr, base * max(1, max_repeats // base)))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(nr * K):
+            step(i, stream)
+    return g, nr
 
 
-def timed_repeats(graphs, stream, warm, min_ms, max_repeats=20000):
-    """Replays the graphs in rotation order: `warm` untimed replays, then timed repeats (one
-    graph each, a pair of CUDA events on the replaying stream around every one) until at
-    least `min_ms` of device time has passed. Returns the milliseconds of every repeat."""
+def timed_replays(g, stream, warm, min_ms, max_replays=10000):
+    """`warm` untimed replays of the graph, then replays, each between two CUDA events on
+    the replaying stream, until they add up to at least `min_ms` of device time. Returns the
+    milliseconds of every timed replay."""
     import torch
-    n = len(graphs)
     with torch.cuda.stream(stream):
-        for r in range(warm):
-            graphs[r % n].replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for r in range(warm, warm + 3):
-            graphs[r % n].replay()
-        e1.record(stream)
-    e1.synchronize()
-    est = max(e0.elapsed_time(e1) / 3, 1e-3)
-    R = int(min(max_repeats, max(5, math.ceil(min_ms / est))))
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(R + 1)]
-    start = warm + 3
-    with torch.cuda.stream(stream):
-        evs[0].record(stream)
-        for r in range(R):
-            graphs[(start + r) % n].replay()
-            evs[r + 1].record(stream)
-    evs[-1].synchronize()
-    return [evs[r].elapsed_time(evs[r + 1]) for r in range(R)]
+        for _ in range(warm):
+            g.replay()
+    stream.synchronize()
+    per = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max_replays):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        per.append(e0.elapsed_time(e1))
+        if sum(per) >= min_ms and len(per) >= 5:
+            break
+    return per
 
 
 def decode_timing(ffn, w, layers, xs, flags, dev, stream, K, warmup, min_ms):
@@ -405,14 +401,14 @@ def decode_timing(ffn, w, layers, xs, flags, dev, stream, K, warmup, min_ms):
             step(i, stream)
     stream.synchronize()
     ffn.check(ffn.moe_workspace_status(ws, stream))
-    graphs = rotation_graphs(step, K, L, stream)
-    warm = max(1, math.ceil(max(warmup, L) / K))
-    per = timed_repeats(graphs, stream, warm, min_ms)
+    g, nr = repeat_graph(step, K, L, stream)
+    warm = max(1, math.ceil(max(warmup, L) / (nr * K)))
+    per = timed_replays(g, stream, warm, min_ms)
     ffn.check(ffn.moe_workspace_status(ws, stream))
     med = statistics.median(per)
-    return {"ms_per_step": med / K, "steps": K, "repeats": len(per), "timed_ms": round(sum(per), 3),
-            "warmup_steps": warm * K, "layers_rotated": L, "graphs": len(graphs),
-            "repeat_ms_min": round(min(per), 5), "repeat_ms_max": round(max(per), 5)}
+    return {"ms_per_step": med / (nr * K), "steps": K, "repeats": len(per) * nr, "timed_ms": round(sum(per), 3),
+            "warmup_steps": warm * nr * K, "layers_rotated": L, "repeats_per_graph": nr, "replays": len(per),
+            "replay_ms_min": round(min(per), 5), "replay_ms_max": round(max(per), 5)}
 
 
 def decode_layers(synth, w, dev, rank, l2, layers=0):
@@ -652,8 +648,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
-    ap.add_argument("--fixed-point", action="store_true",
-                    help="decode with the 16-bit block fixed-point activations (MOE_FIXED_POINT)")
+    ap.add_argument("--f32-act", action="store_true",
+                    help="decode with f32 activations in the block dots (MOE_F32_ACT) instead of the default "
+                         "16-bit block fixed point")
     ap.add_argument("--prefill-steps", type=int, default=480, help="timed batched steps (0: skip)")
     ap.add_argument("--trace", action="store_true",
                     help="after timing, print the kernel's per-CTA phase timeline (stderr)")
@@ -689,14 +686,14 @@ def main():
     layers, xs = decode_layers(synth, w, dev, rank, l2, args.layers)
     L, NX = len(layers), len(xs)
     base_flags = ffn.MOE_NO_PDL if args.no_pdl else 0
-    flags = base_flags | (ffn.MOE_FIXED_POINT if args.fixed_point else 0)
+    flags = base_flags | (ffn.MOE_F32_ACT if args.f32_act else 0)
     stream = torch.cuda.Stream(dev)
     barrier(world)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         head = decode_timing(ffn, w, layers, xs, flags, dev, stream, args.steps, args.warmup, args.min_ms)
         # the other arithmetic of the decode chain, timed the same way (A/B)
-        ab = decode_timing(ffn, w, layers, xs, flags ^ ffn.MOE_FIXED_POINT, dev, stream, args.steps,
+        ab = decode_timing(ffn, w, layers, xs, flags ^ ffn.MOE_F32_ACT, dev, stream, args.steps,
                            args.warmup, args.min_ms / 4)
         torch.cuda.synchronize()
     ms_per_step = max_over_ranks(head["ms_per_step"], world, dev)
@@ -789,7 +786,7 @@ def main():
         else:
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {err}"}
     clocks = clk.summary()
-    fixed = bool(flags & ffn.MOE_FIXED_POINT)
+    fixed = not (flags & ffn.MOE_F32_ACT)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -801,10 +798,11 @@ def main():
                    "l2": f"inputs larger than L2: {L} distinct layers, {L * step_bytes / 1e6:.0f} MB of "
                          f"step bytes between reuses of any weight byte (L2 {l2 / 1e6:.0f} MB)",
                    "pdl": not args.no_pdl},
-        "timing": dict(head, how=f"{head['repeats']} timed repeats of exactly {args.steps} steps (each a CUDA "
-                                 f"graph replay between two CUDA events on the replaying stream), the layer "
-                                 f"rotation continuing from repeat to repeat; ms_per_step is the median repeat "
-                                 f"over the steps"),
+        "timing": dict(head, how=f"{head['repeats']} timed repeats of exactly {args.steps} steps, run "
+                                 f"{head['repeats_per_graph']} to a CUDA graph (one graph launch per "
+                                 f"{head['repeats_per_graph'] * args.steps} steps), {head['replays']} replays each "
+                                 f"between two CUDA events on the replaying stream, the layer rotation continuing "
+                                 f"from repeat to repeat; ms_per_step is the median replay over its steps"),
         "arith": ARITH_TEXT[fixed],
         "roofline": roof,
         "ab_arith": {"dtype": ARITH_DTYPE[not fixed], "arith": ARITH_TEXT[not fixed], "ms_per_step": ab_ms,

@@ -30,7 +30,7 @@ MOE_HOST_IO = 4
 MOE_NO_PDL = 8
 MOE_TRACE = 16
 MOE_BATCHED = 32
-MOE_FIXED_POINT = 64
+MOE_F32_ACT = 64
 
 MOE_OK = 0
 MOE_ERR_INVALID_CFG = -1

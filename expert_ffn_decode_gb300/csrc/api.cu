@@ -108,7 +108,7 @@ int check_cfg(const moe_cfg* c) {
   if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps))
     return fail(MOE_ERR_INVALID_CFG, "rms_eps must be finite and >= 0");
   if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE | MOE_BATCHED |
-                   MOE_FIXED_POINT))
+                   MOE_F32_ACT))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
 }
@@ -221,7 +221,7 @@ bool same_shape(const moe_cfg& a, const moe_cfg& b) {
   return a.hidden == b.hidden && a.n_experts == b.n_experts && a.top_k == b.top_k &&
          a.expert_ff == b.expert_ff && a.shared_ff == b.shared_ff && a.n_groups == b.n_groups &&
          (a.n_groups == 1 || a.groups_used == b.groups_used) && a.qtype == b.qtype &&
-         down_type(&a) == down_type(&b) && (a.flags & MOE_FIXED_POINT) == (b.flags & MOE_FIXED_POINT);
+         down_type(&a) == down_type(&b) && (a.flags & MOE_F32_ACT) == (b.flags & MOE_F32_ACT);
 }
 
 int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
@@ -247,7 +247,7 @@ int make_plan(const moe_cfg* c, int device, PlanEntry* out) {
   p.rep = moe::DEC_REP;
   const uint32_t budget = 200u * 1024u;  // dynamic shared memory of one CTA
   // shared bytes per 32-value activation block: f32 chunks and sum, or fixed-point planes and info
-  const uint32_t blk = (c->flags & MOE_FIXED_POINT) ? moe::ACT_BLOCK_SMEM_FX : moe::ACT_BLOCK_SMEM;
+  const uint32_t blk = (c->flags & MOE_F32_ACT) ? moe::ACT_BLOCK_SMEM : moe::ACT_BLOCK_SMEM_FX;
   // gate/up: 4 windows of 8 rows, the x blocks and the selection
   p.gu_win = moe::window_bytes(8u * p.rb_h);
   p.gu_smem = 4u * p.gu_win + (uint32_t)p.nbH * blk + moe::select_smem(p.E);
@@ -503,7 +503,7 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
     a.out = dout + (size_t)t * c->hidden;
     a.topk_ids = dids ? dids + (size_t)t * c->top_k : nullptr;
     a.topk_w = dw ? dw + (size_t)t * c->top_k : nullptr;
-    e = moe::decode_launch(a, pe.maxb, st, pdl, (c->flags & MOE_FIXED_POINT) != 0, pe.sms);
+    e = moe::decode_launch(a, pe.maxb, st, pdl, (c->flags & MOE_F32_ACT) == 0, pe.sms);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   if (host) {
@@ -742,7 +742,7 @@ extern "C" int moe_ffn_forward_noalloc(const float* x, const float* router_w, co
     a.out = out + (size_t)t * c->hidden;
     a.topk_ids = nullptr;
     a.topk_w = nullptr;
-    e = moe::decode_launch(a, pe.maxb, st, pdl, (c->flags & MOE_FIXED_POINT) != 0, 0);
+    e = moe::decode_launch(a, pe.maxb, st, pdl, (c->flags & MOE_F32_ACT) == 0, 0);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
   // wait, then read the status word; after a device-side timeout the control block

@@ -51,6 +51,11 @@ constexpr int TP_SMEM_MAX = 227 * 1024 - 2048;    // dynamic shared memory (stat
 constexpr uint32_t TP_TMEM_COLS = 512;
 constexpr uint32_t TP_A_COL = 128;                // A slots follow the first accumulator's columns [0, 128)
 constexpr uint32_t TP_ACC1_COL = 384;             // the second accumulator (router, gate/up): [384, 512)
+// Every TMEM column a tile kernel touches lies inside its allocation: the converter groups' A
+// slots (64 columns each) sit between the two accumulators, and a tile's accumulation chains
+// stay inside its accumulator's 128 (down: 64) columns (tile_chains).
+static_assert(TP_A_COL >= 128u && TP_A_COL + 64u * (TP_CONV_WARPS / 4) <= TP_ACC1_COL, "TMEM A slots");
+static_assert(TP_ACC1_COL + 128u <= TP_TMEM_COLS, "TMEM accumulators");
 
 // Stage geometry per contraction. MODE 0 gate/up, 1 down, 2 router.
 template <int MODE, int QT>

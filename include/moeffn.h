@@ -80,8 +80,8 @@ extern "C" {
 #define MOE_NO_PDL 8u     /* launch without programmatic dependent launch             */
 #define MOE_TRACE 16u     /* record a per-CTA timeline in the workspace (see below)   */
 #define MOE_BATCHED 32u   /* take the batched path whatever the token count           */
-#define MOE_FIXED_POINT 64u /* decode chain: block dots on 16-bit block fixed-point
-                             * activations (dp4a) instead of f32 (see below)           */
+#define MOE_F32_ACT 64u   /* decode chain: f32 activations in the block dots (the pages'
+                           * arithmetic) instead of 16-bit block fixed point (see below) */
 
 enum {
   MOE_OK = 0,
@@ -144,11 +144,14 @@ typedef struct moe_cfg {
  * above; they differ in arithmetic only):
  *   n_tokens < 44  the decode chain, up to 16 tokens per launch: a router kernel,
  *                  (with several tokens) a selection kernel, a gate/up kernel and a
- *                  down kernel with the weighted sum. The router is an
- *                  f32 dot; the 4-bit blocks meet activations held in 16-bit block
+ *                  down kernel with the weighted sum. The router is an f32 dot. By
+ *                  default the 4-bit blocks meet activations held in 16-bit block
  *                  fixed point (a power-of-two scale per 32 values, error at most
  *                  2^-15 of the block's largest magnitude), so each block dot is an
- *                  exact int32 sum (dp4a), scaled and accumulated in f32.
+ *                  exact int32 sum (dp4a), scaled and accumulated in f32. With
+ *                  MOE_F32_ACT the activations stay f32 and each block contributes
+ *                  d * sum(q x) + m * sum(x) by f32 fused multiply-adds (the pages'
+ *                  arithmetic); it runs about 12% slower on the Flint-shaped layer.
  *   n_tokens >= 44 (or MOE_BATCHED) the batched path, in passes of at most 512
  *                  tokens. An f32 router
  *                  contraction; one warp per token for the selection; a stable

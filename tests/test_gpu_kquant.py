@@ -2,8 +2,8 @@
 
 The Ling store keeps Q4_K gate/up rows and Q6_K or Q4_K down rows (ling_moe_ssd.js, file
 header and planLayoutLing). Both paths run them: the decode chain (block dots on 16-bit
-fixed-point activations) and the batched path's general contractions (super-blocks
-dequantised to f16). Same bars as every parity test: identical ordered picks, weights
+fixed-point activations by default) and the batched path's general contractions
+(super-blocks dequantised to f16). Same bars as every parity test: identical ordered picks, weights
 within W_REL, each token within relative L2 OUT_REL_L2.
 """
 
@@ -79,12 +79,15 @@ MIXED = [
 ]
 
 
+@pytest.mark.parametrize("flags", [0, 64], ids=["fixed", "f32"])  # 64: MOE_F32_ACT
 @pytest.mark.parametrize("w", MIXED, ids=[f"s{w['seed']}" for w in MIXED])
-def test_mixed_types_decode(w):
+def test_mixed_types_decode(w, flags):
     layer = synth.make_layer(w)
     x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"])
     ref, rid, rwt = _oracle(layer, w, x)
-    compare(*GpuLayer(layer, w).run(x), ref, rid, rwt, f"seed {w['seed']}")
+    g = GpuLayer(layer, w)
+    compare(*g.run(x, flags=flags), ref, rid, rwt, f"seed {w['seed']}")
+    compare(*g.run(x[:1], flags=flags), ref[:1], rid[:1], rwt[:1], f"seed {w['seed']} one token")
 
 
 @pytest.mark.parametrize("w", MIXED, ids=[f"s{w['seed']}" for w in MIXED])
@@ -103,9 +106,10 @@ def test_ling_kquant_decode():
     x, _ = margin_tokens(layer, w, 10, seed=w["seed"])
     ref, rid, rwt = _oracle(layer, w, x)
     g = GpuLayer(layer, w)
-    for t in range(2):
-        compare(*g.run(x[t:t + 1]), ref[t:t + 1], rid[t:t + 1], rwt[t:t + 1], f"ling kq token {t}")
-    compare(*g.run(x[2:]), ref[2:], rid[2:], rwt[2:], "ling kq T=8")
+    for flags in (0, 64):  # 64: MOE_F32_ACT
+        for t in range(2):
+            compare(*g.run(x[t:t + 1], flags=flags), ref[t:t + 1], rid[t:t + 1], rwt[t:t + 1], f"ling kq token {t}")
+        compare(*g.run(x[2:], flags=flags), ref[2:], rid[2:], rwt[2:], "ling kq T=8")
 
 
 def test_ling_kquant_batched_all_tokens():

@@ -64,15 +64,15 @@ def oracle(layer, w, x, **kw):
                       oracle_cfg(w), **kw)
 
 
-FIXED = 64  # MOE_FIXED_POINT
+F32 = 64  # MOE_F32_ACT
 
 
-@pytest.mark.parametrize("flags", [0, FIXED], ids=["f32", "fixed"])
+@pytest.mark.parametrize("flags", [0, F32], ids=["fixed", "f32"])
 @pytest.mark.parametrize("factor", [50.0, 300.0, 1000.0])
 @pytest.mark.parametrize("name", ["flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1"])
 def test_outlier_channels_decode(name, factor, flags):
     # one call of three tokens and three single-token calls (the two decode forms), with f32
-    # activations and with the 16-bit block fixed-point ones
+    # activations and with the 16-bit block fixed-point ones (the default)
     w, base = layer_of(name)
     layer = rescaled(base, factor)
     ch = synth.outlier_channels(w["hidden"], w["seed"])

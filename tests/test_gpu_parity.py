@@ -41,10 +41,10 @@ def layer_of(name):
 DECODE = ["tiny_q4_0_t4", "flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1"]
 
 
-FIXED = 64  # MOE_FIXED_POINT: the decode chain's 16-bit block fixed-point activations
+F32 = 64  # MOE_F32_ACT: the decode chain's f32 activations (the default is 16-bit block fixed point)
 
 
-@pytest.mark.parametrize("flags", [0, FIXED], ids=["f32", "fixed"])
+@pytest.mark.parametrize("flags", [0, F32], ids=["fixed", "f32"])
 @pytest.mark.parametrize("name", DECODE)
 def test_workload_parity(name, flags):
     w, layer = layer_of(name)
@@ -57,7 +57,7 @@ def test_workload_parity(name, flags):
     err = compare(out, ids, wts, ref, rid, rwt, name)
     for t in range(T):  # and one token per call
         compare(*g.run(x[t:t + 1], flags=flags), ref[t:t + 1], rid[t:t + 1], rwt[t:t + 1], f"{name} token {t}")
-    print(f"{name} ({'fixed point' if flags else 'f32'}): max rel-L2 {err:.3e}")
+    print(f"{name} ({'f32' if flags else 'fixed point'}): max rel-L2 {err:.3e}")
 
 
 @pytest.mark.parametrize("name", DECODE[1:])
@@ -102,7 +102,7 @@ def test_random_shapes(w):
     ref, rid, rwt = mo.moe_ffn(x, layer["router_w"], layer["bias"], layer["expert_blocks"],
                                layer["shared_blocks"], oracle_cfg(w))
     g = GpuLayer(layer, w)
-    for flags in (0, FIXED):
+    for flags in (0, F32):
         out, ids, wts = g.run(x, flags=flags)
         compare(out, ids, wts, ref, rid, rwt, f"seed {w['seed']} flags {flags}")
         o1, i1, w1 = g.run(x[:1], flags=flags)

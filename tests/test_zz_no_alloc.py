@@ -53,7 +53,7 @@ def test_noalloc_scratch_holds_the_largest_layer_and_rejects_workspace_flags():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("flags", [0, ffn.MOE_FIXED_POINT], ids=["f32", "fixed"])
+@pytest.mark.parametrize("flags", [0, ffn.MOE_F32_ACT], ids=["fixed", "f32"])
 @pytest.mark.parametrize("name", ["flint_decode_t1", "tiny_q4_0_t4"])
 def test_noalloc_matches_oracle_and_workspace_entry_point_twice(name, flags):
     import torch
