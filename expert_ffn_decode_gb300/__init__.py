@@ -31,6 +31,7 @@ MOE_NO_PDL = 8
 MOE_TRACE = 16
 MOE_BATCHED = 32
 MOE_F32_ACT = 64
+MOE_GRAPH = 128
 
 MOE_OK = 0
 MOE_ERR_INVALID_CFG = -1

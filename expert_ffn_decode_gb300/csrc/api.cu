@@ -108,7 +108,7 @@ int check_cfg(const moe_cfg* c) {
   if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps))
     return fail(MOE_ERR_INVALID_CFG, "rms_eps must be finite and >= 0");
   if (c->flags & ~(MOE_ACCUMULATE | MOE_RESIDUAL | MOE_HOST_IO | MOE_NO_PDL | MOE_TRACE | MOE_BATCHED |
-                   MOE_F32_ACT))
+                   MOE_F32_ACT | MOE_GRAPH))
     return fail(MOE_ERR_INVALID_CFG, "unknown flag bits 0x%x", c->flags);
   return MOE_OK;
 }
@@ -336,9 +336,10 @@ int owned_workspace(size_t bytes, void** ptr) {
   return MOE_OK;
 }
 
-int run(const float* x, const float* router_w, const float* bias, const void* experts,
-        const void* shared, const moe_cfg* c, float* out, void* ws, size_t ws_bytes, cudaStream_t st,
-        int32_t* ids, float* wts) {
+// Checks the call and enqueues all of its work (copies and kernels) on `st`.
+int enqueue(const float* x, const float* router_w, const float* bias, const void* experts,
+            const void* shared, const moe_cfg* c, float* out, void* ws, size_t ws_bytes, cudaStream_t st,
+            int32_t* ids, float* wts) {
   int rc = check_cfg(c);
   if (rc != MOE_OK) return rc;
   const int T = c->n_tokens;
@@ -523,6 +524,148 @@ int run(const float* x, const float* router_w, const float* bias, const void* ex
   return MOE_OK;
 }
 
+// ---- replayed graphs (MOE_GRAPH) ---------------------------------------------------
+// With MOE_GRAPH, an argument set seen before runs as one launch of a CUDA graph of its whole
+// enqueued work, captured the second time the set is seen (the first time it runs as it is,
+// which also sets every kernel's shared-memory limit outside any capture). The cache holds
+// the last GRAPH_SLOTS sets per process. A call made while its stream is being captured, a
+// traced call, and a call whose capture fails run directly.
+constexpr int GRAPH_SLOTS = 64;
+
+struct GraphKey {
+  int device;
+  const void* p[10];  // x, router_w, bias, experts, shared, out, ws, ids, wts, ffn_norm
+  size_t ws_bytes;
+  int32_t i[12];      // the cfg's integer fields (flags included)
+  float f[6];         // the cfg's float fields
+};
+
+bool same_key(const GraphKey& a, const GraphKey& b) {
+  if (a.device != b.device || a.ws_bytes != b.ws_bytes) return false;
+  for (int k = 0; k < 10; ++k)
+    if (a.p[k] != b.p[k]) return false;
+  for (int k = 0; k < 12; ++k)
+    if (a.i[k] != b.i[k]) return false;
+  for (int k = 0; k < 6; ++k)
+    if (std::memcmp(&a.f[k], &b.f[k], sizeof(float)) != 0) return false;
+  return true;
+}
+
+struct GraphSlot {
+  bool used;
+  bool no_graph;       // its capture failed: always run directly
+  GraphKey key;
+  cudaGraphExec_t exec;
+  unsigned long long last;
+};
+GraphSlot g_graphs[GRAPH_SLOTS];
+unsigned long long g_graph_tick = 0;
+std::mutex g_graph_mu;
+cudaStream_t g_capture_stream[64];
+
+int run(const float* x, const float* router_w, const float* bias, const void* experts, const void* shared,
+        const moe_cfg* c, float* out, void* ws, size_t ws_bytes, cudaStream_t st, int32_t* ids, float* wts) {
+  if (!c || !(c->flags & MOE_GRAPH) || (c->flags & MOE_TRACE) || c->n_tokens <= 0)
+    return enqueue(x, router_w, bias, experts, shared, c, out, ws, ws_bytes, st, ids, wts);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    cs = cudaStreamCaptureStatusActive;
+  }
+  int dev = 0;
+  if (cs != cudaStreamCaptureStatusNone || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return enqueue(x, router_w, bias, experts, shared, c, out, ws, ws_bytes, st, ids, wts);
+  }
+  GraphKey k{};
+  k.device = dev;
+  const void* ps[10] = {x, router_w, bias, experts, shared, out, ws, ids, wts, c->ffn_norm};
+  for (int j = 0; j < 10; ++j) k.p[j] = ps[j];
+  k.ws_bytes = ws_bytes;
+  const int32_t is[12] = {c->hidden, c->n_experts, c->top_k, c->expert_ff, c->shared_ff, c->n_groups,
+                          c->groups_used, c->n_tokens, c->qtype, (int32_t)c->flags, c->qtype_down, 0};
+  for (int j = 0; j < 12; ++j) k.i[j] = is[j];
+  const float fs[6] = {c->weights_scale, c->norm_min, c->swiglu_limit, c->swiglu_limit_shared, c->rms_eps, 0.f};
+  for (int j = 0; j < 6; ++j) k.f[j] = fs[j];
+
+  std::unique_lock<std::mutex> lk(g_graph_mu);
+  GraphSlot* hit = nullptr;
+  for (auto& g : g_graphs)
+    if (g.used && same_key(g.key, k)) {
+      hit = &g;
+      break;
+    }
+  if (hit && hit->exec) {
+    hit->last = ++g_graph_tick;
+    const cudaGraphExec_t ex = hit->exec;
+    const cudaError_t e = cudaGraphLaunch(ex, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "graph launch");
+  }
+  if (!hit || hit->no_graph) {
+    if (!hit) {  // first sight: remember the set (evicting the least recently used slot)
+      GraphSlot* v = &g_graphs[0];
+      for (auto& g : g_graphs) {
+        if (!g.used) {
+          v = &g;
+          break;
+        }
+        if (g.last < v->last) v = &g;
+      }
+      if (v->used && v->exec) cudaGraphExecDestroy(v->exec);
+      *v = GraphSlot{true, false, k, nullptr, ++g_graph_tick};
+    }
+    lk.unlock();
+    return enqueue(x, router_w, bias, experts, shared, c, out, ws, ws_bytes, st, ids, wts);
+  }
+  // second sight: capture the call's work on the library's capture stream
+  if (!g_capture_stream[dev]) {
+    cudaError_t e = cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      g_capture_stream[dev] = nullptr;
+      hit->no_graph = true;
+      lk.unlock();
+      cudaGetLastError();
+      return enqueue(x, router_w, bias, experts, shared, c, out, ws, ws_bytes, st, ids, wts);
+    }
+  }
+  const cudaStream_t cap = g_capture_stream[dev];
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int rc = MOE_ERR_CUDA;
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+    rc = enqueue(x, router_w, bias, experts, shared, c, out, ws, ws_bytes, cap, ids, wts);
+    const cudaError_t e = cudaStreamEndCapture(cap, &graph);
+    if (rc == MOE_OK && (e != cudaSuccess || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)) {
+      exec = nullptr;
+      rc = MOE_ERR_CUDA;
+    }
+    if (graph) cudaGraphDestroy(graph);
+  }
+  cudaGetLastError();
+  if (!exec) {
+    hit->no_graph = true;
+    lk.unlock();
+    g_err[0] = 0;
+    return enqueue(x, router_w, bias, experts, shared, c, out, ws, ws_bytes, st, ids, wts);
+  }
+  hit->exec = exec;
+  hit->last = ++g_graph_tick;
+  const cudaError_t e = cudaGraphLaunch(exec, st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "graph launch");
+}
+
+void clear_graphs() {
+  std::lock_guard<std::mutex> lk(g_graph_mu);
+  for (auto& g : g_graphs) {
+    if (g.used && g.exec) cudaGraphExecDestroy(g.exec);
+    g = GraphSlot{};
+  }
+  for (auto& s : g_capture_stream) {
+    if (s) cudaStreamDestroy(s);
+    s = nullptr;
+  }
+}
+
 // The error a nonzero status word reports.
 int status_error(uint32_t bits) {
   if (bits & moe::DEV_ERR_MBAR_TIMEOUT)
@@ -616,6 +759,7 @@ int moe_selftest_timeout(void* workspace, void* stream) {
 const char* moe_last_error(void) { return g_err; }
 
 int moe_shutdown(void) {
+  clear_graphs();
   std::lock_guard<std::mutex> lk(g_mu);
   int rc = MOE_OK;
   for (auto& w : g_ws) {

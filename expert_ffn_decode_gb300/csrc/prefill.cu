@@ -306,9 +306,10 @@ __global__ void prefill_x16(const PrefillArgs a) {
 constexpr int KC = 128;                      // K values per pipeline chunk (4 blocks)
 constexpr int A_STAGE = 128 * KC * 2;        // 32 KB f16
 // B stage: up to 2 * PREFILL_NMAX rows (gate/up: hi and lo rows of each token)
-constexpr int B_STAGE_GU = 2 * PREFILL_NMAX * KC * 2;  // 64 KB f16
-constexpr int B_STAGE_DN = PREFILL_NMAX * KC * 2;      // 32 KB f16
+constexpr int B_STAGE_GU = 2 * PREFILL_NMAX * KC * 2;  // 32 KB f16
+constexpr int B_STAGE_DN = PREFILL_NMAX * KC * 2;      // 16 KB f16
 constexpr uint32_t TMEM_COLS = 256;
+constexpr int NSTAGE = 3;                    // pipeline stages (A and B buffers)
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -491,9 +492,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                "r"(valid ? 16 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most one (wait_group1) or none (wait_group0) of the committed groups of the
+// thread's asynchronous copies is still in flight.
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_group0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // L2 prefetch of the 16-byte-aligned part of [p, p + bytes).
 __device__ __forceinline__ void prefetch_span(const void* p, uint32_t bytes) {
@@ -505,18 +508,17 @@ __device__ __forceinline__ void prefetch_span(const void* p, uint32_t bytes) {
 template <int QT, int MODE>
 __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t gsm[];
-  uint8_t* As = gsm;                      // [2][A_STAGE]
+  uint8_t* As = gsm;                      // [NSTAGE][A_STAGE]
   constexpr int B_STAGE = MODE == 0 ? B_STAGE_GU : B_STAGE_DN;
-  uint8_t* Bs = gsm + 2 * A_STAGE;        // [2][B_STAGE]
-  __shared__ __align__(8) uint64_t mma_bar[2];
+  uint8_t* Bs = gsm + NSTAGE * A_STAGE;   // [NSTAGE][B_STAGE]
+  __shared__ __align__(8) uint64_t mma_bar[NSTAGE];
   __shared__ uint32_t tmem_base;
   __shared__ uint32_t rowsrc[PREFILL_NMAX];  // B source row of each chunk row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (warp == 0) tmem_alloc(&tmem_base, TMEM_COLS);
   if (tid == 0) {
-    mbar_init(&mma_bar[0], 1);
-    mbar_init(&mma_bar[1], 1);
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(&mma_bar[i], 1);
     fence_mbar_init();
   }
   tc_fence_before_sync();
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
   const int mt_r = MODE == 0 ? ceil_div(a.F, 64) : ceil_div(a.H, 128);
   const int mt_s = MODE == 0 ? ceil_div(a.Fs > 0 ? a.Fs : 1, 64) : ceil_div(a.H, 128);
   const int units = nr * mt_r + (ntot - nr) * mt_s;
-  uint32_t g = 0;  // pipeline chunks so far (stage = g % 2, use = g / 2)
+  uint32_t g = 0;  // pipeline chunks so far (stage = g % NSTAGE, use = g / NSTAGE)
   bool ok = true;
 
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -574,63 +576,73 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
     __syncthreads();
     const __half* bsrc = MODE == 0 ? a.x16 : (sh ? a.act16s : a.act16);
     const int bld = MODE == 0 ? a.H : ff;  // B row length (values)
-    RawBlk cur[2], nxt[2];
-    bool vcur[2], vnxt[2] = {false, false};
-    issue_raw<QT>(cur, vcur, 0, nbk, mrows, tid, wrow);
+    // Three stages, each an A and a B buffer that the MMAs of one chunk read. Chunk kc takes
+    // stage g % NSTAGE; its B rows are copied one chunk ahead (into the stage once the MMAs of
+    // its previous use are done), and its A blocks are loaded two chunks ahead into registers.
+    auto stage_free = [&](uint32_t gs) {  // the MMAs of stage use gs - NSTAGE are done
+      if (gs >= (uint32_t)NSTAGE && !mbar_wait(&mma_bar[gs % NSTAGE], ((gs / NSTAGE) - 1) & 1u)) ok = false;
+    };
+    auto copy_b = [&](int kc, uint32_t gs) {  // rows past the chunk are zero-filled
+      uint8_t* B = Bs + (gs % NSTAGE) * B_STAGE;
+      const int kb = min(KC / 32, nbk - kc * (KC / 32));
+      const int pieces = kb * 4;  // 8 values a piece
+      for (int i = tid; i < nb * pieces; i += PREFILL_THREADS) {
+        const int r = i / pieces, pc = i % pieces;
+        const int rr = r < npad ? r : r - npad;  // chunk row (lo rows: second half)
+        const bool valid = rr < ch.n;
+        const size_t src = !valid ? 0 : MODE == 0 ? 2 * (size_t)rowsrc[rr] + (r >= npad) : (size_t)rowsrc[rr];
+        cp_async16(B + (pc * (nb / 8) + (r >> 3)) * 128 + 16 * (r & 7), bsrc + src * bld + kc * KC + pc * 8, valid);
+      }
+      cp_async_commit();
+    };
+    RawBlk r0[2], r1[2], r2[2];
+    bool v0[2], v1[2] = {false, false}, v2[2] = {false, false};
+    issue_raw<QT>(r0, v0, 0, nbk, mrows, tid, wrow);
+    if (nkc > 1) issue_raw<QT>(r1, v1, 1, nbk, mrows, tid, wrow);
+    stage_free(g);
+    copy_b(0, g);
 
     for (int kc = 0; kc < nkc; ++kc, ++g) {
-      const int s = g & 1;
-      const uint32_t use = g >> 1;
-      if (g >= 2 && !mbar_wait(&mma_bar[s], (use - 1) & 1u)) ok = false;  // stage free again
-      uint8_t* A = As + s * A_STAGE;
-      uint8_t* B = Bs + s * B_STAGE;
-      const int kb = min(KC / 32, nbk - kc * (KC / 32));  // blocks in this chunk
-      // A: 128 rows x 4 blocks; a warp takes 32 consecutive rows of one block, so its
-      // 16-byte shared stores of one core row cover all banks
-      // B: rows x (16-byte pieces of this chunk's K slice), copied asynchronously (rows
-      // past the chunk are zero-filled) while the A blocks load and dequantise
-      {
-        const int pieces = kb * 4;  // 8 values a piece
-        for (int i = tid; i < nb * pieces; i += PREFILL_THREADS) {
-          const int r = i / pieces, pc = i % pieces;
-          const int rr = r < npad ? r : r - npad;  // chunk row (lo rows: second half)
-          const bool valid = rr < ch.n;
-          const size_t src = !valid ? 0 : MODE == 0 ? 2 * (size_t)rowsrc[rr] + (r >= npad) : (size_t)rowsrc[rr];
-          cp_async16(B + (pc * (nb / 8) + (r >> 3)) * 128 + 16 * (r & 7), bsrc + src * bld + kc * KC + pc * 8,
-                     valid);
-        }
+      const int s = (int)(g % NSTAGE);
+      const bool more = kc + 1 < nkc;
+      if (more) {  // the next chunk's B rows, into the next stage once its last MMAs are done
+        stage_free(g + 1);
+        copy_b(kc + 1, g + 1);
       }
-      // A: 128 rows x 4 blocks, two per thread. The next chunk's blocks are requested before
-      // this chunk's are dequantised, so two chunks' loads overlap; a warp takes 32
-      // consecutive rows of one block, so its 16-byte shared stores of one core row cover
-      // all banks
-      {
-        if (kc + 1 < nkc) issue_raw<QT>(nxt, vnxt, kc + 1, nbk, mrows, tid, wrow);
+      if (kc + 2 < nkc) issue_raw<QT>(r2, v2, kc + 2, nbk, mrows, tid, wrow);
+      // A: 128 rows x 4 blocks, two per thread; a warp takes 32 consecutive rows of one
+      // block, so its 16-byte shared stores of one core row cover all banks
+      uint8_t* A = As + s * A_STAGE;
+      const int kb = min(KC / 32, nbk - kc * (KC / 32));  // blocks in this chunk
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-          const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
-          if (vcur[pass]) {
-            uint4 o[4];
-            dequant_raw<QT>(cur[pass], kc * (KC / 32) + b, o);
+      for (int pass = 0; pass < 2; ++pass) {
+        const int i = pass * PREFILL_THREADS + tid, m = i & 127, b = i >> 7;
+        if (v0[pass]) {
+          uint4 o[4];
+          dequant_raw<QT>(r0[pass], kc * (KC / 32) + b, o);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const int kcore = 4 * b + w, mcore = m >> 3;
-              *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = o[w];
-            }
+          for (int w = 0; w < 4; ++w) {
+            const int kcore = 4 * b + w, mcore = m >> 3;
+            *reinterpret_cast<uint4*>(A + (kcore * 16 + mcore) * 128 + 16 * (m & 7)) = o[w];
           }
         }
       }
-      cp_async_wait_all();
+      if (more) cp_async_wait_group1();  // this chunk's B rows (the next chunk's may still fly)
+      else cp_async_wait_group0();
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
-        cur[pass] = nxt[pass];
-        vcur[pass] = vnxt[pass];
+        r0[pass] = r1[pass];
+        v0[pass] = v1[pass];
+        r1[pass] = r2[pass];
+        v1[pass] = v2[pass];
+        v2[pass] = false;
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncthreads();
       if (tid == 0) {
         tc_fence_after_sync();
+        const uint8_t* B = Bs + s * B_STAGE;
         const uint32_t idesc = idesc_f16_f32(128, nb);
         for (int j = 0; j < 2 * kb; ++j) {  // K = 16 per MMA: two core matrices along K
           const uint64_t ad = smem_desc(A + 2 * j * 2048, 2048, 128);
@@ -643,7 +655,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1) prefill_gemm(const Prefill
     // epilogue: the last commit covers every MMA of the tile
     {
       const uint32_t gl = g - 1;
-      if (!mbar_wait(&mma_bar[gl & 1], (gl >> 1) & 1u)) ok = false;
+      if (!mbar_wait(&mma_bar[gl % NSTAGE], (gl / NSTAGE) & 1u)) ok = false;
     }
     tc_fence_after_sync();
     if (warp < 4) {
@@ -805,7 +817,7 @@ PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile
 template <int QT, int MODE>
 static cudaError_t launch_gemm(const PrefillArgs& a, cudaStream_t st) {
   auto kern = prefill_gemm<QT, MODE>;
-  const int smem = 2 * A_STAGE + 2 * (MODE == 0 ? B_STAGE_GU : B_STAGE_DN);
+  const int smem = NSTAGE * (A_STAGE + (MODE == 0 ? B_STAGE_GU : B_STAGE_DN));
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   kern<<<a.nc, PREFILL_THREADS, smem, st>>>(a);

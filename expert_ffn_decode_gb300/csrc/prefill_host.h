@@ -11,7 +11,7 @@ namespace moe {
 constexpr int PREFILL_MIN_T = 44;     // calls of at least this many tokens take the batched path
                                       // (measured crossover with the multi-token decode chain)
 constexpr int PREFILL_CHUNK_T = 512;  // tokens per prefill pass (larger batches run in passes)
-constexpr int PREFILL_NMAX = 128;     // tokens (or pairs) per GEMM work unit (general path)
+constexpr int PREFILL_NMAX = 64;      // tokens (or pairs) per GEMM work unit (general path)
 constexpr int PREFILL_TILE_NMAX = 64; // tokens (or pairs) per GEMM work unit (tile pipeline)
 constexpr int PREFILL_THREADS = 256;
 

@@ -82,6 +82,8 @@ extern "C" {
 #define MOE_BATCHED 32u   /* take the batched path whatever the token count           */
 #define MOE_F32_ACT 64u   /* decode chain: f32 activations in the block dots (the pages'
                            * arithmetic) instead of 16-bit block fixed point (see below) */
+#define MOE_GRAPH 128u    /* replay a captured CUDA graph for an argument set seen before
+                           * (see moe_ffn_forward_ex)                                  */
 
 enum {
   MOE_OK = 0,
@@ -184,7 +186,15 @@ int moe_ffn_forward(const float* x, const float* router_w, const float* router_b
  * be ordered (same stream, or synchronised); calls with different configurations
  * may share one.
  * Asynchronous: device-side errors surface through moe_workspace_status.
- * topk_ids / topk_w may be NULL. */
+ * topk_ids / topk_w may be NULL.
+ * With MOE_GRAPH the library remembers the 64 argument sets (every pointer, the sizes and
+ * the cfg) used most recently in the process. The second call with a set captures all of
+ * its work into a CUDA graph on a library-owned stream, and every later call with that set
+ * is one launch of the graph on `stream`: the same kernels and arguments, so the same
+ * results, with less host time per call. The buffers of a remembered set must stay
+ * allocated, and host buffers page-locked, until moe_shutdown or until 64 other sets have
+ * been used since. A call made while `stream` is being captured, a MOE_TRACE call, and a
+ * set whose capture fails run directly. */
 int moe_ffn_forward_ex(const float* x, const float* router_w, const float* router_bias,
                        const void* expert_blocks, const void* shared_blocks, const moe_cfg* cfg,
                        float* out, void* workspace, size_t workspace_bytes, void* stream,

@@ -48,7 +48,7 @@ BAD = [
     dict(n_groups=3), dict(n_groups=256), dict(n_groups=8, groups_used=0),
     dict(n_groups=8, groups_used=9), dict(n_groups=16, groups_used=1, top_k=17),
     dict(n_tokens=-1), dict(qtype=8), dict(weights_scale=float("inf")), dict(norm_min=-1.0),
-    dict(flags=128), dict(swiglu_limit=-1.0), dict(swiglu_limit_shared=float("nan")),
+    dict(flags=256), dict(swiglu_limit=-1.0), dict(swiglu_limit_shared=float("nan")),
     dict(swiglu_limit=float("inf")), dict(rms_eps=-1.0), dict(rms_eps=float("nan")),
     dict(qtype=14), dict(qtype_down=13), dict(qtype_down=-1),
     dict(qtype=12, hidden=96),                      # K-quant gate/up rows: hidden % 256

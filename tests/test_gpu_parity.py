@@ -253,6 +253,41 @@ def test_plain_entry_point_and_repeat_determinism():
         assert np.array_equal(again, first)
 
 
+@pytest.mark.parametrize("name,T", [("flint_decode_t1", 1), ("lfm25_decode_t1", 3), ("tiny_q4_0_t4", 48)])
+def test_graph_replay_matches_direct_calls(name, T):
+    # MOE_GRAPH: the first call runs directly, the second captures, later ones replay the
+    # graph; every call must equal the direct path bit for bit, with device and host buffers
+    import expert_ffn_decode_gb300 as ffn
+    import torch
+    w, layer = layer_of(name)
+    x, _ = margin_tokens(layer, w, T, seed=w["seed"], stream=15)
+    g = GpuLayer(layer, w)
+    want, wid, ww = g.run(x)
+    st = torch.cuda.current_stream()
+    for host in (False, True):
+        flags = ffn.MOE_GRAPH | (ffn.MOE_HOST_IO if host else 0)
+        cfg = ffn.make_cfg(**{**w, "n_tokens": T, "flags": flags})
+        ws = torch.zeros(ffn.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+        if host:
+            xd = torch.from_numpy(x).pin_memory()
+            out = torch.full((T, w["hidden"]), float("nan")).pin_memory()
+            ids = torch.full((T, w["top_k"]), -1, dtype=torch.int32).pin_memory()
+            wts = torch.full((T, w["top_k"]), float("nan")).pin_memory()
+        else:
+            xd = torch.from_numpy(x).cuda()
+            out = torch.full((T, w["hidden"]), float("nan"), device="cuda")
+            ids = torch.full((T, w["top_k"]), -1, dtype=torch.int32, device="cuda")
+            wts = torch.full((T, w["top_k"]), float("nan"), device="cuda")
+        for call in range(4):
+            out.fill_(float("nan"))
+            ffn.check(ffn.moe_ffn_forward_ex(xd, g.router_w, g.bias, g.experts, g.shared, cfg, out, ws,
+                                             ws.numel(), st, ids, wts))
+            ffn.check(ffn.moe_workspace_status(ws, st))
+            assert np.array_equal(out.cpu().numpy(), want), (host, call)
+            assert np.array_equal(ids.cpu().numpy(), wid) and np.array_equal(wts.cpu().numpy(), ww), (host, call)
+    ffn.moe_shutdown()  # drops the cached graphs
+
+
 def test_bias_none_equals_zero_bias_and_empty_batch():
     import expert_ffn_decode_gb300 as ffn
     w = _small(30, bias_std=None)
