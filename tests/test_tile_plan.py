@@ -1,7 +1,7 @@
 """CPU check of the batched path's chunk plan against the operand-image sizes.
 
 The expert sort (csrc/prefill.cu, prefill_sort) cuts each expert's sorted (token, pick) pairs
-into chunks of at most `nmax` pairs (64 on the tile pipeline, 128 on the general path) and
+into chunks of at most `nmax` pairs (64 on both batched paths; 128 is checked as well) and
 gives every chunk a first padded row: each chunk's rows are rounded up to 16 for the MMA's N
 dimension, and the chunks follow each other in expert order. The workspace sizes the tile
 pipeline's routed operand images for P + 15 * max_routed padded rows (csrc/prefill.cu,
