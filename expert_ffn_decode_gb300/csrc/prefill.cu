@@ -773,6 +773,11 @@ __global__ void __launch_bounds__(256) prefill_rmsnorm(const PrefillArgs a) {
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 bool prefill_tile_ok(int H, int F, int Fs, int qtype, int qtype_dn) {
+  if (qtype == 12 && (qtype_dn == 12 || qtype_dn == 14)) {
+    // Q4_K gate/up rows in 256-value super-blocks; Q6_K down rows as whole rows in one stage
+    if (H % 256 || F % 256 || Fs % 256) return false;
+    return qtype_dn == 12 || (F <= 768 && Fs <= 768);
+  }
   if (qtype != qtype_dn || (qtype != 2 && qtype != 3)) return false;
   const int kc = qtype == 3 ? 128 : 256;
   return H % kc == 0 && F % kc == 0 && Fs % kc == 0;
@@ -861,7 +866,7 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
     // gate/up runs weights-as-A; the down contraction runs tokens-as-A when its
     // 256-row weight tiles cover H exactly (the faster of the two layouts for each)
     if ((e = tile_gemm_launch(a, 0, st)) != cudaSuccess) return e;
-    const bool swap = a.H % 256 == 0;
+    const bool swap = a.H % 256 == 0 && (a.qtype_dn == 2 || a.qtype_dn == 3);
     if ((e = swap ? swap_down_launch(a, st) : tile_gemm_launch(a, 1, st)) != cudaSuccess) return e;
   } else {
     prefill_x16<<<(unsigned)((nx + 255) / 256), 256, 0, st>>>(a);

@@ -80,10 +80,12 @@ struct PrefillWs {
 };
 PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile);
 
-// True when all three matrices are Q4_0 or all Q4_1 and the layer's K dimensions are whole
-// pipeline chunks (128 values for Q4_1, 256 for Q4_0): every weight-row segment a chunk
-// copies then starts and ends on a 16-byte boundary, which the bulk copies of the tile
-// pipeline need. Other layers (K-quants among them) take the general contractions.
+// True when the layer's rows suit the tile pipeline's copies: all three matrices Q4_0 or all
+// Q4_1, with K dimensions in whole pipeline chunks (128 values for Q4_1, 256 for Q4_0), so
+// every weight-row segment a chunk copies starts and ends on a 16-byte boundary; or Q4_K
+// gate/up rows with Q4_K or Q6_K down rows and H, F, Fs multiples of 256 (Q4_K: one 144-byte
+// super-block per row segment; Q6_K: F, Fs <= 768, a stage holds 128 whole down rows, whose
+// span is a multiple of 16 bytes). Other layers take the general contractions.
 bool prefill_tile_ok(int H, int F, int Fs, int qtype, int qtype_dn);
 
 // Tile pipeline launches (prefill_tc.cu).

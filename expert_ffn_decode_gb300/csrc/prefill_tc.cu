@@ -57,16 +57,26 @@ constexpr uint32_t TP_ACC1_COL = 384;             // the second accumulator (rou
 static_assert(TP_A_COL >= 128u && TP_A_COL + 64u * (TP_CONV_WARPS / 4) <= TP_ACC1_COL, "TMEM A slots");
 static_assert(TP_ACC1_COL + 128u <= TP_TMEM_COLS, "TMEM accumulators");
 
+// Q6_K down rows on the tile pipeline: a raw stage holds 128 whole rows of at most this many
+// values (a Q6_K row of 768 values is 630 bytes, so single rows do not start on 16-byte
+// bounds, but 128 consecutive rows span a multiple of 16 bytes).
+constexpr int TP_Q6_KMAX = 768;
+
 // Stage geometry per contraction. MODE 0 gate/up, 1 down, 2 router.
 template <int MODE, int QT>
 struct Geo {
   // A raw chunk is ROWS rows x KR K values. Its row segments (SEG bytes) are odd multiples
   // of 16 bytes, stored densely by the TMA: a quarter warp reading one 16-byte word of 8
   // consecutive rows then hits 8 different bank groups. Wide segments keep each TMA row
-  // request long (240 and 144 bytes against 80 for a single 128-value unit).
+  // request long (240 and 144 bytes against 80 for a single 128-value unit). A Q4_K chunk
+  // is one 144-byte super-block of each row; a Q6_K chunk is whole rows (one bulk copy).
+  static constexpr bool Q6 = QT == 14;
   static constexpr int ROWS = MODE == 2 ? 64 : 128;                  // raw rows per stage
-  static constexpr int KR = MODE == 2 ? 128 : (QT == 3 ? 384 : 256);  // K values per raw chunk
-  static constexpr int SEG = MODE == 2 ? 512 : KR / 32 * (QT == 3 ? 20 : 18);  // bytes per row
+  static constexpr int KR = MODE == 2 ? 128 : (QT == 3 ? 384 : (Q6 ? TP_Q6_KMAX : 256));  // K values per raw chunk
+  static constexpr int SEG = MODE == 2   ? 512
+                             : Q6        ? TP_Q6_KMAX / 256 * 210
+                             : QT == 12  ? 144
+                                         : KR / 32 * (QT == 3 ? 20 : 18);  // bytes per row (at most, Q6_K)
   static constexpr int STAGE = ROWS * SEG;
   static constexpr int NAU = KR / TP_KB;                             // 128-value A units per chunk
   static constexpr int NSB = 2;                                      // token-operand stages
@@ -74,7 +84,8 @@ struct Geo {
   static constexpr int NSA0 = (TP_SMEM_MAX - NSB * TP_B_STAGE - SCR - 1024) / STAGE;
   static constexpr int NSA = NSA0 > 16 ? 16 : NSA0;                  // raw stages (one shared ring)
   static constexpr int NACC = 2;                                     // accumulators (down tiles: N <= 64)
-  static constexpr int SMEM = NSA * STAGE + NSB * TP_B_STAGE + SCR;
+  static constexpr int RAW_BYTES = (NSA * STAGE + 1023) / 1024 * 1024;  // token stages start 1024-aligned
+  static constexpr int SMEM = RAW_BYTES + NSB * TP_B_STAGE + SCR;
   static_assert(NSA >= 2 && SMEM + 1024 <= TP_SMEM_MAX, "shared memory");
 };
 
@@ -229,6 +240,106 @@ __device__ __forceinline__ void convert_q40(const uint8_t* row, uint32_t (&o)[32
   }
 }
 
+// Q4_K super-block (144 bytes: f16 d and dmin, 12 packed 6-bit scale and min bytes, then
+// four runs of 32 bytes; run c holds sub-block 2c in its low nibbles and 2c + 1 in its high
+// nibbles, value i of each in byte i). Sub-block s takes scale sc and min mn (s < 4: the low
+// six bits of bytes s and s + 4; s >= 4: the nibbles of byte s + 4 with the top two bits of
+// bytes s - 4 and s); value = d sc q - dmin mn. Here d sc and -dmin mn are rounded to f16 and
+// the value is one f16 fused multiply-add of the exact nibble, as for a Q4_1 block.
+__device__ __forceinline__ void q4k_scale(const uint4& hd, int s, __half2& d2, __half2& m2) {
+  const int i0 = s < 4 ? s : s + 4, i1 = s < 4 ? s + 4 : s - 4, i2 = s;  // bytes read
+  auto byte = [&](int i) -> uint32_t {
+    const uint32_t w = i < 4 ? hd.y : (i < 8 ? hd.z : hd.w);
+    return (w >> (8 * (i & 3))) & 0xFFu;
+  };
+  uint32_t sc, mn;
+  if (s < 4) {
+    sc = byte(i0) & 63u;
+    mn = byte(i1) & 63u;
+  } else {
+    sc = (byte(i0) & 15u) | ((byte(i1) >> 6) << 4);
+    mn = (byte(i0) >> 4) | ((byte(i2) >> 6) << 4);
+  }
+  const float2 f = __half22float2(u2h(hd.x));
+  d2 = __float2half2_rn(f.x * (float)sc);
+  m2 = __float2half2_rn(-(f.y * (float)mn));
+}
+
+// A unit J (sub-blocks 4J .. 4J + 3, 128 values) of the thread's Q4_K row segment -> TMEM
+// columns col .. col + 63. Each sub-block's nibbles are regrouped into the Q4_1 block order
+// (values 4w .. 4w + 3 in the low and 16 + 4w .. in the high nibbles of word w) first.
+__device__ __forceinline__ void convert_q4k(const uint8_t* row, int J, uint32_t col) {
+  const uint4 hd = *reinterpret_cast<const uint4*>(row);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4* run = reinterpret_cast<const uint4*>(row + 16 + 32 * (2 * J + h));
+    const uint4 ra = run[0], rb = run[1];
+    const uint32_t R[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+    for (int hi = 0; hi < 2; ++hi) {
+      __half2 d2, m2;
+      q4k_scale(hd, 4 * J + 2 * h + hi, d2, m2);
+      uint32_t o[16];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t qw = ((R[w] >> (4 * hi)) & 0x0F0F0F0Fu) | (((R[w + 4] >> (4 * hi)) & 0x0F0F0F0Fu) << 4);
+        dequant4<3>(qw, d2, m2, o + 4 * w);
+      }
+      tmem_st16(col + 16u * (2 * h + hi), o);
+    }
+  }
+}
+
+// N words of shared memory from an address on a 2-byte bound: aligned words, funnel-shifted.
+// Reads one word past the N (the callers' stages are followed by more shared memory).
+template <int N>
+__device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&o)[N]) {
+  const uintptr_t u = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(u & ~uintptr_t(3));
+  const uint32_t sh = (uint32_t)(u & 3u) * 8u;
+  uint32_t t[N + 1];
+#pragma unroll
+  for (int i = 0; i <= N; ++i) t[i] = w[i];
+#pragma unroll
+  for (int i = 0; i < N; ++i) o[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
+// Q6_K super-block (210 bytes: ql[128], qh[64], 16 int8 scales, f16 d) in two halves of 128
+// values; sub-block r of half n, value i: the nibble (low for r < 2) of ql[64n + 32 (r % 2) + i]
+// with bits 2r, 2r + 1 of qh[32n + i] above it, scale[8n + 2r + i / 16]; value = d scale (q - 32).
+// A unit J is half J % 2 of super-block J / 2 -> TMEM columns col .. col + 63. The 6-bit q
+// enters an f16 mantissa (1024 + q), 1056 is subtracted exactly, one f16 multiply by the
+// f16-rounded d scale follows.
+__device__ __forceinline__ void convert_q6k(const uint8_t* row, int J, uint32_t col) {
+  const uint8_t* sb = row + 210 * (J >> 1);
+  const int n = J & 1;
+  uint32_t ql[16], qh[8], sc[2], dw[1];
+  lds_words(sb + 64 * n, ql);
+  lds_words(sb + 128 + 32 * n, qh);
+  lds_words(sb + 192 + 8 * n, sc);
+  lds_words(sb + 208, dw);
+  const float d = __half2float(__ushort_as_half((unsigned short)(dw[0] & 0xFFFFu)));
+  const __half2 b1056 = __float2half2_rn(1056.f);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t scw = sc[r >> 1] >> (16 * (r & 1));
+    const __half2 d0 = __float2half2_rn(d * (float)(int)(int8_t)(scw & 0xFFu));
+    const __half2 d1 = __float2half2_rn(d * (float)(int)(int8_t)((scw >> 8) & 0xFFu));
+    const int ls = 4 * (r >> 1), hs = 2 * r, qo = 8 * (r & 1);
+    uint32_t o[16];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t ulo = ((ql[qo + w] >> ls) & 0x0F0F0F0Fu) | (((qh[w] >> hs) & 0x03030303u) << 4);
+      const uint32_t uhi = ((ql[qo + 4 + w] >> ls) & 0x0F0F0F0Fu) | (((qh[4 + w] >> hs) & 0x03030303u) << 4);
+      o[4 * w + 0] = h2u(__hmul2(__hsub2(u2h((ulo & 0x00FF00FFu) | 0x64006400u), b1056), d0));
+      o[4 * w + 1] = h2u(__hmul2(__hsub2(u2h(((ulo >> 8) & 0x00FF00FFu) | 0x64006400u), b1056), d0));
+      o[4 * w + 2] = h2u(__hmul2(__hsub2(u2h((uhi & 0x00FF00FFu) | 0x64006400u), b1056), d1));
+      o[4 * w + 3] = h2u(__hmul2(__hsub2(u2h(((uhi >> 8) & 0x00FF00FFu) | 0x64006400u), b1056), d1));
+    }
+    tmem_st16(col + 16u * r, o);
+  }
+}
+
 // Router rows: the 32 f32 values of sub-box H of a row (values 32H .. 32H + 31 of the
 // 128-value chunk; the sub-box is stored with the 128-byte swizzle: 16-byte chunk j of
 // row r sits at chunk j ^ (r & 7)) -> f16 hi or lo parts in the permuted slot order.
@@ -273,10 +384,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same from a 3-D map (K-quant records: x = byte of the row, y = row of the record's
+// gate/up or down rows, z = expert).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // ---- work units ----------------------------------------------------------------------------
 struct TileUnit {
   const CUtensorMap* map;  // weight rows
   int y0, y1;              // first map row of the tile (gate/up: gate rows, up rows)
+  int z;                   // K-quant maps: the expert (0 for the shared expert)
+  const uint8_t* src;      // Q6_K down: the tile's first row (128 whole rows, one bulk copy)
+  int rbs;                 // Q6_K down: bytes per row
   const uint8_t* b;        // token-operand image of the chunk (first 128-value block)
   int nk;                  // raw chunks (the last one may hold fewer than NAU A units)
   int kdim;                // reduction length
@@ -346,10 +471,14 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, const TileMa
   t.e0 = 0;
   t.npad = (t.n + 15) & ~15;
   const int ff = t.shared ? a.Fs : a.F;
+  constexpr bool KQ = QT == 12 || QT == 14;
+  t.z = t.shared ? 0 : slot;
+  t.src = nullptr;
+  t.rbs = 0;
   if (MODE == 0) {
     t.map = t.shared ? &maps.gu_s : &maps.gu;
-    t.y0 = slot * 3 * ff + 64 * mt;  // gate rows
-    t.y1 = t.y0 + ff;                // up rows
+    t.y0 = KQ ? 64 * mt : slot * 3 * ff + 64 * mt;  // gate rows
+    t.y1 = t.y0 + ff;                                // up rows
     t.nb = 2 * t.npad;
     t.nk = (a.H + G::KR - 1) / G::KR;
     t.kdim = a.H;
@@ -357,7 +486,12 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, const TileMa
     t.b = img + (size_t)2 * t.prow * nkh * 256;
   } else {
     t.map = t.shared ? &maps.dn_s : &maps.dn;
-    t.y0 = t.y1 = slot * 3 * a.H + 2 * a.H + 128 * mt;
+    t.y0 = t.y1 = KQ ? 128 * mt : slot * 3 * a.H + 2 * a.H + 128 * mt;
+    if (QT == 14) {  // the expert's down matrix follows its 2 ff gate/up rows
+      t.rbs = (int)(t.shared ? a.rb_fs : a.rb_f);
+      const uint8_t* rec = t.shared ? a.shared : a.experts + (size_t)slot * a.rec_bytes;
+      t.src = rec + (size_t)2 * ff * a.rb_h + (size_t)128 * mt * t.rbs;
+    }
     t.nb = t.npad;
     t.nk = (ff + G::KR - 1) / G::KR;
     t.kdim = ff;
@@ -406,7 +540,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
   extern __shared__ __align__(1024) uint8_t tsm_dyn[];
   // stages start on a 1024-byte boundary (the router's swizzled boxes need it)
   uint8_t* raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tsm_dyn) + 1023) & ~uintptr_t(1023));
-  uint8_t* bring = raw + G::NSA * G::STAGE;                                 // [NSB][B_STAGE]
+  uint8_t* bring = raw + G::RAW_BYTES;                                      // [NSB][B_STAGE]
   float* scratch = reinterpret_cast<float*>(bring + G::NSB * TP_B_STAGE);  // gate/up and router epilogues
   __shared__ __align__(8) uint64_t raw_full[G::NSA], raw_empty[G::NSA];
   __shared__ __align__(8) uint64_t a_full[TP_GROUPS], a_empty[TP_GROUPS], b_full[G::NSB], b_empty[G::NSB];
@@ -462,10 +596,19 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
         }
         if (lane == 0) {
           uint8_t* dst = raw + sa * G::STAGE;
-          mbar_arrive_expect_tx(&raw_full[sa], (uint32_t)G::STAGE);
+          mbar_arrive_expect_tx(&raw_full[sa], QT == 14 ? (uint32_t)(128 * t.rbs) : (uint32_t)G::STAGE);
           if (MODE == 2) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) tma_load_2d(dst + j * 8192, t.map, kc * 128 + 32 * j, t.y0, &raw_full[sa], pol_w);
+          } else if (QT == 14) {  // 128 whole down rows: one contiguous span of 128 rbs bytes
+            asm volatile(
+                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+                    smem_addr(dst)),
+                "l"(t.src), "r"((uint32_t)(128 * t.rbs)), "r"(smem_addr(&raw_full[sa])), "l"(pol_w)
+                : "memory");
+          } else if (QT == 12) {  // K-quant records through 3-D maps (x byte, y row, z expert)
+            tma_load_3d(dst, t.map, kc * G::SEG, t.y0, t.z, &raw_full[sa], pol_w);
+            if (MODE == 0) tma_load_3d(dst + 64 * G::SEG, t.map, kc * G::SEG, t.y1, t.z, &raw_full[sa], pol_w);
           } else if (MODE == 0) {
             tma_load_2d(dst, t.map, kc * G::SEG, t.y0, &raw_full[sa], pol_w);
             tma_load_2d(dst + 64 * G::SEG, t.map, kc * G::SEG, t.y1, &raw_full[sa], pol_w);
@@ -603,6 +746,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
               convert_f32(stage + jj * 8192, m & 63, m >= 64, o);
               tmem_st16(col + 16u * jj, o);
             }
+          } else if (QT == 12) {
+            convert_q4k(stage + m * G::SEG, j, col);
+          } else if (QT == 14) {
+            convert_q6k(stage + m * t.rbs, j, col);
           } else if (QT == 3) {
             const uint8_t* row = stage + m * G::SEG + 80 * j;  // blocks 4j .. 4j + 3
             uint32_t o[16];
@@ -865,10 +1012,47 @@ cudaError_t launch_tile(const PrefillArgs& a, const TileMaps& maps, cudaStream_t
   return cudaGetLastError();
 }
 
+// 3-D map over `n` blocks of `rows` rows of `row_bytes` bytes, block i at base + i * stride2
+// (the K-quant expert records: rows of a record are whole super-blocks, but a record need
+// not be a whole number of them); boxes of box_x bytes x box_y rows x 1 block.
+cudaError_t encode_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t n,
+                      uint64_t stride2, uint32_t box_x, uint32_t box_y) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {row_bytes, rows, n};
+  const cuuint64_t strides[2] = {row_bytes, stride2};
+  const cuuint32_t box[3] = {box_x, box_y, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_maps(const PrefillArgs& a, TileMaps* m) {
   std::memset(m, 0, sizeof *m);
-  const uint32_t seg = a.qtype == 3 ? Geo<0, 3>::SEG : Geo<0, 2>::SEG;
   cudaError_t e;
+  if (a.qtype == 12) {
+    // K-quant records: gate and up rows (2F of rb_h bytes), then H down rows of rb_f bytes;
+    // Q4_K down rows through a map as well, Q6_K down rows by bulk copies of whole rows
+    const uint32_t seg = Geo<0, 12>::SEG;
+    if ((e = encode_3d(&m->gu, a.experts, a.rb_h, (uint64_t)2 * a.F, (uint64_t)a.E, a.rec_bytes, seg, 64)) !=
+        cudaSuccess)
+      return e;
+    if (a.qtype_dn == 12 &&
+        (e = encode_3d(&m->dn, a.experts + (size_t)2 * a.F * a.rb_h, a.rb_f, (uint64_t)a.H, (uint64_t)a.E,
+                       a.rec_bytes, seg, 128)) != cudaSuccess)
+      return e;
+    if (a.Fs) {
+      const uint64_t srec = (uint64_t)2 * a.Fs * a.rb_h + (uint64_t)a.H * a.rb_fs;
+      if ((e = encode_3d(&m->gu_s, a.shared, a.rb_h, (uint64_t)2 * a.Fs, 1, srec, seg, 64)) != cudaSuccess) return e;
+      if (a.qtype_dn == 12 && (e = encode_3d(&m->dn_s, a.shared + (size_t)2 * a.Fs * a.rb_h, a.rb_fs, (uint64_t)a.H,
+                                             1, srec, seg, 128)) != cudaSuccess)
+        return e;
+    }
+    return encode_2d(&m->rt, a.router_w, true, (uint64_t)a.H, (uint64_t)a.E, 32, 64, true);
+  }
+  const uint32_t seg = a.qtype == 3 ? Geo<0, 3>::SEG : Geo<0, 2>::SEG;
   if ((e = encode_2d(&m->gu, a.experts, false, a.rb_h, (uint64_t)a.E * 3 * a.F, seg, 64, false)) != cudaSuccess)
     return e;
   if ((e = encode_2d(&m->dn, a.experts, false, a.rb_f, (uint64_t)a.E * 3 * a.H, seg, 128, false)) != cudaSuccess)
@@ -1336,8 +1520,14 @@ cudaError_t tile_gemm_launch(const PrefillArgs& a, int mode, cudaStream_t st) {
   TileMaps maps;
   cudaError_t e = make_maps(a, &maps);
   if (e != cudaSuccess) return e;
-  if (mode == 0) return a.qtype == 3 ? launch_tile<0, 3>(a, maps, st) : launch_tile<0, 2>(a, maps, st);
-  return a.qtype == 3 ? launch_tile<1, 3>(a, maps, st) : launch_tile<1, 2>(a, maps, st);
+  const int qt = mode == 0 ? a.qtype : a.qtype_dn;
+  switch (qt) {
+    case 2: return mode == 0 ? launch_tile<0, 2>(a, maps, st) : launch_tile<1, 2>(a, maps, st);
+    case 3: return mode == 0 ? launch_tile<0, 3>(a, maps, st) : launch_tile<1, 3>(a, maps, st);
+    case 12: return mode == 0 ? launch_tile<0, 12>(a, maps, st) : launch_tile<1, 12>(a, maps, st);
+    case 14: return mode == 0 ? cudaErrorInvalidValue : launch_tile<1, 14>(a, maps, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace moe

@@ -87,3 +87,68 @@ def test_flint_eight_tokens():
     cap, _ = image_rows(8, 6, 256, 64)
     assert all(1 <= n <= 8 for _, _, n, _ in chunks)
     assert rows == 16 * len(chunks) <= cap
+
+
+# ---- K-quant layers on the tile pipeline: every copy's bounds ------------------------------
+# Q4_K gate/up rows go through 3-D tensor maps (x = byte of the row, y = row, z = expert) in
+# boxes of one 144-byte super-block x 64 rows; Q4_K down rows in boxes of 144 bytes x 128
+# rows; Q6_K down rows by one bulk copy of 128 whole rows (prefill_tc.cu, tile_unit and the
+# weight producer). A bulk copy and a map's base and strides need 16-byte multiples, and a
+# box's x coordinate times the element size too.
+
+def kq_tile_ok(H, F, Fs, qt, qd):
+    """prefill.cu, prefill_tile_ok, for the K-quant types."""
+    if qt != 12 or qd not in (12, 14):
+        return False
+    if H % 256 or F % 256 or Fs % 256:
+        return False
+    return qd == 12 or (F <= 768 and Fs <= 768)
+
+
+ROW_BYTES = {12: lambda n: n // 256 * 144, 14: lambda n: n // 256 * 210}
+STAGE_Q6 = 128 * 630          # a Q6_K raw stage: 128 rows of up to 768 values
+SMEM_MAX = 227 * 1024 - 2048  # the tile kernels' dynamic shared memory bound
+
+
+@pytest.mark.parametrize("H,F,Fs,qd", [(2560, 768, 768, 14), (256, 256, 256, 14), (256, 256, 256, 12),
+                                      (512, 768, 512, 14), (256, 3072, 0, 12), (2048, 512, 1024, 12),
+                                      (4096, 256, 0, 14), (256, 512, 768, 14)])
+def test_kquant_tile_copies_aligned(H, F, Fs, qd):
+    assert kq_tile_ok(H, F, Fs, 12, qd)
+    rb_h = ROW_BYTES[12](H)
+    rb_f, rb_fs = ROW_BYTES[qd](F), ROW_BYTES[qd](Fs)
+    rec = 2 * F * rb_h + H * rb_f
+    srec = 2 * Fs * rb_h + H * rb_fs
+    for v in (rb_h, rec, srec, 2 * F * rb_h, 2 * Fs * rb_h):
+        assert v % 16 == 0
+    # gate/up boxes: x = 144 kc inside the row, y rows inside the 2F rows of a record
+    for kc in range(H // 256):
+        assert (144 * kc) % 16 == 0 and 144 * kc + 144 <= rb_h
+    assert F % 64 == 0 and (Fs % 64 == 0)
+    if qd == 12:
+        assert rb_f % 16 == 0 and H % 128 == 0
+        for kc in range(F // 256):
+            assert 144 * kc + 144 <= rb_f
+    else:
+        # one bulk copy of 128 whole rows per down tile, from the record's down matrix
+        for ff, rb in ((F, rb_f), (Fs, rb_fs)):
+            if not ff:
+                continue
+            assert (128 * rb) % 16 == 0 and 128 * rb <= STAGE_Q6
+            for mt in range(H // 128):
+                off = 2 * ff * rb_h + 128 * mt * rb
+                assert off % 16 == 0
+                assert off + 128 * rb <= 2 * ff * rb_h + H * rb
+            # the converter's last reads: the d word of the last super-block of row 127, read
+            # as two aligned words, stay within 8 bytes past the stage
+            last = 127 * rb + 210 * (ff // 256 - 1) + 208
+            assert (last & ~3) + 8 <= STAGE_Q6 + 8
+    # shared memory: two Q6_K stages (1024-aligned), two 32 KB token stages, alignment slack
+    raw = ((2 * STAGE_Q6 + 1023) // 1024) * 1024
+    assert raw + 2 * 32768 + 1024 <= SMEM_MAX
+
+
+@pytest.mark.parametrize("H,F,Fs,qd", [(96, 256, 0, 14), (256, 96, 0, 12), (256, 1024, 0, 14),
+                                      (256, 256, 1024, 14), (256, 256, 160, 12)])
+def test_kquant_shapes_left_to_the_general_path(H, F, Fs, qd):
+    assert not kq_tile_ok(H, F, Fs, 12, qd)
