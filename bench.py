@@ -12,8 +12,9 @@ replayed CUDA graph of the steps; rank 0 prints one JSON line.
 
 The line also carries a "prefill" object: the same layer over a batch of 512
 tokens per step (the batched path: router GEMM, selection, expert sort, tensor-
-core grouped GEMMs), timed the same way. With ``--workload flint_prefill_t512``
-the batched step is the headline instead.
+core grouped GEMMs), timed the same way, and under "prefill_configs" the
+Ling-shaped K-quant layer (Q4_K gate/up, Q6_K down) over 512 tokens. With
+``--workload flint_prefill_t512`` the batched step is the headline instead.
 
 ``--impl reference`` times the CPU oracle (float64, one thread) on a bounded
 sample of the same workload instead.
@@ -49,6 +50,8 @@ ARITH_TEXT = {
 }
 # Decode workloads timed beside the headline, each in a sub-object of the line.
 OTHER_DECODE = ("flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1", "ling_kq_decode_t1")
+# batched workloads besides the Flint one, each a sub-object of the line's "prefill_configs"
+OTHER_PREFILL = ("ling_kq_prefill_t512",)
 
 
 def record_bytes(w, ff):
@@ -483,12 +486,17 @@ def bound_calls(ffn, layers, xs_host):
 
 def prefill_launches(w):
     """Kernel launches of one batched pass of at most 512 tokens. The tile path (all three
-    matrices Q4_1, or all Q4_0, with H, F and Fs whole multiples of 128 (Q4_1) or 256 (Q4_0)):
+    matrices Q4_1, or all Q4_0, with H, F and Fs whole multiples of 128 (Q4_1) or 256 (Q4_0);
+    or Q4_K gate/up with Q4_K or Q6_K down rows, H, F, Fs multiples of 256, Q6_K F, Fs <= 768):
     token images, router, top-k, sort, routed images, gate/up, down, combine. The general
     path: router, top-k, sort, x operand, gate/up, down, combine."""
     qt, qd = w["qtype"], w.get("qtype_down") or w["qtype"]
-    kc = 128 if qt == 3 else 256
-    tile = qt == qd and qt in (2, 3) and all(v % kc == 0 for v in (w["hidden"], w["expert_ff"], w["shared_ff"]))
+    H, F, Fs = w["hidden"], w["expert_ff"], w["shared_ff"]
+    if qt == 12 and qd in (12, 14):
+        tile = all(v % 256 == 0 for v in (H, F, Fs)) and (qd == 12 or (F <= 768 and Fs <= 768))
+    else:
+        kc = 128 if qt == 3 else 256
+        tile = qt == qd and qt in (2, 3) and all(v % kc == 0 for v in (H, F, Fs))
     return 8 if tile else 7
 
 
@@ -750,19 +758,25 @@ def main():
     e2e_val = job_rate(n_e2e * T, e2e_sec, world, dev)
 
     pre = None
+    pre_other = {}
     if args.prefill_steps > 0:
         pre = bench_prefill(ffn, synth, "flint_prefill_t512", dev, rank, args.prefill_steps, 24)
         reduce_prefill(pre, world, dev)
+        for name in OTHER_PREFILL:
+            pre_other[name] = bench_prefill(ffn, synth, name, dev, rank, args.prefill_steps, 24)
+            reduce_prefill(pre_other[name], world, dev)
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
-    if pre is not None:
-        a = pre["bytes_per_step"] / (pre["ms_per_step"] * 1e-3) / 1e9
-        pp = profile_counters("tile_gemm_flint_prefill_t512", "tile_gemm")
-        pre["roofline"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s",
-                           "frac": round(a / peak, 4), "peak_kind": peak_kind, "over": "the whole batched step",
-                           "traffic": pp["dram_bytes_per_step"] if pp else None,
-                           "tensor_pipe_active": pp["tensor_pipe_active"] if pp else None}
+    for p in [pre, *pre_other.values()]:
+        if p is None:
+            continue
+        a = p["bytes_per_step"] / (p["ms_per_step"] * 1e-3) / 1e9
+        pp = profile_counters(f"tile_gemm_{p['workload']}", "tile_gemm")
+        p["roofline"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(a / peak, 4), "peak_kind": peak_kind, "over": "the whole batched step",
+                         "traffic": pp["dram_bytes_per_step"] if pp else None,
+                         "tensor_pipe_active": pp["tensor_pipe_active"] if pp else None}
     prof = profile_counters(f"decode_chain_{args.workload}", "decode_chain")
     roof = decode_roofline(w, ms_per_step, peak, peak_kind)
     roof.update({"traffic": prof["dram_bytes_per_step"] if prof else None,
@@ -824,6 +838,7 @@ def main():
         "gpu_launches": 3 * args.steps * head["repeats"],
         "clocks": clocks,
         "prefill": pre,
+        "prefill_configs": pre_other,
     }
     print(json.dumps(line))
 

@@ -3,7 +3,8 @@
 //
 // One CTA per SM, 608 threads:
 //   warp 0       weight producer: 2-D TMA tensor copies of the raw weight rows of each
-//                pipeline chunk (one box of 64 or 128 rows) into shared-memory stages
+//                pipeline chunk (one box of 64 or 128 rows) into shared-memory stages (3-D
+//                maps for K-quant records; one bulk copy of 128 whole rows for Q6_K down rows)
 //   warp 1       MMA issuer: tcgen05.mma with A in tensor memory, B in shared memory,
 //                f32 accumulator in tensor memory; commits release the stages
 //   warp 2       token-operand producer: one bulk copy per 128 K values of a pre-tiled
@@ -11,8 +12,8 @@
 //   warps 3..14  converters in three groups of four warps (one per TMEM lane quarter;
 //                thread = tile row = TMEM lane). Every converter warp waits for every raw
 //                chunk and releases it; 128-value A unit n of the tile stream goes to group
-//                n % 3, which owns one TMEM A slot: raw 4-bit blocks (or f32 router rows)
-//                -> f16 rows of A, written with tcgen05.st
+//                n % 3, which owns one TMEM A slot: raw 4-bit blocks, Q4_K or Q6_K
+//                super-blocks (or f32 router rows) -> f16 rows of A, written with tcgen05.st
 //   warps 15..18 the epilogue, one warp per TMEM lane quarter (tcgen05.ld), on one of two
 //                accumulators while the MMAs of the next tile run on the other
 //

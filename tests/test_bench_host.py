@@ -30,10 +30,13 @@ def test_kquant_record_bytes():
 
 
 def test_batched_launch_count():
-    # the tile path (all Q4_1 or all Q4_0, K dimensions in whole chunks) launches eight kernels
-    # a pass, the general path seven
+    # the tile path (all Q4_1 or all Q4_0 with K dimensions in whole chunks; Q4_K gate/up with
+    # Q4_K or Q6_K down in whole super-blocks) launches eight kernels a pass, the general path seven
     assert bench.prefill_launches(synth.WORKLOADS["flint_prefill_t512"]) == 8
-    assert bench.prefill_launches(synth.WORKLOADS["ling_kq_prefill_t512"]) == 7
+    assert bench.prefill_launches(synth.WORKLOADS["ling_kq_prefill_t512"]) == 8
+    wide_q6 = {**synth.WORKLOADS["ling_kq_prefill_t512"], "expert_ff": 1024}  # Q6_K rows past 768 values
+    assert bench.prefill_launches(wide_q6) == 7
+    assert bench.prefill_launches({**wide_q6, "qtype_down": synth.Q4_K}) == 8
     odd = {**synth.WORKLOADS["flint_prefill_t512"], "hidden": 96, "expert_ff": 96, "shared_ff": 0}
     assert bench.prefill_launches(odd) == 7
     q40 = {**synth.WORKLOADS["flint_prefill_t512"], "qtype": synth.Q4_0}  # Q4_0 chunks are 256 values

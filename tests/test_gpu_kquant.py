@@ -2,8 +2,9 @@
 
 The Ling store keeps Q4_K gate/up rows and Q6_K or Q4_K down rows (ling_moe_ssd.js, file
 header and planLayoutLing). Both paths run them: the decode chain (block dots on 16-bit
-fixed-point activations by default) and the batched path's general contractions
-(super-blocks dequantised to f16). Same bars as every parity test: identical ordered picks, weights
+fixed-point activations by default) and the batched path (the tile pipeline where the shapes fit
+its copies, H, F, Fs multiples of 256 and Q6_K rows of at most 768 values; the general
+contractions otherwise; super-blocks dequantised to f16 in both). Same bars as every parity test: identical ordered picks, weights
 within W_REL, each token within relative L2 OUT_REL_L2.
 """
 
@@ -92,7 +93,8 @@ def test_mixed_types_decode(w, flags):
 
 @pytest.mark.parametrize("w", MIXED, ids=[f"s{w['seed']}" for w in MIXED])
 def test_mixed_types_batched(w):
-    # the same layers through the batched path's general contractions
+    # the same layers through the batched path (tile pipeline: seeds 70, 71, 74, 75, 77, 78;
+    # general contractions: 72, 73, 76)
     w = {**w, "n_tokens": 37}
     layer = synth.make_layer(w)
     x, _ = margin_tokens(layer, w, w["n_tokens"], seed=w["seed"], stream=3)
