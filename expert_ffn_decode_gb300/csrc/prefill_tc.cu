@@ -5,8 +5,11 @@
 //   warp 0       weight producer: 2-D TMA tensor copies of the raw weight rows of each
 //                pipeline chunk (one box of 64 or 128 rows) into shared-memory stages (3-D
 //                maps for K-quant records; one bulk copy of 128 whole rows for Q6_K down rows)
-//   warp 1       MMA issuer: tcgen05.mma with A in tensor memory, B in shared memory,
-//                f32 accumulator in tensor memory; commits release the stages
+//   warps 1, 19  MMA issuers: tcgen05.mma with A in tensor memory, B in shared memory,
+//                f32 accumulator in tensor memory; commits release the stages. One thread
+//                issues a small-N MMA only every ~50-100 cycles (its waits, fence and commits
+//                included), so two threads share the A units of a tile: unit n goes to issuer
+//                n % 2, which owns its own accumulation chains (the sums stay deterministic)
 //   warp 2       token-operand producer: one bulk copy per 128 K values of a pre-tiled
 //                image of the chunk's token rows
 //   warps 3..14  converters in three groups of four warps (one per TMEM lane quarter;
@@ -44,7 +47,9 @@ constexpr int TP_CONV_WARPS = 12;                 // three groups of four (one w
 constexpr int TP_GROUPS = TP_CONV_WARPS / 4;      // A unit n is converted by group n % TP_GROUPS
 constexpr int TP_EPI_WARPS = 4;                   // one per lane quarter
 constexpr int TP_EPI_WARP0 = 3 + TP_CONV_WARPS;   // first epilogue warp
-constexpr int TP_THREADS = 96 + 32 * (TP_CONV_WARPS + TP_EPI_WARPS);  // producers, MMA, converters, epilogue
+constexpr int TP_MMA_WARP2 = TP_EPI_WARP0 + TP_EPI_WARPS;  // the second MMA issuer
+// producers, the first MMA issuer, converters, epilogue, the second MMA issuer
+constexpr int TP_THREADS = 96 + 32 * (TP_CONV_WARPS + TP_EPI_WARPS) + 32;
 constexpr int TP_KB = 128;                        // K values per token-operand stage
 constexpr int TP_B_STAGE = 128 * TP_KB * 2;       // up to 128 rows: 32 KB
 constexpr int TP_SCRATCH = 64 * 65 * 4;           // gate/up and router epilogue exchange
@@ -517,6 +522,13 @@ __device__ __forceinline__ int tile_chains(int nb) {
   return nb * 4 <= cols ? 4 : (nb * 2 <= cols ? 2 : 1);
 }
 
+// A tile whose A units the two MMA issuers share (unit n to issuer n % 2): it has at least two
+// accumulation chains and two A units. Every role derives the owner of a unit from this.
+template <int MODE>
+__device__ __forceinline__ bool tile_split(const TileUnit& t) {
+  return tile_chains<MODE>(t.nb) >= 2 && t.kdim / TP_KB >= 2;
+}
+
 // Sum over the tile's chains of 8 accumulator columns starting at column c.
 template <int MODE>
 __device__ __forceinline__ void acc_ld8(uint32_t acc, int nb, int c, float (&v)[8]) {
@@ -544,7 +556,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
   uint8_t* bring = raw + G::RAW_BYTES;                                      // [NSB][B_STAGE]
   float* scratch = reinterpret_cast<float*>(bring + G::NSB * TP_B_STAGE);  // gate/up and router epilogues
   __shared__ __align__(8) uint64_t raw_full[G::NSA], raw_empty[G::NSA];
-  __shared__ __align__(8) uint64_t a_full[TP_GROUPS], a_empty[TP_GROUPS], b_full[G::NSB], b_empty[G::NSB];
+  // a_full and b_full have one barrier per owning MMA issuer: an issuer skips the other's
+  // units, and a parity wait must never fall two phases behind the barrier it waits on
+  __shared__ __align__(8) uint64_t a_full[TP_GROUPS][2], a_empty[TP_GROUPS], b_full[G::NSB][2], b_empty[G::NSB];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin, scr_full, scr_empty;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -557,18 +571,20 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
       mbar_init(&raw_empty[i], TP_CONV_WARPS);  // every converter warp releases every chunk
     }
     for (int i = 0; i < TP_GROUPS; ++i) {
-      mbar_init(&a_full[i], 4);  // the group's four warps
+      mbar_init(&a_full[i][0], 4);  // the group's four warps
+      mbar_init(&a_full[i][1], 4);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < G::NSB; ++i) {
-      mbar_init(&b_full[i], 1);
+      mbar_init(&b_full[i][0], 1);
+      mbar_init(&b_full[i][1], 1);
       mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_full[i], 2);  // both issuers commit every tile
       mbar_init(&acc_empty[i], TP_EPI_WARPS);
     }
-    mbar_init(&fin, 1);
+    mbar_init(&fin, 2);
     mbar_init(&scr_full, TP_EPI_WARPS / 2);   // epilogue warps of lanes 64..127
     mbar_init(&scr_empty, TP_EPI_WARPS / 2);  // epilogue warps of lanes 0..63
     abort_flag = 0;
@@ -632,45 +648,60 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
   } else if (warp == 2) {
     // ------------------------------ token-operand producer ------------------------------
     uint32_t rb = 0;
+    // bit 2 sb + o: (stage sb, issuer o) filled at least once / its fill count is odd
+    uint32_t filled = 0, fodd = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
       const uint32_t bbytes = (uint32_t)t.nb * 256u;
+      const bool split = tile_split<MODE>(t);
       for (int kk = 0; kk < t.kdim / TP_KB; ++kk) {  // one stage per 128-value A unit
         const int sb = (int)(rb % G::NSB);
+        const int own = split ? (int)(rb & 1u) : 0;
         if (rb >= (uint32_t)G::NSB && !tp_wait_warp(&b_empty[sb], ((rb / G::NSB) - 1) & 1u, abrt)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&b_full[sb], bbytes);
+          mbar_arrive_expect_tx(&b_full[sb][own], bbytes);
           const uint8_t* src = t.b + (size_t)kk * bbytes;
           asm volatile(
               "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                   smem_addr(bring + sb * TP_B_STAGE)),
-              "l"(src), "r"(bbytes), "r"(smem_addr(&b_full[sb]))
+              "l"(src), "r"(bbytes), "r"(smem_addr(&b_full[sb][own]))
               : "memory");
         }
         __syncwarp();
+        filled |= 1u << (2 * sb + own);
+        fodd ^= 1u << (2 * sb + own);
         ++rb;
       }
     }
     if (lane == 0) {
-      for (int sb = 0; sb < G::NSB; ++sb) {
-        const uint32_t f = rb > (uint32_t)sb ? (rb - sb - 1) / G::NSB + 1 : 0u;
-        if (f) mbar_wait(&b_full[sb], (f - 1) & 1u);
-      }
+      for (int sb = 0; sb < G::NSB; ++sb)
+        for (int o = 0; o < 2; ++o)  // the last fill's phase parity is (count - 1) & 1
+          if ((filled >> (2 * sb + o)) & 1u) mbar_wait(&b_full[sb][o], ((fodd >> (2 * sb + o)) & 1u) ^ 1u);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
+  } else if (warp == 1 || warp == TP_MMA_WARP2) {
+    // ------------------------------ MMA issuers ------------------------------
+    // Both issuers walk every tile and A unit in order (so their unit, stage and parity
+    // counts agree) and issue the units they own. A tile with at least two chains and two
+    // A units is split: unit n goes to issuer n % 2, and each issuer accumulates into its
+    // own chains only (four chains: chains iss and 2 + iss; two: chain iss), so every chain
+    // receives its MMAs from one thread in a fixed order. Other tiles go to issuer 0 alone.
+    const int iss = warp == 1 ? 0 : 1;
     if (lane == 0) {
       uint32_t n = 0, rb = 0, uc = 0;
+      // bit g / sb: parity of this issuer's next wait on a_full[g][iss] / b_full[sb][iss]
+      uint32_t pa = 0, pb = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
         const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
         const uint32_t idesc = idesc_f16_f32(128, t.nb);
         const int nch = tile_chains<MODE>(t.nb);
+        const int nku = t.kdim / TP_KB;  // A units of the tile
+        const bool split = tile_split<MODE>(t);
         const int ab = (int)(uc % G::NACC);
         const uint32_t acc = tmem + acc_col<MODE>(ab);  // accumulator columns
         if (uc >= (uint32_t)G::NACC && !tp_wait(&acc_empty[ab], ((uc / G::NACC) - 1) & 1u, abrt)) {
@@ -678,37 +709,53 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
           break;
         }
         tc_fence_after_sync();
-        for (int kk = 0; kk < t.kdim / TP_KB && ok; ++kk, ++n) {  // A units in order
-          const int g = (int)(n % TP_GROUPS);  // A unit n was converted by group n % 4
-          if (!tp_wait(&a_full[g], (n / TP_GROUPS) & 1u, abrt)) {
+        bool fresh = true;  // no MMA of this issuer in this tile yet
+        for (int kk = 0; kk < nku && ok; ++kk, ++n, ++rb) {  // A units in order
+          if ((split ? (int)(n & 1u) : 0) != iss) continue;
+          const int g = (int)(n % TP_GROUPS);  // A unit n was converted by group n % 3
+          if (!tp_wait(&a_full[g][iss], (pa >> g) & 1u, abrt)) {
             ok = false;
             break;
           }
+          pa ^= 1u << g;
           const int sb = (int)(rb % G::NSB);
-          if (!tp_wait(&b_full[sb], (rb / G::NSB) & 1u, abrt)) {
+          if (!tp_wait(&b_full[sb][iss], (pb >> sb) & 1u, abrt)) {
             ok = false;
             break;
           }
+          pb ^= 1u << sb;
           tc_fence_after_sync();
           const uint8_t* B = bring + sb * TP_B_STAGE;
           const uint32_t ta0 = tmem + TP_A_COL + 64u * g;  // the group's A slot
 #pragma unroll
           for (int j = 0; j < TP_KB / 16; ++j) {
-            // MMA j accumulates into chain j % nch: narrow tiles keep several independent
-            // accumulation chains in flight instead of one latency-bound chain
-            const int ch = j & (nch - 1);
+            // narrow tiles keep several independent accumulation chains in flight instead of
+            // one latency-bound chain; the first MMA into a chain in the tile overwrites it
+            int ch;
+            bool accum;
+            if (!split) {
+              ch = j & (nch - 1);
+              accum = kk > 0 || j >= nch;
+            } else if (nch == 4) {
+              ch = 2 * (j & 1) + iss;
+              accum = !fresh || j >= 2;
+            } else {
+              ch = iss;
+              accum = !fresh || j >= 1;
+            }
             const uint64_t bd = smem_desc(B + 2 * j * 16 * t.nb, 16u * t.nb, 128);
-            mma_f16_ta(acc + (uint32_t)(ch * t.nb), ta0 + 8u * j, bd, idesc, kk > 0 || j >= nch);
+            mma_f16_ta(acc + (uint32_t)(ch * t.nb), ta0 + 8u * j, bd, idesc, accum);
           }
+          fresh = false;
           mma_commit(&b_empty[sb]);
           mma_commit(&a_empty[g]);
-          ++rb;
         }
-        if (ok) mma_commit(&acc_full[ab]);
+        if (ok) mma_commit(&acc_full[ab]);  // arrives once this issuer's MMAs are done
       }
-      // every MMA issued has completed before the columns are freed
+      // every MMA issued has completed before the columns are freed: this wait ignores the
+      // abort flag (MMAs in flight complete by themselves; freeing TMEM under them would not)
       mma_commit(&fin);
-      tp_wait(&fin, 0, abrt);
+      mbar_wait(&fin, 0);
     }
     __syncwarp();
   } else if (warp < TP_EPI_WARP0) {
@@ -720,6 +767,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
       const TileUnit t = tile_unit<MODE, QT>(a, maps, u);
+      const bool split = tile_split<MODE>(t);  // unit nj then goes to MMA issuer nj % 2
       for (int kc = 0; kc < t.nk; ++kc, ++ka) {
         // every warp waits for every chunk and releases it: a warp can then never release
         // a stage's next use before its current one has landed
@@ -780,7 +828,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
           tmem_st_wait();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[grp]);
+          if (lane == 0) mbar_arrive(&a_full[grp][split ? (int)(nj & 1u) : 0]);
         }
         if (!ok) break;
         n += nau;
@@ -1369,7 +1417,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1) swap_down(const PrefillArgs a, 
         if (ok) mma_commit(&acc_full[ab]);
       }
       mma_commit(&fin);
-      tp_wait(&fin, 0, abrt);
+      mbar_wait(&fin, 0);  // not cut short by an abort: the MMAs in flight end before TMEM is freed
     }
     __syncwarp();
   } else if (warp < SW_EPI_WARP0) {
