@@ -85,7 +85,10 @@ struct Geo {
                                          : KR / 32 * (QT == 3 ? 20 : 18);  // bytes per row (at most, Q6_K)
   static constexpr int STAGE = ROWS * SEG;
   static constexpr int NAU = KR / TP_KB;                             // 128-value A units per chunk
-  static constexpr int NSB = 2;                                      // token-operand stages
+  // token-operand stages: with two MMA issuers each owns every other unit's stage, so gate/up
+  // keeps three (a stage refill is an L2 round trip); the down contraction's Q6_K stages leave
+  // room for two
+  static constexpr int NSB = MODE == 0 ? 3 : 2;
   static constexpr int SCR = MODE == 1 ? 0 : TP_SCRATCH;
   static constexpr int NSA0 = (TP_SMEM_MAX - NSB * TP_B_STAGE - SCR - 1024) / STAGE;
   static constexpr int NSA = NSA0 > 16 ? 16 : NSA0;                  // raw stages (one shared ring)

@@ -46,7 +46,7 @@ def split_of(nku, nch):
     return nch >= 2 and nku >= 2
 
 
-def simulate(seed, tiles, per_issuer_full=True):
+def simulate(seed, tiles, per_issuer_full=True, nsb=NSB):
     """tiles: (A units of the tile, accumulation chains, A units per raw chunk) per tile."""
     rng = random.Random(seed)
     nfull = 2 if per_issuer_full else 1
@@ -54,11 +54,11 @@ def simulate(seed, tiles, per_issuer_full=True):
     raw_empty = [Bar(G * 4) for _ in range(NSA)]
     a_full = [[Bar(4) for _ in range(nfull)] for _ in range(G)]
     a_empty = [Bar(1) for _ in range(G)]
-    b_full = [[Bar(1) for _ in range(nfull)] for _ in range(NSB)]
-    b_empty = [Bar(1) for _ in range(NSB)]
+    b_full = [[Bar(1) for _ in range(nfull)] for _ in range(nsb)]
+    b_empty = [Bar(1) for _ in range(nsb)]
     acc_full = [Bar(2) for _ in range(NACC)]
     acc_empty = [Bar(4) for _ in range(NACC)]
-    slot_unit, slot_reads, stage_reads = [None] * G, [0] * G, [0] * NSB
+    slot_unit, slot_reads, stage_reads = [None] * G, [0] * G, [0] * nsb
     pending = {0: [], 1: []}
     chains = {}
 
@@ -82,9 +82,9 @@ def simulate(seed, tiles, per_issuer_full=True):
         for nku, nch, nau in tiles:
             split = split_of(nku, nch)
             for _ in range(nku):
-                sb = rb % NSB
-                if rb >= NSB:
-                    while not b_empty[sb].done(rb // NSB - 1):
+                sb = rb % nsb
+                if rb >= nsb:
+                    while not b_empty[sb].done(rb // nsb - 1):
                         yield 0
                 assert stage_reads[sb] == 0, "token stage refilled while MMAs read it"
                 b_full[sb][owner(split, rb) if per_issuer_full else 0].arrive()
@@ -120,7 +120,7 @@ def simulate(seed, tiles, per_issuer_full=True):
 
     def issuer(iss):
         n = rb = uc = 0
-        pa, pb = [0] * G, [0] * NSB  # this issuer's waits on each slot's / stage's full barrier
+        pa, pb = [0] * G, [0] * nsb  # this issuer's waits on each slot's / stage's full barrier
         for ti, (nku, nch, nau) in enumerate(tiles):
             split = split_of(nku, nch)
             ab = uc % NACC
@@ -130,12 +130,12 @@ def simulate(seed, tiles, per_issuer_full=True):
             fresh = True
             for kk in range(nku):
                 if owner(split, n) == iss:
-                    g, sb = n % G, rb % NSB
+                    g, sb = n % G, rb % nsb
                     ka_ = pa[g] if per_issuer_full else n // G
                     while not a_full[g][iss if per_issuer_full else 0].done(ka_):
                         yield 0
                     pa[g] += 1
-                    kb_ = pb[sb] if per_issuer_full else rb // NSB
+                    kb_ = pb[sb] if per_issuer_full else rb // nsb
                     while not b_full[sb][iss if per_issuer_full else 0].done(kb_):
                         yield 0
                     pb[sb] += 1
@@ -213,11 +213,12 @@ def random_tiles(rng, real):
             for _ in range(rng.randint(1, 7))]
 
 
+@pytest.mark.parametrize("nsb", [2, 3])  # token stages: down / router keep 2, gate/up 3
 @pytest.mark.parametrize("real", [False, True])
-def test_two_issuer_protocol(real):
+def test_two_issuer_protocol(real, nsb):
     rng = random.Random(7 if real else 3)
     for seed in range(40 if real else 120):
-        simulate(seed, random_tiles(rng, real))
+        simulate(seed, random_tiles(rng, real), nsb=nsb)
 
 
 def test_shared_full_barriers_would_alias():
