@@ -298,6 +298,7 @@ def print_trace(ffn, w, layers, xs, L, NX, flags, dev, stream, chain=8, reps=5):
     off = ffn.moe_trace_offset(cfg)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     out = torch.empty(w["hidden"], device=dev)
+    torch.cuda.synchronize(dev)  # the zeroed workspace before `stream` uses it
     nc = torch.cuda.get_device_properties(dev).multi_processor_count
     rows = []
     # the chain is captured in a CUDA graph and replayed, as the timed steps are, so the
@@ -393,6 +394,7 @@ def decode_timing(ffn, w, layers, xs, flags, dev, stream, K, warmup, min_ms):
     ws_bytes = ffn.moe_workspace_size(cfg)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     outs = torch.zeros((2, H), device=dev)
+    torch.cuda.synchronize(dev)  # the default stream's buffers are complete before `stream` uses them
 
     def step(i, st):
         lay = layers[i % L]
@@ -445,6 +447,7 @@ def bench_chained(ffn, w, layers, L, dev, stream, reps=10, flags=0):
     ws_bytes = ffn.moe_workspace_size(cfg)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     bufs = torch.empty((2, H), device=dev)
+    torch.cuda.synchronize(dev)  # norm, x0 and the zeroed workspace before `stream` reads them
 
     def step(i):
         lay = layers[i % L]
@@ -527,6 +530,9 @@ def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, 
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
     ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    # the layers, tokens and zeroed buffers are drawn on the default stream: complete them
+    # before the side stream reads them (and before it reuses memory their temporaries held)
+    torch.cuda.synchronize(dev)
 
     def step(i, st, want_ids=False):
         lay = layers[i % L]
@@ -538,8 +544,12 @@ def bench_prefill(ffn, synth, workload, dev, rank, steps, warmup, e2e_steps=20, 
     distinct = []
     with torch.cuda.stream(stream):
         for i in range(L * NX):
+            ids.fill_(-1)
             step(i, stream, want_ids=True)
             stream.synchronize()
+            lo, hi = int(ids.min()), int(ids.max())
+            if lo < 0 or hi >= w["n_experts"]:  # every pick is an expert of the layer
+                raise RuntimeError(f"{workload}: routing call {i} returned picks in [{lo}, {hi}]")
             distinct.append(int(torch.unique(ids).numel()))
     ffn.check(ffn.moe_workspace_status(ws, stream))
     G = L * NX * max(1, 24 // (L * NX))
@@ -606,6 +616,7 @@ def sweep_tokens(args, ffn, synth, w, dev, layers_n=4, calls=8, reps=5):
         n_t, n_1 = ffn.moe_workspace_size(cfg_t), ffn.moe_workspace_size(cfg_1)
         ws_t = torch.zeros(n_t, dtype=torch.uint8, device=dev)
         ws_1 = torch.zeros(n_1, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)  # before the side stream uses them
 
         def whole(i):
             lay = layers[i % layers_n]

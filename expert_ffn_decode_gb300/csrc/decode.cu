@@ -25,11 +25,11 @@
 // every exchange, and every mbarrier wait is bounded in time.
 //
 // Dequant-dot: a 4-bit block (ggml Q4_0/Q4_1, 32 values) times 32 activations.
-// Activations are held per 32-block as 16-bit integers v = x * 2^k with |v| <= 2^14
-// (power-of-two block scale; error at most 2^-15 of the block's largest magnitude),
-// split into a low (unsigned) and a high (signed) byte plane; dp4a forms sum(q * v)
-// exactly in int32, and the block result d * s * sum(q v) (+ m * s * sum(v) for
-// Q4_1, - 8 d s sum(v) for Q4_0) is accumulated in fp32. The block formats and the
+// Activations are held per 16 values (half a block) as 16-bit integers v = x * 2^k with
+// |v| <= 2^14 (a power-of-two scale per half; error at most 2^-15 of the half's largest
+// magnitude), split into a low (unsigned) and a high (signed) byte plane; dp4a forms
+// sum(q * v) of each half exactly in int32, and the block result d * (s0 S0 + s1 S1)
+// (+ m * sum(x) for Q4_1, - 8 d sum(x) for Q4_0) is accumulated in fp32. The block formats and the
 // per-block dot identity follow flint_moe_ssd.js (WGSL section, Q41DOT and its
 // comment). K-quant rows (256-value super-blocks: Q4_K gate/up, Q6_K or Q4_K down, as
 // the Ling store holds them) are walked in the same 32-value blocks: a Q4_K sub-block
@@ -55,20 +55,20 @@ constexpr int DN_THREADS = 256;  // down: 8 warps
 // ---------------------------------------------------------------------------
 
 // One quantisation task: 8 consecutive values (part qq of block b) of a block whose
-// four tasks sit in four consecutive lanes. The block's 32 values v_i become integers
-// q_i = v_i * 2^k, |q_i| <= 2^14, the power of two chosen from the block's largest
-// magnitude; a block whose values are all below 2^-97 in magnitude is taken as zero.
-// Plane P (0: low byte, 1: signed high byte) of the block holds byte P of every q_i;
-// the planes' 16 words are stored as 4 chunks of 4 words, chunk c of block b at
-// planes + (c * stride + b) * 16, so that lanes reading consecutive blocks hit
-// consecutive 16-byte words; info[b] = {2^-k, sum q_i}.
+// four tasks sit in four consecutive lanes. Each half of the block (values 0..15: tasks
+// 0, 1; values 16..31: tasks 2, 3) becomes integers q_i = v_i * 2^k, |q_i| <= 2^14, the
+// power of two chosen from the half's largest magnitude; a half whose values are all below
+// 2^-97 in magnitude is taken as zero. Plane P (0: low byte, 1: signed high byte) of the
+// block holds byte P of every q_i; the planes' 16 words are stored as 4 chunks of 4 words
+// (chunk 2P + h: plane P of half h), chunk c of block b at planes + (c * stride + b) * 16,
+// so that lanes reading consecutive blocks hit consecutive 16-byte words;
+// info[b] = {2^-k0, sum of half 0's q_i, 2^-k1, sum of half 1's q_i}.
 __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int b, int qq, int stride,
-                                           uint8_t* planes, float2* info) {
+                                           uint8_t* planes, float4* info) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the half's other task
   const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFF);  // amax < 2^(eb - 126)
   float inv = 0.f, sc = 0.f;
   if (eb >= 30) {
@@ -83,7 +83,6 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
     X += q[i];
   }
   X += __shfl_xor_sync(0xffffffffu, X, 1);
-  X += __shfl_xor_sync(0xffffffffu, X, 2);
   if (active) {
 #pragma unroll
     for (int P = 0; P < 2; ++P) {
@@ -98,7 +97,7 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
       const int c = 2 * P + (qq >> 1);
       *reinterpret_cast<uint2*>(planes + ((size_t)c * stride + b) * 16 + 8 * (qq & 1)) = make_uint2(w[0], w[1]);
     }
-    if (qq == 0) info[b] = make_float2(sc, (float)X);
+    if ((qq & 1) == 0) reinterpret_cast<float2*>(info + b)[qq >> 1] = make_float2(sc, (float)X);
   }
 }
 
@@ -109,7 +108,7 @@ __device__ __forceinline__ void quant_task(const float (&v)[8], bool active, int
 // before computing; every thread runs the same number of rounds and whole warps call it
 // (the groups use shuffles). TPR: tasks a thread loads per round.
 template <int TPR, bool kShared = false>
-__device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float2* info,
+__device__ __forceinline__ void quant_blocks(const float* src, int nb, int stride, uint8_t* planes, float4* info,
                                              int t, int nthreads, const float* mul = nullptr, float scal = 1.f,
                                              float* ss = nullptr) {
   #pragma unroll 1
@@ -155,8 +154,9 @@ __device__ __forceinline__ void quant_blocks(const float* src, int nb, int strid
 }
 
 struct ActBlock {
-  uint32_t p[16];  // planes: [0,8) low bytes, [8,16) signed high bytes
-  float s, X;
+  uint32_t p[16];  // planes: [0,8) low bytes, [8,16) signed high bytes (words 0-3, 8-11: half 0)
+  float s0, s1;    // the halves' scales 2^-k
+  float XS;        // s0 X0 + s1 X1: the block's sum of activations
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -186,24 +186,26 @@ __device__ __forceinline__ void load_act_block_s(ActBlock& a, uint32_t planes, u
     a.p[4 * c + 2] = v.z;
     a.p[4 * c + 3] = v.w;
   }
-  const float2 f = lds64f(info + (uint32_t)b * 8u);
-  a.s = f.x;
-  a.X = f.y;
+  const uint4 f = lds128(info + (uint32_t)b * 16u);
+  a.s0 = __uint_as_float(f.x);
+  a.s1 = __uint_as_float(f.z);
+  a.XS = fmaf(a.s0, __uint_as_float(f.y), a.s1 * __uint_as_float(f.w));
 }
 
-// sum(q * v) over the block for the four nibble words (exact: |sum| < 2^24).
+// s0 S0 + s1 S1, S_h = sum(q * v) over half h of the block for the four nibble words (exact:
+// |S_h| < 2^24): the low nibbles hold half 0, the high nibbles half 1.
 __device__ __forceinline__ float nibble_dot(const uint32_t (&qw)[4], const ActBlock& a) {
-  int a0 = 0, a1 = 0;
+  int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t lo = qw[i] & 0x0F0F0F0Fu;         // values 4i .. 4i+3
     const uint32_t hi = (qw[i] >> 4) & 0x0F0F0F0Fu;  // values 16+4i .. 16+4i+3
     a0 = dp4a_uu(lo, a.p[i], a0);
-    a0 = dp4a_uu(hi, a.p[4 + i], a0);
     a1 = dp4a_us(lo, a.p[8 + i], a1);
-    a1 = dp4a_us(hi, a.p[12 + i], a1);
+    b0 = dp4a_uu(hi, a.p[4 + i], b0);
+    b1 = dp4a_us(hi, a.p[12 + i], b1);
   }
-  return (float)(a1 * 256 + a0);
+  return fmaf(a.s0, (float)(a1 * 256 + a0), a.s1 * (float)(b1 * 256 + b0));
 }
 
 // A block of a row as five 32-bit words read from the 4-byte boundary at or below
@@ -228,14 +230,14 @@ __device__ __forceinline__ float raw_block_dot(const RawBlock& r, const ActBlock
     const uint32_t qw[4] = {r.w[1], r.w[2], r.w[3], r.w[4]};
     const float S = nibble_dot(qw, a);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r.w[0]));
-    return a.s * fmaf(f.x, S, f.y * a.X);
+    return fmaf(f.x, S, f.y * a.XS);
   } else {
     const uint32_t dbits = __funnelshift_rc(r.w[0], r.w[1], r.sh) & 0xFFFFu;
     const uint32_t qw[4] = {__funnelshift_rc(r.w[0], r.w[1], 16 + r.sh), __funnelshift_rc(r.w[1], r.w[2], 16 + r.sh),
                             __funnelshift_rc(r.w[2], r.w[3], 16 + r.sh), __funnelshift_rc(r.w[3], r.w[4], 16 + r.sh)};
     const float S = nibble_dot(qw, a);
     const float d = __half2float(__ushort_as_half((unsigned short)dbits));
-    return a.s * d * fmaf(-8.f, a.X, S);
+    return d * fmaf(-8.f, a.XS, S);
   }
 }
 
@@ -266,16 +268,16 @@ __device__ __forceinline__ float q4k_sub_dot(uint32_t row, int b, const ActBlock
   const uint32_t mn = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
   const int ns = 4 * (j & 1);  // the run's low or high nibbles
   const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-  int s0 = 0, s1 = 0;
+  int s0[2] = {0, 0}, s1[2] = {0, 0};  // per half
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t q = (w[i] >> ns) & 0x0F0F0F0Fu;  // values 4i .. 4i + 3
-    s0 = dp4a_uu(q, a.p[i], s0);
-    s1 = dp4a_us(q, a.p[8 + i], s1);
+    s0[i >> 2] = dp4a_uu(q, a.p[i], s0[i >> 2]);
+    s1[i >> 2] = dp4a_us(q, a.p[8 + i], s1[i >> 2]);
   }
-  const float S = (float)(s1 * 256 + s0);
+  const float S = fmaf(a.s0, (float)(s1[0] * 256 + s0[0]), a.s1 * (float)(s1[1] * 256 + s0[1]));
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));  // d, dmin
-  return a.s * fmaf(f.x * (float)sc, S, -(f.y * (float)mn) * a.X);
+  return fmaf(f.x * (float)sc, S, -(f.y * (float)mn) * a.XS);
 }
 
 // 32 bytes from a 2-byte aligned shared address as 8 words (9 aligned words read; the run
@@ -314,7 +316,7 @@ __device__ __forceinline__ float q6k_sub_dot(uint32_t row, int b, const ActBlock
   }
   const float sc0 = (float)(int)(int8_t)(scp & 0xFFu), sc1 = (float)(int)(int8_t)(scp >> 8);
   const float S0 = (float)(s1[0] * 256 + s0[0]), S1 = (float)(s1[1] * 256 + s0[1]);
-  return a.s * d * fmaf(sc1, S1, sc0 * S0);
+  return d * fmaf(sc1 * a.s1, S1, (sc0 * a.s0) * S0);
 }
 
 // ---- f32 activations (the default) -------------------------------------------------
@@ -916,6 +918,7 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   extern __shared__ __align__(128) uint8_t gsm[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ float rowdot[GU_THREADS / 32][4];
+  __shared__ float actv[GU_VALUES];  // fixed point: the CTA's activations, quantised by warp 0
   __shared__ float gscore[64];
   __shared__ int rids[32];
   __shared__ float rw[32];
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   tr(a, TR_GU_START, trows);
   uint8_t* win = gsm;
   uint8_t* xplanes = gsm + (size_t)4 * p.gu_win;  // x: fixed-point planes, or f32 chunks
-  float2* xinfo = reinterpret_cast<float2*>(xplanes + (size_t)p.nbH * 64);
+  float4* xinfo = reinterpret_cast<float4*>(xplanes + (size_t)p.nbH * 64);
   float4* xs = reinterpret_cast<float4*>(xplanes);
   float* xsum = reinterpret_cast<float*>(xplanes + (size_t)p.nbH * 128);
   uint8_t* sel = xplanes + (size_t)p.nbH * (FX ? ACT_BLOCK_SMEM_FX : ACT_BLOCK_SMEM);
@@ -1076,7 +1079,52 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
   if (lane < 2) {
     const float act =
         swiglu_act(rowdot[warp][2 * lane] * r, rowdot[warp][2 * lane + 1] * r, shared ? a.lim_s : a.lim);
-    for (int c = 0; c < p.rep; ++c) a.act[(size_t)c * a.act_copy + (size_t)tok * p.act_stride + v0 + 2 * warp + lane] = act;
+    if constexpr (FX) actv[2 * warp + lane] = act;
+    else
+      for (int c = 0; c < p.rep; ++c) a.act[(size_t)c * a.act_copy + (size_t)tok * p.act_stride + v0 + 2 * warp + lane] = act;
+  }
+  if constexpr (FX) {
+    // The CTA's 16 activations are half h of activation block gb: warp 0 quantises them as
+    // quant_task does a half (one power of two from their largest magnitude) and writes the
+    // half's two plane chunks and its {scale, sum} into every copy, in the layout the down
+    // kernel stages as is: per token, planes [4][nact][16 B] (chunk 2P + h: plane P of half
+    // h), then info [nact][16 B] ({s0, X0, s1, X1}).
+    static_assert(GU_VALUES == 16, "one CTA makes half an activation block");
+    __syncthreads();
+    if (warp == 0) {
+      const float v = lane < GU_VALUES ? actv[lane] : 0.f;
+      float amax = fabsf(v);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+      float inv = 0.f, sc = 0.f;
+      if (eb >= 30) {
+        inv = __uint_as_float((uint32_t)(140 - eb + 127) << 23);
+        sc = __uint_as_float((uint32_t)(eb - 140 + 127) << 23);
+      }
+      const int q = round_small(v * inv);
+      int X = q;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) X += __shfl_xor_sync(0xffffffffu, X, o);
+      // word w of plane P: byte P of q of values 4w .. 4w + 3 (lanes 4w .. 4w + 3)
+      uint32_t b0 = ((uint32_t)q & 0xFFu) << (8 * (lane & 3));
+      uint32_t b1 = (((uint32_t)q >> 8) & 0xFFu) << (8 * (lane & 3));
+      b0 |= __shfl_xor_sync(0xffffffffu, b0, 1);
+      b1 |= __shfl_xor_sync(0xffffffffu, b1, 1);
+      b0 |= __shfl_xor_sync(0xffffffffu, b0, 2);
+      b1 |= __shfl_xor_sync(0xffffffffu, b1, 2);
+      const uint4 lo = make_uint4(__shfl_sync(0xffffffffu, b0, 0), __shfl_sync(0xffffffffu, b0, 4),
+                                  __shfl_sync(0xffffffffu, b0, 8), __shfl_sync(0xffffffffu, b0, 12));
+      const uint4 hi = make_uint4(__shfl_sync(0xffffffffu, b1, 0), __shfl_sync(0xffffffffu, b1, 4),
+                                  __shfl_sync(0xffffffffu, b1, 8), __shfl_sync(0xffffffffu, b1, 12));
+      const int gb = v0 >> 5, h = (v0 >> 4) & 1;
+      if (lane < p.rep) {
+        uint8_t* rec = reinterpret_cast<uint8_t*>(a.act + (size_t)lane * a.act_copy + (size_t)tok * p.act_stride);
+        *reinterpret_cast<uint4*>(rec + ((size_t)h * p.nact + gb) * 16) = lo;
+        *reinterpret_cast<uint4*>(rec + ((size_t)(2 + h) * p.nact + gb) * 16) = hi;
+        *reinterpret_cast<float2*>(rec + (size_t)64 * p.nact + (size_t)gb * 16 + 8 * h) = make_float2(sc, (float)X);
+      }
+    }
   }
   tr(a, TR_GU_END, trows);
 }
@@ -1107,7 +1155,7 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   tr(a, TR_DN_START, trows);
   const size_t win_r = (size_t)p.dn_win_fs;  // first routed window
   uint8_t* aplanes = dsm + win_r + (size_t)p.K * p.dn_win_f;  // activations: fixed-point planes, or f32 chunks
-  float2* ainfo = reinterpret_cast<float2*>(aplanes + (size_t)p.dn_piece * 64);
+  float4* ainfo = reinterpret_cast<float4*>(aplanes + (size_t)p.dn_piece * 64);
   float4* axs = reinterpret_cast<float4*>(aplanes);
   float* axsum = reinterpret_cast<float*>(aplanes + (size_t)p.dn_piece * 128);
   uint8_t* sel = aplanes + (size_t)p.dn_piece * (FX ? ACT_BLOCK_SMEM_FX : ACT_BLOCK_SMEM);
@@ -1179,11 +1227,33 @@ __global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int t
   #pragma unroll 1
   for (int pb = 0; pb < nact; pb += p.dn_piece) {
     const int np = nact - pb < p.dn_piece ? nact - pb : p.dn_piece;
-    const float* act = a.act + (size_t)cp * a.act_copy + (size_t)tok * p.act_stride + (size_t)pb * 32;
-    if constexpr (FX)
-      quant_blocks<4>(act, np, p.dn_piece, aplanes, ainfo, tid, DN_THREADS);
-    else
+    if constexpr (FX) {
+      // the gate/up kernel wrote the blocks already quantised: planes chunk c of block
+      // pb + i and its info, 16 bytes each, go to shared memory as they are (all loads of a
+      // thread are issued before its stores)
+      const uint8_t* rec = reinterpret_cast<const uint8_t*>(a.act + (size_t)cp * a.act_copy + (size_t)tok * p.act_stride);
+      constexpr int U = 4;
+      for (int i0 = tid; i0 < 5 * np; i0 += U * DN_THREADS) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * DN_THREADS, c = i / np, bi = i - c * np;
+          if (i < 5 * np)
+            v[u] = __ldcg(reinterpret_cast<const uint4*>(c < 4 ? rec + ((size_t)c * nact + pb + bi) * 16
+                                                               : rec + (size_t)64 * nact + (size_t)(pb + bi) * 16));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * DN_THREADS, c = i / np, bi = i - c * np;
+          if (i < 5 * np)
+            *reinterpret_cast<uint4*>(c < 4 ? aplanes + ((size_t)c * p.dn_piece + bi) * 16
+                                            : reinterpret_cast<uint8_t*>(ainfo) + (size_t)bi * 16) = v[u];
+        }
+      }
+    } else {
+      const float* act = a.act + (size_t)cp * a.act_copy + (size_t)tok * p.act_stride + (size_t)pb * 32;
       store_blocks_f32<4>(act, np, p.dn_piece, axs, axsum, tid, DN_THREADS);
+    }
     __syncthreads();  // the piece; on the first pass also the window offsets
     if (pb == 0) {
       tr(a, TR_DN_QUANT, trows);
