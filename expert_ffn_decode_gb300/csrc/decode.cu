@@ -1139,7 +1139,7 @@ __global__ void __launch_bounds__(GU_THREADS, 3) dec_gate_up(const DecodeArgs a,
 // t + 256 / RG, ... of each piece with all of the group's rows: an activation block
 // is read once for R / RG block dots.
 template <int QT, bool FX>
-__global__ void __launch_bounds__(DN_THREADS) dec_down(const DecodeArgs a, int trows) {
+__global__ void __launch_bounds__(DN_THREADS, 3) dec_down(const DecodeArgs a, int trows) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ float gscore[64];
