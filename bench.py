@@ -46,7 +46,8 @@ ARITH_TEXT = {
     False: "4-bit weights dequantised exactly to f32 (d*q + m), f32 activations, f32 FMA accumulation "
            "(d * sum(q x) + m * sum(x) per block); router and routing in f32",
     True: "4-bit weights x activations in 16-bit block fixed point (15 bits and sign, power-of-two scale per "
-          "32 values): exact int32 block dots (dp4a), f32 scaling and accumulation; router and routing in f32",
+          "16 values): exact int32 dots per half block (dp4a), f32 scaling and accumulation; router and routing "
+          "in f32",
 }
 # Decode workloads timed beside the headline, each in a sub-object of the line.
 OTHER_DECODE = ("flint_decode_t1", "lfm25_decode_t1", "ling_decode_t1", "ling_kq_decode_t1")

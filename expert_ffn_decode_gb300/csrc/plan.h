@@ -49,7 +49,7 @@ struct DecodePlan {
 
 constexpr int GU_VALUES = 16;  // intermediate values per gate/up CTA
 // Shared-memory bytes per 32-value activation block: f32 chunks (128) and the block sum (4),
-// or the 16-bit fixed-point form: planes (64) and the scale and sum (8).
+// or the 16-bit fixed-point form: planes (64) and each half's scale and sum (16).
 constexpr uint32_t ACT_BLOCK_SMEM = 132;
 constexpr uint32_t ACT_BLOCK_SMEM_FX = 80;  // 64 B of planes, {s0, X0, s1, X1}
 constexpr int DEC_TMAX = 16;   // tokens per decode call (the chain takes up to this many at once)

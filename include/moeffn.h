@@ -148,8 +148,8 @@ typedef struct moe_cfg {
  *                  (with several tokens) a selection kernel, a gate/up kernel and a
  *                  down kernel with the weighted sum. The router is an f32 dot. By
  *                  default the 4-bit blocks meet activations held in 16-bit block
- *                  fixed point (a power-of-two scale per 32 values, error at most
- *                  2^-15 of the block's largest magnitude), so each block dot is an
+ *                  fixed point (a power-of-two scale per 16 values, error at most
+ *                  2^-15 of the largest magnitude among those 16), so each block dot is an
  *                  exact int32 sum (dp4a), scaled and accumulated in f32. With
  *                  MOE_F32_ACT the activations stay f32 and each block contributes
  *                  d * sum(q x) + m * sum(x) by f32 fused multiply-adds (the pages'
