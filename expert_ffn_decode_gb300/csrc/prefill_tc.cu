@@ -954,12 +954,15 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
 }
 
 // ---- token-operand images ------------------------------------------------------------------
-// x rows of each chunk as f16 hi and lo parts, tiled as the MMA's B operand. Grid (chunk,
-// row group): warp w of block (c, y) writes row 8y + w of chunk c (token chunks, or routed
-// chunks when `routed`), 8 K values a lane per step.
+// x rows of each chunk as f16 hi and lo parts, tiled as the MMA's B operand. Grid (chunk, row
+// group slice): CTA (c, y) takes the chunk's 8-row groups y, y + gridDim.y, ... (token chunks,
+// or routed chunks when `routed`), warp w the 128-value K blocks w, w + 8, ... of each. Lane
+// (q = lane / 8, r = lane % 8) takes row r of the group and pieces q, q + 4, q + 8, q + 12 of
+// the block (a piece: 8 values, one 16-byte core-matrix row), so the eight lanes of a piece
+// write one whole 128-byte core matrix with each store.
 __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int routed) {
   const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = 8 * blockIdx.y + warp;
+  const int r = lane & 7, q = lane >> 3;
   int n, row0, prow;
   uint8_t* base;
   const int nkh = a.H / TP_KB;
@@ -979,32 +982,30 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
   }
   const int npad = (n + 15) & ~15, nb = 2 * npad;
   base += (size_t)2 * prow * nkh * 256;
-  // warp w of row group y takes rows 8 y + w, then 8 gridDim.y further on
-  for (int r = r0; r < n; r += 8 * (int)gridDim.y) {
-    const int tok = routed ? (int)(a.perm[row0 + r] / (uint32_t)a.K) : row0 + r;
+  for (int g = blockIdx.y; 8 * g < n; g += gridDim.y) {
+    const int row = 8 * g + r;
+    const bool valid = row < n;
+    const int tok = !valid ? 0 : routed ? (int)(a.perm[row0 + row] / (uint32_t)a.K) : row0 + row;
     const float* xrow = a.x + (size_t)tok * a.H;
-    const int rl = npad + r;
-    const uint32_t hi_off = (uint32_t)((r >> 3) * 128 + (r & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
-    // four pieces a lane at a time: their loads are all issued before any store (the stores
-    // could alias x as far as the compiler knows, so it would not hoist the loads itself)
-    const int np = a.H / 8;
-    for (int p0 = lane; p0 < np; p0 += 4 * 32) {
+    const int rl = npad + row;  // the lo part's row
+    const uint32_t hi_off = (uint32_t)((row >> 3) * 128 + (row & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
+    for (int kk = warp; kk < nkh; kk += 8) {
+      // the four pieces' loads are all issued before any store (the stores could alias x as
+      // far as the compiler knows, so it would not hoist the loads itself)
       float4 x0[4], x1[4];
-  #pragma unroll
+#pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int p = p0 + 32 * u;
-        if (p < np) {
-          const int g = (p >> 4) * TP_KB + 8 * (p & 15);  // first slot of the piece
-          const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * (g >> 5));
-          x0[u] = __ldg(xr + ((g & 31) >> 3));
-          x1[u] = __ldg(xr + 4 + ((g & 31) >> 3));
+        const int gs = kk * TP_KB + 8 * (q + 4 * u);  // first slot of the piece
+        const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * (gs >> 5));
+        if (valid) {
+          x0[u] = __ldg(xr + ((gs & 31) >> 3));
+          x1[u] = __ldg(xr + 4 + ((gs & 31) >> 3));
         }
       }
-  #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int p = p0 + 32 * u;
-        if (p < np) {
-          const int kk = p >> 4, kc8 = p & 15;
+      if (valid) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int kc8 = q + 4 * u;
           uint4 hi, lo;
           hi.x = pack_h2(x0[u].x, x0[u].z);
           hi.y = pack_h2(x0[u].y, x0[u].w);
@@ -1555,8 +1556,8 @@ cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t s
   } else {
     grid = (a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX;
   }
-  // routed chunks hold about P / E rows (a dozen for the Flint batch): two row groups, looping
-  // over any further rows, launch far fewer CTAs that would exit at once
+  // routed chunks hold about P / E rows (a dozen for the Flint batch): two 8-row groups a chunk,
+  // looping over any further groups, launch far fewer CTAs that would exit at once
   tile_images<<<dim3(grid, routed ? 2 : PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
   return cudaGetLastError();
 }
