@@ -15,7 +15,6 @@ namespace moe {
 // A workspace starts zeroed. The status word is sticky until the host clears it.
 enum CtrlWord : int {
   CTRL_STATUS = 8,   // device error bits (see DEV_ERR_*)
-  CTRL_TICKET = 16,  // decode router: CTAs that have written their logits in this call
 };
 constexpr int CTRL_BYTES = 512;
 
