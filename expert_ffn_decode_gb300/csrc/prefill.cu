@@ -125,10 +125,14 @@ __global__ void __launch_bounds__(256) prefill_router(const PrefillArgs a) {
 // ---------------------------------------------------------------------------
 // top-k: one warp per token
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) prefill_topk(const PrefillArgs a) {
+// One warp per token, TOPK_WARPS tokens a CTA: few warps a CTA spread a batch's tokens over
+// every SM (a token's work is a serial chain of shared-memory passes, so SMs, not warps per
+// SM, set the pace).
+constexpr int TOPK_WARPS = 2;
+__global__ void __launch_bounds__(32 * TOPK_WARPS) prefill_topk(const PrefillArgs a) {
   extern __shared__ __align__(16) uint8_t tsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  const int t = blockIdx.x * TOPK_WARPS + warp;
   if (t >= a.T) return;  // whole warp
   uint8_t* base = tsm + (size_t)warp * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
   uint32_t* keys = reinterpret_cast<uint32_t*>(base);
@@ -848,10 +852,10 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
     prefill_router<<<dim3((a.E + RT_TILE - 1) / RT_TILE, (a.T + RT_TILE - 1) / RT_TILE), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const size_t topk_smem = (size_t)8 * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
+  const size_t topk_smem = (size_t)TOPK_WARPS * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
   e = ensure_smem(reinterpret_cast<const void*>(prefill_topk), (int)topk_smem);
   if (e != cudaSuccess) return e;
-  prefill_topk<<<(a.T + 7) / 8, 256, topk_smem, st>>>(a);
+  prefill_topk<<<(a.T + TOPK_WARPS - 1) / TOPK_WARPS, 32 * TOPK_WARPS, topk_smem, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     const size_t tbytes = (size_t)((a.T * a.K + 31) / 32) * a.E * 2;
