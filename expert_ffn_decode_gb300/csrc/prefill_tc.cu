@@ -661,7 +661,11 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
       for (int kk = 0; kk < t.kdim / TP_KB; ++kk) {  // one stage per 128-value A unit
         const int sb = (int)(rb % G::NSB);
         const int own = split ? (int)(rb & 1u) : 0;
-        if (rb >= (uint32_t)G::NSB && !tp_wait_warp(&b_empty[sb], ((rb / G::NSB) - 1) & 1u, abrt)) {
+        // with as many token stages as A slots, unit n's stage and slot have the same index and
+        // one commit (on a_empty) releases both
+        constexpr bool kOneRelease = G::NSB == TP_GROUPS;
+        if (rb >= (uint32_t)G::NSB &&
+            !tp_wait_warp(kOneRelease ? &a_empty[sb] : &b_empty[sb], ((rb / G::NSB) - 1) & 1u, abrt)) {
           ok = false;
           break;
         }
@@ -750,7 +754,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
             mma_f16_ta(acc + (uint32_t)(ch * t.nb), ta0 + 8u * j, bd, idesc, accum);
           }
           fresh = false;
-          mma_commit(&b_empty[sb]);
+          if constexpr (G::NSB != TP_GROUPS) mma_commit(&b_empty[sb]);  // else sb == g: a_empty releases both
           mma_commit(&a_empty[g]);
         }
         if (ok) mma_commit(&acc_full[ab]);  // arrives once this issuer's MMAs are done

@@ -9,7 +9,9 @@ phases behind or ahead of the barrier it waits on (a parity wait cannot tell tho
 no A slot or B stage is refilled while MMAs read it, that every accumulation chain of a tile is
 written by one issuer and initialised before it is accumulated into, and that no schedule
 deadlocks. An MMA commit arrives when the issuing thread's earlier MMAs complete: completions
-are modelled per issuer, in issue order, at random later times.
+are modelled per issuer, in issue order, at random later times. (With three token stages, as
+many as A slots, the kernel's gate/up contraction releases a unit's stage and slot with one
+commit on the slot's barrier; both arrivals of the model then happen at the same point.)
 
 A first version of the two-issuer protocol waited on one a_full / b_full barrier per slot for
 both issuers; an issuer that skipped the other's units could then wait two phases ahead of a
