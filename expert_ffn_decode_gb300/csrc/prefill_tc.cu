@@ -734,6 +734,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
           tc_fence_after_sync();
           const uint8_t* B = bring + sb * TP_B_STAGE;
           const uint32_t ta0 = tmem + TP_A_COL + 64u * g;  // the group's A slot
+          // B descriptor of K step j: the stage's, its start address (in 16-byte units, bits
+          // 0-13; a stage ends below 228 KB, so the field does not carry) advanced 2 j nb units
+          const uint64_t bd0 = smem_desc(B, 16u * t.nb, 128);
 #pragma unroll
           for (int j = 0; j < TP_KB / 16; ++j) {
             // narrow tiles keep several independent accumulation chains in flight instead of
@@ -750,8 +753,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
               ch = iss;
               accum = !fresh || j >= 1;
             }
-            const uint64_t bd = smem_desc(B + 2 * j * 16 * t.nb, 16u * t.nb, 128);
-            mma_f16_ta(acc + (uint32_t)(ch * t.nb), ta0 + 8u * j, bd, idesc, accum);
+            mma_f16_ta(acc + (uint32_t)(ch * t.nb), ta0 + 8u * j, bd0 + (uint64_t)(2 * j * t.nb), idesc, accum);
           }
           fresh = false;
           if constexpr (G::NSB != TP_GROUPS) mma_commit(&b_empty[sb]);  // else sb == g: a_empty releases both
