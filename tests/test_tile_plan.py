@@ -78,7 +78,7 @@ def test_chunks_fit_the_operand_images(E, K, nmax):
 
 
 def test_flint_eight_tokens():
-    # the shape of the run whose fault round 1 recorded: the Flint layer (256 experts, top-6)
+    # the shape of the run whose fault is on record: the Flint layer (256 experts, top-6)
     # with 8 tokens on the tile pipeline: at most 48 chunks of 1 .. 8 pairs, 16 padded rows each
     rng = np.random.default_rng(8)
     ids = np.stack([rng.choice(256, 6, replace=False) for _ in range(8)])
