@@ -158,15 +158,18 @@ typedef struct moe_cfg {
  *                  tokens. An f32 router
  *                  contraction; one warp per token for the selection; a stable
  *                  counting sort of the (token, pick) pairs by expert; grouped
- *                  contractions on the tensor cores. The blocks are dequantised
- *                  exactly to f16 before a single rounding. x enters as an f16 hi + lo
- *                  pair (22 bits). The SwiGLU activations are rounded once to f16.
- *                  Products accumulate in f32. Requires |x| and every activation to
- *                  stay below 65504 (the f16 range).
- *   Layers whose three matrices are all Q4_1 (or all Q4_0) and whose hidden, expert_ff
- *   and shared_ff are whole multiples of 128 (Q4_1) or 256 (Q4_0) run the batched
- *   contractions as warp-specialised TMA/TMEM pipelines; other layers (K-quant ones
- *   among them) run a general form of the same contractions.
+ *                  contractions on the tensor cores. The 4-bit blocks are dequantised
+ *                  exactly to f16 before a single rounding; K-quant values on the tile
+ *                  pipeline below take their f16-rounded scale and offset (up to three
+ *                  roundings of 2^-11). x enters as an f16 hi + lo pair (22 bits). The
+ *                  SwiGLU activations are rounded once to f16. Products accumulate in
+ *                  f32. Requires |x| and every activation to stay below 65504 (the f16
+ *                  range).
+ *   The batched contractions run as warp-specialised TMA/TMEM pipelines for layers whose
+ *   three matrices are all Q4_1 (or all Q4_0) with hidden, expert_ff and shared_ff whole
+ *   multiples of 128 (Q4_1) or 256 (Q4_0), and for Q4_K gate/up rows with Q4_K or Q6_K down
+ *   rows with all three multiples of 256 (Q6_K down rows of at most 768 values); other
+ *   layers run a general form of the same contractions.
  * Both paths give the same picks; outputs agree to the tolerance of their arithmetic
  * (relative L2 well under 2e-3 against a float64 evaluation). */
 
