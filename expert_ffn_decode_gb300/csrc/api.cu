@@ -418,7 +418,6 @@ int enqueue(const float* x, const float* router_w, const float* bias, const void
     pa.ids = reinterpret_cast<int32_t*>(pb + P.ids);
     pa.wts = reinterpret_cast<float*>(pb + P.wts);
     pa.offsets = reinterpret_cast<uint32_t*>(pb + P.offsets);
-    pa.table = reinterpret_cast<uint16_t*>(pb + P.table);
     pa.perm = reinterpret_cast<uint32_t*>(pb + P.perm);
     pa.wsorted = reinterpret_cast<float*>(pb + P.wsorted);
     pa.pos_of = reinterpret_cast<uint32_t*>(pb + P.pos_of);

@@ -126,60 +126,87 @@ __global__ void __launch_bounds__(256) prefill_router(const PrefillArgs a) {
 // top-k: one warp per token
 // ---------------------------------------------------------------------------
 // One warp per token, TOPK_WARPS tokens a CTA: few warps a CTA spread a batch's tokens over
-// every SM (a token's work is a serial chain of shared-memory passes, so SMs, not warps per
-// SM, set the pace).
+// every SM (a token's work is a serial chain of warp steps, so SMs, not warps per SM, set
+// the pace). Lane l holds the keys of experts l + 32 i (i < EPL) in registers; every logit
+// and bias is loaded before the first is used, so the token waits on one round trip.
 constexpr int TOPK_WARPS = 2;
-__global__ void __launch_bounds__(32 * TOPK_WARPS) prefill_topk(const PrefillArgs a) {
-  extern __shared__ __align__(16) uint8_t tsm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * TOPK_WARPS + warp;
-  if (t >= a.T) return;  // whole warp
-  uint8_t* base = tsm + (size_t)warp * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(base);
-  float* probs = reinterpret_cast<float*>(base + (size_t)a.E * 4);
-  float* gscore = reinterpret_cast<float*>(base + (size_t)a.E * 8);
-  int* picks = reinterpret_cast<int*>(base + (size_t)a.E * 8 + 64 * 4);
-  for (int e = lane; e < a.E; e += 32) {
-    const float l = a.logits[(size_t)t * a.E + e];
-    const float pr = 1.f / (1.f + expf(-l));
-    probs[e] = pr;
-    keys[e] = order_key(pr + (a.bias ? __ldg(a.bias + e) : 0.f));
+template <int EPL>
+__device__ __forceinline__ void topk_token(const PrefillArgs& a, int t, int lane, uint8_t* base) {
+  float* probs = reinterpret_cast<float*>(base);                            // [E]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(base + (size_t)a.E * 4);    // [E] (groups only)
+  float* gscore = reinterpret_cast<float*>(base + (size_t)a.E * 8);        // [64]
+  int* picks = reinterpret_cast<int*>(base + (size_t)a.E * 8 + 64 * 4);    // [32]
+  float lg[EPL], bs[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < a.E ? __ldcg(a.logits + (size_t)t * a.E + e) : 0.f;
+    bs[i] = (a.bias && e < a.E) ? __ldg(a.bias + e) : 0.f;
+  }
+  uint32_t kv[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    kv[i] = 0u;
+    if (e < a.E) {
+      const float pr = 1.f / (1.f + expf(-lg[i]));
+      probs[e] = pr;
+      kv[i] = order_key(pr + bs[i]);
+      if (a.G > 1) keys[e] = kv[i];
+    }
   }
   __syncwarp();
   if (a.G > 1) {
-    // group score: the two largest s of the group, summed (multiset top-2)
+    // group score: the two largest s of the group, summed (multiset top-2): each lane's two
+    // largest over its experts of the group, then a butterfly that keeps the two largest
     const int per = a.E / a.G;
-    for (int g = lane; g < a.G; g += 32) {
+#pragma unroll 1
+    for (int g = 0; g < a.G; ++g) {
       float x1 = -INFINITY, x2 = -INFINITY;
-      for (int e = g * per; e < (g + 1) * per; ++e) {
+#pragma unroll 1
+      for (int e = g * per + lane; e < (g + 1) * per; e += 32) {
         const uint32_t k = keys[e];
         const float v = __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
         if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
       }
-      gscore[g] = x1 + x2;
-    }
-    __syncwarp();
-    // kept groups: groups_used rounds of the largest score, lowest group on ties
-    uint32_t keep_lo = 0, keep_hi = 0;
-    for (int j = 0; j < a.Gu; ++j) {
-      int best = -1;
-      float bv = 0.f;
-      for (int g = 0; g < a.G; ++g) {
-        const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
-        if (!kept && (best < 0 || gscore[g] > bv)) { best = g; bv = gscore[g]; }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ox1 = __shfl_xor_sync(0xffffffffu, x1, o);
+        const float ox2 = __shfl_xor_sync(0xffffffffu, x2, o);
+        const float hi = fmaxf(x1, ox1), lo = fminf(x1, ox1);
+        x2 = fmaxf(lo, fmaxf(x2, ox2));
+        x1 = hi;
       }
-      if (best < 32) keep_lo |= 1u << best; else keep_hi |= 1u << (best - 32);
-    }
-    for (int e = lane; e < a.E; e += 32) {
-      const int g = e / per;
-      const bool kept = g < 32 ? ((keep_lo >> g) & 1u) : ((keep_hi >> (g - 32)) & 1u);
-      if (!kept) keys[e] = 0u;
+      if (lane == 0) gscore[g] = x1 + x2;
     }
     __syncwarp();
+    // kept groups: groups_used rounds of the largest score, lowest group on ties. Lane l
+    // offers groups l and l + 32, the larger first (a score's key is never 0: only a NaN's is)
+    uint32_t gk0 = lane < a.G ? order_key(gscore[lane]) : 0u;
+    uint32_t gk1 = lane + 32 < a.G ? order_key(gscore[lane + 32]) : 0u;
+    int gi0 = lane, gi1 = lane + 32;
+    if (gk1 > gk0) {
+      const uint32_t tk = gk0; gk0 = gk1; gk1 = tk;
+      gi0 = lane + 32; gi1 = lane;
+    }
+    unsigned long long kept = 0ull;
+#pragma unroll 1
+    for (int j = 0; j < a.Gu; ++j) {
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, gk0);
+      const int win = (int)__reduce_min_sync(0xffffffffu, gk0 == mk && mk != 0u ? (unsigned)gi0 : 0xffffffffu);
+      kept |= 1ull << (win & 63);
+      if (gk0 == mk && gi0 == win) {
+        gk0 = gk1; gi0 = gi1; gk1 = 0u;
+      }
+    }
+    // experts of dropped groups take key 0
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < a.E && !((kept >> (e / per)) & 1ull)) kv[i] = 0u;
+    }
   }
-  if (a.E <= 256) topk_rounds<8>(keys, a.E, a.K, picks, lane);
-  else if (a.E <= 512) topk_rounds<16>(keys, a.E, a.K, picks, lane);
-  else topk_rounds<32>(keys, a.E, a.K, picks, lane);
+  topk_rounds_kv<EPL>(kv, a.E, a.K, picks, lane);
   __syncwarp();
   const float pj = lane < a.K ? probs[picks[lane]] : 0.f;
   const float wsum = fmaxf(warp_sum(pj), a.norm_min);
@@ -193,71 +220,122 @@ __global__ void __launch_bounds__(32 * TOPK_WARPS) prefill_topk(const PrefillArg
   }
 }
 
+__global__ void __launch_bounds__(32 * TOPK_WARPS) prefill_topk(const PrefillArgs a) {
+  extern __shared__ __align__(16) uint8_t tsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * TOPK_WARPS + warp;
+  if (t >= a.T) return;  // whole warp
+  uint8_t* base = tsm + (size_t)warp * ((size_t)a.E * 8 + 64 * 4 + 32 * 4);
+  if (a.E <= 256) topk_token<8>(a, t, lane, base);
+  else if (a.E <= 512) topk_token<16>(a, t, lane, base);
+  else topk_token<32>(a, t, lane, base);
+}
+
 // ---------------------------------------------------------------------------
 // sort: one CTA of 1024 threads (E <= 1024: thread e owns expert e)
 // ---------------------------------------------------------------------------
-// Exclusive prefix sum of v over the CTA; `total` gets the sum of all v.
-__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+// Warp w owns the contiguous pair range of SORT_MAXC-bounded 32-pair chunks w * nc .. w * nc +
+// nc - 1 (nc = ceil(P / 1024)); a pass of T <= PREFILL_CHUNK_T tokens with K <= 32 has
+// P <= 16384 pairs, so nc <= 16.
+constexpr int SORT_WARPS = 32, SORT_MAXC = 16;
+static_assert(SORT_WARPS * 32 * SORT_MAXC >= PREFILL_CHUNK_T * 32, "a pass's pairs fit the sort's chunks");
+
+// Exclusive prefix sums over the CTA of three values at once; `tot` gets their sums.
+__device__ __forceinline__ void cta_excl_scan3(uint32_t v[3], uint32_t (*wsum)[SORT_WARPS], uint32_t tot[3]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t inc = v;
+  uint32_t inc[3] = {v[0], v[1], v[2]};
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, inc[c], o);
+      if (lane >= o) inc[c] += y;
+    }
   }
-  if (lane == 31) wsum[warp] = inc;
+  if (lane == 31)
+    for (int c = 0; c < 3; ++c) wsum[c][warp] = inc[c];
   __syncthreads();
-  if (warp == 0) {
-    uint32_t w = wsum[lane];
+  if (warp < 3) {
+    uint32_t w = wsum[warp][lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    wsum[lane] = w;  // inclusive over warps
+    wsum[warp][lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  const uint32_t ex = inc - v + (warp ? wsum[warp - 1] : 0u);
-  total = wsum[31];
-  __syncthreads();  // wsum is reused by the next scan
-  return ex;
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    tot[c] = wsum[c][SORT_WARPS - 1];
+    v[c] = inc[c] - v[c] + (warp ? wsum[c][warp - 1] : 0u);
+  }
 }
 
-// The count table lives in shared memory when it fits (in_smem), else in the workspace.
-__global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a, int in_smem) {
-  extern __shared__ __align__(16) uint16_t stab[];
+// Dynamic shared memory of the sort for P pairs and E experts: the per-warp count table
+// [SORT_WARPS][E] (u16), then the sorted pair ids and weights [P] (u32, f32), written out in
+// order at the end (one coalesced pass instead of scattered stores from one SM).
+__host__ __device__ __forceinline__ int sort_table_bytes(int E) { return (SORT_WARPS * E * 2 + 15) & ~15; }
+__host__ __device__ __forceinline__ int sort_smem(int P, int E) { return sort_table_bytes(E) + P * 8; }
+
+__global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
+  extern __shared__ __align__(16) uint8_t ssm[];
   __shared__ uint32_t offs[1024];
-  __shared__ uint32_t wsum[32];
+  __shared__ uint32_t wsum[3][SORT_WARPS];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int P = a.T * a.K, nch = (P + 31) / 32, E = a.E;
+  const int P = a.T * a.K, E = a.E, nc = (P + SORT_WARPS * 32 - 1) / (SORT_WARPS * 32);
+  uint16_t* cnt_w = reinterpret_cast<uint16_t*>(ssm);
+  uint32_t* s_perm = reinterpret_cast<uint32_t*>(ssm + sort_table_bytes(E));
+  float* s_w = reinterpret_cast<float*>(s_perm + P);
   const uint32_t lt = (1u << lane) - 1u;
-  uint16_t* table = in_smem ? stab : a.table;
-  // (a) per 32-pair chunk: how many of its pairs picked each expert
-  for (int i = tid; i < nch * E; i += 1024) table[i] = 0;
+  // every pick and weight of this warp's range, loaded at once
+  uint32_t pk[SORT_MAXC];  // the pick (E: none), then its rank in bits 16..31
+  float wv[SORT_MAXC];
+#pragma unroll
+  for (int i = 0; i < SORT_MAXC; ++i) {
+    if (i >= nc) break;
+    const int p = (warp * nc + i) * 32 + lane;
+    pk[i] = p < P ? (uint32_t)__ldg(a.ids + p) : (uint32_t)E;
+    wv[i] = p < P ? __ldg(a.wts + p) : 0.f;
+  }
+  for (int i = tid; i < SORT_WARPS * E; i += 1024) cnt_w[i] = 0;
   __syncthreads();
-  for (int c = warp; c < nch; c += 32) {
-    const int p = c * 32 + lane;
-    const int e = p < P ? a.ids[p] : E;
+  // (a) the warp's count of each expert over its range; each pair's rank among the range's
+  // pairs of its expert (earlier chunks, then earlier lanes)
+  uint16_t* row = cnt_w + (size_t)warp * E;
+#pragma unroll
+  for (int i = 0; i < SORT_MAXC; ++i) {
+    if (i >= nc) break;
+    const int e = (int)pk[i];
     const uint32_t m = __match_any_sync(0xffffffffu, e);
-    if (e < E && (m & lt) == 0) table[(size_t)c * E + e] = (uint16_t)__popc(m);
+    if (e < E) pk[i] |= (uint32_t)(row[e] + __popc(m & lt)) << 16;
+    __syncwarp();
+    if (e < E && (m & lt) == 0) row[e] = (uint16_t)(row[e] + __popc(m));
+    __syncwarp();
   }
   __syncthreads();
-  // (b) per expert: counts of the earlier chunks (in place), total
+  // (b) per expert: the counts of the earlier warps (in place), and the total
   uint32_t cnt = 0;
-  if (tid < E)
-    for (int c = 0; c < nch; ++c) {
-      const uint32_t v = table[(size_t)c * E + tid];
-      table[(size_t)c * E + tid] = (uint16_t)cnt;
-      cnt += v;
+  if (tid < E) {
+#pragma unroll
+    for (int w0 = 0; w0 < SORT_WARPS; w0 += 8) {
+      uint16_t c[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) c[w] = cnt_w[(w0 + w) * E + tid];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        cnt_w[(w0 + w) * E + tid] = (uint16_t)cnt;
+        cnt += c[w];
+      }
     }
+  }
   // (c) first sorted position, first chunk and first padded row of each expert
   const int nmax = a.nmax;
-  uint32_t total = 0, nrouted = 0, ptotal = 0;
-  const uint32_t off = cta_excl_scan(cnt, wsum, total);
   const uint32_t nck = (cnt + nmax - 1) / nmax;
-  const uint32_t cbase = cta_excl_scan(nck, wsum, nrouted);
   const uint32_t prows = nck ? (nck - 1) * nmax + ((cnt - (nck - 1) * nmax + 15) & ~15u) : 0u;
-  const uint32_t pbase = cta_excl_scan(prows, wsum, ptotal);
+  uint32_t v[3] = {cnt, nck, prows}, tot[3];
+  cta_excl_scan3(v, wsum, tot);
+  const uint32_t off = v[0], cbase = v[1], pbase = v[2], nrouted = tot[1];
   if (tid < E) {
     offs[tid] = off;
     a.offsets[tid] = off;
@@ -266,7 +344,7 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a, int in
       a.chunks[cbase + r] = GemmChunk{tid, row0, n, (int)(pbase + r * nmax)};
     }
   }
-  if (tid == 0) a.offsets[E] = total;
+  if (tid == 0) a.offsets[E] = tot[0];
   // shared-expert chunks (token chunks) follow the routed ones
   const int nsh = a.Fs ? (a.T + nmax - 1) / nmax : 0;
   if (tid < nsh) a.chunks[nrouted + tid] = GemmChunk{E, tid * nmax, min(a.T - tid * nmax, nmax), tid * nmax};
@@ -275,17 +353,23 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a, int in
     a.nchunks[1] = nrouted + (uint32_t)nsh;
   }
   __syncthreads();
-  // (d) stable positions: expert's first position + earlier chunks + earlier lanes
-  for (int c = warp; c < nch; c += 32) {
-    const int p = c * 32 + lane;
-    const int e = p < P ? a.ids[p] : E;
-    const uint32_t m = __match_any_sync(0xffffffffu, e);
+  // (d) stable positions: expert's first position + earlier warps + rank in the range
+#pragma unroll
+  for (int i = 0; i < SORT_MAXC; ++i) {
+    if (i >= nc) break;
+    const int e = (int)(pk[i] & 0xffffu);
     if (e < E) {
-      const uint32_t pos = offs[e] + table[(size_t)c * E + e] + __popc(m & lt);
-      a.perm[pos] = (uint32_t)p;
+      const int p = (warp * nc + i) * 32 + lane;
+      const uint32_t pos = offs[e] + row[e] + (pk[i] >> 16);
+      s_perm[pos] = (uint32_t)p;
+      s_w[pos] = wv[i];
       a.pos_of[p] = pos;
-      a.wsorted[pos] = a.wts[p];
     }
+  }
+  __syncthreads();
+  for (int i = tid; i < P; i += 1024) {
+    a.perm[i] = s_perm[i];
+    a.wsorted[i] = s_w[i];
   }
 }
 
@@ -799,7 +883,6 @@ PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile
   w.ids = take(P * 4);
   w.wts = take(P * 4);
   w.offsets = take((size_t)(E + 1) * 4);
-  w.table = take(((P + 31) / 32) * (size_t)E * 2);
   w.perm = take(P * 4);
   w.wsorted = take(P * 4);
   w.pos_of = take(P * 4);
@@ -858,13 +941,11 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
   prefill_topk<<<(a.T + TOPK_WARPS - 1) / TOPK_WARPS, 32 * TOPK_WARPS, topk_smem, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
-    const size_t tbytes = (size_t)((a.T * a.K + 31) / 32) * a.E * 2;
-    const int in_smem = tbytes <= 160 * 1024 ? 1 : 0;
-    if (in_smem && (e = ensure_smem(reinterpret_cast<const void*>(prefill_sort), (int)tbytes)) != cudaSuccess)
-      return e;
-    prefill_sort<<<1, 1024, in_smem ? tbytes : 0, st>>>(a, in_smem);
+    const int sbytes = sort_smem(a.T * a.K, a.E);
+    if ((e = ensure_smem(reinterpret_cast<const void*>(prefill_sort), sbytes)) != cudaSuccess) return e;
+    prefill_sort<<<1, 1024, sbytes, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.tile) {
     if ((e = tile_images_launch(a, true, st)) != cudaSuccess) return e;
     // gate/up runs weights-as-A; the down contraction runs tokens-as-A when its

@@ -38,7 +38,6 @@ struct PrefillArgs {
   int32_t* ids;             // [T][K]
   float* wts;               // [T][K]
   uint32_t* offsets;        // [E + 1] first sorted position of each expert
-  uint16_t* table;          // [ceil(P / 32)][E] per-32-pair counts, then their prefixes
   uint32_t* perm;           // [P] pair (t * K + j) at each sorted position
   float* wsorted;           // [P] routing weight at each sorted position
   uint32_t* pos_of;         // [P] sorted position of each pair
@@ -75,7 +74,7 @@ struct PrefillArgs {
 
 // Bytes of each prefill workspace region for a pass of T tokens (host).
 struct PrefillWs {
-  size_t logits, ids, wts, offsets, table, perm, wsorted, pos_of, chunks, nchunks, x16, act16, act16s,
+  size_t logits, ids, wts, offsets, perm, wsorted, pos_of, chunks, nchunks, x16, act16, act16s,
       ybuf, sbuf, ximg, ximg_routed, aimg, aimg_s, total;
 };
 PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile);

@@ -31,14 +31,9 @@ __device__ __forceinline__ void lane_best(const uint32_t (&kv)[EPL], int lane, u
   bi = lane + 32 * ti[0];
 }
 
+// k rounds over the lane keys kv (kv[i]: expert lane + 32 i); kv is consumed.
 template <int EPL>
-__device__ __forceinline__ void topk_rounds(const uint32_t* keys, int E, int k, int* ids, int lane) {
-  uint32_t kv[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    kv[i] = e < E ? keys[e] : 0u;
-  }
+__device__ __forceinline__ void topk_rounds_kv(uint32_t (&kv)[EPL], int E, int k, int* ids, int lane) {
   uint32_t bk;
   int bi;
   lane_best(kv, lane, bk, bi);
