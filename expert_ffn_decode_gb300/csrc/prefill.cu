@@ -37,6 +37,7 @@
 // 16+4w+3. Every operand uses the same order, so the dot products are unchanged.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -140,7 +141,17 @@ __device__ __forceinline__ void topk_token(const PrefillArgs& a, int t, int lane
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    lg[i] = e < a.E ? __ldcg(a.logits + (size_t)t * a.E + e) : 0.f;
+    // the logit: the router's partial sums over its K slices, in slice order. Every slice
+    // array is read (the workspace holds PREFILL_RT_SLICES of them) so that the loads issue
+    // together, unpredicated; the unused ones drop out of the sum.
+    const int ec = min(e, a.E - 1);
+    float pk[PREFILL_RT_SLICES];
+#pragma unroll
+    for (int k = 0; k < PREFILL_RT_SLICES; ++k) pk[k] = __ldcg(a.logits + ((size_t)k * a.T + t) * a.E + ec);
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < PREFILL_RT_SLICES; ++k) l = k < a.rt_slices ? l + pk[k] : l;
+    lg[i] = e < a.E ? l : 0.f;
     bs[i] = (a.bias && e < a.E) ? __ldg(a.bias + e) : 0.f;
   }
   uint32_t kv[EPL];
@@ -879,7 +890,7 @@ PrefillWs prefill_ws_layout(int T, int H, int E, int K, int F, int Fs, bool tile
   const size_t tok_chunks = ((size_t)T + nmax - 1) / nmax;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
-  w.logits = take((size_t)T * E * 4);
+  w.logits = take((size_t)T * E * 4 * PREFILL_RT_SLICES);  // the tile router's partial sums (top-k reads all)
   w.ids = take(P * 4);
   w.wts = take(P * 4);
   w.offsets = take((size_t)(E + 1) * 4);
@@ -927,7 +938,14 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     a.x = a.xn;
   }
+  a.rt_slices = a.rt_ups = 1;
   if (a.tile) {
+    // the router's (token chunk, 64 experts) tiles are cut into up to PREFILL_RT_SLICES K slices
+    // while the tiles still fit one wave of the persistent grid
+    const int nkh = a.H / 128, tiles = ((a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX) * ((a.E + 63) / 64);
+    const int s = std::max(1, std::min(std::min(PREFILL_RT_SLICES, nkh), a.nc / tiles));
+    a.rt_ups = (nkh + s - 1) / s;
+    a.rt_slices = (nkh + a.rt_ups - 1) / a.rt_ups;
     // token-chunk images first: the router and the shared expert read them
     if ((e = tile_images_launch(a, false, st)) != cudaSuccess) return e;
     if ((e = tile_router_launch(a, st)) != cudaSuccess) return e;

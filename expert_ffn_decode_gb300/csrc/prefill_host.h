@@ -13,6 +13,7 @@ constexpr int PREFILL_MIN_T = 44;     // calls of at least this many tokens take
 constexpr int PREFILL_CHUNK_T = 512;  // tokens per prefill pass (larger batches run in passes)
 constexpr int PREFILL_NMAX = 64;      // tokens (or pairs) per GEMM work unit (general path)
 constexpr int PREFILL_TILE_NMAX = 64; // tokens (or pairs) per GEMM work unit (tile pipeline)
+constexpr int PREFILL_RT_SLICES = 4;  // tile router: K slices at most
 constexpr int PREFILL_THREADS = 256;
 
 // One token-chunk of a GEMM: `slot` = expert id (or n_experts for the shared expert),
@@ -70,6 +71,8 @@ struct PrefillArgs {
   int nc;                   // CTAs of the persistent GEMM kernels
   int nmax;                 // rows per chunk: PREFILL_NMAX or PREFILL_TILE_NMAX
   int tile;                 // 1: tile pipeline (prefill_tile_ok), 0: general path
+  int rt_slices, rt_ups;    // tile router: K slices (logits = the sum of rt_slices partial
+                            // arrays [T][E], in slice order) of rt_ups 128-value units; 1 elsewhere
 };
 
 // Bytes of each prefill workspace region for a pass of T tokens (host).

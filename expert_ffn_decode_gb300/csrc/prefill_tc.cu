@@ -418,12 +418,13 @@ struct TileUnit {
   int row0, prow, mt;      // chunk's first row, padded-row offset, M tile
   bool shared;             // shared expert (token chunk)
   int e0;                  // router: first expert of the tile
+  int k0, ks;              // router: the K slice's first 128-value unit, the slice
 };
 
 template <int MODE, int QT>
 __device__ __forceinline__ int tile_units(const PrefillArgs& a) {
   const int ntok = (a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX;
-  if (MODE == 2) return ntok * ((a.E + 63) / 64);
+  if (MODE == 2) return ntok * ((a.E + 63) / 64) * a.rt_slices;
   const int nr = (int)a.nchunks[0];
   const int nsh = a.Fs ? ntok : 0;
   const int mt_r = MODE == 0 ? a.F / 64 : a.H / 128;
@@ -437,9 +438,13 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, const TileMa
   TileUnit t;
   const int nkh = a.H / TP_KB;
   if (MODE == 2) {
+    // unit u: K slice u % slices of tile u / slices (token chunk j, experts 64 e ...)
     const int et = (a.E + 63) / 64;
+    t.ks = u % a.rt_slices;
+    u /= a.rt_slices;
     const int j = u / et, e = u % et;
     t.e0 = 64 * e;
+    t.k0 = t.ks * a.rt_ups;
     t.map = &maps.rt;
     t.y0 = t.y1 = t.e0;
     t.row0 = j * PREFILL_TILE_NMAX;
@@ -447,9 +452,9 @@ __device__ __forceinline__ TileUnit tile_unit(const PrefillArgs& a, const TileMa
     t.npad = (t.n + 15) & ~15;
     t.nb = 2 * t.npad;
     t.prow = t.row0;
-    t.b = a.ximg + (size_t)2 * t.prow * nkh * 256;
-    t.nk = (a.H + G::KR - 1) / G::KR;
-    t.kdim = a.H;
+    t.nk = min(a.rt_ups, nkh - t.k0);  // KR = 128: one raw chunk per A unit
+    t.kdim = t.nk * TP_KB;
+    t.b = a.ximg + (size_t)2 * t.prow * nkh * 256 + (size_t)t.k0 * t.nb * 256;
     t.mt = 0;
     t.shared = false;
     return t;
@@ -619,7 +624,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
           mbar_arrive_expect_tx(&raw_full[sa], QT == 14 ? (uint32_t)(128 * t.rbs) : (uint32_t)G::STAGE);
           if (MODE == 2) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(dst + j * 8192, t.map, kc * 128 + 32 * j, t.y0, &raw_full[sa], pol_w);
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(dst + j * 8192, t.map, (t.k0 + kc) * 128 + 32 * j, t.y0, &raw_full[sa], pol_w);
           } else if (QT == 14) {  // 128 whole down rows: one contiguous span of 128 rbs bytes
             asm volatile(
                 "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
@@ -904,7 +910,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
               const float v = v0[i] + v1[i];
               const float other = scratch[m * 65 + c];
               if (MODE == 2) {
-                if (c < t.n && t.e0 + m < a.E) a.logits[(size_t)(t.row0 + c) * a.E + t.e0 + m] = v + other;
+                if (c < t.n && t.e0 + m < a.E)
+                  a.logits[((size_t)t.ks * a.T + t.row0 + c) * a.E + t.e0 + m] = v + other;
               } else {
                 // act = silu(gate) * up (clamped) for f = f0 + lane, gathered into the four 16-byte
                 // pieces of the block (slot 8w + k holds value 4w + {0,2,1,3}[k], +16 for k >= 4)
@@ -962,7 +969,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
 // ---- token-operand images ------------------------------------------------------------------
 // x rows of each chunk as f16 hi and lo parts, tiled as the MMA's B operand. Grid (chunk, row
 // group slice): CTA (c, y) takes the chunk's 8-row groups y, y + gridDim.y, ... (token chunks,
-// or routed chunks when `routed`), warp w the 128-value K blocks w, w + 8, ... of each. Lane
+// or routed chunks when `routed`), warp w the 128-value K blocks w, w + 8, ... of each, two
+// blocks a round with all their loads issued before the first store. Lane
 // (q = lane / 8, r = lane % 8) takes row r of the group and pieces q, q + 4, q + 8, q + 12 of
 // the block (a piece: 8 values, one 16-byte core-matrix row), so the eight lanes of a piece
 // write one whole 128-byte core matrix with each store.
@@ -995,35 +1003,43 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
     const float* xrow = a.x + (size_t)tok * a.H;
     const int rl = npad + row;  // the lo part's row
     const uint32_t hi_off = (uint32_t)((row >> 3) * 128 + (row & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
-    for (int kk = warp; kk < nkh; kk += 8) {
-      // the four pieces' loads are all issued before any store (the stores could alias x as
-      // far as the compiler knows, so it would not hoist the loads itself)
-      float4 x0[4], x1[4];
+    for (int kk0 = warp; kk0 < nkh; kk0 += 16) {
+      // two K blocks (kk0, kk0 + 8) a round: all their loads are issued before any store
+      float4 x0[2][4], x1[2][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int gs = kk * TP_KB + 8 * (q + 4 * u);  // first slot of the piece
-        const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * (gs >> 5));
-        if (valid) {
-          x0[u] = __ldg(xr + ((gs & 31) >> 3));
-          x1[u] = __ldg(xr + 4 + ((gs & 31) >> 3));
+      for (int h = 0; h < 2; ++h) {
+        const int kk = kk0 + 8 * h;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int gs = kk * TP_KB + 8 * (q + 4 * u);  // first slot of the piece
+          const float4* xr = reinterpret_cast<const float4*>(xrow + 32 * (gs >> 5));
+          if (valid && kk < nkh) {
+            x0[h][u] = __ldg(xr + ((gs & 31) >> 3));
+            x1[h][u] = __ldg(xr + 4 + ((gs & 31) >> 3));
+          }
         }
       }
       if (valid) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int kc8 = q + 4 * u;
-          uint4 hi, lo;
-          hi.x = pack_h2(x0[u].x, x0[u].z);
-          hi.y = pack_h2(x0[u].y, x0[u].w);
-          hi.z = pack_h2(x1[u].x, x1[u].z);
-          hi.w = pack_h2(x1[u].y, x1[u].w);
-          lo.x = pack_lo(x0[u].x, x0[u].z, hi.x);
-          lo.y = pack_lo(x0[u].y, x0[u].w, hi.y);
-          lo.z = pack_lo(x1[u].x, x1[u].z, hi.z);
-          lo.w = pack_lo(x1[u].y, x1[u].w, hi.w);
-          uint8_t* blk = base + (size_t)kk * nb * 256 + (size_t)kc8 * (nb >> 3) * 128;
-          *reinterpret_cast<uint4*>(blk + hi_off) = hi;
-          *reinterpret_cast<uint4*>(blk + lo_off) = lo;
+        for (int h = 0; h < 2; ++h) {
+          const int kk = kk0 + 8 * h;
+          if (kk >= nkh) break;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int kc8 = q + 4 * u;
+            uint4 hi, lo;
+            hi.x = pack_h2(x0[h][u].x, x0[h][u].z);
+            hi.y = pack_h2(x0[h][u].y, x0[h][u].w);
+            hi.z = pack_h2(x1[h][u].x, x1[h][u].z);
+            hi.w = pack_h2(x1[h][u].y, x1[h][u].w);
+            lo.x = pack_lo(x0[h][u].x, x0[h][u].z, hi.x);
+            lo.y = pack_lo(x0[h][u].y, x0[h][u].w, hi.y);
+            lo.z = pack_lo(x1[h][u].x, x1[h][u].z, hi.z);
+            lo.w = pack_lo(x1[h][u].y, x1[h][u].w, hi.w);
+            uint8_t* blk = base + (size_t)kk * nb * 256 + (size_t)kc8 * (nb >> 3) * 128;
+            *reinterpret_cast<uint4*>(blk + hi_off) = hi;
+            *reinterpret_cast<uint4*>(blk + lo_off) = lo;
+          }
         }
       }
     }
@@ -1562,9 +1578,10 @@ cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t s
   } else {
     grid = (a.T + PREFILL_TILE_NMAX - 1) / PREFILL_TILE_NMAX;
   }
-  // routed chunks hold about P / E rows (a dozen for the Flint batch): two 8-row groups a chunk,
-  // looping over any further groups, launch far fewer CTAs that would exit at once
-  tile_images<<<dim3(grid, routed ? 2 : PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
+  // one CTA per 8-row group of a chunk: the CTAs past a routed chunk's rows exit at once, and
+  // a full chunk's eight groups run side by side (two groups a CTA, looping, measured 12 us
+  // slower on the Ling K-quant batch, whose most-picked experts fill several chunks)
+  tile_images<<<dim3(grid, PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
   return cudaGetLastError();
 }
 
