@@ -245,9 +245,10 @@ __global__ void __launch_bounds__(32 * TOPK_WARPS) prefill_topk(const PrefillArg
 // ---------------------------------------------------------------------------
 // sort: one CTA of 1024 threads (E <= 1024: thread e owns expert e)
 // ---------------------------------------------------------------------------
-// Warp w owns the contiguous pair range of SORT_MAXC-bounded 32-pair chunks w * nc .. w * nc +
-// nc - 1 (nc = ceil(P / 1024)); a pass of T <= PREFILL_CHUNK_T tokens with K <= 32 has
-// P <= 16384 pairs, so nc <= 16.
+// Warp w owns the contiguous pair range of 32-pair chunks w * nc .. w * nc + nc - 1 (nc =
+// ceil(P / 1024)), held in registers: MAXC >= nc is a template bound, the smallest of 4, 8, 16
+// that fits (short straight-line code for the common sizes); a pass of T <= PREFILL_CHUNK_T
+// tokens with K <= 32 has P <= 16384 pairs, so nc <= 16.
 constexpr int SORT_WARPS = 32, SORT_MAXC = 16;
 static_assert(SORT_WARPS * 32 * SORT_MAXC >= PREFILL_CHUNK_T * 32, "a pass's pairs fit the sort's chunks");
 
@@ -289,6 +290,7 @@ __device__ __forceinline__ void cta_excl_scan3(uint32_t v[3], uint32_t (*wsum)[S
 __host__ __device__ __forceinline__ int sort_table_bytes(int E) { return (SORT_WARPS * E * 2 + 15) & ~15; }
 __host__ __device__ __forceinline__ int sort_smem(int P, int E) { return sort_table_bytes(E) + P * 8; }
 
+template <int MAXC>
 __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
   extern __shared__ __align__(16) uint8_t ssm[];
   __shared__ uint32_t offs[1024];
@@ -300,10 +302,10 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
   float* s_w = reinterpret_cast<float*>(s_perm + P);
   const uint32_t lt = (1u << lane) - 1u;
   // every pick and weight of this warp's range, loaded at once
-  uint32_t pk[SORT_MAXC];  // the pick (E: none), then its rank in bits 16..31
-  float wv[SORT_MAXC];
+  uint32_t pk[MAXC];  // the pick (E: none), then its rank in bits 16..31
+  float wv[MAXC];
 #pragma unroll
-  for (int i = 0; i < SORT_MAXC; ++i) {
+  for (int i = 0; i < MAXC; ++i) {
     if (i >= nc) break;
     const int p = (warp * nc + i) * 32 + lane;
     pk[i] = p < P ? (uint32_t)__ldg(a.ids + p) : (uint32_t)E;
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
   // pairs of its expert (earlier chunks, then earlier lanes)
   uint16_t* row = cnt_w + (size_t)warp * E;
 #pragma unroll
-  for (int i = 0; i < SORT_MAXC; ++i) {
+  for (int i = 0; i < MAXC; ++i) {
     if (i >= nc) break;
     const int e = (int)pk[i];
     const uint32_t m = __match_any_sync(0xffffffffu, e);
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(1024) prefill_sort(const PrefillArgs a) {
   __syncthreads();
   // (d) stable positions: expert's first position + earlier warps + rank in the range
 #pragma unroll
-  for (int i = 0; i < SORT_MAXC; ++i) {
+  for (int i = 0; i < MAXC; ++i) {
     if (i >= nc) break;
     const int e = (int)(pk[i] & 0xffffu);
     if (e < E) {
@@ -960,8 +962,10 @@ cudaError_t prefill_launch(const PrefillArgs& a_in, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     const int sbytes = sort_smem(a.T * a.K, a.E);
-    if ((e = ensure_smem(reinterpret_cast<const void*>(prefill_sort), sbytes)) != cudaSuccess) return e;
-    prefill_sort<<<1, 1024, sbytes, st>>>(a);
+    const int nc = (a.T * a.K + SORT_WARPS * 32 - 1) / (SORT_WARPS * 32);
+    auto kern = nc <= 4 ? prefill_sort<4> : nc <= 8 ? prefill_sort<8> : prefill_sort<SORT_MAXC>;
+    if ((e = ensure_smem(reinterpret_cast<const void*>(kern), sbytes)) != cudaSuccess) return e;
+    kern<<<1, 1024, sbytes, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.tile) {

@@ -968,12 +968,12 @@ __global__ void __launch_bounds__(TP_THREADS, 1) tile_gemm(const PrefillArgs a, 
 
 // ---- token-operand images ------------------------------------------------------------------
 // x rows of each chunk as f16 hi and lo parts, tiled as the MMA's B operand. Grid (chunk, row
-// group slice): CTA (c, y) takes the chunk's 8-row groups y, y + gridDim.y, ... (token chunks,
-// or routed chunks when `routed`), warp w the 128-value K blocks w, w + 8, ... of each, two
-// blocks a round with all their loads issued before the first store. Lane
-// (q = lane / 8, r = lane % 8) takes row r of the group and pieces q, q + 4, q + 8, q + 12 of
-// the block (a piece: 8 values, one 16-byte core-matrix row), so the eight lanes of a piece
-// write one whole 128-byte core matrix with each store.
+// group slice, K slice): CTA (c, y, z) takes the chunk's 8-row groups y, y + gridDim.y, ...
+// (token chunks, or routed chunks when `routed`), warp w the 128-value K blocks w + 8 m with
+// m = z modulo gridDim.z of each, two blocks a round with all their loads issued before the
+// first store. Lane (q = lane / 8, r = lane % 8) takes row r of the group and pieces q, q + 4,
+// q + 8, q + 12 of the block (a piece: 8 values, one 16-byte core-matrix row), so the eight
+// lanes of a piece write one whole 128-byte core matrix with each store.
 __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int routed) {
   const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane & 7, q = lane >> 3;
@@ -1003,12 +1003,14 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
     const float* xrow = a.x + (size_t)tok * a.H;
     const int rl = npad + row;  // the lo part's row
     const uint32_t hi_off = (uint32_t)((row >> 3) * 128 + (row & 7) * 16), lo_off = (uint32_t)((rl >> 3) * 128 + (rl & 7) * 16);
-    for (int kk0 = warp; kk0 < nkh; kk0 += 16) {
-      // two K blocks (kk0, kk0 + 8) a round: all their loads are issued before any store
+    // K blocks warp + 8 m with m = z (mod Z), Z = gridDim.z; two (m0, m0 + Z) a round, all
+    // their loads issued before any store
+    const int Z = (int)gridDim.z;
+    for (int m0 = (int)blockIdx.z; warp + 8 * m0 < nkh; m0 += 2 * Z) {
       float4 x0[2][4], x1[2][4];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int kk = kk0 + 8 * h;
+        const int kk = warp + 8 * (m0 + h * Z);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int gs = kk * TP_KB + 8 * (q + 4 * u);  // first slot of the piece
@@ -1022,7 +1024,7 @@ __global__ void __launch_bounds__(256) tile_images(const PrefillArgs a, int rout
       if (valid) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int kk = kk0 + 8 * h;
+          const int kk = warp + 8 * (m0 + h * Z);
           if (kk >= nkh) break;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -1580,8 +1582,9 @@ cudaError_t tile_images_launch(const PrefillArgs& a, bool routed, cudaStream_t s
   }
   // one CTA per 8-row group of a chunk: the CTAs past a routed chunk's rows exit at once, and
   // a full chunk's eight groups run side by side (two groups a CTA, looping, measured 12 us
-  // slower on the Ling K-quant batch, whose most-picked experts fill several chunks)
-  tile_images<<<dim3(grid, PREFILL_TILE_NMAX / 8), 256, 0, st>>>(a, routed ? 1 : 0);
+  // slower on the Ling K-quant batch, whose most-picked experts fill several chunks). The few
+  // token chunks also split their K blocks over two CTAs.
+  tile_images<<<dim3(grid, PREFILL_TILE_NMAX / 8, routed ? 1 : 2), 256, 0, st>>>(a, routed ? 1 : 0);
   return cudaGetLastError();
 }
 
