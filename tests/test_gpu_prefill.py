@@ -63,6 +63,10 @@ SHAPES = [
            n_tokens=40),                                                 # ragged 64-expert router tile
     _small(57, n_experts=64, n_groups=8, groups_used=3, top_k=6, bias_std=0.1, n_tokens=130,
            shared_ff=128),
+    # the tile router's K slices: 7 units of 128 values in slices of 2, the last holding one
+    _small(65, hidden=896, expert_ff=128, shared_ff=128, n_tokens=50),
+    # 3 units, one a slice; a ragged 64-expert tile; two passes (512 and 128 tokens)
+    _small(66, hidden=384, expert_ff=256, n_experts=96, top_k=5, n_tokens=640),
 ]
 
 
