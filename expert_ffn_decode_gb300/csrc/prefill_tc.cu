@@ -1,7 +1,7 @@
 // Tile pipeline of the batched MoE-FFN step for sm_103a: the router, gate/up and
 // down contractions as warp-specialised persistent kernels on the tensor cores.
 //
-// One CTA per SM, 608 threads:
+// One CTA per SM, 640 threads:
 //   warp 0       weight producer: 2-D TMA tensor copies of the raw weight rows of each
 //                pipeline chunk (one box of 64 or 128 rows) into shared-memory stages (3-D
 //                maps for K-quant records; one bulk copy of 128 whole rows for Q6_K down rows)
