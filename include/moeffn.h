@@ -155,8 +155,9 @@ typedef struct moe_cfg {
  *                  d * sum(q x) + m * sum(x) by f32 fused multiply-adds (the pages'
  *                  arithmetic); it runs about 12% slower on the Flint-shaped layer.
  *   n_tokens >= 44 (or MOE_BATCHED) the batched path, in passes of at most 512
- *                  tokens. An f32 router
- *                  contraction; one warp per token for the selection; a stable
+ *                  tokens. A router contraction accumulated in f32 (on the tile pipeline
+ *                  from f16 hi + lo parts of the f32 rows and tokens, in up to four K
+ *                  slices summed in order); one warp per token for the selection; a stable
  *                  counting sort of the (token, pick) pairs by expert; grouped
  *                  contractions on the tensor cores. The 4-bit blocks are dequantised
  *                  exactly to f16 before a single rounding; K-quant values on the tile
@@ -185,7 +186,7 @@ int moe_ffn_forward(const float* x, const float* router_w, const float* router_b
  * with a caller-owned device workspace of at least moe_workspace_size(cfg) bytes,
  * 256-byte aligned. A workspace must be zero-filled before its first use and then
  * only touched by this library: its first 512 bytes are control words (the
- * router's arrival counter and a status word). Calls sharing one workspace must
+ * status word that moe_workspace_status reads). Calls sharing one workspace must
  * be ordered (same stream, or synchronised); calls with different configurations
  * may share one.
  * Asynchronous: device-side errors surface through moe_workspace_status.
